@@ -1,0 +1,159 @@
+"""fp64 CPU oracle for exact attention.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+leg of ``bench.py`` may import this package.  The CUDA library never calls it,
+and the two share no code: this package holds its own C source
+(``attn_oracle.c``), built with the host C compiler, and a ctypes binding.
+
+Functions (NumPy float64 in, NumPy float64 out; layouts as in the C file):
+    attn_fwd          standard attention, materialised score rows, 3-loop safe
+                      softmax (FlashAttention blog, "(Safe) Softmax"); optional
+                      row subset and optional P output.
+    attn_fwd_online   one-pass online-softmax attention in key blocks, normalised
+                      (blog "FlashAttention", o_N = o'_N) or deferred division
+                      (FlashAttention-2 answer on non-matmul FLOPs).
+    attn_bwd          analytic gradients dQ, dK, dV and D = rowsum(dO * O).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_lock = threading.Lock()
+_libs: dict[int, ctypes.CDLL] = {}
+
+
+def lib_path(mutant: int = 0) -> str:
+    name = "liboracle.so" if mutant == 0 else f"liboracle_mutant{mutant}.so"
+    return os.path.join(_BUILD, name)
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the oracle (or one planted-mistake copy of it) with gcc."""
+    out = lib_path(mutant)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
+        return out
+    os.makedirs(_BUILD, exist_ok=True)
+    tmp = f"{out}.{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-Wall",
+           f"-DORACLE_MUTANT={int(mutant)}", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    dp = ctypes.POINTER(ctypes.c_double)
+    i, d = ctypes.c_int, ctypes.c_double
+    lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, d,
+                                    ctypes.POINTER(ctypes.c_longlong), ctypes.c_longlong]
+    lib.oracle_attn_fwd.restype = i
+    lib.oracle_attn_fwd_online.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, d, i, i]
+    lib.oracle_attn_fwd_online.restype = i
+    lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, d]
+    lib.oracle_attn_bwd.restype = i
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i
+    return lib
+
+
+def load(mutant: int = 0) -> ctypes.CDLL:
+    with _lock:
+        if mutant not in _libs:
+            _libs[mutant] = _bind(ctypes.CDLL(build(mutant)))
+        return _libs[mutant]
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _shape(q: np.ndarray, k: np.ndarray):
+    B, H, N, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if (Bk, Nk, dk) != (B, N, d):
+        raise ValueError(f"q {q.shape} and k {k.shape} disagree")
+    return B, H, Hkv, N, d
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise RuntimeError(f"{what} failed with code {rc}")
+
+
+def num_threads(mutant: int = 0) -> int:
+    return int(load(mutant).oracle_num_threads())
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, rows=None, return_p: bool = False,
+             mutant: int = 0):
+    """Standard attention.  q [B,H,N,d], k/v [B,Hkv,N,d].
+
+    rows=None: returns (O [B,H,N,d], LSE [B,H,N]) (+ P [B,H,N,N] if return_p).
+    rows=array of flat row ids (b*H + h)*N + i: returns (O [R,d], LSE [R]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Hkv, N, d = _shape(q, k)
+    lib = load(mutant)
+    if rows is None:
+        o = np.empty_like(q)
+        lse = np.empty((B, H, N))
+        p = np.empty((B, H, N, N)) if return_p else None
+        rc = lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p),
+                                 B, H, Hkv, N, d, int(causal), float(scale), None, 0)
+        _check(rc, "oracle_attn_fwd")
+        return (o, lse, p) if return_p else (o, lse)
+    if return_p:
+        raise ValueError("return_p needs rows=None")
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    o = np.empty((r.size, d))
+    lse = np.empty(r.size)
+    rc = lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), None,
+                             B, H, Hkv, N, d, int(causal), float(scale),
+                             r.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)), r.size)
+    _check(rc, "oracle_attn_fwd(rows)")
+    return o, lse
+
+
+def attn_fwd_online(q, k, v, causal: bool, scale: float, block: int = 1,
+                    deferred: bool = False, mutant: int = 0):
+    """One-pass online-softmax attention; returns (O, LSE)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Hkv, N, d = _shape(q, k)
+    o = np.empty_like(q)
+    lse = np.empty((B, H, N))
+    rc = load(mutant).oracle_attn_fwd_online(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                             B, H, Hkv, N, d, int(causal), float(scale),
+                                             int(block), int(deferred))
+    _check(rc, "oracle_attn_fwd_online")
+    return o, lse
+
+
+def attn_bwd(q, k, v, dout, causal: bool, scale: float, mutant: int = 0):
+    """Analytic backward; returns (dQ, dK, dV, D)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, Hkv, N, d = _shape(q, k)
+    if dout.shape != q.shape:
+        raise ValueError("dout must have q's shape")
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    D = np.empty((B, H, N))
+    rc = load(mutant).oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
+                                      _ptr(dk), _ptr(dv), _ptr(D), B, H, Hkv, N, d,
+                                      int(causal), float(scale))
+    _check(rc, "oracle_attn_bwd")
+    return dq, dk, dv, D

@@ -1,0 +1,286 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics
+fix, never against the oracle itself.  Each pin takes ``mutant`` (0 = the real
+oracle; >0 = a planted-mistake build used by the mutation test) and raises
+AssertionError when the oracle violates it.
+
+Citations name the page and section of the exact_attention_online pages:
+  [blog]  FlashAttention (NeurIPS 2022) summary blog
+  [fa2]   FlashAttention-2 review thread
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def rand_qkv(B, H, Hkv, N, d, seed, dout=False):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, H, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = rng.standard_normal((B, Hkv, N, d))
+    if dout:
+        return q, k, v, rng.standard_normal((B, H, N, d))
+    return q, k, v
+
+
+def torch_attention(q, k, v, causal, scale):
+    """Library special case: torch fp64 CPU matmul + softmax (+ logsumexp)."""
+    q, k, v = (torch.as_tensor(x, dtype=torch.float64) for x in (q, k, v))
+    G = q.shape[1] // k.shape[1]
+    k = k.repeat_interleave(G, dim=1)
+    v = v.repeat_interleave(G, dim=1)
+    s = (q @ k.transpose(-1, -2)) * scale
+    if causal:
+        N = q.shape[2]
+        mask = torch.ones(N, N, dtype=torch.bool).triu(1)
+        s = s.masked_fill(mask, float("-inf"))
+    return torch.softmax(s, dim=-1) @ v, torch.logsumexp(s, dim=-1)
+
+
+# ---------------------------------------------------------------- forward pins
+
+def pin_rows_sum_to_one(mutant=0):
+    """[blog] "(Safe) Softmax": every row of P is a probability vector; with
+    the causal mask, P_ij = 0 for j > i."""
+    for causal in (False, True):
+        q, k, v = rand_qkv(1, 2, 1, 37, 8, seed=11)
+        _, _, p = oracle.attn_fwd(q, k, v, causal, 0.35, return_p=True, mutant=mutant)
+        assert np.all(p >= 0)
+        assert np.max(np.abs(p.sum(-1) - 1.0)) <= 1e-12, "rows of P must sum to 1"
+        if causal:
+            assert np.all(np.triu(p[0, 0], 1) == 0) and np.all(np.triu(p[0, 1], 1) == 0)
+
+
+def pin_torch_library(mutant=0):
+    """[blog] "From Online Softmax to FlashAttention": standard attention
+    S = QK^T*scale, P = softmax(S), O = PV equals torch's fp64 matmul/softmax
+    and its scaled_dot_product_attention (math kernel, GQA by
+    repeat_interleave); LSE equals torch.logsumexp of the scaled scores."""
+    for (B, H, Hkv, N, d, causal) in [(2, 4, 2, 33, 16, True), (1, 3, 3, 20, 8, False),
+                                      (1, 4, 1, 65, 32, True)]:
+        q, k, v = rand_qkv(B, H, Hkv, N, d, seed=N)
+        scale = 1 / math.sqrt(d)
+        o, lse = oracle.attn_fwd(q, k, v, causal, scale, mutant=mutant)
+        to, tl = torch_attention(q, k, v, causal, scale)
+        assert np.max(np.abs(o - to.numpy())) <= 1e-12
+        assert np.max(np.abs(lse - tl.numpy())) <= 1e-12
+        tq, tk, tv = (torch.as_tensor(x) for x in (q, k, v))
+        sd = torch.nn.functional.scaled_dot_product_attention(
+            tq, tk, tv, is_causal=causal, scale=scale, enable_gqa=(H != Hkv))
+        assert np.max(np.abs(o - sd.numpy())) <= 1e-12
+
+
+def pin_online_matches_three_pass(mutant=0):
+    """[blog] "Online Softmax" (d_N = d'_N) and "FlashAttention" (o_N = o'_N,
+    tiles of b keys); [fa2] deferred division by l.  Both one-pass forms agree
+    with the three-loop safe softmax to 1e-12 relative."""
+    q, k, v = rand_qkv(2, 2, 1, 70, 16, seed=5)
+    q *= 3.0  # wide score range, so rescaling really happens
+    for causal in (False, True):
+        o3, l3 = oracle.attn_fwd(q, k, v, causal, 0.5, mutant=mutant)
+        for block in (1, 7, 64, 128):
+            for deferred in (False, True):
+                o1, l1 = oracle.attn_fwd_online(q, k, v, causal, 0.5, block, deferred,
+                                                mutant=mutant)
+                rel = np.max(np.abs(o1 - o3)) / np.max(np.abs(o3))
+                assert rel <= 1e-12, (block, deferred, rel)
+                assert np.max(np.abs(l1 - l3)) <= 1e-12 * np.max(np.abs(l3))
+
+
+def pin_identical_keys(mutant=0):
+    """Closed form: if every key is the same vector k, all visible scores of a
+    row are equal, so O_i is the plain mean of the visible V rows and
+    LSE_i = scale*<q_i,k> + ln(#visible)."""
+    rng = np.random.default_rng(3)
+    N, d, scale = 29, 8, 0.7
+    kk = rng.standard_normal(d)
+    q = rng.standard_normal((1, 1, N, d))
+    k = np.broadcast_to(kk, (1, 1, N, d)).copy()
+    v = rng.standard_normal((1, 1, N, d))
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal, scale, mutant=mutant)
+        for i in range(N):
+            cnt = i + 1 if causal else N
+            assert np.max(np.abs(o[0, 0, i] - v[0, 0, :cnt].mean(0))) <= 1e-13
+            want = scale * float(q[0, 0, i] @ kk) + math.log(cnt)
+            assert abs(lse[0, 0, i] - want) <= 1e-13
+
+
+def pin_one_hot(mutant=0):
+    """Closed form: Q_i = e_i and K_j = a*e_pi(j) give s_ij = a*scale when
+    pi(j) = i and 0 otherwise, so O_i = (E v_{pi^-1(i)} + sum_{j != pi^-1(i)} v_j)
+    / (E + N - 1) with E = exp(a*scale); for large a this selects one V row."""
+    N = d = 12
+    rng = np.random.default_rng(4)
+    perm = rng.permutation(N)
+    inv = np.argsort(perm)
+    q = np.eye(N)[None, None]
+    v = rng.standard_normal((1, 1, N, d))
+    for a, tol in ((2.0, 1e-13), (400.0, 1e-13)):
+        k = (a * np.eye(N)[perm])[None, None]
+        o, lse = oracle.attn_fwd(q, k, v, False, 0.25, mutant=mutant)
+        E = math.exp(a * 0.25)
+        for i in range(N):
+            sel = inv[i]
+            want = (E * v[0, 0, sel] + v[0, 0].sum(0) - v[0, 0, sel]) / (E + N - 1)
+            assert np.max(np.abs(o[0, 0, i] - want)) <= tol * max(1.0, np.abs(want).max())
+            assert abs(lse[0, 0, i] - math.log(E + N - 1)) <= 1e-12
+        if a > 100:
+            assert np.max(np.abs(o[0, 0] - v[0, 0, inv])) <= 1e-12
+
+
+def pin_causal_row0_and_single_key(mutant=0):
+    """Special cases: with the causal mask, query 0 sees only key 0, so O_0 = V_0
+    and LSE_0 = scale*<q_0,k_0>; with N = 1 the same holds without a mask."""
+    q, k, v = rand_qkv(1, 2, 2, 19, 8, seed=8)
+    o, lse = oracle.attn_fwd(q, k, v, True, 0.4, mutant=mutant)
+    for h in range(2):
+        assert np.array_equal(o[0, h, 0], v[0, h, 0])
+        assert abs(lse[0, h, 0] - 0.4 * float(q[0, h, 0] @ k[0, h, 0])) <= 1e-14
+    q1, k1, v1 = q[:, :, :1], k[:, :, :1], v[:, :, :1]
+    o, lse = oracle.attn_fwd(q1, k1, v1, False, 0.4, mutant=mutant)
+    assert np.array_equal(o[0, :, 0], v1[0, :, 0])
+
+
+def pin_shift_invariance(mutant=0):
+    """Invariance: adding one vector u to every key adds scale*<q_i,u> to every
+    score of row i, which softmax ignores: O, dQ and dV are unchanged and LSE_i
+    moves by scale*<q_i,u>."""
+    q, k, v, do = rand_qkv(1, 2, 1, 24, 8, seed=9, dout=True)
+    u = np.random.default_rng(10).standard_normal(8)
+    for causal in (False, True):
+        o0, l0 = oracle.attn_fwd(q, k, v, causal, 0.3, mutant=mutant)
+        o1, l1 = oracle.attn_fwd(q, k + u, v, causal, 0.3, mutant=mutant)
+        assert np.max(np.abs(o1 - o0)) <= 1e-12
+        assert np.max(np.abs(l1 - l0 - 0.3 * (q @ u))) <= 1e-12
+        g0 = oracle.attn_bwd(q, k, v, do, causal, 0.3, mutant=mutant)
+        g1 = oracle.attn_bwd(q, k + u, v, do, causal, 0.3, mutant=mutant)
+        assert np.max(np.abs(g1[0] - g0[0])) <= 1e-11
+        assert np.max(np.abs(g1[2] - g0[2])) <= 1e-12
+
+
+def pin_golden_closed_form(mutant=0):
+    """tests/golden/closed_form.json: integer score exponentials, exact
+    rational O and exp(LSE) (see make_closed_form.py)."""
+    with open(os.path.join(GOLDEN, "closed_form.json")) as f:
+        data = json.load(f)
+    for c in data["cases"]:
+        q, k, v = (np.array(c[x], dtype=np.float64) for x in ("q", "k", "v"))
+        o, lse = oracle.attn_fwd(q, k, v, c["causal"], c["scale"], mutant=mutant)
+        want_o = np.vectorize(lambda s: float(Fraction(s)))(np.array(c["o_exact"]))
+        want_l = np.vectorize(lambda s: math.log(Fraction(s)))(np.array(c["lse_exp_exact"]))
+        assert np.max(np.abs(o - want_o)) <= 1e-13, c["name"]
+        assert np.max(np.abs(lse - want_l)) <= 1e-13, c["name"]
+
+
+# --------------------------------------------------------------- backward pins
+
+def _loss_and_grads(q, k, v, w, causal, scale, mutant):
+    o, _ = oracle.attn_fwd(q, k, v, causal, scale, mutant=mutant)
+    return float((o * w).sum())
+
+
+def pin_finite_differences(mutant=0):
+    """Central finite differences (h = 1e-6, fp64) of L = sum(O * W) equal the
+    analytic dQ, dK, dV with dO = W (relative error <= 1e-6), on tiny MHA and
+    GQA cases with and without the causal mask."""
+    for (H, Hkv, N, d, causal) in [(2, 1, 9, 4, True), (1, 1, 16, 8, False), (2, 2, 7, 3, True)]:
+        q, k, v, w = rand_qkv(1, H, Hkv, N, d, seed=100 + N, dout=True)
+        scale = 1 / math.sqrt(d)
+        dq, dk, dv, _ = oracle.attn_bwd(q, k, v, w, causal, scale, mutant=mutant)
+        h = 1e-6
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            num = np.zeros_like(x)
+            it = np.nditer(x, flags=["multi_index"])
+            for _ in it:
+                idx = it.multi_index
+                old = x[idx]
+                x[idx] = old + h
+                lp = _loss_and_grads(q, k, v, w, causal, scale, mutant)
+                x[idx] = old - h
+                lm = _loss_and_grads(q, k, v, w, causal, scale, mutant)
+                x[idx] = old
+                num[idx] = (lp - lm) / (2 * h)
+            rel = np.linalg.norm(num - g) / max(np.linalg.norm(num), 1e-300)
+            assert rel <= 1e-6, (name, H, Hkv, N, d, causal, rel)
+
+
+def pin_torch_autograd(mutant=0):
+    """Library special case: torch fp64 autograd through matmul/softmax gives the
+    same dQ, dK, dV (GQA through repeat_interleave, whose backward sums the
+    group)."""
+    for (B, H, Hkv, N, d, causal) in [(1, 4, 2, 40, 16, True), (2, 2, 2, 33, 8, False)]:
+        q, k, v, do = rand_qkv(B, H, Hkv, N, d, seed=200 + N, dout=True)
+        scale = 1 / math.sqrt(d)
+        dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, causal, scale, mutant=mutant)
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        o, _ = torch_attention(tq, tk, tv, causal, scale)
+        o.backward(torch.as_tensor(do))
+        for mine, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            assert np.max(np.abs(mine - ref.numpy())) <= 1e-11
+
+
+def pin_backward_invariants(mutant=0):
+    """Invariants of the gradients: rows of P sum to 1, so sum_j dV_j equals the
+    sum of dO over the group's query rows; sum_j dS_ij = 0, so sum_j dK_j = 0;
+    and D_i = <dO_i, O_i> equals rowsum(P o dP) with dP = dO V^T."""
+    for causal in (False, True):
+        B, H, Hkv, N, d = 1, 4, 2, 31, 8
+        q, k, v, do = rand_qkv(B, H, Hkv, N, d, seed=300, dout=True)
+        dq, dk, dv, D = oracle.attn_bwd(q, k, v, do, causal, 0.4, mutant=mutant)
+        G = H // Hkv
+        for g in range(Hkv):
+            want = do[0, g * G:(g + 1) * G].sum(axis=(0, 1))
+            assert np.max(np.abs(dv[0, g].sum(0) - want)) <= 1e-12
+            assert np.max(np.abs(dk[0, g].sum(0))) <= 1e-12
+        _, _, p = oracle.attn_fwd(q, k, v, causal, 0.4, return_p=True, mutant=mutant)
+        vr = np.repeat(v, G, axis=1)
+        dp = do @ vr.transpose(0, 1, 3, 2)
+        assert np.max(np.abs((p * dp).sum(-1) - D)) <= 1e-12
+
+
+def pin_gqa_equals_repeated_mha(mutant=0):
+    """GQA/MQA: query head h uses key/value head h / (H/Hkv); the result equals
+    MHA on K, V repeated per group, and dK, dV equal the group sums of the MHA
+    gradients."""
+    B, H, Hkv, N, d = 1, 6, 2, 18, 8
+    q, k, v, do = rand_qkv(B, H, Hkv, N, d, seed=400, dout=True)
+    G = H // Hkv
+    kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)
+    for causal in (False, True):
+        o, lse = oracle.attn_fwd(q, k, v, causal, 0.3, mutant=mutant)
+        om, lm = oracle.attn_fwd(q, kr, vr, causal, 0.3, mutant=mutant)
+        assert np.max(np.abs(o - om)) <= 1e-14 and np.max(np.abs(lse - lm)) <= 1e-14
+        dq, dk, dv, _ = oracle.attn_bwd(q, k, v, do, causal, 0.3, mutant=mutant)
+        dqm, dkm, dvm, _ = oracle.attn_bwd(q, kr, vr, do, causal, 0.3, mutant=mutant)
+        assert np.max(np.abs(dq - dqm)) <= 1e-13
+        assert np.max(np.abs(dk - dkm.reshape(B, Hkv, G, N, d).sum(2))) <= 1e-12
+        assert np.max(np.abs(dv - dvm.reshape(B, Hkv, G, N, d).sum(2))) <= 1e-12
+
+
+def pin_row_subset(mutant=0):
+    """The row-subset entry point returns exactly the rows of the full result."""
+    q, k, v = rand_qkv(2, 2, 1, 21, 8, seed=500)
+    o, lse = oracle.attn_fwd(q, k, v, True, 0.3, mutant=mutant)
+    rows = np.array([0, 5, 20, 21, 42, 83])
+    os_, ls = oracle.attn_fwd(q, k, v, True, 0.3, rows=rows, mutant=mutant)
+    assert np.array_equal(os_, o.reshape(-1, 8)[rows])
+    assert np.array_equal(ls, lse.reshape(-1)[rows])
+
+
+ALL_PINS = [
+    pin_rows_sum_to_one, pin_torch_library, pin_online_matches_three_pass,
+    pin_identical_keys, pin_one_hot, pin_causal_row0_and_single_key,
+    pin_shift_invariance, pin_golden_closed_form, pin_finite_differences,
+    pin_torch_autograd, pin_backward_invariants, pin_gqa_equals_repeated_mha,
+    pin_row_subset,
+]

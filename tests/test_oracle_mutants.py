@@ -1,0 +1,31 @@
+"""Planted mistakes in the oracle (built as separate copies on the CPU) must
+each fail at least one pin, so the pins really constrain the oracle."""
+import pytest
+
+import oracle
+from _pins import ALL_PINS
+
+# mutant id -> the plausible mistake planted in oracle/attn_oracle.c
+MUTANTS = {
+    1: "scale dropped from the scores",
+    2: "causal mask keeps j < i instead of j <= i",
+    3: "softmax not normalised by l",
+    4: "off-by-one V row in O = P V",
+    5: "LSE missing the row max",
+    6: "GQA head mapping h % Hkv instead of h / (H/Hkv)",
+    7: "dS missing the D term",
+    8: "dS with the wrong sign",
+    9: "dK missing the scale",
+}
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS), ids=lambda m: f"m{m}")
+def test_mutant_is_caught(mutant):
+    oracle.build(mutant)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(mutant=mutant)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches mutant {mutant}: {MUTANTS[mutant]}"
