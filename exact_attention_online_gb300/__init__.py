@@ -1,1 +1,170 @@
-"""GB300-native exact attention (online softmax forward, recompute backward)."""
+"""GB300-native exact attention: online-softmax forward and recomputation
+backward, as hand-written sm_103a kernels behind the C ABI of include/fa.h.
+
+This module is the thin Python binding: each function has the name of the C
+entry point it calls and does argument marshalling only (tensor -> pointer,
+shape -> ints, current CUDA stream).  Every step of the computation runs in
+libfa.so; there is no other code path.  A nonzero fa_status raises FAError.
+
+Layouts (as in include/fa.h): q, o, dout, dq bf16 [B, H, N, d]; k, v, dk, dv
+bf16 [B, Hkv, N, d]; lse fp32 [B, H, N]; all contiguous CUDA tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._native import EXPORTS, LIB_PATH, build, lib
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_ALIGNMENT = -3
+FA_ERR_WORKSPACE = -4
+FA_ERR_CUDA = -5
+FA_ERR_TIMEOUT = -6
+
+__all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_bwd",
+           "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert",
+           "fa_device_status", "fa_device_status_detail", "fa_status_string",
+           "fa_kernel_launches", "fa_watchdog_selftest", "attention", "attention_backward"]
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} ({status})")
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _bf16(t, name):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _f32(t, name):
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA float32 tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dims(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be 4-D [B, H(kv), N, d]")
+    B, H, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError(f"q {tuple(q.shape)} and k {tuple(k.shape)} disagree")
+    return B, H, k.shape[1], N, d
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    B, H, Hkv, N, d = _dims(q, k)
+    _check(lib().fa_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                        _f32(lse, "lse"), B, H, Hkv, N, d, int(bool(causal)), float(scale),
+                        _stream(stream)), "fa_fwd")
+
+
+def fa_bwd_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_size(B, H, Hkv, N, d))
+
+
+def _ws(workspace):
+    import torch
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, scale: float,
+           stream=None) -> None:
+    B, H, Hkv, N, d = _dims(q, k)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                        _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"), _bf16(dk, "dk"),
+                        _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d, int(bool(causal)),
+                        float(scale), _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_preprocess(o, dout, lse, workspace, Hkv: int, stream=None) -> None:
+    B, H, N, d = o.shape
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_preprocess(_bf16(o, "o"), _bf16(dout, "dout"), _f32(lse, "lse"), wp, wb,
+                                   B, H, Hkv, N, d, _stream(stream)), "fa_bwd_preprocess")
+
+
+def fa_bwd_dkdv(q, k, v, dout, dk, dv, workspace, causal: bool, scale: float,
+                stream=None) -> None:
+    B, H, Hkv, N, d = _dims(q, k)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_dkdv(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(dout, "dout"),
+                             _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d,
+                             int(bool(causal)), float(scale), _stream(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_dq_convert(workspace, dq, Hkv: int, scale: float, stream=None) -> None:
+    B, H, N, d = dq.shape
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_dq_convert(wp, wb, _bf16(dq, "dq"), B, H, Hkv, N, d, float(scale),
+                                   _stream(stream)), "fa_bwd_dq_convert")
+
+
+def fa_device_status(stream=None) -> int:
+    return int(lib().fa_device_status(_stream(stream)))
+
+
+def fa_device_status_detail():
+    site, block = ctypes.c_int(0), ctypes.c_int(0)
+    lib().fa_device_status_detail(ctypes.byref(site), ctypes.byref(block))
+    return site.value, block.value
+
+
+def fa_kernel_launches() -> int:
+    return int(lib().fa_kernel_launches())
+
+
+def fa_watchdog_selftest(timeout_ns: int, stream=None) -> None:
+    _check(lib().fa_watchdog_selftest(int(timeout_ns), _stream(stream)), "fa_watchdog_selftest")
+
+
+# Convenience wrappers that allocate outputs with PyTorch (the library itself
+# never allocates).
+def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (o, lse) for bf16 CUDA q [B,H,N,d], k/v [B,Hkv,N,d]."""
+    import torch
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+                       workspace=None, stream=None):
+    """Returns (dq, dk, dv)."""
+    import torch
+    B, H, Hkv, N, d = _dims(q, k)
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(B, H, Hkv, N, d), dtype=torch.uint8,
+                                device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    return dq, dk, dv

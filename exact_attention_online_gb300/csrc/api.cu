@@ -1,0 +1,280 @@
+// C ABI of libfa.so (declared in include/fa.h): argument validation, workspace
+// layout, tensor-map encoding, the device status word and the launches.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// One status word per device context (see DeviceStatus).
+__device__ DeviceStatus g_status_word;
+
+namespace {
+
+std::atomic<long long> g_launches{0};
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+constexpr int kMaxDevices = 64;
+DeviceStatus* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+int g_arch_ok[kMaxDevices] = {};   // 0 unknown, 1 sm_103, -1 other
+DeviceStatus g_last_detail{};      // last non-zero status word read by the host
+
+bool load_encode() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// Checks that the current device is an sm_103 part and fills the per-device
+// caches (status word address, SM count).
+fa_status device_ready(int* dev_out) {
+    const int dev = current_device();
+    if (dev < 0) return FA_ERR_CUDA;
+    *dev_out = dev;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+        g_sm_count[dev] = sms;
+        if (g_arch_ok[dev] == 1) {
+            void* ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) {
+                g_arch_ok[dev] = 0;
+                return FA_ERR_CUDA;
+            }
+            g_status_ptr[dev] = static_cast<DeviceStatus*>(ptr);
+        }
+    }
+    return g_arch_ok[dev] == 1 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+fa_status check_shape(int B, int H, int Hkv, int N, int d) {
+    if (B < 1 || H < 1 || Hkv < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const long long np = padded_rows(N);
+    if ((long long)B * H * np * d >= (1LL << 31) || (long long)B * H * np >= (1LL << 31))
+        return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status check_scale(float scale) {
+    return (std::isfinite(scale) && scale > 0.0f) ? FA_OK : FA_ERR_INVALID_ARG;
+}
+
+fa_status check_ptr(const void* p) {
+    if (!p) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return FA_ERR_ALIGNMENT;
+    return FA_OK;
+}
+
+fa_status first_error(std::initializer_list<fa_status> l) {
+    for (fa_status s : l)
+        if (s != FA_OK) return s;
+    return FA_OK;
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int device_sm_count() {
+    const int dev = current_device();
+    return dev < 0 ? 0 : g_sm_count[dev];
+}
+
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows, int outer,
+                       int box_rows) {
+    if (!load_encode()) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * (cuuint64_t)rows};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t bwd_workspace_bytes(const Shape& s) {
+    const size_t rows = (size_t)s.B * s.H * padded_rows(s.N);
+    return align256(rows * 4) * 2 + align256(rows * (size_t)s.d * 4);
+}
+
+BwdWorkspace bwd_workspace_carve(void* base, const Shape& s) {
+    const size_t rows = (size_t)s.B * s.H * padded_rows(s.N);
+    char* p = static_cast<char*>(base);
+    BwdWorkspace w;
+    w.lse2 = reinterpret_cast<float*>(p);
+    w.delta = reinterpret_cast<float*>(p + align256(rows * 4));
+    w.dq_acc = reinterpret_cast<float*>(p + 2 * align256(rows * 4));
+    return w;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Hkv, int N, int d, int causal, float scale, fa_stream_t stream) {
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(lse)});
+    if (st != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+    return from_cuda(launch_fwd(s, q, k, v, o, lse, g_status_ptr[dev], (cudaStream_t)stream));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
+    if (check_shape(B, H, Hkv, N, d) != FA_OK) return 0;
+    return bwd_workspace_bytes(Shape{B, H, Hkv, N, d, 0, 1.0f});
+}
+
+static fa_status check_workspace(const void* ws, size_t bytes, const Shape& s) {
+    if (!ws) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) % 16 != 0) return FA_ERR_ALIGNMENT;
+    if (bytes < bwd_workspace_bytes(s)) return FA_ERR_WORKSPACE;
+    return FA_OK;
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
+                            size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                            fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, 0, 1.0f};
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_ptr(o), check_ptr(dout),
+                                check_ptr(lse)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    return from_cuda(launch_bwd_preprocess(s, o, dout, lse, bwd_workspace_carve(workspace, s),
+                                           g_status_ptr[dev], (cudaStream_t)stream));
+}
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                      void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                      int N, int d, int causal, float scale, fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(v), check_ptr(dout), check_ptr(dk),
+                                check_ptr(dv)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    return from_cuda(launch_bwd_dkdv(s, q, k, v, dout, dk, dv, bwd_workspace_carve(workspace, s),
+                                     g_status_ptr[dev], (cudaStream_t)stream));
+}
+
+fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void* dq, int B, int H,
+                            int Hkv, int N, int d, float scale, fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, 0, scale};
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(dq)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    return from_cuda(launch_bwd_dq_convert(s, bwd_workspace_carve(const_cast<void*>(workspace), s),
+                                           dq, (cudaStream_t)stream));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal,
+                 float scale, fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(dout),
+                                check_ptr(lse), check_ptr(dq), check_ptr(dk), check_ptr(dv)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    const BwdWorkspace ws = bwd_workspace_carve(workspace, s);
+    cudaStream_t cs = (cudaStream_t)stream;
+    cudaError_t e = launch_bwd_preprocess(s, o, dout, lse, ws, g_status_ptr[dev], cs);
+    if (e == cudaSuccess) e = launch_bwd_dkdv(s, q, k, v, dout, dk, dv, ws, g_status_ptr[dev], cs);
+    if (e == cudaSuccess) e = launch_bwd_dq_convert(s, ws, dq, cs);
+    return from_cuda(e);
+}
+
+fa_status fa_device_status(fa_stream_t stream) {
+    int dev;
+    fa_status st = device_ready(&dev);
+    if (st != FA_OK) return st;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceStatus w{};
+    if (cudaMemcpyFromSymbol(&w, g_status_word, sizeof(w)) != cudaSuccess) return FA_ERR_CUDA;
+    if (w.code != 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_last_detail = w;
+    }
+    const DeviceStatus zero{};
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+    return static_cast<fa_status>(w.code);
+}
+
+void fa_device_status_detail(int* site, int* block) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (site) *site = g_last_detail.site;
+    if (block) *block = g_last_detail.block;
+}
+
+fa_status fa_watchdog_selftest(long long timeout_ns, fa_stream_t stream) {
+    int dev;
+    fa_status st = device_ready(&dev);
+    if (st != FA_OK) return st;
+    if (timeout_ns < 1000) timeout_ns = 1000;
+    if (timeout_ns > 5000000000LL) timeout_ns = 5000000000LL;
+    return from_cuda(launch_watchdog_selftest(timeout_ns, g_status_ptr[dev], (cudaStream_t)stream));
+}
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+long long fa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,570 @@
+// Backward kernels: recomputation-based attention backward (FlashAttention
+// blog, "Backward - Recomputation"; dV = P^T dO from the FlashAttention-2
+// review thread's public comment; the other gradients by the calculus of
+// softmax attention: dP = dO V^T, D = rowsum(dO o O), dS = P o (dP - D),
+// dQ = scale dS K, dK = scale dS^T Q).
+//
+//   preprocess  D_i = <dO_i, O_i>, lse2_i = LSE_i * log2(e) with padded rows
+//               (+inf, so P = 0 there), dQ accumulator zeroed.
+//   dkdv        one CTA per (batch, kv head, block j of 128 keys).  K_j and V_j
+//               stay in shared memory; dK_j and dV_j accumulate in TMEM over
+//               every query head of the GQA group and every query block i that
+//               can see the keys (causal: i*Br + Br - 1 >= 128 j).  Per block i:
+//                 S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T          (SS MMA)
+//                 P^T  = 2^(S^T c - lse2),  dS^T = P^T o (dP^T - D)  (threads)
+//                 dV  += P^T dO_i  (A = P^T in TMEM),  dK += dS^T Q_i  (SS)
+//                 d=128: dQ_i^T = K_j^T dS^T;  d=64: dQ_i = dS K_j    (SS)
+//               and the dQ partial is added into the fp32 accumulator with
+//               red.global (FlashAttention-2 review 2: the query-derivative
+//               update is shared between the workers of one query block).
+//   dq_convert  dQ = bf16(scale * accumulator).
+//
+// Roles in dkdv: warps 0-3 compute (one key row, or for dQ^T one head-dim row,
+// per thread), warp 4 TMA producer, warp 5 MMA issuer.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kBN = 128;   // keys per CTA
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kBR = (D == 128) ? 64 : 128;        // queries per step
+    static constexpr int kKVBytes = kBN * D * 2;              // K_j or V_j
+    static constexpr int kQBytes = kBR * D * 2;               // Q_i or dO_i
+    static constexpr int kDSBytes = kBN * kBR * 2;            // dS^T tile
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kKVBytes;
+    static constexpr int kOffQ = kOffV + kKVBytes;            // 2 stages
+    static constexpr int kOffDO = kOffQ + 2 * kQBytes;        // 2 stages
+    static constexpr int kOffDS = kOffDO + 2 * kQBytes;
+    static constexpr int kOffStat = kOffDS + kDSBytes;        // lse2[2][BR], delta[2][BR]
+    static constexpr int kSmemBytes = kOffStat + 4 * kBR * 4;
+    static constexpr int kSmemAlloc = kSmemBytes + 1024;
+    static constexpr int kStageBytes = 2 * kQBytes + 2 * kBR * 4;
+    // TMEM columns
+    static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + kBR,
+                              kColDQ = 2 * D + 2 * kBR;
+};
+
+struct BwdParams {
+    int H, Hkv, N, Np, G, causal;
+    float scale, scale_log2;
+    const float* lse2;
+    const float* delta;
+    float* dq_acc;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    DeviceStatus* status;
+};
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, int chunk_bytes) {
+    return sdesc_sw128(base + (kk >> 2) * chunk_bytes + (kk & 3) * 32, 16, 1024);
+}
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk, int lbo) {
+    return sdesc_sw128(base + kk * 2048, lbo, 1024);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+    using Cfg = BwdCfg<D>;
+    constexpr int BR = Cfg::kBR;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    __shared__ uint64_t bar_kv, bar_full[2], bar_empty[2], bar_sdp, bar_ds, bar_dq_full,
+        bar_dq_free, bar_done;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+    const WaitCtx wc{p.status, &abort_sh};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // (batch, kv head, key block); key blocks with many visible query blocks first.
+    const int n_kblk = (p.N + kBN - 1) / kBN;
+    const int jblk = blockIdx.x % n_kblk;
+    const int bg = blockIdx.x / n_kblk;           // b * Hkv + g
+    const int b = bg / p.Hkv, g = bg % p.Hkv;
+    const int n_qblk = (p.N + BR - 1) / BR;
+    const int i_start = CAUSAL ? (jblk * kBN) / BR : 0;
+    const int n_i = n_qblk - i_start;
+    const int n_it = p.G * n_i;                   // (head in group) x (query block)
+
+    uint8_t* sK = smem + Cfg::kOffK;
+    uint8_t* sV = smem + Cfg::kOffV;
+    uint8_t* sQ = smem + Cfg::kOffQ;
+    uint8_t* sDO = smem + Cfg::kOffDO;
+    uint8_t* sDS = smem + Cfg::kOffDS;
+    float* sLSE = reinterpret_cast<float*>(smem + Cfg::kOffStat);    // [2][BR]
+    float* sDel = sLSE + 2 * BR;                                     // [2][BR]
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        mbar_init(&bar_kv, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_full[s], 1);
+            mbar_init(&bar_empty[s], 1);
+        }
+        mbar_init(&bar_sdp, 1);
+        mbar_init(&bar_ds, 128);
+        mbar_init(&bar_dq_full, 1);
+        mbar_init(&bar_dq_free, 128);
+        mbar_init(&bar_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0 && n_it > 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_do);
+            mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64, jblk * kBN, bg);
+                tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64, jblk * kBN, bg);
+            }
+            int issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it & 1, u = it >> 1;
+                if (it >= 2 && !fa_wait(&bar_empty[st], (u - 1) & 1, 40, wc)) break;
+                const int hq = g * p.G + it / n_i;        // query head
+                const int i = i_start + it % n_i;
+                const int bh = b * p.H + hq;
+                mbar_arrive_expect_tx(&bar_full[st], Cfg::kStageBytes);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_3d(sQ + st * Cfg::kQBytes + c * (BR * 128), &tm_q, &bar_full[st],
+                                c * 64, i * BR, bh);
+                    tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do, &bar_full[st],
+                                c * 64, i * BR, bh);
+                }
+                const size_t stat = (size_t)bh * p.Np + (size_t)i * BR;
+                bulk_load(sLSE + st * BR, p.lse2 + stat, BR * 4, &bar_full[st]);
+                bulk_load(sDel + st * BR, p.delta + stat, BR * 4, &bar_full[st]);
+                issued = it + 1;
+            }
+            if (abort_sh) {
+                fa_wait(&bar_kv, 0, 41, WaitCtx{p.status, nullptr});
+                for (int it = max(0, issued - 2); it < issued; ++it)
+                    fa_wait(&bar_full[it & 1], (it >> 1) & 1, 41, WaitCtx{p.status, nullptr});
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0 && n_it > 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
+            constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+            constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
+                           sdo = smem_u32(sDO), sds = smem_u32(sDS);
+            bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
+            auto issue_sdp = [&](int st) {
+                const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + Cfg::kColS, kdesc(sk, kk, kBN * 128), kdesc(q_, kk, BR * 128), id_s,
+                           kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + Cfg::kColDP, kdesc(sv, kk, kBN * 128), kdesc(do_, kk, BR * 128),
+                           id_s, kk > 0);
+                mma_commit(&bar_sdp);
+            };
+            if (ok) {
+                tc_fence_after();
+                issue_sdp(0);
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int st = it & 1;
+                if (!fa_wait(&bar_ds, it & 1, 52, wc)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
+                // dV += P^T dO_i, dK += dS^T Q_i   (K dimension = BR queries)
+                for (int kk = 0; kk < BR / 16; ++kk)
+                    mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8, mndesc(do_, kk, BR * 128),
+                           id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BR / 16; ++kk)
+                    mma_ss(tmem + Cfg::kColDK, kdesc(sds, kk, kBN * 128), mndesc(q_, kk, BR * 128),
+                           id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bar_empty[st]);
+                // dQ partial (K dimension = 128 keys)
+                if (it > 0 && !fa_wait(&bar_dq_free, (it - 1) & 1, 53, wc)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t a_ = (D == 128) ? sk : sds;
+                const uint32_t b_ = (D == 128) ? sds : sk;
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ss(tmem + Cfg::kColDQ, mndesc(a_, kk, kBN * 128), mndesc(b_, kk, kBN * 128),
+                           id_dq, kk > 0);
+                mma_commit(&bar_dq_full);
+                if (it + 1 < n_it) {
+                    const int st1 = (it + 1) & 1;
+                    if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_sdp(st1);
+                }
+            }
+            mma_commit(&bar_done);
+            if (!ok) fa_wait(&bar_done, 0, 59, WaitCtx{p.status, nullptr});
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ compute
+        const int quarter = warp;                   // warps 0-3
+        const int rl = quarter * 32 + lane;         // TMEM lane of this thread
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int key = jblk * kBN + rl;            // key row (S^T, dP^T, dK, dV)
+        const float c = p.scale_log2;
+        bool ok = n_it > 0;
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int st = it & 1;
+            const int hq = g * p.G + it / n_i;
+            const int i = i_start + it % n_i;
+            const int bh = b * p.H + hq;
+            if (!fa_wait_warp(&bar_full[st], (it >> 1) & 1, 60, wc) ||
+                !fa_wait_warp(&bar_sdp, it & 1, 61, wc)) { ok = false; break; }
+            tc_fence_after();
+            const float* lse_s = sLSE + st * BR;
+            const float* del_s = sDel + st * BR;
+            const int q0 = i * BR;
+            const bool need_mask = (CAUSAL && q0 < jblk * kBN + kBN - 1) || (jblk * kBN + kBN > p.N);
+            const int key_lim = CAUSAL ? key - q0 : -1;   // query q0+e visible iff e >= key_lim
+            const bool key_valid = key < p.N;
+#pragma unroll
+            for (int ch = 0; ch < BR / 32; ++ch) {
+                uint32_t sr[32], dpr[32];
+                tmem_ld32(lane_addr + Cfg::kColS + ch * 32, sr);
+                tmem_ld32(lane_addr + Cfg::kColDP + ch * 32, dpr);
+                tmem_ld_wait(sr);
+                asm volatile("" : FA_R32(dpr) : : "memory");
+                uint32_t pk[16];
+                uint32_t dsk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float pv[2], dsv[2];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int qe = ch * 32 + e + t;
+                        float pe = ex2(fmaf(__uint_as_float(sr[e + t]), c, -lse_s[qe]));
+                        if (need_mask && (qe < key_lim || !key_valid)) pe = 0.0f;
+                        pv[t] = pe;
+                        dsv[t] = pe * (__uint_as_float(dpr[e + t]) - del_s[qe]);
+                    }
+                    pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                    dsk[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                }
+                // P^T chunk into TMEM (over the S^T columns already read).
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
+                    "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_addr + Cfg::kColS +
+                                                                      ch * 16),
+                    "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]),
+                    "r"(pk[6]), "r"(pk[7]), "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]),
+                    "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+                    : "memory");
+                // dS^T chunk (32 queries = 64 bytes) into the swizzled smem tile.
+                const int qc = ch >> 1;                 // 64-query chunk
+                uint8_t* rowp = sDS + qc * (kBN * 128) + rl * 128;
+#pragma unroll
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const int unit = (ch & 1) * 4 + u4;
+                    uint4 w = make_uint4(dsk[u4 * 4 + 0], dsk[u4 * 4 + 1], dsk[u4 * 4 + 2],
+                                         dsk[u4 * 4 + 3]);
+                    *reinterpret_cast<uint4*>(rowp + ((unit ^ (rl & 7)) * 16)) = w;
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            fence_proxy_async_smem();
+            mbar_arrive(&bar_ds);
+
+            // dQ partial -> fp32 accumulator
+            if (!fa_wait_warp(&bar_dq_full, it & 1, 62, wc)) { ok = false; break; }
+            tc_fence_after();
+            float* acc_head = p.dq_acc + (size_t)bh * p.Np * D;
+            if (D == 128) {
+                // dQ^T: TMEM lane = head-dim index, column = query.
+                const int dd = rl;
+#pragma unroll
+                for (int ch = 0; ch < BR / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + Cfg::kColDQ + ch * 32, r);
+                    tmem_ld_wait(r);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        atomicAdd(acc_head + (size_t)(q0 + ch * 32 + e) * D + dd,
+                                  __uint_as_float(r[e]));
+                }
+            } else {
+                // dQ: TMEM lane = query, column = head-dim index.
+                float* rowp = acc_head + (size_t)(q0 + rl) * D;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + Cfg::kColDQ + ch * 32, r);
+                    tmem_ld_wait(r);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        atomicAdd(reinterpret_cast<float4*>(rowp + ch * 32 + e),
+                                  make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                              __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bar_dq_free);
+        }
+        // ---------------------------------------------------- dK, dV epilogue
+        if (ok && fa_wait_warp(&bar_done, 0, 63, wc)) {
+            tc_fence_after();
+            const bool valid = key < p.N;
+            const size_t row = ((size_t)bg * p.N + (valid ? key : 0)) * D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which ? Cfg::kColDV : Cfg::kColDK;
+                const float mul = which ? 1.0f : p.scale;
+                __nv_bfloat16* dst = (which ? p.dv : p.dk) + row;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col + c0, r);
+                    tmem_ld_wait(r);
+                    if (valid) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 1]) * mul);
+                            w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 3]) * mul);
+                            w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 5]) * mul);
+                            w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 7]) * mul);
+                            d4[q4] = w;
+                        }
+                    }
+                }
+            }
+        } else if (n_it == 0) {
+            // No query block sees these keys (cannot happen with N_q == N_k);
+            // their gradients are zero.
+            if (key < p.N)
+                for (int c0 = 0; c0 < D; ++c0) {
+                    p.dk[((size_t)bg * p.N + key) * D + c0] = __float2bfloat16(0.0f);
+                    p.dv[((size_t)bg * p.N + key) * D + c0] = __float2bfloat16(0.0f);
+                }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// D_i = <dO_i, O_i>, lse2 = LSE * log2(e) (+inf on padded rows), accumulator = 0.
+// One warp per row, grid-stride over the B*H*Np rows.
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                  const float* __restrict__ lse, float* __restrict__ lse2,
+                  float* __restrict__ delta, float* __restrict__ dq_acc, int N, int Np,
+                  long long rows) {
+    constexpr int kPer = D / 32;   // bf16 per lane
+    const int lane = threadIdx.x & 31;
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r = wid; r < rows; r += nw) {
+        const long long bh = r / Np;
+        const int i = (int)(r % Np);
+        float acc = 0.0f;
+        if (i < N) {
+            const long long src = (bh * N + i) * D + lane * kPer;
+            if (kPer == 4) {
+                const uint2 ov = *reinterpret_cast<const uint2*>(o + src);
+                const uint2 dv = *reinterpret_cast<const uint2*>(dout + src);
+                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+                const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const float2 a = __bfloat1622float2(o2[t]), bb = __bfloat1622float2(d2[t]);
+                    acc = fmaf(a.x, bb.x, acc);
+                    acc = fmaf(a.y, bb.y, acc);
+                }
+            } else {
+                const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162*>(o + src);
+                const __nv_bfloat162 dv = *reinterpret_cast<const __nv_bfloat162*>(dout + src);
+                const float2 a = __bfloat1622float2(ov), bb = __bfloat1622float2(dv);
+                acc = fmaf(a.x, bb.x, acc);
+                acc = fmaf(a.y, bb.y, acc);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            delta[r] = acc;
+            lse2[r] = (i < N) ? lse[bh * N + i] * 1.4426950408889634f : CUDART_INF_F;
+        }
+        float4* z = reinterpret_cast<float4*>(dq_acc + r * D);
+        for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// dQ = bf16(scale * accumulator), 8 elements per thread.
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, int N,
+                         int Np, float scale, long long n_vec) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n_vec; t += stride) {
+        const long long e = t * 8;                  // element index in dq
+        const long long row = e / D;                // bh * N + i
+        const int col = (int)(e % D);
+        const long long bh = row / N;
+        const int i = (int)(row % N);
+        const float4* src = reinterpret_cast<const float4*>(acc + (bh * Np + i) * D + col);
+        const float4 a = src[0], bb = src[1];
+        uint4 w;
+        w.x = pack_bf16x2(a.x * scale, a.y * scale);
+        w.y = pack_bf16x2(a.z * scale, a.w * scale);
+        w.z = pack_bf16x2(bb.x * scale, bb.y * scale);
+        w.w = pack_bf16x2(bb.z * scale, bb.w * scale);
+        *reinterpret_cast<uint4*>(dq + e) = w;
+    }
+}
+
+// Bounded-wait self-test: one CTA waits on an mbarrier nobody completes.
+__global__ void fa_watchdog_kernel(DeviceStatus* status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_sh;
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    fa_wait(&bar, 0, 99, WaitCtx{status, &abort_sh}, limit_ns);
+    __syncthreads();
+}
+
+int grid_for(long long work_items, int per_block) {
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+    long long blocks = (work_items + per_block - 1) / per_block;
+    const long long cap = (long long)sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return (int)blocks;
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdParams& p, int grid,
+                          cudaStream_t stream) {
+    auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             BwdCfg<D>::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    kern<<<grid, kThreads, BwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, const void* dout,
+                                  const float* lse, const BwdWorkspace& ws, DeviceStatus* status,
+                                  cudaStream_t stream) {
+    (void)status;
+    const int Np = padded_rows(s.N);
+    const long long rows = (long long)s.B * s.H * Np;
+    const int grid = grid_for(rows, 8);
+    count_launch();
+    auto* o_ = static_cast<const __nv_bfloat16*>(o);
+    auto* d_ = static_cast<const __nv_bfloat16*>(dout);
+    if (s.d == 128)
+        fa_bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(o_, d_, lse, ws.lse2, ws.delta,
+                                                         ws.dq_acc, s.N, Np, rows);
+    else
+        fa_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(o_, d_, lse, ws.lse2, ws.delta,
+                                                        ws.dq_acc, s.N, Np, rows);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const void* v,
+                            const void* dout, void* dk, void* dv, const BwdWorkspace& ws,
+                            DeviceStatus* status, cudaStream_t stream) {
+    const int br = (s.d == 128) ? BwdCfg<128>::kBR : BwdCfg<64>::kBR;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_tmap_bf16_3d(&tq, q, s.d, s.N, s.B * s.H, br) ||
+        !make_tmap_bf16_3d(&tdo, dout, s.d, s.N, s.B * s.H, br) ||
+        !make_tmap_bf16_3d(&tk, k, s.d, s.N, s.B * s.Hkv, kBN) ||
+        !make_tmap_bf16_3d(&tv, v, s.d, s.N, s.B * s.Hkv, kBN))
+        return cudaErrorInvalidValue;
+    BwdParams p;
+    p.H = s.H;
+    p.Hkv = s.Hkv;
+    p.N = s.N;
+    p.Np = padded_rows(s.N);
+    p.G = s.H / s.Hkv;
+    p.causal = s.causal;
+    p.scale = s.scale;
+    p.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
+    p.lse2 = ws.lse2;
+    p.delta = ws.delta;
+    p.dq_acc = ws.dq_acc;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.status = status;
+    const int n_kblk = (s.N + kBN - 1) / kBN;
+    const int grid = n_kblk * s.B * s.Hkv;
+    count_launch();
+    if (s.d == 128)
+        return s.causal ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, p, grid, stream)
+                        : launch_dkdv_t<128, false>(tq, tk, tv, tdo, p, grid, stream);
+    return s.causal ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, p, grid, stream)
+                    : launch_dkdv_t<64, false>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+cudaError_t launch_bwd_dq_convert(const Shape& s, const BwdWorkspace& ws, void* dq,
+                                  cudaStream_t stream) {
+    const long long n_vec = (long long)s.B * s.H * s.N * s.d / 8;
+    const int grid = grid_for(n_vec, 256);
+    count_launch();
+    auto* dq_ = static_cast<__nv_bfloat16*>(dq);
+    if (s.d == 128)
+        fa_bwd_dq_convert_kernel<128><<<grid, 256, 0, stream>>>(ws.dq_acc, dq_, s.N,
+                                                                padded_rows(s.N), s.scale, n_vec);
+    else
+        fa_bwd_dq_convert_kernel<64><<<grid, 256, 0, stream>>>(ws.dq_acc, dq_, s.N,
+                                                               padded_rows(s.N), s.scale, n_vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_watchdog_selftest(long long timeout_ns, DeviceStatus* status,
+                                     cudaStream_t stream) {
+    count_launch();
+    fa_watchdog_kernel<<<1, 32, 0, stream>>>(status, (unsigned long long)timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,59 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+// Plain C++ (no CUDA device code), so every translation unit can include it.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// Shapes of one call, validated by the C ABI before any launcher runs.
+struct Shape {
+    int B, H, Hkv, N, d;
+    int causal;
+    float scale;
+};
+
+// Rows of every per-head buffer in the backward workspace are padded to this.
+constexpr int kRowPad = 128;
+inline int padded_rows(int N) { return (N + kRowPad - 1) / kRowPad * kRowPad; }
+
+// Backward workspace: [lse2 fp32 B*H*Np][D fp32 B*H*Np][dQacc fp32 B*H*Np*d],
+// each region 256-byte aligned.
+struct BwdWorkspace {
+    float* lse2;   // LSE * log2(e), padded rows = +inf
+    float* delta;  // D = rowsum(dO * O), padded rows = 0
+    float* dq_acc; // fp32 accumulator of dQ / scale
+};
+size_t bwd_workspace_bytes(const Shape& s);
+BwdWorkspace bwd_workspace_carve(void* base, const Shape& s);
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void* v, void* o,
+                       float* lse, DeviceStatus* status, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, const void* dout,
+                                  const float* lse, const BwdWorkspace& ws,
+                                  DeviceStatus* status, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const void* v,
+                            const void* dout, void* dk, void* dv, const BwdWorkspace& ws,
+                            DeviceStatus* status, cudaStream_t stream);
+cudaError_t launch_bwd_dq_convert(const Shape& s, const BwdWorkspace& ws, void* dq,
+                                  cudaStream_t stream);
+cudaError_t launch_watchdog_selftest(long long timeout_ns, DeviceStatus* status,
+                                     cudaStream_t stream);
+
+// Tensor-map encoding through the driver entry point (no libcuda link).
+// Builds a 3-D map over a bf16 tensor [outer][rows][d] with a {64, box_rows, 1}
+// box and 128-byte swizzle.  Returns false on failure.
+bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows, int outer,
+                       int box_rows);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// Counts one kernel launch for fa_kernel_launches().
+void count_launch();
+
+}  // namespace fa

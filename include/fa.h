@@ -1,0 +1,169 @@
+/*
+ * fa.h: C ABI of the GB300 (sm_103a) exact-attention library, libfa.so.
+ *
+ * The operation (pages of exact_attention_online):
+ *   Forward, for every batch b and query head h, with key/value head
+ *   g = h / (H / Hkv):
+ *       S = scale * Q K^T   (key j > query i masked out when causal)
+ *       P = softmax(S) row by row,   O = P V,   LSE_i = ln sum_j exp(S_ij)
+ *   This is exact standard attention (FlashAttention blog, "From Online
+ *   Softmax to FlashAttention"), computed tile by tile with the online-softmax
+ *   recurrence (same page, "Online Softmax" and "FlashAttention") so the N x N
+ *   score matrix never reaches device memory.  The division by the softmax
+ *   denominator is deferred to the end, and LSE is saved instead of (m, l)
+ *   (FlashAttention-2 review thread, author answer on non-matmul FLOPs and
+ *   review 2).  Fully masked key blocks are skipped and the mask is applied to
+ *   the diagonal block only (FlashAttention-2 review thread, answers on
+ *   Figure 2 and on non-matmul FLOPs).
+ *
+ *   Backward, by recomputation (FlashAttention blog, "Backward -
+ *   Recomputation"): from Q, K, V, O, dO and LSE it recomputes
+ *   P = exp(S - LSE) and returns
+ *       dV = P^T dO   (FlashAttention-2 review thread, public comment)
+ *       dP = dO V^T,  D_i = sum_c dO_ic O_ic,  dS = P o (dP - D)
+ *       dQ = scale * dS K,  dK = scale * dS^T Q
+ *   with dK and dV summed over the query heads that share a key/value head
+ *   (MQA/GQA).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA tensors) on the
+ *     current device, except where stated.  The caller owns all memory; the
+ *     library never allocates or frees device memory.
+ *   - Layout: q, o, dout, dq are bf16 [B][H][N][d] contiguous; k, v, dk, dv
+ *     are bf16 [B][Hkv][N][d] contiguous; lse is fp32 [B][H][N] (natural
+ *     log).  Every tensor pointer must be 16-byte aligned.
+ *   - Supported: d in {64, 128}; H % Hkv == 0; B, H, Hkv, N >= 1;
+ *     B*H*N*d < 2^31; scale finite and > 0.  N need not be a multiple of the
+ *     tile size.  Queries and keys have the same length N; the causal mask
+ *     keeps key j for query i iff j <= i.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronize, except fa_device_status().
+ *   - Arguments are validated before anything is launched.  A rejected call
+ *     returns a negative fa_status and launches nothing.  A launch failure
+ *     returns FA_ERR_CUDA.  Faults detected inside a kernel (a bounded wait
+ *     that ran out) are recorded in a device status word that
+ *     fa_device_status() reads.
+ *   - Outputs may not alias inputs.  The library is thread-safe.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = -1, /* null pointer, bad size, non-finite scale, H % Hkv != 0 */
+    FA_ERR_UNSUPPORTED = -2, /* head dim not 64/128, sizes past the 32-bit index range,
+                                device is not sm_103 */
+    FA_ERR_ALIGNMENT = -3,   /* a tensor pointer is not 16-byte aligned */
+    FA_ERR_WORKSPACE = -4,   /* workspace null or smaller than fa_bwd_workspace_size() */
+    FA_ERR_CUDA = -5,        /* a CUDA runtime / driver call failed */
+    FA_ERR_TIMEOUT = -6      /* a kernel's bounded wait ran out (device-side report) */
+} fa_status;
+
+/*
+ * Forward.  Writes o (bf16, [B][H][N][d]) and lse (fp32, [B][H][N]).
+ * One launch of the forward kernel.
+ */
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Hkv, int N, int d, int causal, float scale,
+                 fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd() needs: D and a padded copy of LSE
+ * (fp32 [B][H][Np]) and the fp32 dQ accumulator ([B][H][Np][d]), where Np is
+ * N rounded up to 128.  Returns 0 for arguments fa_bwd() would reject.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
+
+/*
+ * Backward.  Reads q, k, v, o, dout (bf16) and lse (fp32, as written by
+ * fa_fwd), writes dq (bf16 [B][H][N][d]), dk, dv (bf16 [B][Hkv][N][d]).
+ * `workspace` (device, >= fa_bwd_workspace_size bytes, 16-byte aligned) is
+ * scratch owned by the caller; its contents on entry do not matter.
+ * Equivalent to fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq_convert in that
+ * order on `stream` (three kernel launches).
+ */
+FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                 void* workspace, size_t workspace_bytes,
+                 int B, int H, int Hkv, int N, int d, int causal, float scale,
+                 fa_stream_t stream);
+
+/*
+ * Backward, stage 1 of 3: D_i = sum_c dO_ic O_ic (fp32), LSE copied into the
+ * workspace in base-2 units with padding rows, and the fp32 dQ accumulator
+ * zeroed.  One launch.
+ */
+FA_API fa_status fa_bwd_preprocess(const void* o, const void* dout, const float* lse,
+                            void* workspace, size_t workspace_bytes,
+                            int B, int H, int Hkv, int N, int d, fa_stream_t stream);
+
+/*
+ * Backward, stage 2 of 3: the main recomputation kernel.  One CTA per
+ * (batch, key/value head, block of 128 keys) keeps K_j and V_j on chip, loops
+ * over every query head of its group and every query block that can see the
+ * keys, writes dK_j and dV_j, and adds its dQ partials into the fp32
+ * accumulator in the workspace.  One launch.
+ */
+FA_API fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout,
+                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                      int B, int H, int Hkv, int N, int d, int causal, float scale,
+                      fa_stream_t stream);
+
+/* Backward, stage 3 of 3: dq = bf16(scale * accumulator).  One launch. */
+FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void* dq,
+                            int B, int H, int Hkv, int N, int d, float scale,
+                            fa_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device status word of the
+ * current device: FA_OK, or the first error a kernel recorded (for example
+ * FA_ERR_TIMEOUT when a bounded wait ran out).  Returns FA_ERR_CUDA if the
+ * synchronization itself fails.
+ */
+FA_API fa_status fa_device_status(fa_stream_t stream);
+
+/*
+ * Where the last recorded device error came from: writes the wait-site id and
+ * the linear block index (either pointer may be NULL).  Host-side read of the
+ * status word; call after fa_device_status() reported an error.
+ */
+FA_API void fa_device_status_detail(int* site, int* block);
+
+/* Static English name of a status code ("FA_OK", ...).  Never NULL. */
+FA_API const char* fa_status_string(fa_status s);
+
+/*
+ * Number of kernels this library has launched in this process (all devices),
+ * a host-side counter for diagnostics.
+ */
+FA_API long long fa_kernel_launches(void);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier that nothing completes, with a limit of `timeout_ns` nanoseconds
+ * (clamped to [1e3, 5e9]).  The kernel gives up, records FA_ERR_TIMEOUT in
+ * the status word and returns; the context stays usable.  Returns FA_OK if
+ * the launch succeeded (read the outcome with fa_device_status()).
+ */
+FA_API fa_status fa_watchdog_selftest(long long timeout_ns, fa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

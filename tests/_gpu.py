@@ -1,0 +1,101 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and
+the fp64 oracle on the same seeded bf16 inputs, on whole heads or sampled rows."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import exact_attention_online_gb300 as fa
+import oracle
+
+# Tolerances for bf16 inputs with fp32 accumulation (same numbers as the
+# acceptance bar for the method's GPU results).
+O_MAX_ABS = 1e-2
+LSE_MAX_ABS = 1e-3
+GRAD_REL_FRO = 2e-2
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def run_fwd(q, k, v, causal, scale):
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    o, lse = fa.attention(qd, kd, vd, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    return o.cpu(), lse.cpu(), (qd, kd, vd, o, lse)
+
+
+def run_bwd(dev_tensors, dout, causal, scale):
+    qd, kd, vd, o, lse = dev_tensors
+    dod = dout.to(qd.device)
+    dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    return dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def rel_fro(a, ref):
+    a = f64(a) if isinstance(a, torch.Tensor) else a
+    return float(np.linalg.norm(a - ref) / max(np.linalg.norm(ref), 1e-30))
+
+
+def check_fwd_heads(q, k, v, o, lse, causal, scale, heads, rows=None):
+    """Compares O and LSE of the given (b, h) heads with the oracle; rows (per
+    head, optional) restricts to sampled query rows."""
+    H, Hkv = q.shape[1], k.shape[1]
+    G = H // Hkv
+    worst_o = worst_l = 0.0
+    for (b, h) in heads:
+        g = h // G
+        qh = f64(q[b:b + 1, h:h + 1])
+        kh, vh = f64(k[b:b + 1, g:g + 1]), f64(v[b:b + 1, g:g + 1])
+        if rows is None:
+            ro, rl = oracle.attn_fwd(qh, kh, vh, causal, scale)
+            go, gl = f64(o[b, h]), lse[b, h].double().numpy()
+            eo = np.abs(go - ro[0, 0]).max()
+            el = np.abs(gl - rl[0, 0]).max()
+        else:
+            r = np.asarray(rows, dtype=np.int64)
+            ro, rl = oracle.attn_fwd(qh, kh, vh, causal, scale, rows=r)
+            go = f64(o[b, h])[r]
+            gl = lse[b, h].double().numpy()[r]
+            eo = np.abs(go - ro).max()
+            el = np.abs(gl - rl).max()
+        worst_o, worst_l = max(worst_o, eo), max(worst_l, el)
+    assert worst_o <= O_MAX_ABS, f"O max abs err {worst_o:.3e}"
+    assert worst_l <= LSE_MAX_ABS, f"LSE max abs err {worst_l:.3e}"
+    return worst_o, worst_l
+
+
+def check_bwd_groups(q, k, v, dout, dq, dk, dv, causal, scale, groups):
+    """Compares dQ (every head of each group) and dK, dV of the given (b, g)
+    key/value heads with the oracle, relative Frobenius error per tensor."""
+    H, Hkv = q.shape[1], k.shape[1]
+    G = H // Hkv
+    worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+    for (b, g) in groups:
+        hs = slice(g * G, (g + 1) * G)
+        rq, rk, rv, _ = oracle.attn_bwd(f64(q[b:b + 1, hs]), f64(k[b:b + 1, g:g + 1]),
+                                        f64(v[b:b + 1, g:g + 1]), f64(dout[b:b + 1, hs]),
+                                        causal, scale)
+        worst["dq"] = max(worst["dq"], rel_fro(dq[b:b + 1, hs], rq))
+        worst["dk"] = max(worst["dk"], rel_fro(dk[b:b + 1, g:g + 1], rk))
+        worst["dv"] = max(worst["dv"], rel_fro(dv[b:b + 1, g:g + 1], rv))
+    for name, e in worst.items():
+        assert e <= GRAD_REL_FRO, f"{name} relative Frobenius error {e:.3e}"
+    return worst
+
+
+def sample_rows(N: int, seed: int, n_random: int = 192):
+    """Query rows to check at large N: the first and last tiles, the rows on
+    both sides of every 1024-row boundary, and random rows."""
+    rng = np.random.default_rng(seed)
+    r = set(range(0, min(N, 130)))
+    r |= set(range(max(0, N - 130), N))
+    for b in range(1024, N, 1024):
+        r |= {b - 1, b}
+    r |= set(rng.integers(0, N, size=n_random).tolist())
+    return sorted(r)

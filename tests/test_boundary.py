@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/fa.h declares, and rejects bad arguments with the documented status
+before touching the device (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_online_gb300 as fa
+from exact_attention_online_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    fa.build()
+    return fa.lib()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "fa.h")) as f:
+        text = f.read()
+    return re.findall(r"^FA_API\s+[\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_exports():
+    assert sorted(declared_symbols()) == sorted(_native.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    names = {0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED",
+             -3: "FA_ERR_ALIGNMENT", -4: "FA_ERR_WORKSPACE", -5: "FA_ERR_CUDA",
+             -6: "FA_ERR_TIMEOUT"}
+    for code, name in names.items():
+        assert fa.fa_status_string(code) == name
+    assert fa.fa_status_string(-99) == "FA_ERR_UNKNOWN"
+
+
+A = 1 << 20          # a 16-byte aligned fake address (never dereferenced)
+MIS = A + 8          # misaligned
+
+
+def fwd(L, q=A, k=A, v=A, o=A, lse=A, B=1, H=2, Hkv=1, N=128, d=64, causal=1, scale=0.125):
+    return L.fa_fwd(q, k, v, o, lse, B, H, Hkv, N, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=3, Hkv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(N=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Hkv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(v=MIS), fa.FA_ERR_ALIGNMENT),
+    (dict(o=MIS), fa.FA_ERR_ALIGNMENT),
+    (dict(B=4096, H=64, Hkv=64, N=4096, d=128), fa.FA_ERR_UNSUPPORTED),
+])
+def test_fwd_rejects_before_launch(L, kw, code):
+    before = fa.fa_kernel_launches()
+    assert fwd(L, **kw) == code
+    assert fa.fa_kernel_launches() == before
+
+
+def test_workspace_size(L):
+    # D and lse2: fp32 [B][H][Np] each, accumulator fp32 [B][H][Np][d]; Np = N rounded to 128.
+    B, H, Hkv, N, d = 2, 4, 2, 200, 64
+    Np = 256
+    rows = B * H * Np
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(B, H, Hkv, N, d) == 2 * r256(rows * 4) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_size(B, H, 3, N, d) == 0
+    assert fa.fa_bwd_workspace_size(B, H, Hkv, N, 80) == 0
+
+
+def bwd(L, ws=A, ws_bytes=None, dq=A, B=1, H=2, Hkv=1, N=128, d=64, scale=0.125):
+    if ws_bytes is None:
+        ws_bytes = L.fa_bwd_workspace_size(B, H, Hkv, N, d)
+    return L.fa_bwd(A, A, A, A, A, A, dq, A, A, ws, ws_bytes, B, H, Hkv, N, d, 1, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), fa.FA_ERR_WORKSPACE),
+    (dict(ws_bytes=16), fa.FA_ERR_WORKSPACE),
+    (dict(ws=MIS), fa.FA_ERR_ALIGNMENT),
+    (dict(dq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=MIS), fa.FA_ERR_ALIGNMENT),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=2, Hkv=4), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+])
+def test_bwd_rejects_before_launch(L, kw, code):
+    before = fa.fa_kernel_launches()
+    assert bwd(L, **kw) == code
+    assert fa.fa_kernel_launches() == before
+
+
+def test_stage_entry_points_validate(L):
+    ws = L.fa_bwd_workspace_size(1, 2, 1, 128, 64)
+    assert L.fa_bwd_preprocess(A, A, A, A, 8, 1, 2, 1, 128, 64, None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_bwd_preprocess(0, A, A, A, ws, 1, 2, 1, 128, 64, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_bwd_dkdv(A, A, A, A, A, MIS, A, ws, 1, 2, 1, 128, 64, 0, 0.1, None) == \
+        fa.FA_ERR_ALIGNMENT
+    assert L.fa_bwd_dq_convert(A, ws, A, 1, 2, 1, 128, 64, float("nan"), None) == \
+        fa.FA_ERR_INVALID_ARG
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, q, torch.zeros(1, 1, 8), False, 0.125, stream=0)

@@ -1,0 +1,95 @@
+"""Backward parity: fa_bwd (preprocess, dK/dV kernel with dQ reduction, dQ
+conversion) on the GPU's own O and LSE, against the fp64 oracle's analytic
+gradients on the same seeded bf16 inputs.  dQ, dK, dV relative Frobenius error
+<= 2e-2 each."""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_online_gb300 as fa
+from _gpu import GRAD_REL_FRO, check_bwd_groups, f64, run_bwd, run_fwd
+from exact_attention_online_gb300.inputs import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name, B, H, Hkv, N, d, causal, seed, **kw):
+    return Workload(name=name, B=B, H=H, Hkv=Hkv, N=N, d=d, causal=causal, seed=seed, **kw)
+
+
+SMALL = [
+    WORKLOADS["tiny"],
+    small("tiny_causal", 1, 1, 1, 128, 64, True, 41),
+    small("n1", 1, 2, 1, 1, 64, True, 42),
+    small("n33_d128", 1, 2, 2, 33, 128, True, 43),
+    small("ragged200_d64", 1, 2, 1, 200, 64, True, 44),
+    small("ragged333_d128", 1, 2, 2, 333, 128, True, 45),
+    small("ragged257_full_d128", 2, 4, 2, 257, 128, False, 46),
+    small("full_d64", 1, 2, 2, 384, 64, False, 47),
+    small("tiles512_d128", 1, 2, 1, 512, 128, True, 48),
+    small("mqa_d64", 1, 4, 1, 300, 64, True, 49),
+    small("gqa_kchan", 1, 4, 2, 384, 128, True, 50, k_outlier_channels=2),
+    small("dout_small", 1, 2, 2, 256, 128, True, 51, dout_std=0.1),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_bwd_small_full(w):
+    q, k, v, do = make_inputs(w)
+    _, _, dev = run_fwd(q, k, v, w.causal, w.scale)
+    dq, dk, dv = run_bwd(dev, do, w.causal, w.scale)
+    groups = [(b, g) for b in range(w.B) for g in range(w.Hkv)]
+    check_bwd_groups(q, k, v, do, dq, dk, dv, w.causal, w.scale, groups)
+
+
+def test_bwd_dv_column_sum_invariant():
+    """Rows of P sum to 1, so sum_j dV_j equals the sum of dO over the group's
+    query rows (checked on the GPU result alone, any size)."""
+    w = small("inv", 2, 4, 2, 700, 64, True, 52)
+    q, k, v, do = make_inputs(w)
+    _, _, dev = run_fwd(q, k, v, w.causal, w.scale)
+    _, _, dv = run_bwd(dev, do, w.causal, w.scale)
+    G = w.H // w.Hkv
+    for b in range(w.B):
+        for g in range(w.Hkv):
+            lhs = f64(dv[b, g]).sum(0)
+            rhs = f64(do[b, g * G:(g + 1) * G]).sum(axis=(0, 1))
+            assert np.abs(lhs - rhs).max() <= 2e-2 * np.abs(rhs).max() + 0.5
+
+
+def test_bwd_stages_equal_fused_call():
+    """fa_bwd equals fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq_convert."""
+    w = small("stages", 1, 4, 2, 300, 128, True, 53)
+    q, k, v, do = make_inputs(w)
+    _, _, dev = run_fwd(q, k, v, w.causal, w.scale)
+    qd, kd, vd, o, lse = dev
+    dod = do.cuda()
+    dq1, dk1, dv1 = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=True, scale=w.scale)
+    ws = torch.empty(fa.fa_bwd_workspace_size(1, 4, 2, 300, 128), dtype=torch.uint8,
+                     device="cuda")
+    dq2, dk2, dv2 = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    fa.fa_bwd_preprocess(o, dod, lse, ws, w.Hkv)
+    fa.fa_bwd_dkdv(qd, kd, vd, dod, dk2, dv2, ws, True, w.scale)
+    fa.fa_bwd_dq_convert(ws, dq2, w.Hkv, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert (dq1.float() - dq2.float()).abs().max() <= 1e-2 * dq1.float().abs().max()
+
+
+FULL = ["mha_d64", "mha_d64_full", "gpt_long", "gqa"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_bwd_full_size(name):
+    """Full workload sizes, same launches as the benchmark; the oracle checks
+    one (first) and one (last) key/value group in full (every query head of the
+    group, every row)."""
+    w = WORKLOADS[name]
+    q, k, v, do = make_inputs(w)
+    _, _, dev = run_fwd(q, k, v, w.causal, w.scale)
+    dq, dk, dv = run_bwd(dev, do, w.causal, w.scale)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    groups = [(0, 0)] if w.N >= 8192 else [(0, 0), (w.B - 1, w.Hkv - 1)]
+    check_bwd_groups(q, k, v, do, dq, dk, dv, w.causal, w.scale, groups)
