@@ -1,0 +1,407 @@
+"""Benchmark: attention forward + backward TFLOP/s on GB300 through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+fa_fwd (online-softmax forward), fa_bwd_preprocess (D, lse2, zeroed dQ
+accumulator), fa_bwd_dkdv (recompute, dK/dV, dQ reduction) and
+fa_bwd_dq_convert, all on the current CUDA stream.  FLOPs per step use the
+headline count: forward 4*B*H*N^2*d (halved under the causal mask) and
+forward+backward 2.5x that.
+
+Default workload: B=8, H=16, N=2048, d=64, causal, bf16 (the multi-head
+workload of the pages' setting).  Under torchrun every rank runs the same
+per-GPU workload on its own GPU (independent batches, no data-path
+collective): weak scaling, value = all ranks' FLOPs / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this path) on a bounded sample of the same workload on the host cores; rank 0
+alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd / fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense BF16 peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+
+# DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read.sum
+# + dram__bytes_write.sum, per launch, scaled to the benchmark workload as
+# described in profiles/), keyed by workload, together with the sha256 of the
+# kernel source it was taken on.  A source change makes the figure stale and
+# it is then reported as null.
+NCU_TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 3 s of timed work)")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mha_d64")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def kernel_source_hash(name: str) -> str:
+    p = os.path.join(ROOT, "exact_attention_online_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ CPU side
+def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int = 16, min_heads: int = 1):
+    """Times the fp64 oracle (forward + analytic backward) on whole heads of the
+    workload until about `budget_s` seconds of CPU work; returns its TFLOP/s on
+    the same FLOP count as the GPU metric."""
+    import oracle
+    from exact_attention_online_gb300.inputs import make_inputs
+    from exact_attention_online_gb300.measure import attention_flops
+
+    one = w.with_(B=1, H=w.H // w.Hkv, Hkv=1)          # one kv group of batch 0
+    q, k, v, do = make_inputs(w.with_(B=1))
+    G = w.H // w.Hkv
+    f64 = lambda t: t.double().numpy()
+    done, t_total = 0, 0.0
+    while done < max_heads and (t_total < budget_s or done < min_heads):
+        g = (done // G) % w.Hkv
+        hs = slice(g * G, (g + 1) * G)
+        qs, ks, vs, ds = f64(q[:, hs]), f64(k[:, g:g + 1]), f64(v[:, g:g + 1]), f64(do[:, hs])
+        t0 = time.perf_counter()
+        oracle.attn_fwd(qs, ks, vs, w.causal, w.scale)
+        oracle.attn_bwd(qs, ks, vs, ds, w.causal, w.scale)
+        t_total += time.perf_counter() - t0
+        done += G
+    flops = attention_flops(one, "fwd_bwd") * (done / G)
+    return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done} query heads (B=1, N={w.N}, d={w.d}, causal={w.causal}) of the "
+                      f"workload, fp64 forward + analytic backward, {t_total:.1f} s"}
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from exact_attention_online_gb300.measure import attention_flops
+    if args.steps is None:
+        args.steps = 5
+    t_steps = []
+    for s in range(args.warmup + args.steps):
+        res = cpu_oracle_sample(w, budget_s=0.0, max_heads=w.H // w.Hkv)
+        if s >= args.warmup:
+            t_steps.append(res)
+    flops_step = attention_flops(w.with_(B=1, H=w.H // w.Hkv, Hkv=1), "fwd_bwd")
+    tflops = statistics.median(r["value"] for r in t_steps)
+    ms = flops_step / (tflops * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} H={w.H} Hkv={w.Hkv} N={w.N} d={w.d} "
+                               f"causal={w.causal} fwd+bwd; each step = one kv-group "
+                               f"sample (B=1, {w.H // w.Hkv} query heads)"},
+        "cpu_baseline": {"value": tflops, "unit": UNIT, "cores": t_steps[0]["cores"],
+                         "kind": "oracle", "sample": t_steps[0]["sample"]},
+        "e2e": {"value": tflops, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU side
+def run_native(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_online_gb300 as fa
+    from exact_attention_online_gb300.inputs import make_inputs
+    from exact_attention_online_gb300.measure import attention_flops
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+    peaks = load_peaks()
+
+    # Each rank draws its own batch (weak scaling: independent shards).
+    q, k, v, do = make_inputs(w.with_(seed=w.seed + 7919 * rank))
+    B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    wsb = fa.fa_bwd_workspace_size(B, H, Hkv, N, d)
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    fwd_ev, dkdv_ev = [], []
+
+    def step(timed: bool):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
+        if timed:
+            e[0].record(stream)
+        fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+        if timed:
+            e[1].record(stream)
+        fa.fa_bwd_preprocess(o, dod, lse, work, Hkv, stream)
+        if timed:
+            e[2].record(stream)
+        fa.fa_bwd_dkdv(qd, kd, vd, dod, dk, dv, work, w.causal, w.scale, stream)
+        if timed:
+            e[3].record(stream)
+        fa.fa_bwd_dq_convert(work, dq, Hkv, w.scale, stream)
+        if timed:
+            fwd_ev.append((e[0], e[1]))
+            dkdv_ev.append((e[2], e[3]))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if args.steps is None:
+        # Calibrate K so the timed region lasts about 3 s (clock sampling
+        # needs several 200 ms samples); the same K is then timed exactly.
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(10):
+            step(False)
+        b.record(stream)
+        torch.cuda.synchronize()
+        per = a.elapsed_time(b) / 10
+        k = int(min(20000, max(50, math.ceil(3000.0 / max(per, 1e-3)))))
+        if ws > 1:
+            kt = torch.tensor([k], device=dev)
+            dist.all_reduce(kt, op=dist.ReduceOp.MAX)
+            k = int(kt.item())
+        args.steps = k
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    launches0 = fa.fa_kernel_launches()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(stream)
+        barrier()
+    launches = fa.fa_kernel_launches() - launches0
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
+    ms_total = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    flops_step = attention_flops(w, "fwd_bwd")
+    value = flops_step * args.steps * ws / (ms_total * 1e-3) / 1e12
+
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
+    dkdv_ms = statistics.mean(a.elapsed_time(b) for a, b in dkdv_ev)
+    fwd_flops = attention_flops(w, "fwd")
+    # Algorithmic work of the dK/dV kernel: the five backward matmuls
+    # (S^T, dP^T, dV, dK, dQ), 2*N^2*d each per head, halved when causal.
+    dkdv_flops = fwd_flops * 2.5
+    peak = peaks["bf16_tflops_sustained"]
+    kernels = {
+        "fa_bwd_dkdv": {"ms": dkdv_ms, "tflops": dkdv_flops / dkdv_ms / 1e9},
+        "fa_fwd": {"ms": fwd_ms, "tflops": fwd_flops / fwd_ms / 1e9},
+    }
+    dom = max(kernels, key=lambda n: kernels[n]["ms"])
+    src = {"fa_bwd_dkdv": "fa_bwd.cu", "fa_fwd": "fa_fwd.cu"}[dom]
+    tr = NCU_TRAFFIC.get((dom, w.name))
+    traffic = tr["bytes"] if tr and tr["src_sha"] == kernel_source_hash(src) else None
+    ach = kernels[dom]["tflops"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
+                "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
+                "frac_of_burst_peak": ach / peaks["bf16_tflops"],
+                "other_kernel": {n: {"ms": kernels[n]["ms"], "tflops": kernels[n]["tflops"],
+                                     "frac": kernels[n]["tflops"] / peak}
+                                 for n in kernels if n != dom}}
+
+    # End to end through the public API with pinned host buffers: H2D of the
+    # step's inputs, fa_fwd + fa_bwd, D2H of every output, inside the timing.
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+        outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                  for t in (o, lse, dq, dk, dv)]
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in outs_h)
+        e2e_steps = max(3, args.steps // 2)
+
+        def e2e_step():
+            for dst, src_ in ((qd, hq), (kd, hk), (vd, hv), (dod, hdo)):
+                dst.copy_(src_, non_blocking=True)
+            fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+            fa.fa_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, work, w.causal, w.scale, stream)
+            for dst, src_ in zip(outs_h, (o, lse, dq, dk, dv)):
+                dst.copy_(src_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        e_ms = a.elapsed_time(b)
+        if ws > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": flops_step * e2e_steps * ws / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / e2e_steps}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w)
+
+    if rank == 0:
+        ws_mb = sum(t.numel() * t.element_size() for t in (qd, kd, vd, o, dod, dq, dk, dv, work))
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={B} H={H} Hkv={Hkv} N={N} d={d} "
+                                   f"causal={w.causal} fwd+bwd",
+                       "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d, "causal": w.causal,
+                       "flops_per_step": flops_step, "flop_count": "fwd 4BHN^2d (/2 causal), "
+                                                                  "fwd+bwd x2.5",
+                       "l2": f"inputs larger than L2: {ws_mb / 2**20:.0f} MiB touched per "
+                             f"step vs {L2_BYTES / 2**20:.0f} MiB L2",
+                       "parallelism": f"replicas x{ws} (independent batches)"},
+            "pct_of_bf16_peak": {"sustained": value / ws / peak,
+                                 "burst": value / ws / peaks["bf16_tflops"],
+                                 "source": peaks["source"]},
+            "fwd": {"tflops": kernels["fa_fwd"]["tflops"], "ms": fwd_ms},
+            "fwd_bwd_alg_tflops": attention_flops(w, "fwd_bwd_alg") * args.steps * ws
+                                  / (ms_total * 1e-3) / 1e12,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clk.summary(), "gpu_launches": launches,
+            "launches_per_step": launches / args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from exact_attention_online_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_native(args, w)
+
+
+if __name__ == "__main__":
+    main()
