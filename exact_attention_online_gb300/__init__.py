@@ -23,8 +23,9 @@ FA_ERR_WORKSPACE = -4
 FA_ERR_CUDA = -5
 FA_ERR_TIMEOUT = -6
 
-__all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_bwd",
-           "fa_bwd_workspace_size", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert",
+__all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_precise", "fa_bwd",
+           "fa_bwd_workspace_size", "fa_bwd_precise", "fa_bwd_preprocess",
+           "fa_bwd_preprocess_precise", "fa_bwd_dkdv", "fa_bwd_dq_convert",
            "fa_device_status", "fa_device_status_detail", "fa_status_string",
            "fa_kernel_launches", "fa_watchdog_selftest", "attention", "attention_backward"]
 
@@ -81,6 +82,14 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
                         _stream(stream)), "fa_fwd")
 
 
+def fa_fwd_precise(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """o: fp32 [B, H, N, d]."""
+    B, H, Hkv, N, d = _dims(q, k)
+    _check(lib().fa_fwd_precise(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _f32(o, "o"),
+                                _f32(lse, "lse"), B, H, Hkv, N, d, int(bool(causal)),
+                                float(scale), _stream(stream)), "fa_fwd_precise")
+
+
 def fa_bwd_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
     return int(lib().fa_bwd_workspace_size(B, H, Hkv, N, d))
 
@@ -102,11 +111,32 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, scale: fl
                         float(scale), _stream(stream)), "fa_bwd")
 
 
+def fa_bwd_precise(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, scale: float,
+                   stream=None) -> None:
+    """o: the fp32 output of fa_fwd_precise."""
+    B, H, Hkv, N, d = _dims(q, k)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_precise(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _f32(o, "o"),
+                                _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"),
+                                _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d,
+                                int(bool(causal)), float(scale), _stream(stream)),
+           "fa_bwd_precise")
+
+
 def fa_bwd_preprocess(o, dout, lse, workspace, Hkv: int, stream=None) -> None:
     B, H, N, d = o.shape
     wp, wb = _ws(workspace)
     _check(lib().fa_bwd_preprocess(_bf16(o, "o"), _bf16(dout, "dout"), _f32(lse, "lse"), wp, wb,
                                    B, H, Hkv, N, d, _stream(stream)), "fa_bwd_preprocess")
+
+
+def fa_bwd_preprocess_precise(o, dout, lse, workspace, Hkv: int, stream=None) -> None:
+    """o: the fp32 output of fa_fwd_precise."""
+    B, H, N, d = o.shape
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_preprocess_precise(_f32(o, "o"), _bf16(dout, "dout"), _f32(lse, "lse"),
+                                           wp, wb, B, H, Hkv, N, d, _stream(stream)),
+           "fa_bwd_preprocess_precise")
 
 
 def fa_bwd_dkdv(q, k, v, dout, dk, dv, workspace, causal: bool, scale: float,
@@ -145,14 +175,20 @@ def fa_watchdog_selftest(timeout_ns: int, stream=None) -> None:
 
 # Convenience wrappers that allocate outputs with PyTorch (the library itself
 # never allocates).
-def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """Returns (o, lse) for bf16 CUDA q [B,H,N,d], k/v [B,Hkv,N,d]."""
+def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
+              precise: bool = False):
+    """Returns (o, lse) for bf16 CUDA q [B,H,N,d], k/v [B,Hkv,N,d]; o is bf16, or
+    fp32 from fa_fwd_precise when precise=True."""
     import torch
     d = q.shape[-1]
     scale = d ** -0.5 if scale is None else scale
-    o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    if precise:
+        o = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        fa_fwd_precise(q, k, v, o, lse, causal, scale, stream)
+    else:
+        o = torch.empty_like(q)
+        fa_fwd(q, k, v, o, lse, causal, scale, stream)
     return o, lse
 
 
@@ -166,5 +202,8 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float
         workspace = torch.empty(fa_bwd_workspace_size(B, H, Hkv, N, d), dtype=torch.uint8,
                                 device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    if o.dtype == torch.float32:
+        fa_bwd_precise(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
+    else:
+        fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal, scale, stream)
     return dq, dk, dv

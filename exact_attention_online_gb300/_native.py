@@ -78,12 +78,19 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     L.fa_fwd.restype = i
+    L.fa_fwd_precise.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_precise.restype = i
     L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     L.fa_bwd_workspace_size.restype = sz
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
     L.fa_bwd.restype = i
+    L.fa_bwd_precise.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f,
+                                 vp]
+    L.fa_bwd_precise.restype = i
     L.fa_bwd_preprocess.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
     L.fa_bwd_preprocess.restype = i
+    L.fa_bwd_preprocess_precise.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
+    L.fa_bwd_preprocess_precise.restype = i
     L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
     L.fa_bwd_dkdv.restype = i
     L.fa_bwd_dq_convert.argtypes = [vp, sz, vp, i, i, i, i, i, f, vp]
@@ -115,6 +122,6 @@ def lib() -> ctypes.CDLL:
 
 
 # Every symbol include/fa.h declares.
-EXPORTS = ["fa_fwd", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_preprocess", "fa_bwd_dkdv",
-           "fa_bwd_dq_convert", "fa_device_status", "fa_device_status_detail",
+EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_precise",
+           "fa_bwd_preprocess", "fa_bwd_preprocess_precise", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_device_status", "fa_device_status_detail",
            "fa_status_string", "fa_kernel_launches", "fa_watchdog_selftest"]

@@ -155,7 +155,21 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     int dev;
     if ((st = device_ready(&dev)) != FA_OK) return st;
     const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
-    return from_cuda(launch_fwd(s, q, k, v, o, lse, g_status_ptr[dev], (cudaStream_t)stream));
+    return from_cuda(
+        launch_fwd(s, q, k, v, o, lse, false, g_status_ptr[dev], (cudaStream_t)stream));
+}
+
+fa_status fa_fwd_precise(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                         int H, int Hkv, int N, int d, int causal, float scale,
+                         fa_stream_t stream) {
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(lse)});
+    if (st != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+    return from_cuda(
+        launch_fwd(s, q, k, v, o, lse, true, g_status_ptr[dev], (cudaStream_t)stream));
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
@@ -170,9 +184,9 @@ static fa_status check_workspace(const void* ws, size_t bytes, const Shape& s) {
     return FA_OK;
 }
 
-fa_status fa_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
-                            size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
-                            fa_stream_t stream) {
+static fa_status bwd_preprocess_impl(const void* o, bool o_f32, const void* dout,
+                                     const float* lse, void* workspace, size_t workspace_bytes,
+                                     int B, int H, int Hkv, int N, int d, fa_stream_t stream) {
     const Shape s{B, H, Hkv, N, d, 0, 1.0f};
     fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_ptr(o), check_ptr(dout),
                                 check_ptr(lse)});
@@ -180,8 +194,23 @@ fa_status fa_bwd_preprocess(const void* o, const void* dout, const float* lse, v
     if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
     int dev;
     if ((st = device_ready(&dev)) != FA_OK) return st;
-    return from_cuda(launch_bwd_preprocess(s, o, dout, lse, bwd_workspace_carve(workspace, s),
-                                           g_status_ptr[dev], (cudaStream_t)stream));
+    return from_cuda(launch_bwd_preprocess(s, o, o_f32, dout, lse,
+                                           bwd_workspace_carve(workspace, s), g_status_ptr[dev],
+                                           (cudaStream_t)stream));
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
+                            size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                            fa_stream_t stream) {
+    return bwd_preprocess_impl(o, false, dout, lse, workspace, workspace_bytes, B, H, Hkv, N, d,
+                               stream);
+}
+
+fa_status fa_bwd_preprocess_precise(const float* o, const void* dout, const float* lse,
+                                    void* workspace, size_t workspace_bytes, int B, int H,
+                                    int Hkv, int N, int d, fa_stream_t stream) {
+    return bwd_preprocess_impl(o, true, dout, lse, workspace, workspace_bytes, B, H, Hkv, N, d,
+                               stream);
 }
 
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
@@ -211,10 +240,10 @@ fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void*
                                            dq, (cudaStream_t)stream));
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
-                 size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal,
-                 float scale, fa_stream_t stream) {
+static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, bool o_f32,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                          int d, int causal, float scale, fa_stream_t stream) {
     const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
     fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
                                 check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(dout),
@@ -225,10 +254,26 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if ((st = device_ready(&dev)) != FA_OK) return st;
     const BwdWorkspace ws = bwd_workspace_carve(workspace, s);
     cudaStream_t cs = (cudaStream_t)stream;
-    cudaError_t e = launch_bwd_preprocess(s, o, dout, lse, ws, g_status_ptr[dev], cs);
+    cudaError_t e = launch_bwd_preprocess(s, o, o_f32, dout, lse, ws, g_status_ptr[dev], cs);
     if (e == cudaSuccess) e = launch_bwd_dkdv(s, q, k, v, dout, dk, dv, ws, g_status_ptr[dev], cs);
     if (e == cudaSuccess) e = launch_bwd_dq_convert(s, ws, dq, cs);
     return from_cuda(e);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal,
+                 float scale, fa_stream_t stream) {
+    return bwd_impl(q, k, v, o, false, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H,
+                    Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_bwd_precise(const void* q, const void* k, const void* v, const float* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                         int d, int causal, float scale, fa_stream_t stream) {
+    return bwd_impl(q, k, v, o, true, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H,
+                    Hkv, N, d, causal, scale, stream);
 }
 
 fa_status fa_device_status(fa_stream_t stream) {

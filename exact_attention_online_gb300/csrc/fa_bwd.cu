@@ -31,9 +31,21 @@ namespace fa {
 namespace {
 
 constexpr int kBN = 128;   // keys per CTA
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+// 16 warps: 0-7 compute (two warpgroups), 8 TMA producer, 9 MMA issuer,
+// 10-11 idle, 12-15 dQ read-out.
+constexpr int kThreads = 512;
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kReadoutWarp0 = 12;
+constexpr int kReadoutThreads = 128;
+// Register split (setmaxnreg) of the 512 x 128 launch registers:
+// 256 x 176 + 128 x 96 + 128 x 56 = 64512 <= 65536.
+constexpr int kRegsCompute = 176;
+constexpr int kRegsReadout = 96;
+constexpr int kRegsControl = 56;
+constexpr int kRegsNeeded = 256 * kRegsCompute + 128 * kRegsReadout + 128 * kRegsControl;
 
 template <int D>
 struct BwdCfg {
@@ -46,7 +58,9 @@ struct BwdCfg {
     static constexpr int kOffQ = kOffV + kKVBytes;            // 2 stages
     static constexpr int kOffDO = kOffQ + 2 * kQBytes;        // 2 stages
     static constexpr int kOffDS = kOffDO + 2 * kQBytes;
-    static constexpr int kOffStat = kOffDS + kDSBytes;        // lse2[2][BR], delta[2][BR]
+    static constexpr int kOffStage = kOffDS + kDSBytes;       // 2 x fp32 dQ staging tile
+    static constexpr int kStageTileBytes = kBR * D * 4;        // 32 KB for both head dims
+    static constexpr int kOffStat = kOffStage + 2 * kStageTileBytes;   // lse2[2][BR], delta[2][BR]
     static constexpr int kSmemBytes = kOffStat + 4 * kBR * 4;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;
     static constexpr int kStageBytes = 2 * kQBytes + 2 * kBR * 4;
@@ -80,17 +94,18 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const BwdParams p) {
     using Cfg = BwdCfg<D>;
     constexpr int BR = Cfg::kBR;
+    constexpr int HALF = BR / 2;                  // query columns per compute warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_kv, bar_full[2], bar_empty[2], bar_sdp, bar_ds, bar_dq_full,
-        bar_dq_free, bar_done;
+    __shared__ uint64_t bar_kv, bar_full[2], bar_empty[2], bar_s, bar_dp, bar_p, bar_ds,
+        bar_dq_full, bar_dq_free, bar_done;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     const WaitCtx wc{p.status, &abort_sh};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // (batch, kv head, key block); key blocks with many visible query blocks first.
+    // (batch, kv head, key block j).
     const int n_kblk = (p.N + kBN - 1) / kBN;
     const int jblk = blockIdx.x % n_kblk;
     const int bg = blockIdx.x / n_kblk;           // b * Hkv + g
@@ -105,8 +120,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint8_t* sQ = smem + Cfg::kOffQ;
     uint8_t* sDO = smem + Cfg::kOffDO;
     uint8_t* sDS = smem + Cfg::kOffDS;
-    float* sLSE = reinterpret_cast<float*>(smem + Cfg::kOffStat);    // [2][BR]
-    float* sDel = sLSE + 2 * BR;                                     // [2][BR]
+    float* sStage = reinterpret_cast<float*>(smem + Cfg::kOffStage);   // [2][BR*D] fp32
+    float* sLSE = reinterpret_cast<float*>(smem + Cfg::kOffStat);      // [2][BR]
+    float* sDel = sLSE + 2 * BR;                                        // [2][BR]
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
@@ -115,10 +131,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], 1);
         }
-        mbar_init(&bar_sdp, 1);
-        mbar_init(&bar_ds, 128);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_dp, 1);
+        mbar_init(&bar_p, kComputeThreads);
+        mbar_init(&bar_ds, kComputeThreads);
         mbar_init(&bar_dq_full, 1);
-        mbar_init(&bar_dq_free, 128);
+        mbar_init(&bar_dq_free, kReadoutThreads);
         mbar_init(&bar_done, 1);
         fence_mbar_init();
     }
@@ -131,212 +149,100 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == kProducerWarp) {
-        if (lane == 0 && n_it > 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_do);
-            mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
-            for (int c = 0; c < D / 64; ++c) {
-                tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64, jblk * kBN, bg);
-                tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64, jblk * kBN, bg);
-            }
-            int issued = 0;
-            for (int it = 0; it < n_it; ++it) {
-                const int st = it & 1, u = it >> 1;
-                if (it >= 2 && !fa_wait(&bar_empty[st], (u - 1) & 1, 40, wc)) break;
-                const int hq = g * p.G + it / n_i;        // query head
-                const int i = i_start + it % n_i;
-                const int bh = b * p.H + hq;
-                mbar_arrive_expect_tx(&bar_full[st], Cfg::kStageBytes);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_3d(sQ + st * Cfg::kQBytes + c * (BR * 128), &tm_q, &bar_full[st],
-                                c * 64, i * BR, bh);
-                    tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do, &bar_full[st],
-                                c * 64, i * BR, bh);
-                }
-                const size_t stat = (size_t)bh * p.Np + (size_t)i * BR;
-                bulk_load(sLSE + st * BR, p.lse2 + stat, BR * 4, &bar_full[st]);
-                bulk_load(sDel + st * BR, p.delta + stat, BR * 4, &bar_full[st]);
-                issued = it + 1;
-            }
-            if (abort_sh) {
-                fa_wait(&bar_kv, 0, 41, WaitCtx{p.status, nullptr});
-                for (int it = max(0, issued - 2); it < issued; ++it)
-                    fa_wait(&bar_full[it & 1], (it >> 1) & 1, 41, WaitCtx{p.status, nullptr});
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        if (lane == 0 && n_it > 0) {
-            constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
-            constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
-            constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
-            const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
-                           sdo = smem_u32(sDO), sds = smem_u32(sDS);
-            bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
-            auto issue_sdp = [&](int st) {
-                const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + Cfg::kColS, kdesc(sk, kk, kBN * 128), kdesc(q_, kk, BR * 128), id_s,
-                           kk > 0);
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + Cfg::kColDP, kdesc(sv, kk, kBN * 128), kdesc(do_, kk, BR * 128),
-                           id_s, kk > 0);
-                mma_commit(&bar_sdp);
-            };
-            if (ok) {
-                tc_fence_after();
-                issue_sdp(0);
-            }
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int st = it & 1;
-                if (!fa_wait(&bar_ds, it & 1, 52, wc)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
-                // dV += P^T dO_i, dK += dS^T Q_i   (K dimension = BR queries)
-                for (int kk = 0; kk < BR / 16; ++kk)
-                    mma_ts(tmem + Cfg::kColDV, tmem + Cfg::kColS + kk * 8, mndesc(do_, kk, BR * 128),
-                           id_kv, (it > 0 || kk > 0) ? 1u : 0u);
-                for (int kk = 0; kk < BR / 16; ++kk)
-                    mma_ss(tmem + Cfg::kColDK, kdesc(sds, kk, kBN * 128), mndesc(q_, kk, BR * 128),
-                           id_kv, (it > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bar_empty[st]);
-                // dQ partial (K dimension = 128 keys)
-                if (it > 0 && !fa_wait(&bar_dq_free, (it - 1) & 1, 53, wc)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t a_ = (D == 128) ? sk : sds;
-                const uint32_t b_ = (D == 128) ? sds : sk;
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ss(tmem + Cfg::kColDQ, mndesc(a_, kk, kBN * 128), mndesc(b_, kk, kBN * 128),
-                           id_dq, kk > 0);
-                mma_commit(&bar_dq_full);
-                if (it + 1 < n_it) {
-                    const int st1 = (it + 1) & 1;
-                    if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    issue_sdp(st1);
-                }
-            }
-            mma_commit(&bar_done);
-            if (!ok) fa_wait(&bar_done, 0, 59, WaitCtx{p.status, nullptr});
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------ compute
-        const int quarter = warp;                   // warps 0-3
-        const int rl = quarter * 32 + lane;         // TMEM lane of this thread
+    // One register-budget change per warpgroup (all its warps, same
+    // instruction); each role below is dominated by exactly one of them.
+    if (warp < kComputeWarps) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
+        // ---------------------------------------------------------- compute
+        // warp w: TMEM lane quarter w % 4 (= 32 key rows), query half w / 4.
+        const int quarter = warp & 3, hf = warp >> 2;
+        const int rl = quarter * 32 + lane;          // key row within the block
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        const int key = jblk * kBN + rl;            // key row (S^T, dP^T, dK, dV)
+        const int key = jblk * kBN + rl;
+        const int cb = hf * HALF;                    // first query column of this warp
         const float c = p.scale_log2;
         bool ok = n_it > 0;
         for (int it = 0; ok && it < n_it; ++it) {
             const int st = it & 1;
-            const int hq = g * p.G + it / n_i;
             const int i = i_start + it % n_i;
-            const int bh = b * p.H + hq;
             if (!fa_wait_warp(&bar_full[st], (it >> 1) & 1, 60, wc) ||
-                !fa_wait_warp(&bar_sdp, it & 1, 61, wc)) { ok = false; break; }
+                !fa_wait_warp(&bar_s, it & 1, 61, wc)) { ok = false; break; }
             tc_fence_after();
             const float* lse_s = sLSE + st * BR;
             const float* del_s = sDel + st * BR;
             const int q0 = i * BR;
             const bool need_mask = (CAUSAL && q0 < jblk * kBN + kBN - 1) || (jblk * kBN + kBN > p.N);
-            const int key_lim = CAUSAL ? key - q0 : -1;   // query q0+e visible iff e >= key_lim
+            const int key_lim = CAUSAL ? key - q0 : -1;    // column e visible iff e >= key_lim
             const bool key_valid = key < p.N;
+            // P^T = 2^(S^T c - lse2), kept in fp32 for dS; bf16 copy into TMEM over
+            // this warp's own S^T columns (already read).
+            float pf[HALF];
 #pragma unroll
-            for (int ch = 0; ch < BR / 32; ++ch) {
-                uint32_t sr[32], dpr[32];
-                tmem_ld32(lane_addr + Cfg::kColS + ch * 32, sr);
-                tmem_ld32(lane_addr + Cfg::kColDP + ch * 32, dpr);
+            for (int ch = 0; ch < HALF / 32; ++ch) {
+                uint32_t sr[32];
+                tmem_ld32(lane_addr + Cfg::kColS + cb + ch * 32, sr);
                 tmem_ld_wait(sr);
-                asm volatile("" : FA_R32(dpr) : : "memory");
                 uint32_t pk[16];
-                uint32_t dsk[16];
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pv[2], dsv[2];
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        const int qe = ch * 32 + e + t;
-                        float pe = ex2(fmaf(__uint_as_float(sr[e + t]), c, -lse_s[qe]));
-                        if (need_mask && (qe < key_lim || !key_valid)) pe = 0.0f;
-                        pv[t] = pe;
-                        dsv[t] = pe * (__uint_as_float(dpr[e + t]) - del_s[qe]);
-                    }
-                    pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-                    dsk[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                for (int e = 0; e < 32; ++e) {
+                    const int qe = cb + ch * 32 + e;
+                    float pe = ex2(fmaf(__uint_as_float(sr[e]), c, -lse_s[qe]));
+                    if (need_mask && (qe < key_lim || !key_valid)) pe = 0.0f;
+                    pf[ch * 32 + e] = pe;
                 }
-                // P^T chunk into TMEM (over the S^T columns already read).
-                asm volatile(
-                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
-                    "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_addr + Cfg::kColS +
-                                                                      ch * 16),
-                    "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]),
-                    "r"(pk[6]), "r"(pk[7]), "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]),
-                    "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
-                    : "memory");
-                // dS^T chunk (32 queries = 64 bytes) into the swizzled smem tile.
-                const int qc = ch >> 1;                 // 64-query chunk
-                uint8_t* rowp = sDS + qc * (kBN * 128) + rl * 128;
 #pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const int unit = (ch & 1) * 4 + u4;
-                    uint4 w = make_uint4(dsk[u4 * 4 + 0], dsk[u4 * 4 + 1], dsk[u4 * 4 + 2],
-                                         dsk[u4 * 4 + 3]);
-                    *reinterpret_cast<uint4*>(rowp + ((unit ^ (rl & 7)) * 16)) = w;
-                }
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = pack_bf16x2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]);
+                tmem_st16(lane_addr + Cfg::kColS + cb + ch * 16, pk);
             }
             tmem_st_wait();
             tc_fence_before();
-            fence_proxy_async_smem();
-            mbar_arrive(&bar_ds);
+            mbar_arrive(&bar_p);
 
-            // dQ partial -> fp32 accumulator
-            if (!fa_wait_warp(&bar_dq_full, it & 1, 62, wc)) { ok = false; break; }
+            // dS^T = P^T o (dP^T - D) -> bf16, swizzled [key][query] tile in smem.
+            if (!fa_wait_warp(&bar_dp, it & 1, 62, wc)) { ok = false; break; }
             tc_fence_after();
-            float* acc_head = p.dq_acc + (size_t)bh * p.Np * D;
-            if (D == 128) {
-                // dQ^T: TMEM lane = head-dim index, column = query.
-                const int dd = rl;
 #pragma unroll
-                for (int ch = 0; ch < BR / 32; ++ch) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + Cfg::kColDQ + ch * 32, r);
-                    tmem_ld_wait(r);
+            for (int ch = 0; ch < HALF / 32; ++ch) {
+                uint32_t dpr[32];
+                tmem_ld32(lane_addr + Cfg::kColDP + cb + ch * 32, dpr);
+                tmem_ld_wait(dpr);
+                uint32_t dsk[16];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        atomicAdd(acc_head + (size_t)(q0 + ch * 32 + e) * D + dd,
-                                  __uint_as_float(r[e]));
+                for (int e = 0; e < 16; ++e) {
+                    const int qe = cb + ch * 32 + 2 * e;
+                    const float d0 = pf[ch * 32 + 2 * e] * (__uint_as_float(dpr[2 * e]) - del_s[qe]);
+                    const float d1 =
+                        pf[ch * 32 + 2 * e + 1] * (__uint_as_float(dpr[2 * e + 1]) - del_s[qe + 1]);
+                    dsk[e] = pack_bf16x2(d0, d1);
                 }
-            } else {
-                // dQ: TMEM lane = query, column = head-dim index.
-                float* rowp = acc_head + (size_t)(q0 + rl) * D;
+                const int qc = (cb + ch * 32) >> 6;       // 64-query chunk of the tile
+                const int u0 = ((cb + ch * 32) & 63) >> 3;  // first 16-byte unit in the row
+                uint8_t* rowp = sDS + qc * (kBN * 128) + rl * 128;
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + Cfg::kColDQ + ch * 32, r);
-                    tmem_ld_wait(r);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        atomicAdd(reinterpret_cast<float4*>(rowp + ch * 32 + e),
-                                  make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                                              __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])));
+                for (int u4 = 0; u4 < 4; ++u4) {
+                    const int unit = u0 + u4;
+                    *reinterpret_cast<uint4*>(rowp + ((unit ^ (rl & 7)) * 16)) =
+                        make_uint4(dsk[u4 * 4 + 0], dsk[u4 * 4 + 1], dsk[u4 * 4 + 2],
+                                   dsk[u4 * 4 + 3]);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&bar_dq_free);
+            fence_proxy_async_smem();
+            mbar_arrive(&bar_ds);
         }
         // ---------------------------------------------------- dK, dV epilogue
         if (ok && fa_wait_warp(&bar_done, 0, 63, wc)) {
             tc_fence_after();
             const bool valid = key < p.N;
             const size_t row = ((size_t)bg * p.N + (valid ? key : 0)) * D;
+            const int c_lo = hf * (D / 2);
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = which ? Cfg::kColDV : Cfg::kColDK;
                 const float mul = which ? 1.0f : p.scale;
                 __nv_bfloat16* dst = (which ? p.dv : p.dk) + row;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = c_lo; c0 < c_lo + D / 2; c0 += 32) {
                     uint32_t r[32];
                     tmem_ld32(lane_addr + col + c0, r);
                     tmem_ld_wait(r);
@@ -358,14 +264,180 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                 }
             }
-        } else if (n_it == 0) {
-            // No query block sees these keys (cannot happen with N_q == N_k);
-            // their gradients are zero.
-            if (key < p.N)
-                for (int c0 = 0; c0 < D; ++c0) {
-                    p.dk[((size_t)bg * p.N + key) * D + c0] = __float2bfloat16(0.0f);
-                    p.dv[((size_t)bg * p.N + key) * D + c0] = __float2bfloat16(0.0f);
+        }
+    } else if (warp >= kReadoutWarp0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsReadout));
+        // ----------------------------------------------------- dQ read-out
+        // TMEM -> registers -> fp32 staging tile laid out like the accumulator
+        // rows -> one bulk reduce-add of BR*D*4 = 32 KB per query block.
+        const int quarter = warp & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int rl = quarter * 32 + lane;
+        const bool leader = (warp == kReadoutWarp0 && lane == 0);
+        bool ok = n_it > 0;
+        for (int it = 0; ok && it < n_it; ++it) {
+            const int hq = g * p.G + it / n_i;
+            const int i = i_start + it % n_i;
+            const int bh = b * p.H + hq;
+            if (!fa_wait_warp(&bar_dq_full, it & 1, 70, wc)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(lane_addr + Cfg::kColDQ, r0);
+            tmem_ld32(lane_addr + Cfg::kColDQ + 32, r1);
+            tmem_ld_wait(r0);
+            asm volatile("" : FA_R32(r1) : : "memory");
+            tc_fence_before();
+            mbar_arrive(&bar_dq_free);
+            float* stg = sStage + (it & 1) * (BR * D);
+            if (leader) bulk_wait_group_read<1>();   // the copy that last read this buffer
+            named_bar_sync(1, kReadoutThreads);
+            if (D == 128) {
+                // dQ^T: lane = head-dim index dd, column = query -> stg[q][dd]
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    stg[e * D + rl] = __uint_as_float(r0[e]);
+                    stg[(32 + e) * D + rl] = __uint_as_float(r1[e]);
                 }
+            } else {
+                // dQ: lane = query row, column = head-dim index -> stg[row][0..63],
+                // 16-byte pieces in an order rotated by (lane & 7) so that eight
+                // neighbouring lanes hit eight different bank groups.
+                float v[64];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    v[e] = __uint_as_float(r0[e]);
+                    v[32 + e] = __uint_as_float(r1[e]);
+                }
+                const int rot = lane & 7;
+#pragma unroll
+                for (int bit = 0; bit < 3; ++bit) {     // v <- v rotated left by rot*4
+                    const int sh = (1 << bit) * 4;
+                    const bool doit = (rot >> bit) & 1;
+                    float t[64];
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) t[e] = v[(e + sh) & 63];
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) v[e] = doit ? t[e] : v[e];
+                }
+                float4* rowp = reinterpret_cast<float4*>(stg + rl * D);
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    rowp[(u + rot) & 15] =
+                        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, kReadoutThreads);
+            if (leader) {
+                bulk_reduce_add_f32(p.dq_acc + ((size_t)bh * p.Np + (size_t)i * BR) * D, stg,
+                                    BR * D * 4);
+                bulk_commit_group();
+            }
+        }
+        if (leader) bulk_wait_group<0>();
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+        if (warp == kProducerWarp) {
+            if (lane == 0 && n_it > 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_do);
+                mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64, jblk * kBN, bg);
+                    tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64, jblk * kBN, bg);
+                }
+                int issued = 0;
+                for (int it = 0; it < n_it; ++it) {
+                    const int st = it & 1, u = it >> 1;
+                    if (it >= 2 && !fa_wait(&bar_empty[st], (u - 1) & 1, 40, wc)) break;
+                    const int hq = g * p.G + it / n_i;
+                    const int i = i_start + it % n_i;
+                    const int bh = b * p.H + hq;
+                    mbar_arrive_expect_tx(&bar_full[st], Cfg::kStageBytes);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_3d(sQ + st * Cfg::kQBytes + c * (BR * 128), &tm_q, &bar_full[st],
+                                    c * 64, i * BR, bh);
+                        tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do,
+                                    &bar_full[st], c * 64, i * BR, bh);
+                    }
+                    const size_t stat = (size_t)bh * p.Np + (size_t)i * BR;
+                    bulk_load(sLSE + st * BR, p.lse2 + stat, BR * 4, &bar_full[st]);
+                    bulk_load(sDel + st * BR, p.delta + stat, BR * 4, &bar_full[st]);
+                    issued = it + 1;
+                }
+                if (abort_sh) {
+                    fa_wait(&bar_kv, 0, 41, WaitCtx{p.status, nullptr});
+                    for (int it = max(0, issued - 2); it < issued; ++it)
+                        fa_wait(&bar_full[it & 1], (it >> 1) & 1, 41, WaitCtx{p.status, nullptr});
+                }
+            }
+        } else if (warp == kMmaWarp) {
+            if (lane == 0 && n_it > 0) {
+                constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
+                constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+                constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
+                const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
+                               sdo = smem_u32(sDO), sds = smem_u32(sDS);
+                auto issue_s = [&](int st) {      // S^T = K_j Q_i^T
+                    const uint32_t q_ = sq + st * Cfg::kQBytes;
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + Cfg::kColS, kdesc(sk, kk, kBN * 128), kdesc(q_, kk, BR * 128),
+                               id_s, kk > 0);
+                    mma_commit(&bar_s);
+                };
+                auto issue_dp = [&](int st) {     // dP^T = V_j dO_i^T
+                    const uint32_t do_ = sdo + st * Cfg::kQBytes;
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + Cfg::kColDP, kdesc(sv, kk, kBN * 128),
+                               kdesc(do_, kk, BR * 128), id_s, kk > 0);
+                    mma_commit(&bar_dp);
+                };
+                bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                    issue_dp(0);
+                }
+                for (int it = 0; ok && it < n_it; ++it) {
+                    const int st = it & 1, st1 = (it + 1) & 1;
+                    const bool next = it + 1 < n_it;
+                    const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
+                    // dV += P^T dO_i  (P^T in TMEM; query half h of the K dimension
+                    // sits in the S^T columns of the warps of half h)
+                    if (!fa_wait(&bar_p, it & 1, 52, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int kk = 0; kk < BR / 16; ++kk) {
+                        const int qs = kk * 16;
+                        const uint32_t pcol = Cfg::kColS + (qs / HALF) * HALF + (qs % HALF) / 2;
+                        mma_ts(tmem + Cfg::kColDV, tmem + pcol, mndesc(do_, kk, BR * 128), id_kv,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (next) {
+                        if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(st1);
+                    }
+                    // dK += dS^T Q_i
+                    if (!fa_wait(&bar_ds, it & 1, 55, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int kk = 0; kk < BR / 16; ++kk)
+                        mma_ss(tmem + Cfg::kColDK, kdesc(sds, kk, kBN * 128), mndesc(q_, kk, BR * 128),
+                               id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bar_empty[st]);
+                    // dQ partial (K dimension = the 128 keys)
+                    if (it > 0 && !fa_wait(&bar_dq_free, (it - 1) & 1, 53, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_ = (D == 128) ? sk : sds;
+                    const uint32_t b_ = (D == 128) ? sds : sk;
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ss(tmem + Cfg::kColDQ, mndesc(a_, kk, kBN * 128), mndesc(b_, kk, kBN * 128),
+                               id_dq, kk > 0);
+                    mma_commit(&bar_dq_full);
+                    if (next) issue_dp(st1);
+                }
+                mma_commit(&bar_done);
+                if (!ok) fa_wait(&bar_done, 0, 59, WaitCtx{p.status, nullptr});
+            }
+            __syncwarp();
         }
     }
 
@@ -378,14 +450,15 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }
 
 // D_i = <dO_i, O_i>, lse2 = LSE * log2(e) (+inf on padded rows), accumulator = 0.
-// One warp per row, grid-stride over the B*H*Np rows.
-template <int D>
+// One warp per row, grid-stride over the B*H*Np rows.  O is bf16, or fp32 when
+// it comes from the precise forward.
+template <int D, typename OT>
 __global__ void __launch_bounds__(256)
-fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, float* __restrict__ lse2,
                   float* __restrict__ delta, float* __restrict__ dq_acc, int N, int Np,
                   long long rows) {
-    constexpr int kPer = D / 32;   // bf16 per lane
+    constexpr int kPer = D / 32;   // elements per lane (2 or 4)
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -395,24 +468,30 @@ fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __re
         float acc = 0.0f;
         if (i < N) {
             const long long src = (bh * N + i) * D + lane * kPer;
+            float ov[kPer], dv[kPer];
             if (kPer == 4) {
-                const uint2 ov = *reinterpret_cast<const uint2*>(o + src);
-                const uint2 dv = *reinterpret_cast<const uint2*>(dout + src);
-                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-                const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const float2 a = __bfloat1622float2(o2[t]), bb = __bfloat1622float2(d2[t]);
-                    acc = fmaf(a.x, bb.x, acc);
-                    acc = fmaf(a.y, bb.y, acc);
-                }
+                const uint2 dd = *reinterpret_cast<const uint2*>(dout + src);
+                const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dd);
+                const float2 a = __bfloat1622float2(d2[0]), c2 = __bfloat1622float2(d2[1]);
+                dv[0] = a.x; dv[1] = a.y; dv[kPer - 2] = c2.x; dv[kPer - 1] = c2.y;
             } else {
-                const __nv_bfloat162 ov = *reinterpret_cast<const __nv_bfloat162*>(o + src);
-                const __nv_bfloat162 dv = *reinterpret_cast<const __nv_bfloat162*>(dout + src);
-                const float2 a = __bfloat1622float2(ov), bb = __bfloat1622float2(dv);
-                acc = fmaf(a.x, bb.x, acc);
-                acc = fmaf(a.y, bb.y, acc);
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + src));
+                dv[0] = a.x; dv[kPer - 1] = a.y;
             }
+            if constexpr (sizeof(OT) == 4) {
+#pragma unroll
+                for (int t = 0; t < kPer; ++t) ov[t] = reinterpret_cast<const float*>(o)[src + t];
+            } else if (kPer == 4) {
+                const uint2 oo = *reinterpret_cast<const uint2*>(o + src);
+                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&oo);
+                const float2 a = __bfloat1622float2(o2[0]), c2 = __bfloat1622float2(o2[1]);
+                ov[0] = a.x; ov[1] = a.y; ov[kPer - 2] = c2.x; ov[kPer - 1] = c2.y;
+            } else {
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + src));
+                ov[0] = a.x; ov[kPer - 1] = a.y;
+            }
+#pragma unroll
+            for (int t = 0; t < kPer; ++t) acc = fmaf(ov[t], dv[t], acc);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -480,8 +559,14 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             BwdCfg<D>::kSmemAlloc);
+        // The register split must fit in what the launch provides, or the
+        // setmaxnreg.inc of the compute warps would wait forever.
+        cudaFuncAttributes attr;
+        cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+        if (e != cudaSuccess) return e;
+        if (attr.numRegs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 BwdCfg<D>::kSmemAlloc);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -491,7 +576,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 
 }  // namespace
 
-cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, const void* dout,
+cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, const void* dout,
                                   const float* lse, const BwdWorkspace& ws, DeviceStatus* status,
                                   cudaStream_t stream) {
     (void)status;
@@ -499,14 +584,24 @@ cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, const void* dou
     const long long rows = (long long)s.B * s.H * Np;
     const int grid = grid_for(rows, 8);
     count_launch();
-    auto* o_ = static_cast<const __nv_bfloat16*>(o);
     auto* d_ = static_cast<const __nv_bfloat16*>(dout);
-    if (s.d == 128)
-        fa_bwd_pre_kernel<128><<<grid, 256, 0, stream>>>(o_, d_, lse, ws.lse2, ws.delta,
-                                                         ws.dq_acc, s.N, Np, rows);
-    else
-        fa_bwd_pre_kernel<64><<<grid, 256, 0, stream>>>(o_, d_, lse, ws.lse2, ws.delta,
-                                                        ws.dq_acc, s.N, Np, rows);
+    auto* ob = static_cast<const __nv_bfloat16*>(o);
+    auto* of = static_cast<const float*>(o);
+    if (s.d == 128) {
+        if (o_f32)
+            fa_bwd_pre_kernel<128, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse2, ws.delta,
+                                                                    ws.dq_acc, s.N, Np, rows);
+        else
+            fa_bwd_pre_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows);
+    } else {
+        if (o_f32)
+            fa_bwd_pre_kernel<64, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse2, ws.delta,
+                                                                   ws.dq_acc, s.N, Np, rows);
+        else
+            fa_bwd_pre_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows);
+    }
     return cudaGetLastError();
 }
 

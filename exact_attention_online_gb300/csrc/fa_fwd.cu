@@ -20,6 +20,12 @@
 // 256), so most blocks skip the O rescale; numerator and denominator always
 // use the same m, so the result is unchanged in exact arithmetic.  O is
 // divided by l once, in the epilogue, and LSE = ln2 * (m + log2 l).
+//
+// PRECISE variant: P enters the P V product as two bf16 terms, P_hi = bf16(p)
+// in the first half of S_t and P_lo = bf16(p - P_hi) in the second half, each
+// multiplied by V_j (two TS MMAs), and O is written in fp32.  This removes the
+// bf16 rounding of P and of O from the error, which matters when values reach
+// tens (outliers of magnitude 30: half a bf16 ulp of 30 is 0.06).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -37,10 +43,11 @@ constexpr int kThreads = 12 * 32;   // 3 warpgroups: softmax 0, softmax 1, contr
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;         // warps 10-11 only take part in set-up and teardown
 // Register split (setmaxnreg): the launch gives 384 x 168; the control
-// warpgroup drops to 56 so each softmax thread can hold a full 128-score row:
-// 128 x 56 + 256 x 224 = 64512 <= 384 x 168 = 64512.
-constexpr int kRegsControl = 56;
-constexpr int kRegsSoftmax = 224;
+// warpgroup drops to 72 so each softmax thread can hold a full 128-score row:
+// 128 x 72 + 256 x 216 = 64512 <= 384 x 168 = 64512.
+constexpr int kRegsControl = 72;
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsNeeded = 128 * kRegsControl + 256 * kRegsSoftmax;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int D>
@@ -59,9 +66,9 @@ struct FwdCfg {
 };
 
 struct FwdParams {
-    int H, Hkv, N, BH, n_mblk, causal;
+    int H, Hkv, N, BH, n_mblk, n_items, causal;
     float scale_log2;                 // scale * log2(e)
-    __nv_bfloat16* o;
+    void* o;                          // bf16, or fp32 in the precise variant
     float* lse;
     DeviceStatus* status;
 };
@@ -75,7 +82,30 @@ __device__ __forceinline__ uint64_t vmn_desc(uint32_t base, int kk) {
     return sdesc_sw128(base + kk * (16 * 128), 128 * 128, 1024);
 }
 
-template <int D, bool CAUSAL>
+// Work item (query-block pair, batch*head) -> coordinates.  Under the causal
+// mask the longest query blocks come first (the tile list is in decreasing
+// cost order, and each CTA takes every gridDim.x-th item).
+struct FwdTile {
+    int bh, kv_bh, row_base;
+    int n_kv[kTiles];          // key blocks each query tile needs
+};
+
+__device__ __forceinline__ FwdTile fwd_tile(int item, const FwdParams& p, bool causal) {
+    FwdTile w;
+    const int mb_rank = item / p.BH;
+    w.bh = item % p.BH;
+    const int m_blk = causal ? (p.n_mblk - 1 - mb_rank) : mb_rank;
+    const int b = w.bh / p.H, h = w.bh % p.H;
+    w.kv_bh = b * p.Hkv + h / (p.H / p.Hkv);
+    w.row_base = m_blk * (kTiles * kBM);
+    const int n_kv_all = (p.N + kBN - 1) / kBN;
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t)
+        w.n_kv[t] = causal ? min(n_kv_all, 2 * m_blk + t + 1) : n_kv_all;
+    return w;
+}
+
+template <int D, bool CAUSAL, bool PRECISE>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -84,38 +114,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_q, bar_k[S], bar_v[S], bar_kv_empty[S];
-    __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_o[kTiles];
+    __shared__ uint64_t bar_k[S], bar_v[S], bar_kv_empty[S];
+    __shared__ uint64_t bar_q[kTiles], bar_q_free[kTiles];
+    __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_o[kTiles], bar_o_free[kTiles];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     const WaitCtx wc{p.status, &abort_sh};
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // Tile -> (query block pair, batch*head).  Under the causal mask the
-    // longest query blocks are dispatched first.
-    const int idx = blockIdx.x;
-    const int mb_rank = idx / p.BH;
-    const int bh = idx % p.BH;
-    const int m_blk = CAUSAL ? (p.n_mblk - 1 - mb_rank) : mb_rank;
-    const int b = bh / p.H, h = bh % p.H;
-    const int kv_bh = b * p.Hkv + h / (p.H / p.Hkv);
-    const int n_kv_all = (p.N + kBN - 1) / kBN;
-    const int n_kv = CAUSAL ? min(n_kv_all, 2 * m_blk + 2) : n_kv_all;
-    const int row_base = m_blk * (kTiles * kBM);
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
-        mbar_init(&bar_q, 1);
         for (int s = 0; s < S; ++s) {
             mbar_init(&bar_k[s], 1);
             mbar_init(&bar_v[s], 1);
             mbar_init(&bar_kv_empty[s], 1);
         }
         for (int t = 0; t < kTiles; ++t) {
+            mbar_init(&bar_q[t], 1);
+            mbar_init(&bar_q_free[t], 1);
             mbar_init(&bar_s[t], 1);
             mbar_init(&bar_p[t], 128);
             mbar_init(&bar_o[t], 1);
+            mbar_init(&bar_o_free[t], 128);
         }
         fence_mbar_init();
     }
@@ -140,120 +160,153 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int t = warp >> 2;                 // query tile of this group
         const int quarter = warp & 3;            // TMEM lane quarter
         const int rl = quarter * 32 + lane;      // row within the tile
-        const int row0 = row_base + t * kBM;
-        const int row = row0 + rl;
         const uint32_t col_s = t ? Cfg::kColS1 : Cfg::kColS0;
         const uint32_t col_o = t ? Cfg::kColO1 : Cfg::kColO0;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         const float c = p.scale_log2;
-        float m2 = -CUDART_INF_F;   // running max, log2-scaled
-        float l = 0.0f;
+        uint32_t cs = 0;                         // S_t completions seen so far
         bool ok = true;
+        int lt = 0;
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+            const FwdTile wt = fwd_tile(item, p, CAUSAL);
+            const int row0 = wt.row_base + t * kBM;
+            const int row = row0 + rl;
+            const int n_kv = wt.n_kv[t];
+            float m2 = -CUDART_INF_F;   // running max, log2-scaled
+            float l = 0.0f;
+            for (int j = 0; j < n_kv; ++j) {
+                if (!fa_wait_warp(&bar_s[t], cs & 1, 30 + t, wc)) { ok = false; break; }
+                ++cs;
+                tc_fence_after();
+                uint32_t r[4][32];
+                tmem_ld32(lane_addr + col_s + 0, r[0]);
+                tmem_ld32(lane_addr + col_s + 32, r[1]);
+                tmem_ld32(lane_addr + col_s + 64, r[2]);
+                tmem_ld32(lane_addr + col_s + 96, r[3]);
+                tmem_ld_wait(r[0]);
+                asm volatile("" : FA_R32(r[1]) : : "memory");
+                asm volatile("" : FA_R32(r[2]) : : "memory");
+                asm volatile("" : FA_R32(r[3]) : : "memory");
+                float sv[kBN];
+#pragma unroll
+                for (int e = 0; e < kBN; ++e) sv[e] = __uint_as_float(r[e >> 5][e & 31]);
 
-        for (int j = 0; j < n_kv; ++j) {
-            if (!fa_wait_warp(&bar_s[t], j & 1, 30 + t, wc)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t r[4][32];
-            tmem_ld32(lane_addr + col_s + 0, r[0]);
-            tmem_ld32(lane_addr + col_s + 32, r[1]);
-            tmem_ld32(lane_addr + col_s + 64, r[2]);
-            tmem_ld32(lane_addr + col_s + 96, r[3]);
-            tmem_ld_wait(r[0]);
-            asm volatile("" : FA_R32(r[1]) : : "memory");
-            asm volatile("" : FA_R32(r[2]) : : "memory");
-            asm volatile("" : FA_R32(r[3]) : : "memory");
-            float sv[kBN];
+                const int col0 = j * kBN;
+                const bool need_mask = (CAUSAL && col0 + kBN - 1 > row0) || (col0 + kBN > p.N);
+                if (need_mask) {
+                    const int lim_causal = CAUSAL ? row - col0 : kBN;   // keep e <= row - col0
+                    const int lim_n = p.N - col0;                        // keep e < N - col0
 #pragma unroll
-            for (int e = 0; e < kBN; ++e) sv[e] = __uint_as_float(r[e >> 5][e & 31]);
-
-            const int col0 = j * kBN;
-            const bool need_mask = (CAUSAL && col0 + kBN - 1 > row0) || (col0 + kBN > p.N);
-            if (need_mask) {
-                const int lim_causal = CAUSAL ? row - col0 : kBN;   // keep e <= row - col0
-                const int lim_n = p.N - col0;                        // keep e < N - col0
-#pragma unroll
-                for (int e = 0; e < kBN; ++e)
-                    if (e > lim_causal || e >= lim_n) sv[e] = -CUDART_INF_F;
-            }
-            float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-            for (int e = 4; e < kBN; e += 4) {
-                mx4[0] = fmaxf(mx4[0], sv[e]);
-                mx4[1] = fmaxf(mx4[1], sv[e + 1]);
-                mx4[2] = fmaxf(mx4[2], sv[e + 2]);
-                mx4[3] = fmaxf(mx4[3], sv[e + 3]);
-            }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-            const float mx2 = mx * c;
-            const bool need = mx2 > m2 + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-                const float m_new = need ? mx2 : m2;
-                const float alpha = (m_new == m2) ? 1.0f : ex2(m2 - m_new);
-                l *= alpha;
-                if (j > 0) {
-#pragma unroll
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t ov[32];
-                        tmem_ld32(lane_addr + col_o + c0, ov);
-                        tmem_ld_wait(ov);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st32(lane_addr + col_o + c0, ov);
-                    }
+                    for (int e = 0; e < kBN; ++e)
+                        if (e > lim_causal || e >= lim_n) sv[e] = -CUDART_INF_F;
                 }
-                m2 = m_new;
-            }
-            const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
-            float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            uint32_t pk[2][32];
+                float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-            for (int e = 0; e < kBN; e += 2) {
-                const float p0 = ex2(fmaf(sv[e], c, -m_use));
-                const float p1 = ex2(fmaf(sv[e + 1], c, -m_use));
-                rs4[(e >> 1) & 3] += p0 + p1;
-                pk[e >> 6][(e >> 1) & 31] = pack_bf16x2(p0, p1);
+                for (int e = 4; e < kBN; e += 4) {
+                    mx4[0] = fmaxf(mx4[0], sv[e]);
+                    mx4[1] = fmaxf(mx4[1], sv[e + 1]);
+                    mx4[2] = fmaxf(mx4[2], sv[e + 2]);
+                    mx4[3] = fmaxf(mx4[3], sv[e + 3]);
+                }
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                const float mx2 = mx * c;
+                const bool need = mx2 > m2 + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = need ? mx2 : m2;
+                    const float alpha = (m_new == m2) ? 1.0f : ex2(m2 - m_new);
+                    l *= alpha;
+                    if (j > 0) {
+#pragma unroll
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t ov[32];
+                            tmem_ld32(lane_addr + col_o + c0, ov);
+                            tmem_ld_wait(ov);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            tmem_st32(lane_addr + col_o + c0, ov);
+                        }
+                    }
+                    m2 = m_new;
+                }
+                const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
+                float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t pk[32], pl[32];
+#pragma unroll
+                    for (int e2 = 0; e2 < 32; ++e2) {
+                        const int e = hh * 64 + 2 * e2;
+                        const float p0 = ex2(fmaf(sv[e], c, -m_use));
+                        const float p1 = ex2(fmaf(sv[e + 1], c, -m_use));
+                        rs4[e2 & 3] += p0 + p1;
+                        pk[e2] = pack_bf16x2(p0, p1);
+                        if (PRECISE) {
+                            // second term: what bf16 rounding of p left out
+                            const float h0 = __uint_as_float(pk[e2] << 16);
+                            const float h1 = __uint_as_float(pk[e2] & 0xffff0000u);
+                            pl[e2] = pack_bf16x2(p0 - h0, p1 - h1);
+                        }
+                    }
+                    tmem_st32(lane_addr + col_s + hh * 32, pk);
+                    if (PRECISE) tmem_st32(lane_addr + col_s + 64 + hh * 32, pl);
+                }
+                l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bar_p[t]);
             }
-            const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
-            l += rs;
-            tmem_st32(lane_addr + col_s + 0, pk[0]);
-            tmem_st32(lane_addr + col_s + 32, pk[1]);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bar_p[t]);
-        }
+            if (!ok) break;
 
-        // ----------------------------------------------------------- epilogue
-        if (ok && fa_wait_warp(&bar_o[t], 0, 32 + t, wc)) {
+            // ------------------------------------------------------- epilogue
+            // O row -> registers, release the O columns to the next item's
+            // MMAs, then normalise and store.
+            if (!fa_wait_warp(&bar_o[t], lt & 1, 32 + t, wc)) { ok = false; break; }
             tc_fence_after();
+            uint32_t ov[D / 32][32];
+#pragma unroll
+            for (int c0 = 0; c0 < D / 32; ++c0) tmem_ld32(lane_addr + col_o + c0 * 32, ov[c0]);
+            tmem_ld_wait(ov[0]);
+#pragma unroll
+            for (int c0 = 1; c0 < D / 32; ++c0) asm volatile("" : FA_R32(ov[c0]) : : "memory");
+            tc_fence_before();
+            mbar_arrive(&bar_o_free[t]);
             const bool valid = row < p.N;
             const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-            __nv_bfloat16* orow = p.o + ((size_t)bh * p.N + (valid ? row : 0)) * D;
+            const size_t orow = ((size_t)wt.bh * p.N + (valid ? row : 0)) * D;
+            if (valid) {
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tmem_ld32(lane_addr + col_o + c0, ov);
-                tmem_ld_wait(ov);
-                if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+                for (int c0 = 0; c0 < D / 32; ++c0) {
+                    if (PRECISE) {
+                        float4* dst =
+                            reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + c0 * 32);
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(ov[q4 * 8 + 0]) * inv_l,
-                                          __uint_as_float(ov[q4 * 8 + 1]) * inv_l);
-                        w.y = pack_bf16x2(__uint_as_float(ov[q4 * 8 + 2]) * inv_l,
-                                          __uint_as_float(ov[q4 * 8 + 3]) * inv_l);
-                        w.z = pack_bf16x2(__uint_as_float(ov[q4 * 8 + 4]) * inv_l,
-                                          __uint_as_float(ov[q4 * 8 + 5]) * inv_l);
-                        w.w = pack_bf16x2(__uint_as_float(ov[q4 * 8 + 6]) * inv_l,
-                                          __uint_as_float(ov[q4 * 8 + 7]) * inv_l);
-                        dst[q4] = w;
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(__uint_as_float(ov[c0][q4 * 4 + 0]) * inv_l,
+                                                  __uint_as_float(ov[c0][q4 * 4 + 1]) * inv_l,
+                                                  __uint_as_float(ov[c0][q4 * 4 + 2]) * inv_l,
+                                                  __uint_as_float(ov[c0][q4 * 4 + 3]) * inv_l);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(
+                            static_cast<__nv_bfloat16*>(p.o) + orow + c0 * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(ov[c0][q4 * 8 + 0]) * inv_l,
+                                              __uint_as_float(ov[c0][q4 * 8 + 1]) * inv_l);
+                            w.y = pack_bf16x2(__uint_as_float(ov[c0][q4 * 8 + 2]) * inv_l,
+                                              __uint_as_float(ov[c0][q4 * 8 + 3]) * inv_l);
+                            w.z = pack_bf16x2(__uint_as_float(ov[c0][q4 * 8 + 4]) * inv_l,
+                                              __uint_as_float(ov[c0][q4 * 8 + 5]) * inv_l);
+                            w.w = pack_bf16x2(__uint_as_float(ov[c0][q4 * 8 + 6]) * inv_l,
+                                              __uint_as_float(ov[c0][q4 * 8 + 7]) * inv_l);
+                            dst[q4] = w;
+                        }
                     }
                 }
-            }
-            if (valid)
-                p.lse[(size_t)bh * p.N + row] =
+                p.lse[(size_t)wt.bh * p.N + row] =
                     (l > 0.0f) ? (m2 + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+            }
         }
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -262,32 +315,47 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_k);
                 tma_prefetch_desc(&tm_v);
-                mbar_arrive_expect_tx(&bar_q, kTiles * Cfg::kTileBytes);
-                for (int t = 0; t < kTiles; ++t)
-                    for (int c = 0; c < Cfg::kChunks; ++c)
-                        tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q, &bar_q,
-                                    c * 64, row_base + t * kBM, bh);
-                int issued = 0;
-                for (int j = 0; j < n_kv; ++j) {
-                    const int s = j % S, u = j / S;
-                    if (j >= S && !fa_wait(&bar_kv_empty[s], (u - 1) & 1, 10, wc)) break;
-                    mbar_arrive_expect_tx(&bar_k[s], Cfg::kTileBytes);
-                    for (int c = 0; c < Cfg::kChunks; ++c)
-                        tma_load_3d(sK + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_k, &bar_k[s],
-                                    c * 64, j * kBN, kv_bh);
-                    mbar_arrive_expect_tx(&bar_v[s], Cfg::kTileBytes);
-                    for (int c = 0; c < Cfg::kChunks; ++c)
-                        tma_load_3d(sV + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_v, &bar_v[s],
-                                    c * 64, j * kBN, kv_bh);
-                    issued = j + 1;
-                }
-                // Drain: on an abort, wait (bounded) for the copies still in flight
-                // so none lands after the CTA has exited.
-                if (abort_sh) {
-                    for (int j = max(0, issued - S); j < issued; ++j) {
-                        fa_wait(&bar_k[j % S], (j / S) & 1, 11, WaitCtx{p.status, nullptr});
-                        fa_wait(&bar_v[j % S], (j / S) & 1, 11, WaitCtx{p.status, nullptr});
+                uint32_t g = 0;          // K/V blocks loaded so far (ring position)
+                int lt = 0, q_loaded = -1;
+                bool ok = true;
+                for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+                    const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                    for (int t = 0; t < kTiles; ++t) {
+                        if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kChunks; ++c)
+                            tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
+                                        &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
                     }
+                    if (!ok) break;
+                    q_loaded = lt;
+                    for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
+                        const int s = g % S;
+                        const uint32_t u = g / S;
+                        if (g >= (uint32_t)S && !fa_wait(&bar_kv_empty[s], (u - 1) & 1, 10, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bar_k[s], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kChunks; ++c)
+                            tma_load_3d(sK + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_k,
+                                        &bar_k[s], c * 64, j * kBN, wt.kv_bh);
+                        mbar_arrive_expect_tx(&bar_v[s], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kChunks; ++c)
+                            tma_load_3d(sV + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_v,
+                                        &bar_v[s], c * 64, j * kBN, wt.kv_bh);
+                    }
+                }
+                // Drain: on an abort, wait (bounded) for the copies still in
+                // flight so none lands after the CTA has exited.
+                if (abort_sh) {
+                    const WaitCtx dc{p.status, nullptr};
+                    for (uint32_t x = (g > (uint32_t)S ? g - S : 0); x < g; ++x) {
+                        fa_wait(&bar_k[x % S], (x / S) & 1, 11, dc);
+                        fa_wait(&bar_v[x % S], (x / S) & 1, 11, dc);
+                    }
+                    if (q_loaded >= 0)
+                        for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 11, dc);
                 }
             }
         } else if (warp == kMmaWarp) {
@@ -295,41 +363,68 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
                 constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
                 const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
-                bool ok = fa_wait(&bar_q, 0, 20, wc) && fa_wait(&bar_k[0], 0, 21, wc);
-                if (ok) {
+                uint32_t g = 0;                     // K/V blocks consumed so far
+                uint32_t cp[kTiles] = {0, 0};       // P_t completions seen so far
+                bool ok = true;
+                int lt = 0;
+                auto issue_s = [&](int t, uint32_t kstage) {
+                    const uint32_t col = Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0);
+                    const uint32_t kb = sk + kstage * Cfg::kTileBytes;
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + col, kmajor_desc(sq + t * Cfg::kTileBytes, kk),
+                               kmajor_desc(kb, kk), idesc_s, kk > 0);
+                    mma_commit(&bar_s[t]);
+                };
+                for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+                    const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                    const int n_last = wt.n_kv[kTiles - 1];
+                    if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc) ||
+                        !fa_wait(&bar_k[g % S], (g / S) & 1, 21, wc)) { ok = false; break; }
                     tc_fence_after();
                     for (int t = 0; t < kTiles; ++t) {
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss(tmem + (Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0)), kmajor_desc(sq + t * Cfg::kTileBytes, kk),
-                                   kmajor_desc(sk, kk), idesc_s, kk > 0);
-                        mma_commit(&bar_s[t]);
+                        issue_s(t, g % S);
+                        if (wt.n_kv[t] == 1) mma_commit(&bar_q_free[t]);
                     }
-                }
-                for (int j = 0; ok && j < n_kv; ++j) {
-                    const int s = j % S, u = j / S;
-                    const bool next = j + 1 < n_kv;
-                    const int s1 = (j + 1) % S, u1 = (j + 1) / S;
-                    if (!fa_wait(&bar_v[s], u & 1, 22, wc)) { ok = false; break; }
-                    if (next && !fa_wait(&bar_k[s1], u1 & 1, 23, wc)) { ok = false; break; }
-                    for (int t = 0; t < kTiles; ++t) {
-                        if (!fa_wait(&bar_p[t], j & 1, 24 + t, wc)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t vb = sv + s * Cfg::kTileBytes;
-                        for (int kk = 0; kk < kBN / 16; ++kk)
-                            mma_ts(tmem + (Cfg::kColO0 + t * (Cfg::kColO1 - Cfg::kColO0)), tmem + (Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0)) + kk * 8, vmn_desc(vb, kk),
-                                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-                        if (next) {
-                            const uint32_t kb = sk + s1 * Cfg::kTileBytes;
-                            for (int kk = 0; kk < D / 16; ++kk)
-                                mma_ss(tmem + (Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0)), kmajor_desc(sq + t * Cfg::kTileBytes, kk),
-                                       kmajor_desc(kb, kk), idesc_s, kk > 0);
-                            mma_commit(&bar_s[t]);
-                        } else {
-                            mma_commit(&bar_o[t]);
+                    for (int j = 0; j < n_last; ++j) {
+                        const uint32_t gj = g + j;
+                        const int s = gj % S;
+                        const bool next = j + 1 < n_last;
+                        if (!fa_wait(&bar_v[s], (gj / S) & 1, 22, wc)) { ok = false; break; }
+                        if (next && !fa_wait(&bar_k[(gj + 1) % S], ((gj + 1) / S) & 1, 23, wc)) {
+                            ok = false;
+                            break;
                         }
+                        for (int t = 0; t < kTiles; ++t) {
+                            if (j >= wt.n_kv[t]) continue;
+                            if (!fa_wait(&bar_p[t], cp[t] & 1, 24 + t, wc)) { ok = false; break; }
+                            ++cp[t];
+                            if (j == 0 && lt > 0 &&
+                                !fa_wait(&bar_o_free[t], (lt - 1) & 1, 26 + t, wc)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t vb = sv + s * Cfg::kTileBytes;
+                            const uint32_t col_s = Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0);
+                            const uint32_t col_o = Cfg::kColO0 + t * (Cfg::kColO1 - Cfg::kColO0);
+                            for (int kk = 0; kk < kBN / 16; ++kk)
+                                mma_ts(tmem + col_o, tmem + col_s + kk * 8, vmn_desc(vb, kk), idesc_o,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                            if (PRECISE)
+                                for (int kk = 0; kk < kBN / 16; ++kk)
+                                    mma_ts(tmem + col_o, tmem + col_s + 64 + kk * 8, vmn_desc(vb, kk),
+                                           idesc_o, 1u);
+                            if (j + 1 < wt.n_kv[t]) {
+                                issue_s(t, (gj + 1) % S);
+                                if (j + 2 == wt.n_kv[t]) mma_commit(&bar_q_free[t]);
+                            } else {
+                                mma_commit(&bar_o[t]);
+                            }
+                        }
+                        if (!ok) break;
+                        mma_commit(&bar_kv_empty[s]);
                     }
-                    if (!ok) break;
-                    mma_commit(&bar_kv_empty[s]);
+                    g += n_last;
                 }
                 // Make sure no MMA is still writing TMEM when the CTA tears down.
                 if (!ok) {
@@ -352,17 +447,23 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PRECISE>
 cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdParams& p, int grid,
                          cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, CAUSAL>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, PRECISE>;
     static int configured_device = -1;   // attribute is per device; cheap to repeat
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             FwdCfg<D>::kSmemAlloc);
+        // The register split must fit in what the launch provides, or the
+        // setmaxnreg.inc of the softmax warps would wait forever.
+        cudaFuncAttributes attr;
+        cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+        if (e != cudaSuccess) return e;
+        if (attr.numRegs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 FwdCfg<D>::kSmemAlloc);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -373,7 +474,7 @@ cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& tq, const CUtensorMa
 }  // namespace
 
 cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void* v, void* o,
-                       float* lse, DeviceStatus* status, cudaStream_t stream) {
+                       float* lse, bool precise, DeviceStatus* status, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
     if (!make_tmap_bf16_3d(&tq, q, s.d, s.N, s.B * s.H, kBM) ||
         !make_tmap_bf16_3d(&tk, k, s.d, s.N, s.B * s.Hkv, kBN) ||
@@ -385,18 +486,30 @@ cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void*
     p.N = s.N;
     p.BH = s.B * s.H;
     p.n_mblk = (s.N + kTiles * kBM - 1) / (kTiles * kBM);
+    p.n_items = p.n_mblk * p.BH;
     p.causal = s.causal;
     p.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
-    p.o = static_cast<__nv_bfloat16*>(o);
+    p.o = o;
     p.lse = lse;
     p.status = status;
-    const int grid = p.n_mblk * p.BH;
+    // Persistent: one CTA per SM (at most one work item per CTA when there
+    // are fewer items than SMs).
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+    const int grid = p.n_items < sms ? p.n_items : sms;
     count_launch();
-    if (s.d == 128)
-        return s.causal ? launch_fwd_t<128, true>(s, tq, tk, tv, p, grid, stream)
-                        : launch_fwd_t<128, false>(s, tq, tk, tv, p, grid, stream);
-    return s.causal ? launch_fwd_t<64, true>(s, tq, tk, tv, p, grid, stream)
-                    : launch_fwd_t<64, false>(s, tq, tk, tv, p, grid, stream);
+    const bool c = s.causal != 0;
+    if (s.d == 128) {
+        if (precise)
+            return c ? launch_fwd_t<128, true, true>(s, tq, tk, tv, p, grid, stream)
+                     : launch_fwd_t<128, false, true>(s, tq, tk, tv, p, grid, stream);
+        return c ? launch_fwd_t<128, true, false>(s, tq, tk, tv, p, grid, stream)
+                 : launch_fwd_t<128, false, false>(s, tq, tk, tv, p, grid, stream);
+    }
+    if (precise)
+        return c ? launch_fwd_t<64, true, true>(s, tq, tk, tv, p, grid, stream)
+                 : launch_fwd_t<64, false, true>(s, tq, tk, tv, p, grid, stream);
+    return c ? launch_fwd_t<64, true, false>(s, tq, tk, tv, p, grid, stream)
+             : launch_fwd_t<64, false, false>(s, tq, tk, tv, p, grid, stream);
 }
 
 }  // namespace fa

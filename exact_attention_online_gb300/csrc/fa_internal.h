@@ -32,8 +32,8 @@ BwdWorkspace bwd_workspace_carve(void* base, const Shape& s);
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void* v, void* o,
-                       float* lse, DeviceStatus* status, cudaStream_t stream);
-cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, const void* dout,
+                       float* lse, bool precise, DeviceStatus* status, cudaStream_t stream);
+cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, const void* dout,
                                   const float* lse, const BwdWorkspace& ws,
                                   DeviceStatus* status, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const void* v,

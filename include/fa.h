@@ -83,6 +83,20 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
                  fa_stream_t stream);
 
 /*
+ * Forward with an fp32 output and a two-term P.  Same operation, layouts and
+ * errors as fa_fwd() except that o is fp32 [B][H][N][d] and that P enters the
+ * P V product as P_hi = bf16(P) plus P_lo = bf16(P - P_hi), so about 16
+ * significant bits of P reach the tensor core instead of 8.  fa_fwd() rounds
+ * P and O to bf16 (relative 2^-9 each), an error that grows with the
+ * magnitude of V and O (about 0.06 at |O| = 30); here the error is that of
+ * the fp32 accumulation.  Costs one extra P V MMA per key block.
+ * One launch of the forward kernel.
+ */
+FA_API fa_status fa_fwd_precise(const void* q, const void* k, const void* v, float* o,
+                                float* lse, int B, int H, int Hkv, int N, int d, int causal,
+                                float scale, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd() needs: D and a padded copy of LSE
  * (fp32 [B][H][Np]) and the fp32 dQ accumulator ([B][H][Np][d]), where Np is
  * N rounded up to 128.  Returns 0 for arguments fa_bwd() would reject.
@@ -104,6 +118,17 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
                  fa_stream_t stream);
 
 /*
+ * Backward after fa_fwd_precise(): identical to fa_bwd() except that o is the
+ * fp32 [B][H][N][d] output of fa_fwd_precise (used for D = rowsum(dO o O)).
+ * Gradients are bf16 as in fa_bwd().  Three kernel launches.
+ */
+FA_API fa_status fa_bwd_precise(const void* q, const void* k, const void* v, const float* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes,
+                                int B, int H, int Hkv, int N, int d, int causal, float scale,
+                                fa_stream_t stream);
+
+/*
  * Backward, stage 1 of 3: D_i = sum_c dO_ic O_ic (fp32), LSE copied into the
  * workspace in base-2 units with padding rows, and the fp32 dQ accumulator
  * zeroed.  One launch.
@@ -111,6 +136,12 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
 FA_API fa_status fa_bwd_preprocess(const void* o, const void* dout, const float* lse,
                             void* workspace, size_t workspace_bytes,
                             int B, int H, int Hkv, int N, int d, fa_stream_t stream);
+
+/* Stage 1 for an fp32 o from fa_fwd_precise().  One launch. */
+FA_API fa_status fa_bwd_preprocess_precise(const float* o, const void* dout, const float* lse,
+                                           void* workspace, size_t workspace_bytes,
+                                           int B, int H, int Hkv, int N, int d,
+                                           fa_stream_t stream);
 
 /*
  * Backward, stage 2 of 3: the main recomputation kernel.  One CTA per

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import exact_attention_online_gb300 as fa
-from _gpu import GRAD_REL_FRO, check_bwd_groups, f64, run_bwd, run_fwd
+from _gpu import GRAD_REL_FRO, check_bwd_groups, f64, run_bwd, run_fwd, stress
 from exact_attention_online_gb300.inputs import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -33,10 +33,12 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("precise", [False, True], ids=["bf16out", "precise"])
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
-def test_bwd_small_full(w):
+def test_bwd_small_full(w, precise):
+    """fa_bwd after fa_fwd, and fa_bwd_precise after fa_fwd_precise."""
     q, k, v, do = make_inputs(w)
-    _, _, dev = run_fwd(q, k, v, w.causal, w.scale)
+    _, _, dev = run_fwd(q, k, v, w.causal, w.scale, precise=precise)
     dq, dk, dv = run_bwd(dev, do, w.causal, w.scale)
     groups = [(b, g) for b in range(w.B) for g in range(w.Hkv)]
     check_bwd_groups(q, k, v, do, dq, dk, dv, w.causal, w.scale, groups)
@@ -82,12 +84,13 @@ FULL = ["mha_d64", "mha_d64_full", "gpt_long", "gqa"]
 @pytest.mark.slow
 @pytest.mark.parametrize("name", FULL)
 def test_bwd_full_size(name):
-    """Full workload sizes, same launches as the benchmark; the oracle checks
-    one (first) and one (last) key/value group in full (every query head of the
-    group, every row)."""
+    """Full workload sizes, same launches as the benchmark (the stress workload
+    with key channels x20 through the precise forward and backward); the oracle
+    checks one (first) and one (last) key/value group in full (every query head
+    of the group, every row)."""
     w = WORKLOADS[name]
     q, k, v, do = make_inputs(w)
-    _, _, dev = run_fwd(q, k, v, w.causal, w.scale)
+    _, _, dev = run_fwd(q, k, v, w.causal, w.scale, precise=stress(w))
     dq, dk, dv = run_bwd(dev, do, w.causal, w.scale)
     for t in (dq, dk, dv):
         assert torch.isfinite(t.float()).all()
