@@ -126,6 +126,20 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows, int 
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_f32_2d(CUtensorMap* map, const void* base, int inner, long long rows,
+                      int box_inner, int box_rows) {
+    if (!load_encode()) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 4};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 size_t bwd_workspace_bytes(const Shape& s) {
     const size_t rows = (size_t)s.B * s.H * padded_rows(s.N);
     return align256(rows * 4) * 2 + align256(rows * (size_t)s.d * 4);

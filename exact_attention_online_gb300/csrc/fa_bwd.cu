@@ -4,8 +4,9 @@
 // softmax attention: dP = dO V^T, D = rowsum(dO o O), dS = P o (dP - D),
 // dQ = scale dS K, dK = scale dS^T Q).
 //
-//   preprocess  D_i = <dO_i, O_i>, lse2_i = LSE_i * log2(e) with padded rows
-//               (+inf, so P = 0 there), dQ accumulator zeroed.
+//   preprocess  writes -D_i = -<dO_i, O_i> and -LSE_i * log2(e) (padded rows:
+//               -inf, so P = 0 there), both negated so that the main kernel
+//               adds them in paired fp32 FMAs; zeroes the dQ accumulator.
 //   dkdv        one CTA per (batch, kv head, block j of 128 keys).  K_j and V_j
 //               stay in shared memory; dK_j and dV_j accumulate in TMEM over
 //               every query head of the GQA group and every query block i that
@@ -14,9 +15,11 @@
 //                 P^T  = 2^(S^T c - lse2),  dS^T = P^T o (dP^T - D)  (threads)
 //                 dV  += P^T dO_i  (A = P^T in TMEM),  dK += dS^T Q_i  (SS)
 //                 d=128: dQ_i^T = K_j^T dS^T;  d=64: dQ_i = dS K_j    (SS)
-//               and the dQ partial is added into the fp32 accumulator with
-//               red.global (FlashAttention-2 review 2: the query-derivative
-//               update is shared between the workers of one query block).
+//               and the dQ partial is staged in shared memory and added into
+//               the fp32 accumulator by one bulk (d=128) or tensor (d=64)
+//               reduce per query block (FlashAttention-2 review 2: the
+//               query-derivative update is shared between the workers of one
+//               query block).
 //   dq_convert  dQ = bf16(scale * accumulator).
 //
 // Roles in dkdv: warps 0-3 compute (one key row, or for dQ^T one head-dim row,
@@ -91,7 +94,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using Cfg = BwdCfg<D>;
     constexpr int BR = Cfg::kBR;
     constexpr int HALF = BR / 2;                  // query columns per compute warp
@@ -168,15 +171,17 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!fa_wait_warp(&bar_full[st], (it >> 1) & 1, 60, wc) ||
                 !fa_wait_warp(&bar_s, it & 1, 61, wc)) { ok = false; break; }
             tc_fence_after();
-            const float* lse_s = sLSE + st * BR;
-            const float* del_s = sDel + st * BR;
+            const float* lse_s = sLSE + st * BR;     // -LSE * log2(e)
+            const float* del_s = sDel + st * BR;     // -D
             const int q0 = i * BR;
             const bool need_mask = (CAUSAL && q0 < jblk * kBN + kBN - 1) || (jblk * kBN + kBN > p.N);
             const int key_lim = CAUSAL ? key - q0 : -1;    // column e visible iff e >= key_lim
             const bool key_valid = key < p.N;
-            // P^T = 2^(S^T c - lse2), kept in fp32 for dS; bf16 copy into TMEM over
-            // this warp's own S^T columns (already read).
+            // P^T = 2^(S^T c - LSE log2 e), kept in fp32 for dS; bf16 copy into
+            // TMEM over this warp's own S^T columns (already read).  Two
+            // columns per paired-fp32 instruction.
             float pf[HALF];
+            const uint64_t c2 = f2(c, c);
 #pragma unroll
             for (int ch = 0; ch < HALF / 32; ++ch) {
                 uint32_t sr[32];
@@ -184,15 +189,22 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_ld_wait(sr);
                 uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int qe = cb + ch * 32 + e;
-                    float pe = ex2(fmaf(__uint_as_float(sr[e]), c, -lse_s[qe]));
-                    if (need_mask && (qe < key_lim || !key_valid)) pe = 0.0f;
-                    pf[ch * 32 + e] = pe;
+                for (int e2 = 0; e2 < 16; ++e2) {
+                    const int qe = cb + ch * 32 + 2 * e2;
+                    const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(lse_s + qe);
+                    float x0, x1;
+                    f2_split(f2_fma(f2(__uint_as_float(sr[2 * e2]), __uint_as_float(sr[2 * e2 + 1])),
+                                    c2, nl2),
+                             x0, x1);
+                    float p0 = ex2(x0), p1 = ex2(x1);
+                    if (need_mask) {
+                        if (qe < key_lim || !key_valid) p0 = 0.0f;
+                        if (qe + 1 < key_lim || !key_valid) p1 = 0.0f;
+                    }
+                    pf[ch * 32 + 2 * e2] = p0;
+                    pf[ch * 32 + 2 * e2 + 1] = p1;
+                    pk[e2] = pack_bf16x2(p0, p1);
                 }
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack_bf16x2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]);
                 tmem_st16(lane_addr + Cfg::kColS + cb + ch * 16, pk);
             }
             tmem_st_wait();
@@ -211,9 +223,13 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int qe = cb + ch * 32 + 2 * e;
-                    const float d0 = pf[ch * 32 + 2 * e] * (__uint_as_float(dpr[2 * e]) - del_s[qe]);
-                    const float d1 =
-                        pf[ch * 32 + 2 * e + 1] * (__uint_as_float(dpr[2 * e + 1]) - del_s[qe + 1]);
+                    const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(del_s + qe);
+                    float d0, d1;
+                    f2_split(f2_mul(f2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]),
+                                    f2_add(f2(__uint_as_float(dpr[2 * e]),
+                                              __uint_as_float(dpr[2 * e + 1])),
+                                           nd2)),
+                             d0, d1);
                     dsk[e] = pack_bf16x2(d0, d1);
                 }
                 const int qc = (cb + ch * 32) >> 6;       // 64-query chunk of the tile
@@ -299,37 +315,31 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     stg[(32 + e) * D + rl] = __uint_as_float(r1[e]);
                 }
             } else {
-                // dQ: lane = query row, column = head-dim index -> stg[row][0..63],
-                // 16-byte pieces in an order rotated by (lane & 7) so that eight
-                // neighbouring lanes hit eight different bank groups.
-                float v[64];
+                // dQ: lane = query row, column = head-dim index.  Two boxes of
+                // 32 columns, 128-byte swizzled (16-byte piece u of row r at
+                // u ^ (r & 7)), so eight neighbouring rows write eight
+                // different bank groups; a tensor reduce undoes the swizzle.
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    v[e] = __uint_as_float(r0[e]);
-                    v[32 + e] = __uint_as_float(r1[e]);
+                for (int box = 0; box < 2; ++box) {
+                    uint8_t* rowp = reinterpret_cast<uint8_t*>(stg) + box * (128 * 128) + rl * 128;
+                    const uint32_t* src = box ? r1 : r0;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<uint4*>(rowp + ((u ^ (rl & 7)) * 16)) =
+                            make_uint4(src[4 * u], src[4 * u + 1], src[4 * u + 2], src[4 * u + 3]);
                 }
-                const int rot = lane & 7;
-#pragma unroll
-                for (int bit = 0; bit < 3; ++bit) {     // v <- v rotated left by rot*4
-                    const int sh = (1 << bit) * 4;
-                    const bool doit = (rot >> bit) & 1;
-                    float t[64];
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) t[e] = v[(e + sh) & 63];
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) v[e] = doit ? t[e] : v[e];
-                }
-                float4* rowp = reinterpret_cast<float4*>(stg + rl * D);
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    rowp[(u + rot) & 15] =
-                        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
             }
             fence_proxy_async_smem();
             named_bar_sync(1, kReadoutThreads);
             if (leader) {
-                bulk_reduce_add_f32(p.dq_acc + ((size_t)bh * p.Np + (size_t)i * BR) * D, stg,
-                                    BR * D * 4);
+                if (D == 128) {
+                    bulk_reduce_add_f32(p.dq_acc + ((size_t)bh * p.Np + (size_t)i * BR) * D, stg,
+                                        BR * D * 4);
+                } else {
+                    const int y = bh * p.Np + i * BR;
+                    tma_reduce_add_2d(&tm_dq, stg, 0, y);
+                    tma_reduce_add_2d(&tm_dq, reinterpret_cast<uint8_t*>(stg) + 128 * 128, 32, y);
+                }
                 bulk_commit_group();
             }
         }
@@ -449,7 +459,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
 }
 
-// D_i = <dO_i, O_i>, lse2 = LSE * log2(e) (+inf on padded rows), accumulator = 0.
+// -D_i = -<dO_i, O_i>, -LSE * log2(e) (-inf on padded rows), accumulator = 0.
 // One warp per row, grid-stride over the B*H*Np rows.  O is bf16, or fp32 when
 // it comes from the precise forward.
 template <int D, typename OT>
@@ -496,8 +506,8 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
-            delta[r] = acc;
-            lse2[r] = (i < N) ? lse[bh * N + i] * 1.4426950408889634f : CUDART_INF_F;
+            delta[r] = -acc;
+            lse2[r] = (i < N) ? -lse[bh * N + i] * 1.4426950408889634f : -CUDART_INF_F;
         }
         float4* z = reinterpret_cast<float4*>(dq_acc + r * D);
         for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -552,8 +562,8 @@ int grid_for(long long work_items, int per_block) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdParams& p, int grid,
-                          cudaStream_t stream) {
+                          const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                          int grid, cudaStream_t stream) {
     auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
     static int configured_device = -1;
     int dev = 0;
@@ -570,7 +580,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    kern<<<grid, kThreads, BwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, tdo, p);
+    kern<<<grid, kThreads, BwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, tdo, tdq, p);
     return cudaGetLastError();
 }
 
@@ -609,11 +619,12 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
                             const void* dout, void* dk, void* dv, const BwdWorkspace& ws,
                             DeviceStatus* status, cudaStream_t stream) {
     const int br = (s.d == 128) ? BwdCfg<128>::kBR : BwdCfg<64>::kBR;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_tmap_bf16_3d(&tq, q, s.d, s.N, s.B * s.H, br) ||
         !make_tmap_bf16_3d(&tdo, dout, s.d, s.N, s.B * s.H, br) ||
         !make_tmap_bf16_3d(&tk, k, s.d, s.N, s.B * s.Hkv, kBN) ||
-        !make_tmap_bf16_3d(&tv, v, s.d, s.N, s.B * s.Hkv, kBN))
+        !make_tmap_bf16_3d(&tv, v, s.d, s.N, s.B * s.Hkv, kBN) ||
+        !make_tmap_f32_2d(&tdq, ws.dq_acc, s.d, (long long)s.B * s.H * padded_rows(s.N), 32, br))
         return cudaErrorInvalidValue;
     BwdParams p;
     p.H = s.H;
@@ -634,10 +645,10 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     const int grid = n_kblk * s.B * s.Hkv;
     count_launch();
     if (s.d == 128)
-        return s.causal ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, p, grid, stream)
-                        : launch_dkdv_t<128, false>(tq, tk, tv, tdo, p, grid, stream);
-    return s.causal ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, p, grid, stream)
-                    : launch_dkdv_t<64, false>(tq, tk, tv, tdo, p, grid, stream);
+        return s.causal ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
+                        : launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdq, p, grid, stream);
+    return s.causal ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
+                    : launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdq, p, grid, stream);
 }
 
 cudaError_t launch_bwd_dq_convert(const Shape& s, const BwdWorkspace& ws, void* dq,

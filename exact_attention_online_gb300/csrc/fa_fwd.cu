@@ -3,13 +3,17 @@
 // Softmax to FlashAttention" and "FlashAttention"; FlashAttention-2 review
 // thread, author answers on non-matmul FLOPs and on Figure 2).
 //
-// One CTA owns two 128-row query tiles (t = 0, 1) of one (batch, head) and
-// streams 128-key K/V tiles through a shared-memory ring:
-//   warp 8      TMA producer: Q tiles once, then K_j, V_j into the ring.
+// Persistent grid, one CTA per SM.  A work item is two 128-row query tiles
+// (t = 0, 1) of one (batch, head); CTA c takes items c, c + gridDim.x, ...
+// (longest causal items first) and streams 128-key K and V tiles through two
+// shared-memory rings:
+//   warps 8, 10, 11  TMA producers of K_j, V_j and the Q tiles.  K_j is
+//               released when both S MMAs that read it are issued, V_j after
+//               both P V MMAs, so K loads run a whole block ahead.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA),
 //               O_t += P_t V_j with P_t read from TMEM (TS MMA).
 //   warps 0-3   softmax for tile 0, warps 4-7 for tile 1: one query row per
-//               thread (warps 10-11 are idle).  While one group does its softmax the tensor core
+//               thread.  While one group does its softmax the tensor core
 //               runs the other tile's MMAs.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t (bf16 pairs) overwrites the
 // first half of S_t; the MMA that next writes S_t is issued after the MMA
@@ -40,8 +44,10 @@ constexpr int kBN = 128;          // keys per K/V tile
 constexpr int kTiles = 2;         // query tiles per CTA
 constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 12 * 32;   // 3 warpgroups: softmax 0, softmax 1, control
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;         // warps 10-11 only take part in set-up and teardown
+constexpr int kProducerWarp = 8;    // K tiles
+constexpr int kMmaWarp = 9;
+constexpr int kVProducerWarp = 10;  // V tiles
+constexpr int kQProducerWarp = 11;  // Q tiles
 // Register split (setmaxnreg): the launch gives 384 x 168; the control
 // warpgroup drops to 72 so each softmax thread can hold a full 128-score row:
 // 128 x 72 + 256 x 216 = 64512 <= 384 x 168 = 64512.
@@ -52,14 +58,17 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 template <int D>
 struct FwdCfg {
-    static constexpr int kStages = (D == 128) ? 2 : 3;
+    // K and V have rings of their own: K is released as soon as both S MMAs of
+    // a block are issued, V after both P V MMAs.
+    static constexpr int kStagesK = (D == 128) ? 3 : 4;
+    static constexpr int kStagesV = (D == 128) ? 2 : 3;
     static constexpr int kTileBytes = kBM * D * 2;          // one Q, K or V tile
     static constexpr int kChunks = D / 64;                  // 128-byte swizzle chunks
     static constexpr int kChunkBytes = 128 * 128;           // 128 rows x 128 bytes
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kTiles * kTileBytes;
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kOffV + kStages * kTileBytes;
+    static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
+    static constexpr int kSmemBytes = kOffV + kStagesV * kTileBytes;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;    // alignment slack
     // TMEM columns
     static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
@@ -110,11 +119,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     using Cfg = FwdCfg<D>;
-    constexpr int S = Cfg::kStages;
+    constexpr int SK = Cfg::kStagesK, SV = Cfg::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_k[S], bar_v[S], bar_kv_empty[S];
+    __shared__ uint64_t bar_k[SK], bar_k_empty[SK], bar_v[SV], bar_v_empty[SV];
     __shared__ uint64_t bar_q[kTiles], bar_q_free[kTiles];
     __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_o[kTiles], bar_o_free[kTiles];
     __shared__ uint32_t tmem_base_sh;
@@ -124,10 +133,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < SK; ++s) {
             mbar_init(&bar_k[s], 1);
+            mbar_init(&bar_k_empty[s], 1);
+        }
+        for (int s = 0; s < SV; ++s) {
             mbar_init(&bar_v[s], 1);
-            mbar_init(&bar_kv_empty[s], 1);
+            mbar_init(&bar_v_empty[s], 1);
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(&bar_q[t], 1);
@@ -200,15 +212,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     for (int e = 0; e < kBN; ++e)
                         if (e > lim_causal || e >= lim_n) sv[e] = -CUDART_INF_F;
                 }
-                float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+                // Row max: three-input max, eight independent chains.
+                float mx8[8];
 #pragma unroll
-                for (int e = 4; e < kBN; e += 4) {
-                    mx4[0] = fmaxf(mx4[0], sv[e]);
-                    mx4[1] = fmaxf(mx4[1], sv[e + 1]);
-                    mx4[2] = fmaxf(mx4[2], sv[e + 2]);
-                    mx4[3] = fmaxf(mx4[3], sv[e + 3]);
-                }
-                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(sv[2 * u], sv[2 * u + 1]);
+#pragma unroll
+                for (int e = 16; e < kBN; e += 16)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) mx8[u] = fmax3(mx8[u], sv[e + 2 * u], sv[e + 2 * u + 1]);
+                const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                                       fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 const float mx2 = mx * c;
                 const bool need = mx2 > m2 + kRescaleThreshold;
                 if (__any_sync(0xffffffffu, need)) {
@@ -230,16 +243,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     m2 = m_new;
                 }
                 const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
-                float rs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                // p = 2^(s c - m): exponent argument two lanes per instruction,
+                // row sum in four paired accumulators.
+                const uint64_t c2 = f2(c, c), negm2 = f2(-m_use, -m_use);
+                uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t pk[32], pl[32];
 #pragma unroll
                     for (int e2 = 0; e2 < 32; ++e2) {
                         const int e = hh * 64 + 2 * e2;
-                        const float p0 = ex2(fmaf(sv[e], c, -m_use));
-                        const float p1 = ex2(fmaf(sv[e + 1], c, -m_use));
-                        rs4[e2 & 3] += p0 + p1;
+                        float x0, x1;
+                        f2_split(f2_fma(f2(sv[e], sv[e + 1]), c2, negm2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        acc2[e2 & 3] = f2_add(acc2[e2 & 3], f2(p0, p1));
                         pk[e2] = pack_bf16x2(p0, p1);
                         if (PRECISE) {
                             // second term: what bf16 rounding of p left out
@@ -251,7 +268,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     tmem_st32(lane_addr + col_s + hh * 32, pk);
                     if (PRECISE) tmem_st32(lane_addr + col_s + 64 + hh * 32, pl);
                 }
-                l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+                {
+                    float a0, a1;
+                    f2_split(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), a0, a1);
+                    l += a0 + a1;
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bar_p[t]);
@@ -310,53 +331,73 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-        if (warp == kProducerWarp) {
-            if (lane == 0) {
-                tma_prefetch_desc(&tm_q);
-                tma_prefetch_desc(&tm_k);
-                tma_prefetch_desc(&tm_v);
-                uint32_t g = 0;          // K/V blocks loaded so far (ring position)
-                int lt = 0, q_loaded = -1;
-                bool ok = true;
-                for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-                    const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                    for (int t = 0; t < kTiles; ++t) {
-                        if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
-                        for (int c = 0; c < Cfg::kChunks; ++c)
-                            tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
-                                        &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
+        if (warp == kProducerWarp && lane == 0) {
+            // ------------------------------------------------- K producer
+            tma_prefetch_desc(&tm_k);
+            uint32_t g = 0;              // K blocks loaded so far (ring position)
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+                const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
+                    const int s = g % SK;
+                    if (g >= (uint32_t)SK && !fa_wait(&bar_k_empty[s], ((g / SK) - 1) & 1, 10, wc)) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
-                    q_loaded = lt;
-                    for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
-                        const int s = g % S;
-                        const uint32_t u = g / S;
-                        if (g >= (uint32_t)S && !fa_wait(&bar_kv_empty[s], (u - 1) & 1, 10, wc)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(&bar_k[s], Cfg::kTileBytes);
-                        for (int c = 0; c < Cfg::kChunks; ++c)
-                            tma_load_3d(sK + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_k,
-                                        &bar_k[s], c * 64, j * kBN, wt.kv_bh);
-                        mbar_arrive_expect_tx(&bar_v[s], Cfg::kTileBytes);
-                        for (int c = 0; c < Cfg::kChunks; ++c)
-                            tma_load_3d(sV + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_v,
-                                        &bar_v[s], c * 64, j * kBN, wt.kv_bh);
-                    }
+                    mbar_arrive_expect_tx(&bar_k[s], Cfg::kTileBytes);
+                    for (int c = 0; c < Cfg::kChunks; ++c)
+                        tma_load_3d(sK + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_k, &bar_k[s],
+                                    c * 64, j * kBN, wt.kv_bh);
                 }
-                // Drain: on an abort, wait (bounded) for the copies still in
-                // flight so none lands after the CTA has exited.
-                if (abort_sh) {
-                    const WaitCtx dc{p.status, nullptr};
-                    for (uint32_t x = (g > (uint32_t)S ? g - S : 0); x < g; ++x) {
-                        fa_wait(&bar_k[x % S], (x / S) & 1, 11, dc);
-                        fa_wait(&bar_v[x % S], (x / S) & 1, 11, dc);
+            }
+            if (abort_sh) {   // drain the copies still in flight (bounded)
+                const WaitCtx dc{p.status, nullptr};
+                for (uint32_t x = (g > (uint32_t)SK ? g - SK : 0); x < g; ++x)
+                    fa_wait(&bar_k[x % SK], (x / SK) & 1, 11, dc);
+            }
+        } else if (warp == kVProducerWarp && lane == 0) {
+            // ------------------------------------------------- V producer
+            tma_prefetch_desc(&tm_v);
+            uint32_t g = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+                const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
+                    const int s = g % SV;
+                    if (g >= (uint32_t)SV && !fa_wait(&bar_v_empty[s], ((g / SV) - 1) & 1, 13, wc)) {
+                        ok = false;
+                        break;
                     }
-                    if (q_loaded >= 0)
-                        for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 11, dc);
+                    mbar_arrive_expect_tx(&bar_v[s], Cfg::kTileBytes);
+                    for (int c = 0; c < Cfg::kChunks; ++c)
+                        tma_load_3d(sV + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_v, &bar_v[s],
+                                    c * 64, j * kBN, wt.kv_bh);
                 }
+            }
+            if (abort_sh) {
+                const WaitCtx dc{p.status, nullptr};
+                for (uint32_t x = (g > (uint32_t)SV ? g - SV : 0); x < g; ++x)
+                    fa_wait(&bar_v[x % SV], (x / SV) & 1, 14, dc);
+            }
+        } else if (warp == kQProducerWarp && lane == 0) {
+            // ------------------------------------------------- Q producer
+            tma_prefetch_desc(&tm_q);
+            int lt = 0, q_loaded = -1;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+                const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                for (int t = 0; t < kTiles; ++t) {
+                    if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
+                    for (int c = 0; c < Cfg::kChunks; ++c)
+                        tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
+                                    &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
+                }
+                if (ok) q_loaded = lt;
+            }
+            if (abort_sh && q_loaded >= 0) {
+                const WaitCtx dc{p.status, nullptr};
+                for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 15, dc);
             }
         } else if (warp == kMmaWarp) {
             if (lane == 0) {
@@ -379,21 +420,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const FwdTile wt = fwd_tile(item, p, CAUSAL);
                     const int n_last = wt.n_kv[kTiles - 1];
                     if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc) ||
-                        !fa_wait(&bar_k[g % S], (g / S) & 1, 21, wc)) { ok = false; break; }
+                        !fa_wait(&bar_k[g % SK], (g / SK) & 1, 21, wc)) { ok = false; break; }
                     tc_fence_after();
                     for (int t = 0; t < kTiles; ++t) {
-                        issue_s(t, g % S);
+                        issue_s(t, g % SK);
                         if (wt.n_kv[t] == 1) mma_commit(&bar_q_free[t]);
                     }
+                    mma_commit(&bar_k_empty[g % SK]);      // K block 0 read by both S MMAs
                     for (int j = 0; j < n_last; ++j) {
                         const uint32_t gj = g + j;
-                        const int s = gj % S;
-                        const bool next = j + 1 < n_last;
-                        if (!fa_wait(&bar_v[s], (gj / S) & 1, 22, wc)) { ok = false; break; }
-                        if (next && !fa_wait(&bar_k[(gj + 1) % S], ((gj + 1) / S) & 1, 23, wc)) {
-                            ok = false;
-                            break;
-                        }
+                        if (!fa_wait(&bar_v[gj % SV], (gj / SV) & 1, 22, wc)) { ok = false; break; }
+                        bool k_next_ready = false;
                         for (int t = 0; t < kTiles; ++t) {
                             if (j >= wt.n_kv[t]) continue;
                             if (!fa_wait(&bar_p[t], cp[t] & 1, 24 + t, wc)) { ok = false; break; }
@@ -404,7 +441,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t vb = sv + s * Cfg::kTileBytes;
+                            const uint32_t vb = sv + (gj % SV) * Cfg::kTileBytes;
                             const uint32_t col_s = Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0);
                             const uint32_t col_o = Cfg::kColO0 + t * (Cfg::kColO1 - Cfg::kColO0);
                             for (int kk = 0; kk < kBN / 16; ++kk)
@@ -415,14 +452,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                     mma_ts(tmem + col_o, tmem + col_s + 64 + kk * 8, vmn_desc(vb, kk),
                                            idesc_o, 1u);
                             if (j + 1 < wt.n_kv[t]) {
-                                issue_s(t, (gj + 1) % S);
+                                // K_{j+1} is waited for only now, after this PV.
+                                if (!k_next_ready) {
+                                    if (!fa_wait(&bar_k[(gj + 1) % SK], ((gj + 1) / SK) & 1, 23, wc)) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    tc_fence_after();
+                                    k_next_ready = true;
+                                }
+                                issue_s(t, (gj + 1) % SK);
                                 if (j + 2 == wt.n_kv[t]) mma_commit(&bar_q_free[t]);
                             } else {
                                 mma_commit(&bar_o[t]);
                             }
                         }
                         if (!ok) break;
-                        mma_commit(&bar_kv_empty[s]);
+                        mma_commit(&bar_v_empty[gj % SV]);            // V_j read by both PVs
+                        if (j + 1 < n_last) mma_commit(&bar_k_empty[(gj + 1) % SK]);   // K_{j+1} by both S
                     }
                     g += n_last;
                 }

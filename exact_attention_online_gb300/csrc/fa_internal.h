@@ -23,8 +23,8 @@ inline int padded_rows(int N) { return (N + kRowPad - 1) / kRowPad * kRowPad; }
 // Backward workspace: [lse2 fp32 B*H*Np][D fp32 B*H*Np][dQacc fp32 B*H*Np*d],
 // each region 256-byte aligned.
 struct BwdWorkspace {
-    float* lse2;   // LSE * log2(e), padded rows = +inf
-    float* delta;  // D = rowsum(dO * O), padded rows = 0
+    float* lse2;   // -LSE * log2(e), padded rows = -inf
+    float* delta;  // -D = -rowsum(dO * O), padded rows = 0
     float* dq_acc; // fp32 accumulator of dQ / scale
 };
 size_t bwd_workspace_bytes(const Shape& s);
@@ -49,6 +49,11 @@ cudaError_t launch_watchdog_selftest(long long timeout_ns, DeviceStatus* status,
 // box and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows, int outer,
                        int box_rows);
+
+// 2-D map over an fp32 matrix [rows][inner] with a {box_inner, box_rows} box
+// and 128-byte swizzle (box_inner * 4 <= 128).
+bool make_tmap_f32_2d(CUtensorMap* map, const void* base, int inner, long long rows,
+                      int box_inner, int box_rows);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

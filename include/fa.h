@@ -87,9 +87,10 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
  * errors as fa_fwd() except that o is fp32 [B][H][N][d] and that P enters the
  * P V product as P_hi = bf16(P) plus P_lo = bf16(P - P_hi), so about 16
  * significant bits of P reach the tensor core instead of 8.  fa_fwd() rounds
- * P and O to bf16 (relative 2^-9 each), an error that grows with the
- * magnitude of V and O (about 0.06 at |O| = 30); here the error is that of
- * the fp32 accumulation.  Costs one extra P V MMA per key block.
+ * P and O to bf16 (unit roundoff 2^-8 each), an error that grows with the
+ * magnitude of V and O (up to 0.06 at |O| = 30, already 0.016 for |O| in
+ * [4, 8)); here the error is that of the fp32 accumulation.  Costs one extra
+ * P V MMA per key block.
  * One launch of the forward kernel.
  */
 FA_API fa_status fa_fwd_precise(const void* q, const void* k, const void* v, float* o,

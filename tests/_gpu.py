@@ -57,10 +57,11 @@ def rel_fro(a, ref):
 
 
 def bf16_output_bound(vh, ro):
-    """Error bound of the bf16-output forward: the benchmark spec 1e-2 plus the bf16
-    rounding of P (relative 2^-9, so |dO| <= 2^-9 max|V|) and of O itself
-    (2^-9 |O|).  Used only for inputs whose values reach tens (outliers)."""
-    return O_MAX_ABS + 2.0 ** -9 * (np.abs(vh).max() + np.abs(ro))
+    """Error bound of the bf16-output forward: the 1e-2 of the parity bar plus
+    the bf16 rounding of P (unit roundoff 2^-8, so |dO| <= 2^-8 max|V|) and of
+    O itself (2^-8 |O|).  Used only for the stress inputs whose values reach
+    magnitudes where bf16 rounding alone exceeds 1e-2."""
+    return O_MAX_ABS + 2.0 ** -8 * (np.abs(vh).max() + np.abs(ro))
 
 
 def check_fwd_heads(q, k, v, o, lse, causal, scale, heads, rows=None, bf16_bound=False):
