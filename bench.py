@@ -72,10 +72,8 @@ def load_peaks():
 
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    from exact_attention_online_gb300.replicas import dist_env as _env
+    return _env()
 
 
 class ClockSampler:
@@ -221,6 +219,7 @@ def run_native(args, w):
     import torch.distributed as dist
 
     import exact_attention_online_gb300 as fa
+    from exact_attention_online_gb300 import replicas
     from exact_attention_online_gb300.inputs import make_inputs
     from exact_attention_online_gb300.measure import attention_flops
 
@@ -234,7 +233,7 @@ def run_native(args, w):
     peaks = load_peaks()
 
     # Each rank draws its own batch (weak scaling: independent shards).
-    q, k, v, do = make_inputs(w.with_(seed=w.seed + 7919 * rank))
+    q, k, v, do = make_inputs(replicas.rank_workload(w, rank))
     B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     fwd_only = "bwd" not in w.passes          # the long-context sweep is forward only
@@ -321,14 +320,10 @@ def run_native(args, w):
     st = fa.fa_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
-    ms_total = t0.elapsed_time(t1)
-    if ws > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = replicas.max_over_ranks(t0.elapsed_time(t1), dev)
     ms_step = ms_total / args.steps
     flops_step = attention_flops(w, "fwd" if fwd_only else "fwd_bwd")
-    value = flops_step * args.steps * ws / (ms_total * 1e-3) / 1e12
+    value = replicas.whole_job_rate(flops_step, args.steps, ws, ms_total) / 1e12
 
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
     dkdv_ms = statistics.mean(a.elapsed_time(b) for a, b in dkdv_ev) if dkdv_ev else 0.0
@@ -395,12 +390,9 @@ def run_native(args, w):
             e2e_step()
         b.record(stream)
         barrier()
-        e_ms = a.elapsed_time(b)
-        if ws > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": flops_step * e2e_steps * ws / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e_ms = replicas.max_over_ranks(a.elapsed_time(b), dev)
+        e2e = {"value": replicas.whole_job_rate(flops_step, e2e_steps, ws, e_ms) / 1e12,
+               "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / e2e_steps}
 
