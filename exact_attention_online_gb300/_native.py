@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfa.so")
 
-SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu"]
+SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"]
 HEADERS = ["sm103_ptx.cuh", "fa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -95,6 +95,9 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_bwd_dkdv.restype = i
     L.fa_bwd_dq_convert.argtypes = [vp, sz, vp, i, i, i, i, i, f, vp]
     L.fa_bwd_dq_convert.restype = i
+    L.fa_bwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
+                                        vp]
+    L.fa_bwd_static_scratch.restype = i
     L.fa_device_status.argtypes = [vp]
     L.fa_device_status.restype = i
     L.fa_device_status_detail.argtypes = [ctypes.POINTER(i), ctypes.POINTER(i)]
@@ -123,5 +126,6 @@ def lib() -> ctypes.CDLL:
 
 # Every symbol include/fa.h declares.
 EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_precise",
-           "fa_bwd_preprocess", "fa_bwd_preprocess_precise", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_device_status", "fa_device_status_detail",
+           "fa_bwd_preprocess", "fa_bwd_preprocess_precise", "fa_bwd_dkdv", "fa_bwd_dq_convert",
+           "fa_bwd_static_scratch", "fa_device_status", "fa_device_status_detail",
            "fa_status_string", "fa_kernel_launches", "fa_watchdog_selftest"]

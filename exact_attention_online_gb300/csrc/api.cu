@@ -107,6 +107,22 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// For entry points defined in other files: the same argument checks as
+// fa_bwd() (without the workspace) and the same per-device set-up.
+fa_status validate_bwd_args(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, const void* dq, const void* dk,
+                            const void* dv, int B, int H, int Hkv, int N, int d, float scale) {
+    return first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                        check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(dout), check_ptr(lse),
+                        check_ptr(dq), check_ptr(dk), check_ptr(dv)});
+}
+
+fa_status ready_device(int* dev, DeviceStatus** status) {
+    const fa_status st = device_ready(dev);
+    if (st == FA_OK) *status = g_status_ptr[*dev];
+    return st;
+}
+
 int device_sm_count() {
     const int dev = current_device();
     return dev < 0 ? 0 : g_sm_count[dev];

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "fa.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -60,5 +61,12 @@ int device_sm_count();
 
 // Counts one kernel launch for fa_kernel_launches().
 void count_launch();
+
+// Argument checks of fa_bwd() (without the workspace) and the per-device
+// set-up (sm_103 check, status word), for entry points in other files.
+fa_status validate_bwd_args(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, const void* dq, const void* dk,
+                            const void* dv, int B, int H, int Hkv, int N, int d, float scale);
+fa_status ready_device(int* dev, DeviceStatus** status);
 
 }  // namespace fa

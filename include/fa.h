@@ -162,6 +162,28 @@ FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes
                             fa_stream_t stream);
 
 /*
+ * Backward without a workspace argument, for callers that cannot allocate
+ * device memory (a runtime that owns all device memory in a fixed pool, a
+ * latency-critical loop that must not risk the synchronisation cudaMalloc can
+ * cause, a plugin without access to the host application's allocator).  The
+ * pages have no counterpart to this; it is a deployment convenience.
+ * Same operation, arguments (minus workspace) and results as fa_bwd().  The
+ * scratch fa_bwd() takes from the caller lives instead in one fixed 32 MiB
+ * array in device memory owned by the library; every GPU that loads the
+ * library holds it until the process exits.  Calls whose
+ * fa_bwd_workspace_size() exceeds 32 MiB return FA_ERR_WORKSPACE.  All calls
+ * on a device share the array: calls that overlap on the GPU race, so order
+ * them on one stream.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Allocates nothing.  Three launches.
+ */
+FA_API fa_status fa_bwd_static_scratch(const void* q, const void* k, const void* v,
+                                       const void* o, const void* dout, const float* lse,
+                                       void* dq, void* dk, void* dv,
+                                       int B, int H, int Hkv, int N, int d, int causal,
+                                       float scale, fa_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device status word of the
  * current device: FA_OK, or the first error a kernel recorded (for example
  * FA_ERR_TIMEOUT when a bounded wait ran out).  Returns FA_ERR_CUDA if the
