@@ -44,10 +44,10 @@ constexpr int kMmaWarp = 9;
 constexpr int kReadoutWarp0 = 12;
 constexpr int kReadoutThreads = 128;
 // Register split (setmaxnreg) of the 512 x 128 launch registers:
-// 256 x 176 + 128 x 96 + 128 x 56 = 64512 <= 65536.
-constexpr int kRegsCompute = 176;
+// 256 x 160 + 128 x 96 + 128 x 96 = 65536.
+constexpr int kRegsCompute = 160;
 constexpr int kRegsReadout = 96;
-constexpr int kRegsControl = 56;
+constexpr int kRegsControl = 96;
 constexpr int kRegsNeeded = 256 * kRegsCompute + 128 * kRegsReadout + 128 * kRegsControl;
 
 template <int D>
@@ -82,13 +82,6 @@ struct BwdParams {
     __nv_bfloat16* dv;
     DeviceStatus* status;
 };
-
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, int chunk_bytes) {
-    return sdesc_sw128(base + (kk >> 2) * chunk_bytes + (kk & 3) * 32, 16, 1024);
-}
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk, int lbo) {
-    return sdesc_sw128(base + kk * 2048, lbo, 1024);
-}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -387,18 +380,23 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
                 const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
                                sdo = smem_u32(sDO), sds = smem_u32(sDS);
+                // Descriptors are built once per operand tile and stepped by
+                // constants, keeping the issuing thread's work between MMAs small.
+                const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
                 auto issue_s = [&](int st) {      // S^T = K_j Q_i^T
-                    const uint32_t q_ = sq + st * Cfg::kQBytes;
+                    const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
+#pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColS, kdesc(sk, kk, kBN * 128), kdesc(q_, kk, BR * 128),
-                               id_s, kk > 0);
+                        mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
+                               qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
                     mma_commit(&bar_s);
                 };
                 auto issue_dp = [&](int st) {     // dP^T = V_j dO_i^T
-                    const uint32_t do_ = sdo + st * Cfg::kQBytes;
+                    const uint64_t dod = sdesc_sw128(sdo + st * Cfg::kQBytes, 16, 1024);
+#pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDP, kdesc(sv, kk, kBN * 128),
-                               kdesc(do_, kk, BR * 128), id_s, kk > 0);
+                        mma_ss(tmem + Cfg::kColDP, vd + kmajor_step(kk, kBN * 128),
+                               dod + kmajor_step(kk, BR * 128), id_s, kk > 0);
                     mma_commit(&bar_dp);
                 };
                 bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
@@ -415,10 +413,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     // sits in the S^T columns of the warps of half h)
                     if (!fa_wait(&bar_p, it & 1, 52, wc)) { ok = false; break; }
                     tc_fence_after();
+                    const uint64_t dod_mn = sdesc_sw128(do_, BR * 128, 1024);
+#pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk) {
                         const int qs = kk * 16;
                         const uint32_t pcol = Cfg::kColS + (qs / HALF) * HALF + (qs % HALF) / 2;
-                        mma_ts(tmem + Cfg::kColDV, tmem + pcol, mndesc(do_, kk, BR * 128), id_kv,
+                        mma_ts(tmem + Cfg::kColDV, tmem + pcol, dod_mn + mnmajor_step(kk), id_kv,
                                (it > 0 || kk > 0) ? 1u : 0u);
                     }
                     if (next) {
@@ -429,17 +429,23 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     // dK += dS^T Q_i
                     if (!fa_wait(&bar_ds, it & 1, 55, wc)) { ok = false; break; }
                     tc_fence_after();
+                    const uint64_t dsd = sdesc_sw128(sds, 16, 1024);
+                    const uint64_t qd_mn = sdesc_sw128(q_, BR * 128, 1024);
+#pragma unroll
                     for (int kk = 0; kk < BR / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDK, kdesc(sds, kk, kBN * 128), mndesc(q_, kk, BR * 128),
-                               id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                        mma_ss(tmem + Cfg::kColDK, dsd + kmajor_step(kk, kBN * 128),
+                               qd_mn + mnmajor_step(kk), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&bar_empty[st]);
                     // dQ partial (K dimension = the 128 keys)
                     if (it > 0 && !fa_wait(&bar_dq_free, (it - 1) & 1, 53, wc)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_ = (D == 128) ? sk : sds;
                     const uint32_t b_ = (D == 128) ? sds : sk;
+                    const uint64_t ad_mn = sdesc_sw128(a_, kBN * 128, 1024);
+                    const uint64_t bd_mn = sdesc_sw128(b_, kBN * 128, 1024);
+#pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDQ, mndesc(a_, kk, kBN * 128), mndesc(b_, kk, kBN * 128),
+                        mma_ss(tmem + Cfg::kColDQ, ad_mn + mnmajor_step(kk), bd_mn + mnmajor_step(kk),
                                id_dq, kk > 0);
                     mma_commit(&bar_dq_full);
                     if (next) issue_dp(st1);

@@ -82,15 +82,6 @@ struct FwdParams {
     DeviceStatus* status;
 };
 
-// K-major operand tile with 128-byte swizzle: 16-element K step kk.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
-    return sdesc_sw128(base + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
-}
-// MN-major V tile (keys x d, d contiguous): 16-key step kk.
-__device__ __forceinline__ uint64_t vmn_desc(uint32_t base, int kk) {
-    return sdesc_sw128(base + kk * (16 * 128), 128 * 128, 1024);
-}
-
 // Work item (query-block pair, batch*head) -> coordinates.  Under the causal
 // mask the longest query blocks come first (the tile list is in decreasing
 // cost order, and each CTA takes every gridDim.x-th item).
@@ -408,12 +399,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 uint32_t cp[kTiles] = {0, 0};       // P_t completions seen so far
                 bool ok = true;
                 int lt = 0;
+                // Descriptors are built once per operand tile and stepped by
+                // constants, keeping the issuing thread's work between MMAs small.
                 auto issue_s = [&](int t, uint32_t kstage) {
                     const uint32_t col = Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0);
-                    const uint32_t kb = sk + kstage * Cfg::kTileBytes;
+                    const uint64_t qd = sdesc_sw128(sq + t * Cfg::kTileBytes, 16, 1024);
+                    const uint64_t kd = sdesc_sw128(sk + kstage * Cfg::kTileBytes, 16, 1024);
+#pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + col, kmajor_desc(sq + t * Cfg::kTileBytes, kk),
-                               kmajor_desc(kb, kk), idesc_s, kk > 0);
+                        mma_ss(tmem + col, qd + kmajor_step(kk, Cfg::kChunkBytes),
+                               kd + kmajor_step(kk, Cfg::kChunkBytes), idesc_s, kk > 0);
                     mma_commit(&bar_s[t]);
                 };
                 for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
@@ -444,13 +439,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             const uint32_t vb = sv + (gj % SV) * Cfg::kTileBytes;
                             const uint32_t col_s = Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0);
                             const uint32_t col_o = Cfg::kColO0 + t * (Cfg::kColO1 - Cfg::kColO0);
+                            const uint64_t vd = sdesc_sw128(vb, Cfg::kChunkBytes, 1024);
+#pragma unroll
                             for (int kk = 0; kk < kBN / 16; ++kk)
-                                mma_ts(tmem + col_o, tmem + col_s + kk * 8, vmn_desc(vb, kk), idesc_o,
-                                       (j > 0 || kk > 0) ? 1u : 0u);
-                            if (PRECISE)
+                                mma_ts(tmem + col_o, tmem + col_s + kk * 8, vd + mnmajor_step(kk),
+                                       idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                            if (PRECISE) {
+#pragma unroll
                                 for (int kk = 0; kk < kBN / 16; ++kk)
-                                    mma_ts(tmem + col_o, tmem + col_s + 64 + kk * 8, vmn_desc(vb, kk),
-                                           idesc_o, 1u);
+                                    mma_ts(tmem + col_o, tmem + col_s + 64 + kk * 8,
+                                           vd + mnmajor_step(kk), idesc_o, 1u);
+                            }
                             if (j + 1 < wt.n_kv[t]) {
                                 // K_{j+1} is waited for only now, after this PV.
                                 if (!k_next_ready) {

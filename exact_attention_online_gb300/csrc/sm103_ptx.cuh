@@ -217,6 +217,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Offset, in the descriptor's 16-byte address units, of 16-element K step kk
+// of a K-major 128B-swizzled tile whose 64-element chunks lie chunk_bytes
+// apart.  A descriptor for step kk is the step-0 descriptor plus this value:
+// the address field holds addr >> 4 and cannot carry (shared memory < 256 KB),
+// so one 64-bit add per MMA replaces rebuilding the descriptor.
+__host__ __device__ constexpr uint64_t kmajor_step(int kk, int chunk_bytes) {
+    return (uint64_t)(((kk >> 2) * chunk_bytes + (kk & 3) * 32) >> 4);
+}
+// Same for an MN-major 128B-swizzled tile: step kk moves 16 rows of 128 bytes.
+__host__ __device__ constexpr uint64_t mnmajor_step(int kk) { return (uint64_t)(kk * 2048 >> 4); }
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(dst_smem)),
