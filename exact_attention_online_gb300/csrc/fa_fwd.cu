@@ -12,12 +12,22 @@
 //               both P V MMAs, so K loads run a whole block ahead.
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA),
 //               O_t += P_t V_j with P_t read from TMEM (TS MMA).
+//   At d = 64 the work is split over two issuing threads: warp 9 issues the
+//   S MMAs, warp 11 the P V MMAs, and warp 10 loads Q as well as V.  An MMA
+//   issue blocks while the tensor pipe is busy and every barrier wait, fence
+//   and commit of the issuing thread costs on the order of a hundred cycles,
+//   so one thread left the pipe idle for half of each key block.
 //   warps 0-3   softmax for tile 0, warps 4-7 for tile 1: one query row per
 //               thread.  While one group does its softmax the tensor core
 //               runs the other tile's MMAs.
-// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  P_t (bf16 pairs) overwrites the
-// first half of S_t; the MMA that next writes S_t is issued after the MMA
-// that reads P_t, and tcgen05 MMAs of one thread execute in order.
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  At d = 128, P_t (bf16 pairs)
+// overwrites the first half of S_t; the MMA that next writes S_t is issued
+// after the MMA that reads P_t, and tcgen05 MMAs of one thread execute in order.
+// At d = 64 (bf16 output) P_t has columns of its own after O_1, which breaks
+// that chain: the softmax releases S_t as soon as it has loaded it, the next
+// S_t MMA is issued at once, and the softmax waits for the previous P V MMA
+// only just before it writes P_t.  The tensor core then works on S_t(j+1) and
+// P_t(j-1) V while the softmax of block j runs.
 //
 // Softmax in base 2: p = 2^(S*c - m) with c = scale*log2(e).  The running max
 // m is only raised when the block max exceeds it by more than 8 (a factor
@@ -31,6 +41,7 @@
 // bf16 rounding of P and of O from the error, which matters when values reach
 // tens (outliers of magnitude 30: half a bf16 ulp of 30 is 0.06).
 #include <cuda_bf16.h>
+#include <type_traits>
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -47,12 +58,13 @@ constexpr int kThreads = 12 * 32;   // 3 warpgroups: softmax 0, softmax 1, contr
 constexpr int kProducerWarp = 8;    // K tiles
 constexpr int kMmaWarp = 9;
 constexpr int kVProducerWarp = 10;  // V tiles
-constexpr int kQProducerWarp = 11;  // Q tiles
+constexpr int kQProducerWarp = 11;  // Q tiles (d = 128)
+constexpr int kPvWarp = 11;         // P V MMA issuer (d = 64, separate P)
 // Register split (setmaxnreg): the launch gives 384 x 168; the control
-// warpgroup drops to 72 so each softmax thread can hold a full 128-score row:
-// 128 x 72 + 256 x 216 = 64512 <= 384 x 168 = 64512.
-constexpr int kRegsControl = 72;
-constexpr int kRegsSoftmax = 216;
+// warpgroup drops to 88 so each softmax thread can hold a full 128-score row:
+// 128 x 88 + 256 x 208 = 64512 <= 384 x 168 = 64512.
+constexpr int kRegsControl = 88;
+constexpr int kRegsSoftmax = 208;
 constexpr int kRegsNeeded = 128 * kRegsControl + 256 * kRegsSoftmax;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -72,6 +84,9 @@ struct FwdCfg {
     static constexpr int kSmemAlloc = kSmemBytes + 1024;    // alignment slack
     // TMEM columns
     static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + D;
+    // At d = 64, S_0 | S_1 | O_0 | O_1 fill 384 columns and P_t (64 columns of
+    // bf16 pairs) gets columns of its own.
+    static constexpr uint32_t kColP0 = 384, kColP1 = 448;
 };
 
 struct FwdParams {
@@ -117,6 +132,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __shared__ uint64_t bar_k[SK], bar_k_empty[SK], bar_v[SV], bar_v_empty[SV];
     __shared__ uint64_t bar_q[kTiles], bar_q_free[kTiles];
     __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_o[kTiles], bar_o_free[kTiles];
+    __shared__ uint64_t bar_s_free[kTiles], bar_pv[kTiles];   // separate-P form only
+    constexpr bool SEP = (D == 64) && !PRECISE;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     const WaitCtx wc{p.status, &abort_sh};
@@ -139,6 +156,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bar_p[t], 128);
             mbar_init(&bar_o[t], 1);
             mbar_init(&bar_o_free[t], 128);
+            mbar_init(&bar_s_free[t], 128);
+            mbar_init(&bar_pv[t], 1);
         }
         fence_mbar_init();
     }
@@ -165,9 +184,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int rl = quarter * 32 + lane;      // row within the tile
         const uint32_t col_s = t ? Cfg::kColS1 : Cfg::kColS0;
         const uint32_t col_o = t ? Cfg::kColO1 : Cfg::kColO0;
+        const uint32_t col_p = SEP ? (t ? Cfg::kColP1 : Cfg::kColP0) : col_s;
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         const float c = p.scale_log2;
         uint32_t cs = 0;                         // S_t completions seen so far
+        uint32_t cpv = 0;                        // P_t V completions seen (separate P)
         bool ok = true;
         int lt = 0;
         for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
@@ -190,6 +211,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 asm volatile("" : FA_R32(r[1]) : : "memory");
                 asm volatile("" : FA_R32(r[2]) : : "memory");
                 asm volatile("" : FA_R32(r[3]) : : "memory");
+                if (SEP) {   // S_t is in registers: the next S_t MMA may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(&bar_s_free[t]);
+                }
                 float sv[kBN];
 #pragma unroll
                 for (int e = 0; e < kBN; ++e) sv[e] = __uint_as_float(r[e >> 5][e & 31]);
@@ -215,22 +240,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                        fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
                 const float mx2 = mx * c;
                 const bool need = mx2 > m2 + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = need ? mx2 : m2;
-                    const float alpha = (m_new == m2) ? 1.0f : ex2(m2 - m_new);
-                    l *= alpha;
-                    if (j > 0) {
+                // O rescale of this block (only when some row raised its max);
+                // the O columns may be touched only after the P V MMA of the
+                // previous block has completed.
+                auto rescale_o = [&](float alpha) {
 #pragma unroll
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t ov[32];
-                            tmem_ld32(lane_addr + col_o + c0, ov);
-                            tmem_ld_wait(ov);
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_addr + col_o + c0, ov);
+                        tmem_ld_wait(ov);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e)
-                                ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            tmem_st32(lane_addr + col_o + c0, ov);
-                        }
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(lane_addr + col_o + c0, ov);
                     }
+                };
+                const bool any_need = __any_sync(0xffffffffu, need);
+                float alpha = 1.0f;
+                if (any_need) {
+                    const float m_new = need ? mx2 : m2;
+                    alpha = (m_new == m2) ? 1.0f : ex2(m2 - m_new);
+                    l *= alpha;
+                    if (!SEP && j > 0) rescale_o(alpha);
                     m2 = m_new;
                 }
                 const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
@@ -238,9 +269,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 // row sum in four paired accumulators.
                 const uint64_t c2 = f2(c, c), negm2 = f2(-m_use, -m_use);
                 uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+                uint32_t pk[2][32];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t pk[32], pl[32];
+                    uint32_t pl[32];
 #pragma unroll
                     for (int e2 = 0; e2 < 32; ++e2) {
                         const int e = hh * 64 + 2 * e2;
@@ -248,16 +280,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         f2_split(f2_fma(f2(sv[e], sv[e + 1]), c2, negm2), x0, x1);
                         const float p0 = ex2(x0), p1 = ex2(x1);
                         acc2[e2 & 3] = f2_add(acc2[e2 & 3], f2(p0, p1));
-                        pk[e2] = pack_bf16x2(p0, p1);
+                        pk[hh][e2] = pack_bf16x2(p0, p1);
                         if (PRECISE) {
                             // second term: what bf16 rounding of p left out
-                            const float h0 = __uint_as_float(pk[e2] << 16);
-                            const float h1 = __uint_as_float(pk[e2] & 0xffff0000u);
+                            const float h0 = __uint_as_float(pk[hh][e2] << 16);
+                            const float h1 = __uint_as_float(pk[hh][e2] & 0xffff0000u);
                             pl[e2] = pack_bf16x2(p0 - h0, p1 - h1);
                         }
                     }
-                    tmem_st32(lane_addr + col_s + hh * 32, pk);
+                    if (!SEP) tmem_st32(lane_addr + col_s + hh * 32, pk[hh]);
                     if (PRECISE) tmem_st32(lane_addr + col_s + 64 + hh * 32, pl);
+                }
+                if (SEP) {
+                    // P_t and O_t are free once P_t(j-1) V has completed.
+                    if (j > 0) {
+                        if (!fa_wait_warp(&bar_pv[t], cpv & 1, 34 + t, wc)) { ok = false; break; }
+                        ++cpv;
+                        tc_fence_after();
+                        if (any_need) rescale_o(alpha);
+                    }
+                    tmem_st32(lane_addr + col_p, pk[0]);
+                    tmem_st32(lane_addr + col_p + 32, pk[1]);
                 }
                 {
                     float a0, a1;
@@ -273,7 +316,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // ------------------------------------------------------- epilogue
             // O row -> registers, release the O columns to the next item's
             // MMAs, then normalise and store.
-            if (!fa_wait_warp(&bar_o[t], lt & 1, 32 + t, wc)) { ok = false; break; }
+            if (SEP) {
+                if (!fa_wait_warp(&bar_pv[t], cpv & 1, 34 + t, wc)) { ok = false; break; }
+                ++cpv;
+            } else if (!fa_wait_warp(&bar_o[t], lt & 1, 32 + t, wc)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             uint32_t ov[D / 32][32];
 #pragma unroll
@@ -348,11 +397,25 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
         } else if (warp == kVProducerWarp && lane == 0) {
             // ------------------------------------------------- V producer
+            // (separate-P form: also the Q tiles, loaded ahead of each item's V)
             tma_prefetch_desc(&tm_v);
+            if (SEP) tma_prefetch_desc(&tm_q);
             uint32_t g = 0;
+            int lt = 0, q_loaded = -1;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
                 const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                if (SEP) {
+                    for (int t = 0; t < kTiles; ++t) {
+                        if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kChunks; ++c)
+                            tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
+                                        &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
+                    }
+                    if (!ok) break;
+                    q_loaded = lt;
+                }
                 for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
                     const int s = g % SV;
                     if (g >= (uint32_t)SV && !fa_wait(&bar_v_empty[s], ((g / SV) - 1) & 1, 13, wc)) {
@@ -369,8 +432,58 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const WaitCtx dc{p.status, nullptr};
                 for (uint32_t x = (g > (uint32_t)SV ? g - SV : 0); x < g; ++x)
                     fa_wait(&bar_v[x % SV], (x / SV) & 1, 14, dc);
+                if (SEP && q_loaded >= 0)
+                    for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 15, dc);
             }
-        } else if (warp == kQProducerWarp && lane == 0) {
+        } else if (SEP && warp == kPvWarp && lane == 0) {
+            // ------------------------------------------- P V MMA issuer
+            // A second issuing thread: while the S issuer waits or commits,
+            // this one keeps the tensor core busy, and the other way round.
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+            const uint32_t sv = smem_u32(sV);
+            uint32_t g = 0, cp0 = 0, cp1 = 0;
+            bool ok = true;
+            int lt = 0;
+            auto pv = [&](auto tc, uint32_t vstage, bool first, bool wait_o) -> bool {
+                constexpr int T = decltype(tc)::value;
+                uint32_t& c = T ? cp1 : cp0;
+                if (!fa_wait(&bar_p[T], c & 1, 24 + T, wc)) return false;
+                ++c;
+                if (wait_o && !fa_wait(&bar_o_free[T], (lt - 1) & 1, 26 + T, wc)) return false;
+                tc_fence_after();
+                const uint64_t vd = sdesc_sw128(sv + vstage * Cfg::kTileBytes, Cfg::kChunkBytes, 1024);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_ts(tmem + (T ? Cfg::kColO1 : Cfg::kColO0),
+                           tmem + (T ? Cfg::kColP1 : Cfg::kColP0) + kk * 8,
+                           vd + mnmajor_step(kk), idesc_o, (!first || kk > 0) ? 1u : 0u);
+                mma_commit(&bar_pv[T]);
+                return true;
+            };
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+                const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];   // n0 <= n1
+                for (int j = 0; j < n1; ++j) {
+                    const uint32_t gj = g + j, vs = gj % SV;
+                    if (!fa_wait(&bar_v[vs], (gj / SV) & 1, 22, wc)) { ok = false; break; }
+                    const bool wait_o = (j == 0 && lt > 0);
+                    if (j < n0 && !pv(std::integral_constant<int, 0>{}, vs, j == 0, wait_o)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!pv(std::integral_constant<int, 1>{}, vs, j == 0, wait_o)) { ok = false; break; }
+                    mma_commit(&bar_v_empty[vs]);            // V_j read by both PVs
+                }
+                g += n1;
+            }
+            if (!ok) {   // no MMA of this thread may still write TMEM at teardown
+                __shared__ uint64_t bar_drain_pv;
+                mbar_init(&bar_drain_pv, 1);
+                fence_mbar_init();
+                mma_commit(&bar_drain_pv);
+                fa_wait(&bar_drain_pv, 0, 29, WaitCtx{p.status, nullptr});
+            }
+        } else if (!SEP && warp == kQProducerWarp && lane == 0) {
             // ------------------------------------------------- Q producer
             tma_prefetch_desc(&tm_q);
             int lt = 0, q_loaded = -1;
@@ -411,7 +524,50 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                kd + kmajor_step(kk, Cfg::kChunkBytes), idesc_s, kk > 0);
                     mma_commit(&bar_s[t]);
                 };
-                for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+                // Separate-P form: this thread issues only the S MMAs; S_t(j)
+                // goes out as soon as K_j has landed and the softmax has
+                // loaded S_t(j-1).  The P V MMAs come from warp kPvWarp.  The
+                // tile index is a compile-time constant in every MMA.
+                uint32_t ns0 = 0, ns1 = 0;          // S_t MMAs issued so far
+                auto s_sep = [&](auto tc, uint32_t kstage) -> bool {
+                    constexpr int T = decltype(tc)::value;
+                    uint32_t& n = T ? ns1 : ns0;
+                    if (n > 0 && !fa_wait(&bar_s_free[T], (n - 1) & 1, 36 + T, wc)) return false;
+                    ++n;
+                    tc_fence_after();
+                    const uint64_t qd = sdesc_sw128(sq + T * Cfg::kTileBytes, 16, 1024);
+                    const uint64_t kd = sdesc_sw128(sk + kstage * Cfg::kTileBytes, 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + (T ? Cfg::kColS1 : Cfg::kColS0),
+                               qd + kmajor_step(kk, Cfg::kChunkBytes),
+                               kd + kmajor_step(kk, Cfg::kChunkBytes), idesc_s, kk > 0);
+                    mma_commit(&bar_s[T]);
+                    return true;
+                };
+                for (int item = blockIdx.x; SEP && ok && item < p.n_items;
+                     item += gridDim.x, ++lt) {
+                    const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                    const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];   // n0 <= n1
+                    if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int j = 0; j < n1; ++j) {
+                        const uint32_t gj = g + j, ks = gj % SK;
+                        if (!fa_wait(&bar_k[ks], (gj / SK) & 1, 21, wc)) { ok = false; break; }
+                        if (j < n0) {
+                            if (!s_sep(std::integral_constant<int, 0>{}, ks)) { ok = false; break; }
+                            if (j + 1 == n0) mma_commit(&bar_q_free[0]);
+                        }
+                        if (!s_sep(std::integral_constant<int, 1>{}, ks)) { ok = false; break; }
+                        if (j + 1 == n1) mma_commit(&bar_q_free[1]);
+                        mma_commit(&bar_k_empty[ks]);            // K_j read by both S MMAs
+                    }
+                    g += n1;
+                }
+                for (int item = blockIdx.x; !SEP && ok && item < p.n_items;
+                     item += gridDim.x, ++lt) {
                     const FwdTile wt = fwd_tile(item, p, CAUSAL);
                     const int n_last = wt.n_kv[kTiles - 1];
                     if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc) ||
