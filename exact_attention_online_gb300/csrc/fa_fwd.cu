@@ -7,22 +7,22 @@
 // (t = 0, 1) of one (batch, head); CTA c takes items c, c + gridDim.x, ...
 // (longest causal items first) and streams 128-key K and V tiles through two
 // shared-memory rings:
-//   warps 8, 10, 11  TMA producers of K_j, V_j and the Q tiles.  K_j is
-//               released when both S MMAs that read it are issued, V_j after
-//               both P V MMAs, so K loads run a whole block ahead.
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA),
-//               O_t += P_t V_j with P_t read from TMEM (TS MMA).
-//   At d = 64 the work is split over two issuing threads: warp 9 issues the
-//   S MMAs, warp 11 the P V MMAs, and warp 10 loads Q as well as V.  An MMA
-//   issue blocks while the tensor pipe is busy and every barrier wait, fence
-//   and commit of the issuing thread costs on the order of a hundred cycles,
-//   so one thread left the pipe idle for half of each key block.
+//   warp 8      TMA producer of K_j; K_j is released when both S MMAs that
+//               read it have completed, so K loads run whole blocks ahead.
+//   warp 10     TMA producer of V_j and of the Q tiles (each item's Q ahead of
+//               its V blocks); V_j is released after both P V MMAs.
+//   warp 9      S MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA).
+//   warp 11     P V MMA issuer (one thread): O_t += P_t V_j, P_t read from
+//               TMEM (TS MMA).  An MMA issue blocks while the tensor pipe is
+//               busy, and every barrier wait, fence and commit of an issuing
+//               thread costs on the order of a hundred cycles; with two
+//               issuers one thread's waits overlap the other's MMAs.
 //   warps 0-3   softmax for tile 0, warps 4-7 for tile 1: one query row per
 //               thread.  While one group does its softmax the tensor core
 //               runs the other tile's MMAs.
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1.  At d = 128, P_t (bf16 pairs)
 // overwrites the first half of S_t; the MMA that next writes S_t is issued
-// after the MMA that reads P_t, and tcgen05 MMAs of one thread execute in order.
+// only after the P_t V MMA that reads P_t has completed.
 // At d = 64 (bf16 output) P_t has columns of its own after O_1, which breaks
 // that chain: the softmax releases S_t as soon as it has loaded it, the next
 // S_t MMA is issued at once, and the softmax waits for the previous P V MMA
@@ -57,9 +57,8 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kThreads = 12 * 32;   // 3 warpgroups: softmax 0, softmax 1, control
 constexpr int kProducerWarp = 8;    // K tiles
 constexpr int kMmaWarp = 9;
-constexpr int kVProducerWarp = 10;  // V tiles
-constexpr int kQProducerWarp = 11;  // Q tiles (d = 128)
-constexpr int kPvWarp = 11;         // P V MMA issuer (d = 64, separate P)
+constexpr int kVProducerWarp = 10;  // V and Q tiles
+constexpr int kPvWarp = 11;         // P V MMA issuer
 // Register split (setmaxnreg): the launch gives 384 x 168; the control
 // warpgroup drops to 88 so each softmax thread can hold a full 128-score row:
 // 128 x 88 + 256 x 208 = 64512 <= 384 x 168 = 64512.
@@ -131,8 +130,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                                ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_k[SK], bar_k_empty[SK], bar_v[SV], bar_v_empty[SV];
     __shared__ uint64_t bar_q[kTiles], bar_q_free[kTiles];
-    __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_o[kTiles], bar_o_free[kTiles];
-    __shared__ uint64_t bar_s_free[kTiles], bar_pv[kTiles];   // separate-P form only
+    __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_pv[kTiles], bar_o_free[kTiles];
+    __shared__ uint64_t bar_s_free[kTiles];   // separate-P form only
     constexpr bool SEP = (D == 64) && !PRECISE;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -154,7 +153,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bar_q_free[t], 1);
             mbar_init(&bar_s[t], 1);
             mbar_init(&bar_p[t], 128);
-            mbar_init(&bar_o[t], 1);
             mbar_init(&bar_o_free[t], 128);
             mbar_init(&bar_s_free[t], 128);
             mbar_init(&bar_pv[t], 1);
@@ -316,13 +314,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // ------------------------------------------------------- epilogue
             // O row -> registers, release the O columns to the next item's
             // MMAs, then normalise and store.
-            if (SEP) {
-                if (!fa_wait_warp(&bar_pv[t], cpv & 1, 34 + t, wc)) { ok = false; break; }
-                ++cpv;
-            } else if (!fa_wait_warp(&bar_o[t], lt & 1, 32 + t, wc)) {
-                ok = false;
-                break;
-            }
+            // The last P_t V MMA of the item has completed.  Without separate
+            // P columns the softmax did not wait for the earlier ones; each S
+            // MMA was issued only after the P V MMA before it had completed,
+            // so those are complete already.
+            if (!SEP) cpv += n_kv - 1;
+            if (!fa_wait_warp(&bar_pv[t], cpv & 1, 34 + t, wc)) { ok = false; break; }
+            ++cpv;
             tc_fence_after();
             uint32_t ov[D / 32][32];
 #pragma unroll
@@ -396,26 +394,25 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     fa_wait(&bar_k[x % SK], (x / SK) & 1, 11, dc);
             }
         } else if (warp == kVProducerWarp && lane == 0) {
-            // ------------------------------------------------- V producer
-            // (separate-P form: also the Q tiles, loaded ahead of each item's V)
+            // ---------------------------------------------- V and Q producer
+            // The Q tiles of an item are loaded ahead of its V blocks, as soon
+            // as the last S MMAs of the previous item have read the old ones.
             tma_prefetch_desc(&tm_v);
-            if (SEP) tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_q);
             uint32_t g = 0;
             int lt = 0, q_loaded = -1;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
                 const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                if (SEP) {
-                    for (int t = 0; t < kTiles; ++t) {
-                        if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
-                        for (int c = 0; c < Cfg::kChunks; ++c)
-                            tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
-                                        &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
-                    }
-                    if (!ok) break;
-                    q_loaded = lt;
+                for (int t = 0; t < kTiles; ++t) {
+                    if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
+                    for (int c = 0; c < Cfg::kChunks; ++c)
+                        tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
+                                    &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
                 }
+                if (!ok) break;
+                q_loaded = lt;
                 for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
                     const int s = g % SV;
                     if (g >= (uint32_t)SV && !fa_wait(&bar_v_empty[s], ((g / SV) - 1) & 1, 13, wc)) {
@@ -428,24 +425,28 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                     c * 64, j * kBN, wt.kv_bh);
                 }
             }
-            if (abort_sh) {
+            if (abort_sh) {   // drain the copies still in flight (bounded)
                 const WaitCtx dc{p.status, nullptr};
                 for (uint32_t x = (g > (uint32_t)SV ? g - SV : 0); x < g; ++x)
                     fa_wait(&bar_v[x % SV], (x / SV) & 1, 14, dc);
-                if (SEP && q_loaded >= 0)
+                if (q_loaded >= 0)
                     for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 15, dc);
             }
-        } else if (SEP && warp == kPvWarp && lane == 0) {
+        } else if (warp == kPvWarp && lane == 0) {
             // ------------------------------------------- P V MMA issuer
-            // A second issuing thread: while the S issuer waits or commits,
-            // this one keeps the tensor core busy, and the other way round.
+            // O_t += P_t V_j, P_t read from TMEM.  A second issuing thread:
+            // while the S issuer waits or commits, this one keeps the tensor
+            // core busy, and the other way round.
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
             const uint32_t sv = smem_u32(sV);
-            uint32_t g = 0, cp0 = 0, cp1 = 0;
+            uint32_t g = 0, cp0 = 0, cp1 = 0;       // V blocks used; P_t arrivals seen
             bool ok = true;
             int lt = 0;
             auto pv = [&](auto tc, uint32_t vstage, bool first, bool wait_o) -> bool {
                 constexpr int T = decltype(tc)::value;
+                constexpr uint32_t col_o = T ? Cfg::kColO1 : Cfg::kColO0;
+                constexpr uint32_t col_s = T ? Cfg::kColS1 : Cfg::kColS0;
+                constexpr uint32_t col_p = SEP ? (T ? Cfg::kColP1 : Cfg::kColP0) : col_s;
                 uint32_t& c = T ? cp1 : cp0;
                 if (!fa_wait(&bar_p[T], c & 1, 24 + T, wc)) return false;
                 ++c;
@@ -454,9 +455,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const uint64_t vd = sdesc_sw128(sv + vstage * Cfg::kTileBytes, Cfg::kChunkBytes, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + (T ? Cfg::kColO1 : Cfg::kColO0),
-                           tmem + (T ? Cfg::kColP1 : Cfg::kColP0) + kk * 8,
-                           vd + mnmajor_step(kk), idesc_o, (!first || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + col_o, tmem + col_p + kk * 8, vd + mnmajor_step(kk), idesc_o,
+                           (!first || kk > 0) ? 1u : 0u);
+                if (PRECISE) {   // second term of P
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ts(tmem + col_o, tmem + col_s + 64 + kk * 8, vd + mnmajor_step(kk),
+                               idesc_o, 1u);
+                }
                 mma_commit(&bar_pv[T]);
                 return true;
             };
@@ -483,162 +489,65 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 mma_commit(&bar_drain_pv);
                 fa_wait(&bar_drain_pv, 0, 29, WaitCtx{p.status, nullptr});
             }
-        } else if (!SEP && warp == kQProducerWarp && lane == 0) {
-            // ------------------------------------------------- Q producer
-            tma_prefetch_desc(&tm_q);
-            int lt = 0, q_loaded = -1;
+        } else if (warp == kMmaWarp && lane == 0) {
+            // ---------------------------------------------- S MMA issuer
+            // S_t(j) = Q_t K_j^T goes out as soon as K_j has landed and the
+            // columns of S_t are free again: loaded by the softmax (P in
+            // columns of its own), or read by the P_t V MMA of the previous
+            // block (P written over S).  The tile index is a compile-time
+            // constant in every MMA, so operand addresses fold into the
+            // instruction stream.
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
+            const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK);
+            uint32_t g = 0, ns0 = 0, ns1 = 0;       // K blocks used; S_t MMAs issued
             bool ok = true;
+            int lt = 0;
+            auto s_mma = [&](auto tc, uint32_t kstage) -> bool {
+                constexpr int T = decltype(tc)::value;
+                uint32_t& n = T ? ns1 : ns0;
+                if (n > 0 && !fa_wait(SEP ? &bar_s_free[T] : &bar_pv[T], (n - 1) & 1, 36 + T, wc))
+                    return false;
+                ++n;
+                tc_fence_after();
+                const uint64_t qd = sdesc_sw128(sq + T * Cfg::kTileBytes, 16, 1024);
+                const uint64_t kd = sdesc_sw128(sk + kstage * Cfg::kTileBytes, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + (T ? Cfg::kColS1 : Cfg::kColS0),
+                           qd + kmajor_step(kk, Cfg::kChunkBytes),
+                           kd + kmajor_step(kk, Cfg::kChunkBytes), idesc_s, kk > 0);
+                mma_commit(&bar_s[T]);
+                return true;
+            };
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
                 const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                for (int t = 0; t < kTiles; ++t) {
-                    if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
-                    for (int c = 0; c < Cfg::kChunks; ++c)
-                        tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
-                                    &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
+                const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];   // n0 <= n1
+                if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc)) {
+                    ok = false;
+                    break;
                 }
-                if (ok) q_loaded = lt;
+                for (int j = 0; j < n1; ++j) {
+                    const uint32_t gj = g + j, ks = gj % SK;
+                    if (!fa_wait(&bar_k[ks], (gj / SK) & 1, 21, wc)) { ok = false; break; }
+                    if (j < n0) {
+                        if (!s_mma(std::integral_constant<int, 0>{}, ks)) { ok = false; break; }
+                        if (j + 1 == n0) mma_commit(&bar_q_free[0]);
+                    }
+                    if (!s_mma(std::integral_constant<int, 1>{}, ks)) { ok = false; break; }
+                    if (j + 1 == n1) mma_commit(&bar_q_free[1]);
+                    mma_commit(&bar_k_empty[ks]);            // K_j read by both S MMAs
+                }
+                g += n1;
             }
-            if (abort_sh && q_loaded >= 0) {
-                const WaitCtx dc{p.status, nullptr};
-                for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 15, dc);
+            if (!ok) {
+                __shared__ uint64_t bar_drain;
+                mbar_init(&bar_drain, 1);
+                fence_mbar_init();
+                mma_commit(&bar_drain);
+                fa_wait(&bar_drain, 0, 29, WaitCtx{p.status, nullptr});
             }
-        } else if (warp == kMmaWarp) {
-            if (lane == 0) {
-                constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
-                constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
-                const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
-                uint32_t g = 0;                     // K/V blocks consumed so far
-                uint32_t cp[kTiles] = {0, 0};       // P_t completions seen so far
-                bool ok = true;
-                int lt = 0;
-                // Descriptors are built once per operand tile and stepped by
-                // constants, keeping the issuing thread's work between MMAs small.
-                auto issue_s = [&](int t, uint32_t kstage) {
-                    const uint32_t col = Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0);
-                    const uint64_t qd = sdesc_sw128(sq + t * Cfg::kTileBytes, 16, 1024);
-                    const uint64_t kd = sdesc_sw128(sk + kstage * Cfg::kTileBytes, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + col, qd + kmajor_step(kk, Cfg::kChunkBytes),
-                               kd + kmajor_step(kk, Cfg::kChunkBytes), idesc_s, kk > 0);
-                    mma_commit(&bar_s[t]);
-                };
-                // Separate-P form: this thread issues only the S MMAs; S_t(j)
-                // goes out as soon as K_j has landed and the softmax has
-                // loaded S_t(j-1).  The P V MMAs come from warp kPvWarp.  The
-                // tile index is a compile-time constant in every MMA.
-                uint32_t ns0 = 0, ns1 = 0;          // S_t MMAs issued so far
-                auto s_sep = [&](auto tc, uint32_t kstage) -> bool {
-                    constexpr int T = decltype(tc)::value;
-                    uint32_t& n = T ? ns1 : ns0;
-                    if (n > 0 && !fa_wait(&bar_s_free[T], (n - 1) & 1, 36 + T, wc)) return false;
-                    ++n;
-                    tc_fence_after();
-                    const uint64_t qd = sdesc_sw128(sq + T * Cfg::kTileBytes, 16, 1024);
-                    const uint64_t kd = sdesc_sw128(sk + kstage * Cfg::kTileBytes, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + (T ? Cfg::kColS1 : Cfg::kColS0),
-                               qd + kmajor_step(kk, Cfg::kChunkBytes),
-                               kd + kmajor_step(kk, Cfg::kChunkBytes), idesc_s, kk > 0);
-                    mma_commit(&bar_s[T]);
-                    return true;
-                };
-                for (int item = blockIdx.x; SEP && ok && item < p.n_items;
-                     item += gridDim.x, ++lt) {
-                    const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                    const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];   // n0 <= n1
-                    if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    for (int j = 0; j < n1; ++j) {
-                        const uint32_t gj = g + j, ks = gj % SK;
-                        if (!fa_wait(&bar_k[ks], (gj / SK) & 1, 21, wc)) { ok = false; break; }
-                        if (j < n0) {
-                            if (!s_sep(std::integral_constant<int, 0>{}, ks)) { ok = false; break; }
-                            if (j + 1 == n0) mma_commit(&bar_q_free[0]);
-                        }
-                        if (!s_sep(std::integral_constant<int, 1>{}, ks)) { ok = false; break; }
-                        if (j + 1 == n1) mma_commit(&bar_q_free[1]);
-                        mma_commit(&bar_k_empty[ks]);            // K_j read by both S MMAs
-                    }
-                    g += n1;
-                }
-                for (int item = blockIdx.x; !SEP && ok && item < p.n_items;
-                     item += gridDim.x, ++lt) {
-                    const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                    const int n_last = wt.n_kv[kTiles - 1];
-                    if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc) ||
-                        !fa_wait(&bar_k[g % SK], (g / SK) & 1, 21, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    for (int t = 0; t < kTiles; ++t) {
-                        issue_s(t, g % SK);
-                        if (wt.n_kv[t] == 1) mma_commit(&bar_q_free[t]);
-                    }
-                    mma_commit(&bar_k_empty[g % SK]);      // K block 0 read by both S MMAs
-                    for (int j = 0; j < n_last; ++j) {
-                        const uint32_t gj = g + j;
-                        if (!fa_wait(&bar_v[gj % SV], (gj / SV) & 1, 22, wc)) { ok = false; break; }
-                        bool k_next_ready = false;
-                        for (int t = 0; t < kTiles; ++t) {
-                            if (j >= wt.n_kv[t]) continue;
-                            if (!fa_wait(&bar_p[t], cp[t] & 1, 24 + t, wc)) { ok = false; break; }
-                            ++cp[t];
-                            if (j == 0 && lt > 0 &&
-                                !fa_wait(&bar_o_free[t], (lt - 1) & 1, 26 + t, wc)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t vb = sv + (gj % SV) * Cfg::kTileBytes;
-                            const uint32_t col_s = Cfg::kColS0 + t * (Cfg::kColS1 - Cfg::kColS0);
-                            const uint32_t col_o = Cfg::kColO0 + t * (Cfg::kColO1 - Cfg::kColO0);
-                            const uint64_t vd = sdesc_sw128(vb, Cfg::kChunkBytes, 1024);
-#pragma unroll
-                            for (int kk = 0; kk < kBN / 16; ++kk)
-                                mma_ts(tmem + col_o, tmem + col_s + kk * 8, vd + mnmajor_step(kk),
-                                       idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-                            if (PRECISE) {
-#pragma unroll
-                                for (int kk = 0; kk < kBN / 16; ++kk)
-                                    mma_ts(tmem + col_o, tmem + col_s + 64 + kk * 8,
-                                           vd + mnmajor_step(kk), idesc_o, 1u);
-                            }
-                            if (j + 1 < wt.n_kv[t]) {
-                                // K_{j+1} is waited for only now, after this PV.
-                                if (!k_next_ready) {
-                                    if (!fa_wait(&bar_k[(gj + 1) % SK], ((gj + 1) / SK) & 1, 23, wc)) {
-                                        ok = false;
-                                        break;
-                                    }
-                                    tc_fence_after();
-                                    k_next_ready = true;
-                                }
-                                issue_s(t, (gj + 1) % SK);
-                                if (j + 2 == wt.n_kv[t]) mma_commit(&bar_q_free[t]);
-                            } else {
-                                mma_commit(&bar_o[t]);
-                            }
-                        }
-                        if (!ok) break;
-                        mma_commit(&bar_v_empty[gj % SV]);            // V_j read by both PVs
-                        if (j + 1 < n_last) mma_commit(&bar_k_empty[(gj + 1) % SK]);   // K_{j+1} by both S
-                    }
-                    g += n_last;
-                }
-                // Make sure no MMA is still writing TMEM when the CTA tears down.
-                if (!ok) {
-                    __shared__ uint64_t bar_drain;
-                    mbar_init(&bar_drain, 1);
-                    fence_mbar_init();
-                    mma_commit(&bar_drain);
-                    fa_wait(&bar_drain, 0, 29, WaitCtx{p.status, nullptr});
-                }
-            }
-            __syncwarp();
         }
+        __syncwarp();
     }
 
     tc_fence_before();
