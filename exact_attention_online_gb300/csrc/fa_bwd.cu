@@ -22,8 +22,9 @@
 //               query block).
 //   dq_convert  dQ = bf16(scale * accumulator).
 //
-// Roles in dkdv: warps 0-3 compute (one key row, or for dQ^T one head-dim row,
-// per thread), warp 4 TMA producer, warp 5 MMA issuer.
+// Roles in dkdv: warps 0-7 compute (one key row per thread, two warps per row
+// splitting the query columns), warp 8 TMA producer, warps 9 and 10 MMA
+// issuers, warps 12-15 read the dQ partial out of TMEM.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -34,13 +35,14 @@ namespace fa {
 namespace {
 
 constexpr int kBN = 128;   // keys per CTA
-// 16 warps: 0-7 compute (two warpgroups), 8 TMA producer, 9 MMA issuer,
-// 10-11 idle, 12-15 dQ read-out.
+// 16 warps: 0-7 compute (two warpgroups), 8 TMA producer, 9 and 10 MMA
+// issuers, 11 idle, 12-15 dQ read-out.
 constexpr int kThreads = 512;
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;      // dV and S^T MMAs; allocates TMEM
+constexpr int kMma2Warp = 10;    // dK, dQ and dP^T MMAs
 constexpr int kReadoutWarp0 = 12;
 constexpr int kReadoutThreads = 128;
 // Register split (setmaxnreg) of the 512 x 128 launch registers:
@@ -90,6 +92,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using Cfg = BwdCfg<D>;
     constexpr int BR = Cfg::kBR;
+    constexpr bool kTwoIssuers = (D == 128);
     constexpr int HALF = BR / 2;                  // query columns per compute warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -125,7 +128,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(&bar_kv, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], 1);
+            mbar_init(&bar_empty[s], kTwoIssuers ? 2 : 1);   // every MMA issuer lets go of the stage
         }
         mbar_init(&bar_s, 1);
         mbar_init(&bar_dp, 1);
@@ -133,7 +136,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(&bar_ds, kComputeThreads);
         mbar_init(&bar_dq_full, 1);
         mbar_init(&bar_dq_free, kReadoutThreads);
-        mbar_init(&bar_done, 1);
+        mbar_init(&bar_done, kTwoIssuers ? 2 : 1);   // one arrival per MMA issuer
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -373,7 +376,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         fa_wait(&bar_full[it & 1], (it >> 1) & 1, 41, WaitCtx{p.status, nullptr});
                 }
             }
-        } else if (warp == kMmaWarp) {
+            __syncwarp();
+        } else if (!kTwoIssuers && warp == kMmaWarp) {
+            // One MMA-issuing thread (d = 64): dV, S^T for the next block, dK,
+            // the dQ partial, dP^T for the next block, in that order.
             if (lane == 0 && n_it > 0) {
                 constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
                 constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
@@ -454,6 +460,114 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (!ok) fa_wait(&bar_done, 0, 59, WaitCtx{p.status, nullptr});
             }
             __syncwarp();
+        } else if (kTwoIssuers && (warp == kMmaWarp || warp == kMma2Warp)) {
+          if (lane == 0 && n_it > 0) {
+            // MMA issue.  Half A: dV += P^T dO_i, then S^T for block i+1 (it
+            // overwrites P^T, so after the dV MMA, in issue order).  Half B:
+            // dK += dS^T Q_i, the dQ partial, then dP^T for block i+1 (its
+            // completion also tells the compute warps that dS^T may be
+            // overwritten).  An MMA issue blocks while the tensor pipe is busy
+            // and each barrier wait and commit of an issuing thread costs on
+            // the order of a hundred cycles; at d = 128 the halves go to two
+            // threads (warps kMmaWarp and kMma2Warp) so that one's waits overlap
+            // the other's MMAs.  At d = 64 the halves hardly overlap in time and
+            // one thread issues both, in the order A, B.
+            constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
+            constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+            constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
+                           sdo = smem_u32(sDO), sds = smem_u32(sDS);
+            const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
+            const bool half_a = (warp == kMmaWarp);
+            const bool half_b = (warp == kMma2Warp);
+            auto issue_s = [&](int st) {      // S^T = K_j Q_i^T
+                const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
+                           qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                mma_commit(&bar_s);
+            };
+            auto issue_dp = [&](int st) {     // dP^T = V_j dO_i^T
+                const uint64_t dod = sdesc_sw128(sdo + st * Cfg::kQBytes, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + Cfg::kColDP, vd + kmajor_step(kk, kBN * 128),
+                           dod + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                mma_commit(&bar_dp);
+            };
+            bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
+            if (ok) {
+                tc_fence_after();
+                if (half_a) issue_s(0);
+                if (half_b) issue_dp(0);
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int st = it & 1, st1 = (it + 1) & 1;
+                const bool next = it + 1 < n_it;
+                if (half_a) {
+                    // dV += P^T dO_i  (P^T in TMEM; query half h of the K
+                    // dimension sits in the S^T columns of the warps of half h)
+                    if (!fa_wait(&bar_p, it & 1, 52, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dod_mn = sdesc_sw128(sdo + st * Cfg::kQBytes, BR * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BR / 16; ++kk) {
+                        const int qs = kk * 16;
+                        const uint32_t pcol = Cfg::kColS + (qs / HALF) * HALF + (qs % HALF) / 2;
+                        mma_ts(tmem + Cfg::kColDV, tmem + pcol, dod_mn + mnmajor_step(kk), id_kv,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bar_empty[st]);      // half A is done with Q_i, dO_i
+                    if (next) {
+                        if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_s(st1);
+                    }
+                }
+                if (half_b) {
+                    // dK += dS^T Q_i
+                    if (!fa_wait(&bar_ds, it & 1, 55, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t dsd = sdesc_sw128(sds, 16, 1024);
+                    const uint64_t qd_mn = sdesc_sw128(sq + st * Cfg::kQBytes, BR * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BR / 16; ++kk)
+                        mma_ss(tmem + Cfg::kColDK, dsd + kmajor_step(kk, kBN * 128),
+                               qd_mn + mnmajor_step(kk), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bar_empty[st]);      // half B is done with Q_i, dO_i
+                    // dQ partial (K dimension = the 128 keys)
+                    if (it > 0 && !fa_wait(&bar_dq_free, (it - 1) & 1, 53, wc)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_ = (D == 128) ? sk : sds;
+                    const uint32_t b_ = (D == 128) ? sds : sk;
+                    const uint64_t ad_mn = sdesc_sw128(a_, kBN * 128, 1024);
+                    const uint64_t bd_mn = sdesc_sw128(b_, kBN * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ss(tmem + Cfg::kColDQ, ad_mn + mnmajor_step(kk), bd_mn + mnmajor_step(kk),
+                               id_dq, kk > 0);
+                    mma_commit(&bar_dq_full);
+                    if (next) {
+                        if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 56, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        issue_dp(st1);
+                    }
+                }
+            }
+            const bool first = half_a;
+            if (ok) {
+                mma_commit(&bar_done);               // one arrival per issuing thread
+            } else {   // no MMA of this thread may still write TMEM at teardown
+                __shared__ uint64_t bar_drain[2];
+                uint64_t* dbar = &bar_drain[first ? 0 : 1];
+                mbar_init(dbar, 1);
+                fence_mbar_init();
+                mma_commit(dbar);
+                fa_wait(dbar, 0, 59, WaitCtx{p.status, nullptr});
+            }
+          }
+          __syncwarp();   // reconverge before the block-wide barrier below
         }
     }
 
