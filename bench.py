@@ -43,7 +43,12 @@ L2_BYTES = 129 * 1024 * 1024
 # described in profiles/), keyed by workload, together with the sha256 of the
 # kernel source it was taken on.  A source change makes the figure stale and
 # it is then reported as null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/fa_bwd_dkdv_mha_d64.md: 203.5 MB read + 88.3 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 291.84e6, "src_sha": "b9a8b2f4a0ecb419"},
+    # profiles/fa_fwd_mha_d64.md: 112.8 MB read + 13.1 MB written, one launch
+    ("fa_fwd", "mha_d64"): {"bytes": 125.84e6, "src_sha": "7d54771fdf717a16"},
+}
 
 
 def parse():
