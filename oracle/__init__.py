@@ -13,6 +13,12 @@ Functions (NumPy float64 in, NumPy float64 out; layouts as in the C file):
                       (blog "FlashAttention", o_N = o'_N) or deferred division
                       (FlashAttention-2 answer on non-matmul FLOPs).
     attn_bwd          analytic gradients dQ, dK, dV and D = rowsum(dO * O).
+    e4m3_encode/decode  the e4m3 format from its definition (round to nearest,
+                      ties to even, saturating at 448).
+    fp8_quantize      per-(batch, head, 128-row block) quantisation of Q, K, V
+                      with scale amax / 448 (FlashAttention-3 summary, "block
+                      quantization"; the granularity is this repository's
+                      reading), V also transposed.
 """
 from __future__ import annotations
 
@@ -61,6 +67,15 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attn_bwd.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
+    u8p = ctypes.POINTER(ctypes.c_ubyte)
+    fp = ctypes.POINTER(ctypes.c_float)
+    ll = ctypes.c_longlong
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_encode.restype = ctypes.c_ubyte
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_ubyte]
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_fp8_quant_block.argtypes = [fp, i, i, ll, u8p, ll, u8p, ll, fp]
+    lib.oracle_fp8_quant_block.restype = i
     return lib
 
 
@@ -157,3 +172,88 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float, mutant: int = 0):
                                       int(causal), float(scale))
     _check(rc, "oracle_attn_bwd")
     return dq, dk, dv, D
+
+
+# --------------------------------------------------------------------- FP8
+FP8_BLOCK = 128
+
+
+def e4m3_encode(x: float, mutant: int = 0) -> int:
+    return int(load(mutant).oracle_e4m3_encode(ctypes.c_float(float(x))))
+
+
+def e4m3_decode(code: int, mutant: int = 0) -> float:
+    return float(load(mutant).oracle_e4m3_decode(ctypes.c_ubyte(int(code))))
+
+
+def e4m3_decode_table(mutant: int = 0) -> np.ndarray:
+    """Values of all 256 codes (NaN for the two NaN codes)."""
+    return np.array([e4m3_decode(c, mutant) for c in range(256)])
+
+
+def _quant_blocks(x: np.ndarray, transpose: bool, mutant: int):
+    """x: [G][N][d] float32.  Returns (codes, scales): codes [G][Np][d] (or
+    [G][d][Np] when transpose), scales [G][Np / 128] float32."""
+    G, N, d = x.shape
+    Np = (N + FP8_BLOCK - 1) // FP8_BLOCK * FP8_BLOCK
+    nblk = Np // FP8_BLOCK
+    out = np.zeros((G, d, Np) if transpose else (G, Np, d), dtype=np.uint8)
+    scales = np.zeros((G, nblk), dtype=np.float32)
+    lib = load(mutant)
+    u8p = ctypes.POINTER(ctypes.c_ubyte)
+    fp = ctypes.POINTER(ctypes.c_float)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    sc = ctypes.c_float()
+    for g in range(G):
+        for b in range(nblk):
+            r0 = b * FP8_BLOCK
+            rows = min(FP8_BLOCK, N - r0)
+            src = x[g, r0:r0 + rows]
+            if transpose:
+                dst = out[g]
+                rc = lib.oracle_fp8_quant_block(
+                    src.ctypes.data_as(fp), rows, d, d, None, 0,
+                    ctypes.cast(dst.ctypes.data + r0, u8p), Np, ctypes.byref(sc))
+            else:
+                dst = out[g, r0:r0 + rows]
+                rc = lib.oracle_fp8_quant_block(
+                    src.ctypes.data_as(fp), rows, d, d, dst.ctypes.data_as(u8p), d,
+                    None, 0, ctypes.byref(sc))
+            _check(rc, "oracle_fp8_quant_block")
+            scales[g, b] = sc.value
+    return out, scales
+
+
+def fp8_quantize(q, k, v, mutant: int = 0) -> dict:
+    """Block quantisation of bf16 Q [B,H,N,d], K and V [B,Hkv,N,d] (given as
+    float32 or float64 arrays holding the bf16 values).  Returns
+    q8 [B*H][Np][d], k8 [B*Hkv][Np][d], v8t [B*Hkv][d][Np] (uint8 codes, zero
+    on padded rows), sq [B*H][nblk], sk, sv [B*Hkv][nblk] (float32 scales) and
+    svmax [B*Hkv] (the largest V scale of each head)."""
+    q = np.asarray(q, dtype=np.float32)
+    k = np.asarray(k, dtype=np.float32)
+    v = np.asarray(v, dtype=np.float32)
+    B, H, N, d = q.shape
+    Hkv = k.shape[1]
+    q8, sq = _quant_blocks(q.reshape(B * H, N, d), False, mutant)
+    k8, sk = _quant_blocks(k.reshape(B * Hkv, N, d), False, mutant)
+    v8t, sv = _quant_blocks(v.reshape(B * Hkv, N, d), True, mutant)
+    return {"q8": q8, "k8": k8, "v8t": v8t, "sq": sq, "sk": sk, "sv": sv,
+            "svmax": sv.max(axis=1).astype(np.float32)}
+
+
+def fp8_dequantize(qd: dict, B: int, H: int, Hkv: int, N: int, d: int):
+    """The values the quantised tensors stand for (codes times block scales),
+    float64, in the [B,H,N,d] / [B,Hkv,N,d] layouts."""
+    table = e4m3_decode_table()
+    nb = FP8_BLOCK
+
+    def expand(codes, scales, G, transpose):
+        vals = table[codes]
+        if transpose:
+            vals = np.swapaxes(vals, 1, 2)
+        s = np.repeat(scales.astype(np.float64), nb, axis=1)[:, :, None]
+        return (vals * s)[:, :N, :]
+    return (expand(qd["q8"], qd["sq"], B * H, False).reshape(B, H, N, d),
+            expand(qd["k8"], qd["sk"], B * Hkv, False).reshape(B, Hkv, N, d),
+            expand(qd["v8t"], qd["sv"], B * Hkv, True).reshape(B, Hkv, N, d))

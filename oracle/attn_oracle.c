@@ -366,3 +366,91 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/*
+ * ---------------------------------------------------------------------------
+ * FP8 (e4m3) block quantisation, for the FP8 forward (FlashAttention-3 summary,
+ * "block quantization" named in the abstract; the granularity is this
+ * repository's reading: one scale per (batch, head, block of 128 rows) of each
+ * of Q, K and V, scale = amax / 448).
+ *
+ * The e4m3 format, from its definition: 1 sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits; exponent field 0 holds subnormals m * 2^-9; no
+ * infinities; the all-ones magnitude S.1111.111 is NaN, so the largest finite
+ * magnitude is 1.110b * 2^8 = 448.  Encoding rounds to the nearest
+ * representable value, ties to an even mantissa, and saturates magnitudes at
+ * or beyond 448 to 448 (no NaN is produced from a finite input).
+ * ---------------------------------------------------------------------------
+ */
+
+/* Round a non-negative double to the nearest integer, ties to even. */
+static double round_half_even(double x) {
+    if (MUT(10)) return floor(x + 0.5);            /* planted: ties away from zero */
+    const double f = floor(x);
+    const double r = x - f;
+    if (r > 0.5) return f + 1.0;
+    if (r < 0.5) return f;
+    return (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+}
+
+unsigned char oracle_e4m3_encode(float x) {
+    const unsigned char sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a >= 448.0) return (unsigned char)(sign | (MUT(11) ? 0x7F : 0x7E));  /* 11: no saturation */
+    if (a < ldexp(1.0, -6)) {                      /* subnormal range: m * 2^-9 */
+        const double m = round_half_even(a * (MUT(12) ? 256.0 : 512.0));   /* m = 8: smallest normal */
+        return (unsigned char)(sign | (unsigned char)m);
+    }
+    int e = (int)floor(log2(a));
+    /* guard against log2 landing one off at exact powers of two */
+    if (ldexp(1.0, e) > a) --e;
+    if (ldexp(1.0, e + 1) <= a) ++e;
+    double m = round_half_even((a / ldexp(1.0, e) - 1.0) * 8.0);
+    if (m == 8.0) { m = 0.0; ++e; }
+    if (e > 8 || (e == 8 && m > 6.0)) return (unsigned char)(sign | 0x7E);
+    return (unsigned char)(sign | (unsigned char)(((e + 7) << 3) | (int)m));
+}
+
+/* Value of a code; NaN for S.1111.111. */
+double oracle_e4m3_decode(unsigned char c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = m * ldexp(1.0, -9);
+    else v = (1.0 + m / 8.0) * ldexp(1.0, e - 7);
+    return s ? -v : v;
+}
+
+/*
+ * One block: x is rows x cols fp32 values (the bf16 inputs, exactly), row
+ * stride ld.  amax = max |x|; scale = amax / 448 and inv = 448 / amax, both as
+ * fp32 divisions (1 and 1 for an all-zero block); code = encode(fp32(x * inv)).
+ * out is written with row stride ld_out; out_t (if given) receives the
+ * transpose, [cols][rows] with row stride ld_t.
+ */
+int oracle_fp8_quant_block(const float* x, int rows, int cols, long long ld,
+                           unsigned char* out, long long ld_out,
+                           unsigned char* out_t, long long ld_t, float* scale) {
+    if (!x || rows < 0 || cols <= 0 || !scale) return ORACLE_EINVAL;
+    float amax = 0.0f;
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            const float a = fabsf(x[r * ld + c]);
+            if (a > amax) amax = a;
+        }
+    volatile float num = MUT(13) ? 240.0f : 448.0f, den = amax;   /* fp32 divisions, as written */
+    float inv = 1.0f, sc = 1.0f;
+    if (amax > 0.0f) {
+        inv = num / den;
+        sc = den / num;
+    }
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c) {
+            volatile float y = x[r * ld + c] * inv;
+            const unsigned char code = oracle_e4m3_encode(y);
+            if (out) out[r * ld_out + c] = code;
+            if (out_t) out_t[MUT(14) ? (r * ld_t + c) : (c * ld_t + r)] = code;
+        }
+    *scale = sc;
+    return ORACLE_OK;
+}

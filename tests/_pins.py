@@ -277,7 +277,97 @@ def pin_row_subset(mutant=0):
     assert np.array_equal(ls, lse.reshape(-1)[rows])
 
 
+# ------------------------------------------------------------------- FP8
+# The e4m3 format as defined (FlashAttention-3 summary names FP8 and block
+# quantization; the format itself is fixed by its definition): sign, 4 exponent
+# bits with bias 7, 3 mantissa bits, subnormals m * 2^-9, no infinities,
+# S.1111.111 = NaN, largest finite magnitude 448.
+
+def _e4m3_value_by_definition(code):
+    s, e, m = code >> 7, (code >> 3) & 15, code & 7
+    if e == 15 and m == 7:
+        return math.nan
+    v = m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+    return -v if s else v
+
+
+def pin_e4m3_definition(mutant=0):
+    """Values fixed by the format: 1.0, the largest finite 448, the smallest
+    subnormal 2^-9, the smallest normal 2^-6, zero and negative zero, a
+    subnormal, ties to the even mantissa, saturation beyond 448."""
+    want = {1.0: 0x38, 448.0: 0x7E, -448.0: 0xFE, 2.0 ** -9: 0x01, 2.0 ** -6: 0x08,
+            7 * 2.0 ** -9: 0x07, 0.0: 0x00, -1.5: 0xBC, 240.0: 0x77,
+            1.0625: 0x38,           # midway 1 (m=0) / 1.125 (m=1): even m=0
+            1.1875: 0x3A,           # midway 1.125 (m=1) / 1.25 (m=2): even m=2
+            1.5 * 2.0 ** -9: 0x02,  # midway 1 and 2 subnormal steps: even 2
+            460.0: 0x7E, 1000.0: 0x7E, -1e6: 0xFE}
+    for x, c in want.items():
+        got = oracle.e4m3_encode(x, mutant)
+        assert got == c, (x, hex(got), hex(c))
+    assert oracle.e4m3_encode(-0.0, mutant) == 0x80
+
+
+def pin_e4m3_nearest(mutant=0):
+    """Brute force: every finite code round-trips, and random values encode
+    to the nearest finite value (ties to the even mantissa; beyond 448: 448)."""
+    vals = np.array([_e4m3_value_by_definition(c) for c in range(256)])
+    finite = [c for c in range(256) if not math.isnan(vals[c])]
+    for c in finite:
+        if c == 0x80:
+            continue
+        assert oracle.e4m3_encode(vals[c], mutant) == c, hex(c)
+    rng = np.random.default_rng(8)
+    xs = np.concatenate([rng.standard_normal(1500) * 10.0 ** rng.uniform(-3.5, 2.8, 1500),
+                         (vals[finite][:-1] + np.roll(vals[finite], -1)[:-1]) / 2])
+    for x in xs.astype(np.float32):
+        x = float(x)
+        if abs(x) >= 448.0:
+            want_v = math.copysign(448.0, x)
+        else:
+            dist = [abs(vals[c] - x) for c in finite]
+            best = min(dist)
+            cands = [c for c, dd in zip(finite, dist) if dd == best]
+            if len(cands) > 1:           # a tie: the even mantissa
+                cands = [c for c in cands if (c & 1) == 0] or cands
+            want_v = vals[cands[0]]
+        got = oracle.e4m3_encode(x, mutant)
+        assert vals[got] == want_v, (x, hex(got), want_v)
+
+
+def pin_fp8_block_quant(mutant=0):
+    """One scale per 128-row block: scale = amax / 448 (fp32), the amax
+    element encodes to +-448, and every value comes back within half a step:
+    |x - decode(code) * scale| <= max(2^-4 |x|, 2^-10 scale).  V's codes are
+    the transpose of the same block quantised without transposing."""
+    rng = np.random.default_rng(9)
+    B, H, Hkv, N, d = 1, 2, 1, 200, 128
+    q = (rng.standard_normal((B, H, N, d)) * 3).astype(np.float32)
+    k = (rng.standard_normal((B, Hkv, N, d)) * 0.01).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, N, d)).astype(np.float32)
+    v[0, 0, 5, 7] = 40.0
+    qd = oracle.fp8_quantize(q, k, v, mutant)
+    table = np.array([_e4m3_value_by_definition(c) for c in range(256)])
+    for name, x, codes, sc in (("q", q.reshape(2, N, d), qd["q8"], qd["sq"]),
+                               ("k", k.reshape(1, N, d), qd["k8"], qd["sk"])):
+        for g in range(x.shape[0]):
+            for b in range(2):
+                blk = x[g, b * 128:(b + 1) * 128]
+                amax = np.float32(np.abs(blk).max())
+                assert sc[g, b] == np.float32(amax / np.float32(448.0)), name
+                cb = codes[g, b * 128:b * 128 + blk.shape[0]]
+                assert (cb & 0x7F).max() == 0x7E, name
+                back = table[cb] * float(sc[g, b])
+                bound = np.maximum(2.0 ** -4 * np.abs(blk), 2.0 ** -10 * float(sc[g, b]))
+                assert np.all(np.abs(blk - back) <= bound + 1e-30), name
+    assert qd["svmax"][0] == np.float32(40.0 / 448.0)
+    plain = oracle.fp8_quantize(v.reshape(1, 1, N, d), v, v, mutant)["q8"]
+    assert np.array_equal(np.swapaxes(qd["v8t"], 1, 2), plain)
+
+
 ALL_PINS = [
+    pin_e4m3_definition,
+    pin_e4m3_nearest,
+    pin_fp8_block_quant,
     pin_rows_sum_to_one, pin_torch_library, pin_online_matches_three_pass,
     pin_identical_keys, pin_one_hot, pin_causal_row0_and_single_key,
     pin_shift_invariance, pin_golden_closed_form, pin_finite_differences,

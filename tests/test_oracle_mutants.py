@@ -16,6 +16,11 @@ MUTANTS = {
     7: "dS missing the D term",
     8: "dS with the wrong sign",
     9: "dK missing the scale",
+    10: "e4m3 ties rounded away from zero",
+    11: "e4m3 without saturation (NaN code beyond 448)",
+    12: "e4m3 subnormal step 2^-8 instead of 2^-9",
+    13: "block scale amax / 240 instead of amax / 448",
+    14: "V codes not transposed",
 }
 
 
