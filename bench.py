@@ -61,6 +61,8 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="the FP8 (e4m3) forward on a forward-only d=128 workload")
     return ap.parse_args()
 
 
@@ -436,12 +438,139 @@ def run_native(args, w):
         dist.destroy_process_group()
 
 
+def run_native_fp8(args, w):
+    """FP8 forward: `value` times fa_fwd_fp8 on inputs already quantised in HBM;
+    the rate with the quantisation step inside the timing is reported beside
+    it, and `e2e` copies the bf16 inputs in and O, LSE out around both calls."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_online_gb300 as fa
+    from exact_attention_online_gb300 import replicas
+    from exact_attention_online_gb300.inputs import make_inputs
+    from exact_attention_online_gb300.measure import attention_flops
+
+    if "bwd" in w.passes or w.d != 128:
+        raise SystemExit("--fp8 needs a forward-only workload with d = 128")
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+    peaks = load_peaks()
+    q, k, v, _ = make_inputs(replicas.rank_workload(w, rank))
+    B, H, Hkv, N, d = w.B, w.H, w.Hkv, w.N, w.d
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    buf = torch.empty(fa.fa_fp8_buffer_size(B, H, Hkv, N, d), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fa.fa_fp8_quantize(qd, kd, vd, buf, stream)
+
+    def fwd():
+        fa.fa_fwd_fp8(buf, o, lse, Hkv, w.causal, w.scale, stream)
+
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    for _ in range(args.warmup):
+        fwd()
+    torch.cuda.synchronize()
+    if args.steps is None:
+        per = timed(fwd, 5) / 5
+        args.steps = int(min(20000, max(50, math.ceil(3000.0 / max(per, 1e-3)))))
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    launches0 = fa.fa_kernel_launches()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        barrier()
+        ms_total = replicas.max_over_ranks(timed(fwd, args.steps), dev)
+        barrier()
+    launches = fa.fa_kernel_launches() - launches0
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
+    flops_step = attention_flops(w, "fwd")
+    value = replicas.whole_job_rate(flops_step, args.steps, ws, ms_total) / 1e12
+    n_q = max(3, args.steps // 4)
+    q_ms = replicas.max_over_ranks(
+        timed(lambda: fa.fa_fp8_quantize(qd, kd, vd, buf, stream), n_q), dev) / n_q
+    fwd_ms = ms_total / args.steps
+    with_quant = flops_step / ((fwd_ms + q_ms) * 1e-3) / 1e12
+    # e4m3 dense peak: the measured bf16 figure times the nominal fp8/bf16 ratio (2).
+    peak = 2.0 * peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": "fa_fwd_fp8", "achieved": value / ws, "peak": peak,
+                "unit": "TFLOP/s", "frac": value / ws / peak, "traffic": None,
+                "peak_kind": f"2 x bf16_tflops_sustained ({peaks['source']}), nominal fp8:bf16 ratio"}
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+        def e2e_step():
+            for dst, src_ in ((qd, hq), (kd, hk), (vd, hv)):
+                dst.copy_(src_, non_blocking=True)
+            fa.fa_fp8_quantize(qd, kd, vd, buf, stream)
+            fwd()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e = max(3, min(args.steps // 2, 100))
+        e_ms = replicas.max_over_ranks(timed(e2e_step, n_e), dev)
+        e2e = {"value": replicas.whole_job_rate(flops_step, n_e, ws, e_ms) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / n_e}
+    if rank == 0:
+        line = {
+            "metric": "attention fwd TFLOP/s (fp8 e4m3, causal) and % of GB300 dense FP8 peak",
+            "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": fwd_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={B} H={H} Hkv={Hkv} N={N} d={d} "
+                                   f"causal={w.causal} fwd, fp8 e4m3 with 128-row block scales",
+                       "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d, "causal": w.causal,
+                       "flops_per_step": flops_step, "flop_count": "fwd 4BHN^2d (/2 causal)",
+                       "l2": "fp8 inputs and bf16 output larger than L2" if
+                             (buf.numel() + o.numel() * 2) > L2_BYTES else "fits in L2",
+                       "parallelism": f"replicas x{ws} (independent batches)"},
+            "with_quantize": {"tflops": with_quant, "quantize_ms": q_ms},
+            "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+            "clocks": clk.summary(), "gpu_launches": launches,
+            "launches_per_step": launches / args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     from exact_attention_online_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.fp8:
+        run_native_fp8(args, w)
     else:
         run_native(args, w)
 

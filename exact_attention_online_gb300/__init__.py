@@ -175,6 +175,45 @@ def fa_watchdog_selftest(timeout_ns: int, stream=None) -> None:
 
 # Convenience wrappers that allocate outputs with PyTorch (the library itself
 # never allocates).
+def fa_fp8_buffer_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
+    return int(lib().fa_fp8_buffer_size(B, H, Hkv, N, d))
+
+
+def fa_fp8_quantize(q, k, v, fp8_buf, stream=None) -> None:
+    """fp8_buf: a contiguous CUDA tensor of at least fa_fp8_buffer_size() bytes."""
+    B, H, Hkv, N, d = _dims(q, k)
+    bp, bb = _ws(fp8_buf)
+    _check(lib().fa_fp8_quantize(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), bp, bb,
+                                 B, H, Hkv, N, d, _stream(stream)), "fa_fp8_quantize")
+
+
+def fa_fwd_fp8(fp8_buf, o, lse, Hkv: int, causal: bool, scale: float, stream=None) -> None:
+    """o: bf16 [B, H, N, d] (its shape gives B, H, N, d), lse: fp32 [B, H, N]."""
+    if o.dim() != 4:
+        raise ValueError("o must be 4-D [B, H, N, d]")
+    B, H, N, d = o.shape
+    bp, bb = _ws(fp8_buf)
+    _check(lib().fa_fwd_fp8(bp, bb, _bf16(o, "o"), _f32(lse, "lse"), B, H, Hkv, N, d,
+                            int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_fp8")
+
+
+def attention_fp8(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """FP8 forward: quantize (into a new buffer) and attend; returns (O, LSE, buffer)."""
+    import torch
+    B, H, Hkv, N, d = _dims(q, k)
+    if scale is None:
+        scale = d ** -0.5
+    n = fa_fp8_buffer_size(B, H, Hkv, N, d)
+    if n == 0:
+        raise FAError(FA_ERR_UNSUPPORTED, "fa_fp8_buffer_size")
+    buf = torch.empty(n, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fp8_quantize(q, k, v, buf, stream)
+    fa_fwd_fp8(buf, o, lse, Hkv, causal, scale, stream)
+    return o, lse, buf
+
+
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
               precise: bool = False):
     """Returns (o, lse) for bf16 CUDA q [B,H,N,d], k/v [B,Hkv,N,d]; o is bf16, or

@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfa.so")
 
-SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu"]
+SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_fp8.cu"]
 HEADERS = ["sm103_ptx.cuh", "fa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -108,6 +108,12 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_kernel_launches.restype = ctypes.c_longlong
     L.fa_watchdog_selftest.argtypes = [ctypes.c_longlong, vp]
     L.fa_watchdog_selftest.restype = i
+    L.fa_fp8_buffer_size.argtypes = [i, i, i, i, i]
+    L.fa_fp8_buffer_size.restype = sz
+    L.fa_fp8_quantize.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
+    L.fa_fp8_quantize.restype = i
+    L.fa_fwd_fp8.argtypes = [vp, sz, vp, vp, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_fp8.restype = i
     return L
 
 
@@ -128,4 +134,5 @@ def lib() -> ctypes.CDLL:
 EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_precise",
            "fa_bwd_preprocess", "fa_bwd_preprocess_precise", "fa_bwd_dkdv", "fa_bwd_dq_convert",
            "fa_bwd_static_scratch", "fa_device_status", "fa_device_status_detail",
-           "fa_status_string", "fa_kernel_launches", "fa_watchdog_selftest"]
+           "fa_status_string", "fa_kernel_launches", "fa_watchdog_selftest",
+           "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8"]

@@ -156,6 +156,19 @@ bool make_tmap_f32_2d(CUtensorMap* map, const void* base, int inner, long long r
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_u8_3d(CUtensorMap* map, const void* base, int inner, int rows, int outer) {
+    if (!load_encode()) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+    cuuint64_t strides[2] = {(cuuint64_t)inner, (cuuint64_t)inner * (cuuint64_t)rows};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 size_t bwd_workspace_bytes(const Shape& s) {
     const size_t rows = (size_t)s.B * s.H * padded_rows(s.N);
     return align256(rows * 4) * 2 + align256(rows * (size_t)s.d * 4);
@@ -351,5 +364,46 @@ const char* fa_status_string(fa_status s) {
 }
 
 long long fa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t fa_fp8_buffer_size(int B, int H, int Hkv, int N, int d) {
+    if (check_shape(B, H, Hkv, N, d) != FA_OK || d != 128) return 0;
+    return fp8_buffer_bytes(Shape{B, H, Hkv, N, d, 0, 1.0f});
+}
+
+static fa_status check_fp8_buffer(const void* buf, size_t bytes, const Shape& s) {
+    if (!buf) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(buf) % 256 != 0) return FA_ERR_ALIGNMENT;
+    if (bytes < fp8_buffer_bytes(s)) return FA_ERR_WORKSPACE;
+    return FA_OK;
+}
+
+fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, void* fp8_buf,
+                          size_t fp8_buf_bytes, int B, int H, int Hkv, int N, int d,
+                          fa_stream_t stream) {
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_ptr(q), check_ptr(k),
+                                check_ptr(v)});
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    const Shape s{B, H, Hkv, N, d, 0, 1.0f};
+    if ((st = check_fp8_buffer(fp8_buf, fp8_buf_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    return from_cuda(launch_fp8_quantize(s, q, k, v, fp8_buffer_carve(fp8_buf, s),
+                                         (cudaStream_t)stream));
+}
+
+fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_buf_bytes, void* o, float* lse, int B, int H,
+                     int Hkv, int N, int d, int causal, float scale, fa_stream_t stream) {
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(o),
+                                check_ptr(lse)});
+    if (st != FA_OK) return st;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+    if ((st = check_fp8_buffer(fp8_buf, fp8_buf_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    return from_cuda(launch_fwd_fp8(s, fp8_buffer_carve(const_cast<void*>(fp8_buf), s), o, lse,
+                                    g_status_ptr[dev], (cudaStream_t)stream));
+}
 
 }  // extern "C"

@@ -56,6 +56,30 @@ bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int rows, int 
 bool make_tmap_f32_2d(CUtensorMap* map, const void* base, int inner, long long rows,
                       int box_inner, int box_rows);
 
+// 3-D map over a byte tensor [outer][rows][inner] with a {128, 128, 1} box and
+// 128-byte swizzle (inner and rows multiples of 128).
+bool make_tmap_u8_3d(CUtensorMap* map, const void* base, int inner, int rows, int outer);
+
+// FP8 buffer: e4m3 codes of Q [B*H][Np][d], K [B*Hkv][Np][d], V transposed
+// [B*Hkv][d][Np], then fp32 block scales of Q [B*H][Np/128], K and V
+// [B*Hkv][Np/128], and the largest V scale of each kv head [B*Hkv]; each
+// region 256-byte aligned.
+struct Fp8Buffer {
+    uint8_t* q8;
+    uint8_t* k8;
+    uint8_t* v8t;
+    float* sq;
+    float* sk;
+    float* sv;
+    float* svmax;
+};
+size_t fp8_buffer_bytes(const Shape& s);
+Fp8Buffer fp8_buffer_carve(void* base, const Shape& s);
+cudaError_t launch_fp8_quantize(const Shape& s, const void* q, const void* k, const void* v,
+                                const Fp8Buffer& buf, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const Shape& s, const Fp8Buffer& buf, void* o, float* lse,
+                           DeviceStatus* status, cudaStream_t stream);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

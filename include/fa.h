@@ -184,6 +184,56 @@ FA_API fa_status fa_bwd_static_scratch(const void* q, const void* k, const void*
                                        float scale, fa_stream_t stream);
 
 /*
+ * FP8 forward (FlashAttention-3 summary, abstract: FP8 with block
+ * quantization).  Two calls: quantize once, then run the forward on the
+ * quantized tensors.  Head dimension 128 only (FA_ERR_UNSUPPORTED otherwise).
+ *
+ * Quantization (the block granularity is this library's reading of "block
+ * quantization"): for each (batch, head) of Q, K and V and each block of 128
+ * rows, amax = max |x| over the block, scale = amax / 448 and
+ * inv = 448 / amax (fp32 divisions; 1 and 1 for an all-zero block), and each
+ * element becomes the e4m3 code of fp32(x * inv): 1 sign, 4 exponent (bias 7)
+ * and 3 mantissa bits, round to nearest even, magnitudes beyond 448 saturate
+ * to 448.
+ *
+ * fp8_buf is one caller-owned device buffer of fa_fp8_buffer_size() bytes,
+ * 256-byte aligned, laid out as consecutive regions each starting on a
+ * 256-byte boundary (Np = N rounded up to 128, nblk = Np / 128):
+ *   q8    uint8 [B*H][Np][128]       e4m3 codes of Q (zero on rows >= N)
+ *   k8    uint8 [B*Hkv][Np][128]     e4m3 codes of K
+ *   v8t   uint8 [B*Hkv][128][Np]     e4m3 codes of V, transposed (keys last)
+ *   sq    fp32  [B*H][nblk]          block scales of Q
+ *   sk    fp32  [B*Hkv][nblk]        block scales of K
+ *   sv    fp32  [B*Hkv][nblk]        block scales of V
+ *   svmax fp32  [B*Hkv]              largest V block scale of each kv head
+ * fa_fp8_buffer_size() returns 0 for an invalid shape or d != 128.
+ */
+FA_API size_t fa_fp8_buffer_size(int B, int H, int Hkv, int N, int d);
+
+/*
+ * Fills fp8_buf from bf16 q [B][H][N][d], k and v [B][Hkv][N][d].  Errors:
+ * FA_ERR_INVALID_ARG (shape, null tensor), FA_ERR_UNSUPPORTED (d != 128),
+ * FA_ERR_WORKSPACE (null or too small buffer), FA_ERR_ALIGNMENT (buffer not
+ * 256-byte aligned), FA_ERR_CUDA.  Asynchronous on `stream`; two launches.
+ */
+FA_API fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, void* fp8_buf,
+                                 size_t fp8_buf_bytes, int B, int H, int Hkv, int N, int d,
+                                 fa_stream_t stream);
+
+/*
+ * Attention forward from a buffer filled by fa_fp8_quantize(): S = Q K^T from
+ * the e4m3 codes with the block scales applied in the exponent, the softmax in
+ * fp32, P quantized to e4m3 (p * 448 * sv_j / svmax for key block j), O
+ * accumulated in fp32 and written as bf16 o [B][H][N][d] with the fp32
+ * natural-log LSE [B][H][N] of the quantized problem.  Same shapes, causal
+ * convention and errors as fa_fwd() (plus FA_ERR_UNSUPPORTED for d != 128 and
+ * the buffer errors above).  Asynchronous on `stream`; one launch.
+ */
+FA_API fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_buf_bytes, void* o, float* lse,
+                            int B, int H, int Hkv, int N, int d, int causal, float scale,
+                            fa_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device status word of the
  * current device: FA_OK, or the first error a kernel recorded (for example
  * FA_ERR_TIMEOUT when a bounded wait ran out).  Returns FA_ERR_CUDA if the
