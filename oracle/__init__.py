@@ -12,6 +12,8 @@ Functions (NumPy float64 in, NumPy float64 out; layouts as in the C file):
     attn_fwd_online   one-pass online-softmax attention in key blocks, normalised
                       (blog "FlashAttention", o_N = o'_N) or deferred division
                       (FlashAttention-2 answer on non-matmul FLOPs).
+    attn_fwd_decode   fewer query rows than keys (the decoding setting), the
+                      queries being the last positions (bottom-right causal).
     attn_bwd          analytic gradients dQ, dK, dV and D = rowsum(dO * O).
     e4m3_encode/decode  the e4m3 format from its definition (round to nearest,
                       ties to even, saturating at 448).
@@ -67,6 +69,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attn_bwd.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
+    lib.oracle_attn_fwd_decode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, i, d]
+    lib.oracle_attn_fwd_decode.restype = i
     u8p = ctypes.POINTER(ctypes.c_ubyte)
     fp = ctypes.POINTER(ctypes.c_float)
     ll = ctypes.c_longlong
@@ -154,6 +158,23 @@ def attn_fwd_online(q, k, v, causal: bool, scale: float, block: int = 1,
                                              B, H, Hkv, N, d, int(causal), float(scale),
                                              int(block), int(deferred))
     _check(rc, "oracle_attn_fwd_online")
+    return o, lse
+
+
+def attn_fwd_decode(q, k, v, causal: bool, scale: float, mutant: int = 0):
+    """Fewer queries than keys: q [B,H,Nq,d], k/v [B,Hkv,Nk,d], Nq <= Nk; the
+    queries are the last Nq positions (causal: query r sees keys
+    j <= r + Nk - Nq).  Returns (O [B,H,Nq,d], LSE [B,H,Nq])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("q, k, v shapes disagree")
+    o = np.empty_like(q)
+    lse = np.empty((B, H, Nq))
+    rc = load(mutant).oracle_attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                             B, H, Hkv, Nq, Nk, d, int(causal), float(scale))
+    _check(rc, "oracle_attn_fwd_decode")
     return o, lse
 
 

@@ -454,3 +454,60 @@ int oracle_fp8_quant_block(const float* x, int rows, int cols, long long ld,
     *scale = sc;
     return ORACLE_OK;
 }
+
+/*
+ * Attention forward with fewer queries than keys, as in decoding with a cache
+ * of Nk keys (the decoding setting of the FlashAttention blog and FA2 review
+ * thread: few new query rows against a long key/value sequence).  q is
+ * [B][H][Nq][d], k and v [B][Hkv][Nk][d], o [B][H][Nq][d], lse [B][H][Nq].
+ * The queries are the last Nq positions of the sequence: under the causal
+ * mask query r sees key j iff j <= r + (Nk - Nq) (bottom-right alignment,
+ * which is the j <= i rule of oracle_attn_fwd when Nq == Nk).  Scores, the
+ * three-loop safe softmax, O and LSE as in oracle_attn_fwd.
+ */
+int oracle_attn_fwd_decode(const double* q, const double* k, const double* v,
+                           double* o, double* lse, int B, int H, int Hkv, int Nq, int Nk,
+                           int d, int causal, double scale) {
+    if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < Nq || d < 1 || H % Hkv) return ORACLE_EINVAL;
+    const long long total = (long long)B * H * Nq;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+        double* p = (double*)malloc(sizeof(double) * (size_t)Nk);
+        if (!s || !p) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long long flat = 0; flat < total; ++flat) {
+                const int r = (int)(flat % Nq);
+                const long long bh = flat / Nq;
+                const int h = (int)(bh % H), b = (int)(bh / H);
+                const int g = kv_head_of(h, H, Hkv);
+                const double* qr = q + (size_t)flat * d;
+                const double* kh = k + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+                const double* vh = v + ((size_t)b * Hkv + g) * (size_t)Nk * d;
+                const int last = MUT(15) ? r : r + (Nk - Nq);   /* 15: top-left alignment */
+                for (int j = 0; j < Nk; ++j) {
+                    if (causal && j > last) { s[j] = -INFINITY; continue; }
+                    double acc = 0.0;
+                    for (int c = 0; c < d; ++c) acc += qr[c] * kh[(size_t)j * d + c];
+                    s[j] = scale * acc;
+                }
+                double m, l;
+                safe_softmax_row(s, Nk, p, &m, &l);
+                double* orow = o + (size_t)flat * d;
+                for (int c = 0; c < d; ++c) orow[c] = 0.0;
+                for (int j = 0; j < Nk; ++j) {
+                    if (p[j] == 0.0) continue;
+                    for (int c = 0; c < d; ++c) orow[c] += p[j] * vh[(size_t)j * d + c];
+                }
+                lse[flat] = (m == -INFINITY) ? -INFINITY : m + log(l);
+            }
+        }
+        free(s);
+        free(p);
+    }
+    return err ? ORACLE_ENOMEM : ORACLE_OK;
+}

@@ -364,7 +364,36 @@ def pin_fp8_block_quant(mutant=0):
     assert np.array_equal(np.swapaxes(qd["v8t"], 1, 2), plain)
 
 
+def pin_decode_rows(mutant=0):
+    """Fewer queries than keys: with the queries taken as the last Nq rows of a
+    square problem, the result equals those rows of the square oracle (causal
+    and not), and a library special case (torch fp64 softmax with an explicit
+    bottom-right mask) agrees."""
+    rng = np.random.default_rng(11)
+    B, H, Hkv, Nk, d, scale = 1, 4, 2, 37, 16, 0.3
+    q = rng.standard_normal((B, H, Nk, d))
+    k = rng.standard_normal((B, Hkv, Nk, d))
+    v = rng.standard_normal((B, Hkv, Nk, d))
+    for causal in (False, True):
+        ro, rl = oracle.attn_fwd(q, k, v, causal, scale)
+        for nq in (1, 5, Nk):
+            o, l = oracle.attn_fwd_decode(q[:, :, Nk - nq:], k, v, causal, scale, mutant)
+            assert np.allclose(o, ro[:, :, Nk - nq:], rtol=1e-12, atol=1e-12), (causal, nq)
+            assert np.allclose(l, rl[:, :, Nk - nq:], rtol=1e-12, atol=1e-12), (causal, nq)
+    nq = 3
+    qt = torch.as_tensor(q[:, :, Nk - nq:])
+    kt = torch.as_tensor(k).repeat_interleave(H // Hkv, dim=1)
+    vt = torch.as_tensor(v).repeat_interleave(H // Hkv, dim=1)
+    s = qt @ kt.transpose(-1, -2) * scale
+    r = torch.arange(nq)[:, None] + (Nk - nq)
+    s = s.masked_fill(torch.arange(Nk)[None, :] > r, float("-inf"))
+    want = torch.softmax(s, -1) @ vt
+    o, _ = oracle.attn_fwd_decode(q[:, :, Nk - nq:], k, v, True, scale, mutant)
+    assert np.allclose(o, want.numpy(), rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [
+    pin_decode_rows,
     pin_e4m3_definition,
     pin_e4m3_nearest,
     pin_fp8_block_quant,

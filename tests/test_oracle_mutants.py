@@ -21,6 +21,7 @@ MUTANTS = {
     12: "e4m3 subnormal step 2^-8 instead of 2^-9",
     13: "block scale amax / 240 instead of amax / 448",
     14: "V codes not transposed",
+    15: "decoding queries aligned top-left instead of bottom-right",
 }
 
 
