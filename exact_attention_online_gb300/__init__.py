@@ -214,6 +214,41 @@ def attention_fp8(q, k, v, causal: bool = False, scale: float | None = None, str
     return o, lse, buf
 
 
+def fa_fwd_decode_workspace_size(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    return int(lib().fa_fwd_decode_workspace_size(B, H, Hkv, Nq, Nk, d))
+
+
+def fa_fwd_decode(q, k, v, o, lse, workspace, causal: bool, scale: float, stream=None) -> None:
+    """q, o: bf16 [B, H, Nq, d]; k, v: bf16 [B, Hkv, Nk, d]; lse: fp32 [B, H, Nq]."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be 4-D")
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)} disagree")
+    wp, wb = _ws(workspace)
+    _check(lib().fa_fwd_decode(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                               _f32(lse, "lse"), wp, wb, B, H, Hkv, Nq, Nk, d,
+                               int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_decode")
+
+
+def attention_decode(q, k, v, causal: bool = True, scale: float | None = None, stream=None):
+    """Decoding forward; allocates the output, LSE and workspace."""
+    import torch
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    n = fa_fwd_decode_workspace_size(B, H, Hkv, Nq, Nk, d)
+    if n == 0:
+        raise FAError(FA_ERR_UNSUPPORTED, "fa_fwd_decode_workspace_size")
+    work = torch.empty(n, dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd_decode(q, k, v, o, lse, work, causal, scale, stream)
+    return o, lse
+
+
 def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
               precise: bool = False):
     """Returns (o, lse) for bf16 CUDA q [B,H,N,d], k/v [B,Hkv,N,d]; o is bf16, or

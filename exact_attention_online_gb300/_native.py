@@ -19,7 +19,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfa.so")
 
-SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_fp8.cu"]
+SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_fp8.cu", "fa_decode.cu"]
 HEADERS = ["sm103_ptx.cuh", "fa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -114,6 +114,10 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_fp8_quantize.restype = i
     L.fa_fwd_fp8.argtypes = [vp, sz, vp, vp, i, i, i, i, i, i, f, vp]
     L.fa_fwd_fp8.restype = i
+    L.fa_fwd_decode_workspace_size.argtypes = [i, i, i, i, i, i]
+    L.fa_fwd_decode_workspace_size.restype = sz
+    L.fa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_decode.restype = i
     return L
 
 
@@ -135,4 +139,5 @@ EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bw
            "fa_bwd_preprocess", "fa_bwd_preprocess_precise", "fa_bwd_dkdv", "fa_bwd_dq_convert",
            "fa_bwd_static_scratch", "fa_device_status", "fa_device_status_detail",
            "fa_status_string", "fa_kernel_launches", "fa_watchdog_selftest",
-           "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8"]
+           "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8",
+           "fa_fwd_decode_workspace_size", "fa_fwd_decode"]

@@ -406,4 +406,36 @@ fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_buf_bytes, void* o, float* 
                                     g_status_ptr[dev], (cudaStream_t)stream));
 }
 
+static fa_status check_decode_shape(int B, int H, int Hkv, int Nq, int Nk, int d) {
+    if (B < 1 || H < 1 || Hkv < 1 || Nq < 1 || Nk < Nq || d < 1 || H % Hkv != 0)
+        return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if ((long long)(H / Hkv) * Nq > kDecodeMaxRows) return FA_ERR_UNSUPPORTED;
+    if ((long long)B * Hkv * Nk * d >= (1LL << 31) || (long long)B * H * Nq * d >= (1LL << 31))
+        return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+size_t fa_fwd_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d) {
+    if (check_decode_shape(B, H, Hkv, Nq, Nk, d) != FA_OK) return 0;
+    return decode_workspace_bytes(B, H, Hkv, Nq, Nk, d);
+}
+
+fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                        void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int Nq,
+                        int Nk, int d, int causal, float scale, fa_stream_t stream) {
+    fa_status st = first_error({check_decode_shape(B, H, Hkv, Nq, Nk, d), check_scale(scale),
+                                check_ptr(q), check_ptr(k), check_ptr(v), check_ptr(o),
+                                check_ptr(lse)});
+    if (st != FA_OK) return st;
+    if (!workspace || workspace_bytes < decode_workspace_bytes(B, H, Hkv, Nq, Nk, d))
+        return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return FA_ERR_ALIGNMENT;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    return from_cuda(launch_fwd_decode(q, k, v, o, lse, workspace, B, H, Hkv, Nq, Nk, d,
+                                       causal ? 1 : 0, scale, g_status_ptr[dev],
+                                       (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -112,3 +112,47 @@ def make_inputs(w: Workload, with_dout: bool = True):
     out = [t.to(torch.bfloat16) for t in (q, k, v)]
     out.append(dout.to(torch.bfloat16) if with_dout else None)
     return tuple(out)
+
+
+# ------------------------------------------------------------------ decoding
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq new query rows against a cache of Nk keys and values (the queries
+    are the last Nq positions)."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+# Decoding shapes (the pages describe the setting, not sizes): a GQA model
+# decoding one token per sequence against a 32K cache (1.07 GB of K and V), a
+# speculative step of 4 tokens against a 16K cache, and an MHA d = 64 step.
+DECODE_WORKLOADS = {
+    "decode_gqa": DecodeWorkload("decode_gqa", B=8, H=32, Hkv=8, Nq=1, Nk=32768, d=128,
+                                 causal=True, seed=1101),
+    "decode_spec4": DecodeWorkload("decode_spec4", B=8, H=32, Hkv=8, Nq=4, Nk=16384, d=128,
+                                   causal=True, seed=1102),
+    "decode_mha_d64": DecodeWorkload("decode_mha_d64", B=16, H=16, Hkv=16, Nq=1, Nk=8192, d=64,
+                                     causal=True, seed=1103),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload):
+    """(q [B, H, Nq, d], k, v [B, Hkv, Nk, d]) as CPU bf16 tensors: one
+    torch.Generator seeded with w.seed, N(0, 1) fp32 draws in the order Q, K,
+    V, rounded to bf16 (round to nearest even)."""
+    gen = torch.Generator().manual_seed(int(w.seed))
+    q = torch.randn((w.B, w.H, w.Nq, w.d), generator=gen, dtype=torch.float32)
+    k = torch.randn((w.B, w.Hkv, w.Nk, w.d), generator=gen, dtype=torch.float32)
+    v = torch.randn((w.B, w.Hkv, w.Nk, w.d), generator=gen, dtype=torch.float32)
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v))

@@ -234,6 +234,26 @@ FA_API fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_buf_bytes, void* o, 
                             fa_stream_t stream);
 
 /*
+ * Split-KV decoding forward (FlashAttention blog, "Flash-Decoding"; the
+ * decoding setting of the FA2 review thread): Nq new query rows against Nk >=
+ * Nq keys.  q and o are bf16 [B][H][Nq][d], k and v bf16 [B][Hkv][Nk][d], lse
+ * fp32 [B][H][Nq] (natural log).  The queries are the last Nq positions:
+ * with causal != 0 query row r sees keys j <= r + Nk - Nq (bottom-right
+ * alignment; the same rule as fa_fwd() when Nq == Nk).  The keys are split
+ * across CTAs, each split's partial output and LSE go to the workspace, and a
+ * second kernel combines them (two launches).  d in {64, 128}; (H / Hkv) * Nq
+ * <= 16 (FA_ERR_UNSUPPORTED otherwise).  workspace: caller-owned device
+ * memory of fa_fwd_decode_workspace_size() bytes, 256-byte aligned
+ * (FA_ERR_WORKSPACE if null or smaller, FA_ERR_ALIGNMENT if misaligned).
+ * Tensors 16-byte aligned.  Asynchronous on `stream`.
+ */
+FA_API size_t fa_fwd_decode_workspace_size(int B, int H, int Hkv, int Nq, int Nk, int d);
+FA_API fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                               void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                               int Nq, int Nk, int d, int causal, float scale,
+                               fa_stream_t stream);
+
+/*
  * Synchronizes `stream`, then reads and clears the device status word of the
  * current device: FA_OK, or the first error a kernel recorded (for example
  * FA_ERR_TIMEOUT when a bounded wait ran out).  Returns FA_ERR_CUDA if the
