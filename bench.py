@@ -48,6 +48,8 @@ NCU_TRAFFIC = {
     ("fa_bwd_dkdv", "mha_d64"): {"bytes": 291.84e6, "src_sha": "b9a8b2f4a0ecb419"},
     # profiles/fa_fwd_mha_d64.md: 112.8 MB read + 13.1 MB written, one launch
     ("fa_fwd", "mha_d64"): {"bytes": 125.84e6, "src_sha": "7d54771fdf717a16"},
+    # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 5.1 MB written, one launch
+    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0790e9, "src_sha": "6f9c75dfde0d8a68"},
 }
 
 
@@ -63,6 +65,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="the FP8 (e4m3) forward on a forward-only d=128 workload")
+    ap.add_argument("--decode", default=None,
+                    help="a split-KV decoding workload (decode_gqa, decode_spec4, decode_mha_d64)")
     return ap.parse_args()
 
 
@@ -563,11 +567,139 @@ def run_native_fp8(args, w):
         dist.destroy_process_group()
 
 
+def run_native_decode(args):
+    """Split-KV decoding forward.  `value` is the whole-job HBM bandwidth of
+    fa_fwd_decode on inputs resident in HBM: algorithmic bytes per step (K and
+    V read once, q read, O and LSE written) over the step time; the roofline
+    is against the measured copy bandwidth.  `e2e` copies the step's new query
+    rows in and O, LSE out around the call (the key/value cache stays on the
+    device, as in decoding)."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_online_gb300 as fa
+    from exact_attention_online_gb300 import replicas
+    from exact_attention_online_gb300.inputs import DECODE_WORKLOADS, make_decode_inputs
+
+    w = DECODE_WORKLOADS[args.decode]
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+    peaks = load_peaks()
+    import dataclasses
+    wr = dataclasses.replace(w, seed=w.seed + 7919 * rank)   # each rank its own batch
+    q, k, v = make_decode_inputs(wr)
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    B, H, Hkv, Nq, Nk, d = w.B, w.H, w.Hkv, w.Nq, w.Nk, w.d
+    work = torch.empty(fa.fa_fwd_decode_workspace_size(B, H, Hkv, Nq, Nk, d), dtype=torch.uint8,
+                       device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_fwd_decode(qd, kd, vd, o, lse, work, w.causal, w.scale, stream)
+
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if args.steps is None:
+        per = timed(step, 10) / 10
+        args.steps = int(min(20000, max(50, math.ceil(3000.0 / max(per, 1e-3)))))
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    launches0 = fa.fa_kernel_launches()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        barrier()
+        ms_total = replicas.max_over_ranks(timed(step, args.steps), dev)
+        barrier()
+    launches = fa.fa_kernel_launches() - launches0
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
+    ms_step = ms_total / args.steps
+    alg_bytes = (kd.numel() + vd.numel() + qd.numel() + o.numel()) * 2 + lse.numel() * 4
+    value = alg_bytes * args.steps * ws / (ms_total * 1e-3) / 1e9
+    flops = 4.0 * B * H * Nq * Nk * d
+    peak = peaks["hbm_gbs"]
+    tr = NCU_TRAFFIC.get(("fa_decode_split", w.name))
+    traffic = tr["bytes"] if tr and tr["src_sha"] == kernel_source_hash("fa_decode.cu") else None
+    roofline = {"bound": "hbm", "kernel": "fa_decode_split_kernel + combine",
+                "achieved": value / ws, "peak": peak, "unit": "GB/s", "frac": value / ws / peak,
+                "traffic": traffic, "bytes_per_step": alg_bytes,
+                "peak_kind": f"hbm_gbs ({peaks['source']})"}
+    e2e = None
+    if not args.no_e2e:
+        hq = q.pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            qd.copy_(hq, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e = max(3, min(args.steps // 2, 300))
+        e_ms = replicas.max_over_ranks(timed(e2e_step, n_e), dev)
+        e2e = {"value": alg_bytes * n_e * ws / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": hq.numel() * 2,
+               "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4,
+               "ms_per_step": e_ms / n_e,
+               "note": "key/value cache resident on the device; the new query rows in, O and LSE out"}
+    if rank == 0:
+        line = {
+            "metric": "decoding forward HBM GB/s (bf16, split-KV) and % of measured HBM bandwidth",
+            "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B={B} H={H} Hkv={Hkv} Nq={Nq} Nk={Nk} d={d} "
+                                   f"causal={w.causal} decoding forward",
+                       "B": B, "H": H, "Hkv": Hkv, "Nq": Nq, "Nk": Nk, "d": d,
+                       "causal": w.causal, "bytes_per_step": alg_bytes,
+                       "l2": f"K and V larger than L2: {(kd.numel() + vd.numel()) * 2 / 2**20:.0f}"
+                             f" MiB per step vs {L2_BYTES / 2**20:.0f} MiB L2",
+                       "parallelism": f"replicas x{ws} (independent batches)"},
+            "tflops": flops * args.steps * ws / (ms_total * 1e-3) / 1e12,
+            "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+            "clocks": clk.summary(), "gpu_launches": launches,
+            "launches_per_step": launches / args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     from exact_attention_online_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if args.decode and args.impl != "reference":
+        run_native_decode(args)
+    elif args.impl == "reference":
         run_reference(args, w)
     elif args.fp8:
         run_native_fp8(args, w)
