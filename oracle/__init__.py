@@ -12,6 +12,8 @@ Functions (NumPy float64 in, NumPy float64 out; layouts as in the C file):
     attn_fwd_online   one-pass online-softmax attention in key blocks, normalised
                       (blog "FlashAttention", o_N = o'_N) or deferred division
                       (FlashAttention-2 answer on non-matmul FLOPs).
+    attn_fwd_window / attn_bwd_window
+                      causal sliding window: query i sees keys i - W < j <= i.
     attn_fwd_decode   fewer query rows than keys (the decoding setting), the
                       queries being the last positions (bottom-right causal).
     attn_bwd          analytic gradients dQ, dK, dV and D = rowsum(dO * O).
@@ -69,6 +71,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_attn_bwd.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
+    lib.oracle_attn_fwd_window.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, d]
+    lib.oracle_attn_fwd_window.restype = i
+    lib.oracle_attn_bwd_window.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, i, d]
+    lib.oracle_attn_bwd_window.restype = i
     lib.oracle_attn_fwd_decode.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, i, i, d]
     lib.oracle_attn_fwd_decode.restype = i
     u8p = ctypes.POINTER(ctypes.c_ubyte)
@@ -159,6 +165,34 @@ def attn_fwd_online(q, k, v, causal: bool, scale: float, block: int = 1,
                                              int(block), int(deferred))
     _check(rc, "oracle_attn_fwd_online")
     return o, lse
+
+
+def attn_fwd_window(q, k, v, window: int, scale: float, mutant: int = 0):
+    """Causal sliding-window attention: query i sees keys i - window < j <= i.
+    Returns (O, LSE)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Hkv, N, d = _shape(q, k)
+    o = np.empty_like(q)
+    lse = np.empty((B, H, N))
+    rc = load(mutant).oracle_attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                             B, H, Hkv, N, d, int(window), float(scale))
+    _check(rc, "oracle_attn_fwd_window")
+    return o, lse
+
+
+def attn_bwd_window(q, k, v, dout, window: int, scale: float, mutant: int = 0):
+    """Analytic backward of attn_fwd_window; returns (dQ, dK, dV, D)."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, H, Hkv, N, d = _shape(q, k)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    D = np.empty((B, H, N))
+    rc = load(mutant).oracle_attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
+                                             _ptr(dk), _ptr(dv), _ptr(D), B, H, Hkv, N, d,
+                                             int(window), float(scale))
+    _check(rc, "oracle_attn_bwd_window")
+    return dq, dk, dv, D
 
 
 def attn_fwd_decode(q, k, v, causal: bool, scale: float, mutant: int = 0):

@@ -70,18 +70,20 @@ static int kv_head_of(int h, int H, int Hkv) {
     return h / (H / Hkv);
 }
 
-/* Visibility of key j to query i. */
-static int visible(int i, int j, int causal) {
+/* Visibility of key j to query i.  window > 0 (with causal): a sliding
+ * window of the window most recent keys, i - window < j <= i. */
+static int visible(int i, int j, int causal, int window) {
     if (!causal) return 1;
+    if (window > 0 && i - j >= (MUT(16) ? window + 1 : window)) return 0;
     if (MUT(2)) return j < i;
     return j <= i;
 }
 
 /* One row of scaled scores: s[j] = scale * <q_i, k_j>, -inf where masked. */
 static void score_row(const double* qi, const double* kh, int N, int d, int i,
-                      int causal, double scale, double* s) {
+                      int causal, int window, double scale, double* s) {
     for (int j = 0; j < N; ++j) {
-        if (!visible(i, j, causal)) { s[j] = -INFINITY; continue; }
+        if (!visible(i, j, causal, window)) { s[j] = -INFINITY; continue; }
         const double* kj = kh + (size_t)j * d;
         double acc = 0.0;
         for (int c = 0; c < d; ++c) acc += qi[c] * kj[c];
@@ -110,10 +112,10 @@ static void safe_softmax_row(const double* s, int N, double* p, double* m_out, d
  *   outputs are written compactly: o[r*d ...], lse[r].
  *   p_out (optional, only with rows == NULL) receives P as [B][H][N][N].
  */
-int oracle_attn_fwd(const double* q, const double* k, const double* v,
-                    double* o, double* lse, double* p_out,
-                    int B, int H, int Hkv, int N, int d, int causal, double scale,
-                    const long long* rows, long long n_rows) {
+static int attn_fwd_impl(const double* q, const double* k, const double* v,
+                         double* o, double* lse, double* p_out,
+                         int B, int H, int Hkv, int N, int d, int causal, int window,
+                         double scale, const long long* rows, long long n_rows) {
     int rc = check_shape(B, H, Hkv, N, d);
     if (rc) return rc;
     if (rows && p_out) return ORACLE_EINVAL;
@@ -143,7 +145,7 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v,
                 const double* kh = k + ((size_t)b * Hkv + g) * (size_t)N * d;
                 const double* vh = v + ((size_t)b * Hkv + g) * (size_t)N * d;
                 double m, l;
-                score_row(qi, kh, N, d, i, causal, scale, s);
+                score_row(qi, kh, N, d, i, causal, window, scale, s);
                 safe_softmax_row(s, N, p, &m, &l);
                 double* oi = o + (size_t)(rows ? r : flat) * d;
                 for (int c = 0; c < d; ++c) oi[c] = 0.0;
@@ -164,6 +166,22 @@ int oracle_attn_fwd(const double* q, const double* k, const double* v,
     if (err == 1) return ORACLE_ENOMEM;
     if (err == 2) return ORACLE_EINVAL;
     return ORACLE_OK;
+}
+
+int oracle_attn_fwd(const double* q, const double* k, const double* v,
+                    double* o, double* lse, double* p_out,
+                    int B, int H, int Hkv, int N, int d, int causal, double scale,
+                    const long long* rows, long long n_rows) {
+    return attn_fwd_impl(q, k, v, o, lse, p_out, B, H, Hkv, N, d, causal, 0, scale, rows, n_rows);
+}
+
+/* The same with a causal sliding window (window > 0: query i sees keys
+ * i - window < j <= i, local attention). */
+int oracle_attn_fwd_window(const double* q, const double* k, const double* v,
+                           double* o, double* lse, int B, int H, int Hkv, int N, int d,
+                           int window, double scale) {
+    if (window < 1) return ORACLE_EINVAL;
+    return attn_fwd_impl(q, k, v, o, lse, NULL, B, H, Hkv, N, d, 1, window, scale, NULL, 0);
 }
 
 /*
@@ -210,7 +228,7 @@ int oracle_attn_fwd_online(const double* q, const double* k, const double* v,
                     double mb = -INFINITY;
                     for (int t = 0; t < nb; ++t) {
                         int j = j0 + t;
-                        if (!visible(i, j, causal)) { s[t] = -INFINITY; continue; }
+                        if (!visible(i, j, causal, 0)) { s[t] = -INFINITY; continue; }
                         const double* kj = kh + (size_t)j * d;
                         double a = 0.0;
                         for (int c = 0; c < d; ++c) a += qi[c] * kj[c];
@@ -272,9 +290,10 @@ int oracle_attn_fwd_online(const double* q, const double* k, const double* v,
  * Work is split over query rows; dK and dV are summed from per-thread
  * accumulators (a plain reduction, no change to what is summed).
  */
-int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
-                    double* dq, double* dk, double* dv, double* D_out,
-                    int B, int H, int Hkv, int N, int d, int causal, double scale) {
+static int attn_bwd_impl(const double* q, const double* k, const double* v, const double* dout,
+                         double* dq, double* dk, double* dv, double* D_out,
+                         int B, int H, int Hkv, int N, int d, int causal, int window,
+                         double scale) {
     int rc = check_shape(B, H, Hkv, N, d);
     if (rc) return rc;
     size_t kv_elems = (size_t)B * Hkv * N * d;
@@ -309,7 +328,7 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
                         const double* qi = q + flat * d;
                         const double* doi = dout + flat * d;
                         double m, l;
-                        score_row(qi, kh, N, d, i, causal, scale, s);
+                        score_row(qi, kh, N, d, i, causal, window, scale, s);
                         safe_softmax_row(s, N, p, &m, &l);
                         for (int c = 0; c < d; ++c) oi[c] = 0.0;
                         for (int j = 0; j < N; ++j) {
@@ -356,6 +375,20 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
         }
     }
     return ORACLE_OK;
+}
+
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv, double* D_out,
+                    int B, int H, int Hkv, int N, int d, int causal, double scale) {
+    return attn_bwd_impl(q, k, v, dout, dq, dk, dv, D_out, B, H, Hkv, N, d, causal, 0, scale);
+}
+
+/* Backward with a causal sliding window (see oracle_attn_fwd_window). */
+int oracle_attn_bwd_window(const double* q, const double* k, const double* v, const double* dout,
+                           double* dq, double* dk, double* dv, double* D_out,
+                           int B, int H, int Hkv, int N, int d, int window, double scale) {
+    if (window < 1) return ORACLE_EINVAL;
+    return attn_bwd_impl(q, k, v, dout, dq, dk, dv, D_out, B, H, Hkv, N, d, 1, window, scale);
 }
 
 /* Number of OpenMP threads the oracle uses (reported beside its timings). */

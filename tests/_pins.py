@@ -392,7 +392,46 @@ def pin_decode_rows(mutant=0):
     assert np.allclose(o, want.numpy(), rtol=1e-12, atol=1e-12)
 
 
+def pin_sliding_window(mutant=0):
+    """Causal sliding window (query i sees keys i - W < j <= i): a window of N
+    or more is the causal result (forward and gradients); W = 1 gives
+    O_i = V_i and LSE_i = scale q_i.k_i exactly; a library special case (torch
+    fp64 softmax with an explicit band mask, and its autograd) agrees."""
+    rng = np.random.default_rng(12)
+    B, H, Hkv, N, d, scale = 1, 4, 2, 29, 8, 0.35
+    q, k, v, do = rand_qkv(B, H, Hkv, N, d, 12, dout=True)
+    ro, rl = oracle.attn_fwd(q, k, v, True, scale)
+    o, l = oracle.attn_fwd_window(q, k, v, N + 3, scale, mutant)
+    assert np.allclose(o, ro, rtol=1e-12, atol=1e-12) and np.allclose(l, rl, rtol=1e-12, atol=1e-12)
+    g_ref = oracle.attn_bwd(q, k, v, do, True, scale)
+    g_w = oracle.attn_bwd_window(q, k, v, do, N, scale, mutant)
+    for a, b in zip(g_ref, g_w):
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+    o1, l1 = oracle.attn_fwd_window(q, k, v, 1, scale, mutant)
+    G = H // Hkv
+    vv = np.repeat(v, G, axis=1)
+    kk = np.repeat(k, G, axis=1)
+    assert np.allclose(o1, vv, rtol=1e-12, atol=1e-12)
+    assert np.allclose(l1, scale * np.einsum("bhnd,bhnd->bhn", q, kk), rtol=1e-12, atol=1e-12)
+    W = 5
+    qt, kt, vt, dot = (torch.tensor(x, requires_grad=True) for x in (q, k, v, do))
+    ke, ve = kt.repeat_interleave(G, dim=1), vt.repeat_interleave(G, dim=1)
+    s = qt @ ke.transpose(-1, -2) * scale
+    i_ = torch.arange(N)[:, None]
+    j_ = torch.arange(N)[None, :]
+    s = s.masked_fill((j_ > i_) | (i_ - j_ >= W), float("-inf"))
+    out = torch.softmax(s, -1) @ ve
+    (out * dot.detach()).sum().backward()
+    ow, _ = oracle.attn_fwd_window(q, k, v, W, scale, mutant)
+    assert np.allclose(ow, out.detach().numpy(), rtol=1e-12, atol=1e-12)
+    gq, gk, gv, _ = oracle.attn_bwd_window(q, k, v, do, W, scale, mutant)
+    assert np.allclose(gq, qt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(gk, kt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(gv, vt.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
 ALL_PINS = [
+    pin_sliding_window,
     pin_decode_rows,
     pin_e4m3_definition,
     pin_e4m3_nearest,

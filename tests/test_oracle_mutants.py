@@ -22,6 +22,7 @@ MUTANTS = {
     13: "block scale amax / 240 instead of amax / 448",
     14: "V codes not transposed",
     15: "decoding queries aligned top-left instead of bottom-right",
+    16: "sliding window one key too wide",
 }
 
 
