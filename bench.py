@@ -156,6 +156,7 @@ def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int = 16, min_heads:
     from exact_attention_online_gb300.inputs import make_inputs
     from exact_attention_online_gb300.measure import attention_flops
 
+    w = oracle_sample_workload(w)
     one = w.with_(B=1, H=w.H // w.Hkv, Hkv=1)          # one kv group of batch 0
     q, k, v, do = make_inputs(w.with_(B=1))
     G = w.H // w.Hkv
@@ -171,6 +172,9 @@ def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int = 16, min_heads:
             # forward rows are independent: a bounded sample of query rows
             rows = list(range(0, G * w.N, max(1, (G * w.N) // 512)))
             oracle.attn_fwd(qs, ks, vs, w.causal, w.scale, rows=rows)
+        elif w.window:
+            oracle.attn_fwd_window(qs, ks, vs, w.window, w.scale)
+            oracle.attn_bwd_window(qs, ks, vs, ds, w.window, w.scale)
         else:
             oracle.attn_fwd(qs, ks, vs, w.causal, w.scale)
             oracle.attn_bwd(qs, ks, vs, ds, w.causal, w.scale)
@@ -189,8 +193,18 @@ def cpu_oracle_sample(w, budget_s: float = 12.0, max_heads: int = 16, min_heads:
     flops = attention_flops(one, "fwd_bwd") * (done / G)
     return {"value": flops / t_total / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{done} query heads (B=1, N={w.N}, d={w.d}, causal={w.causal}) of the "
-                      f"workload, fp64 forward + analytic backward, {t_total:.1f} s"}
+            "sample": f"{done} query heads (B=1, N={w.N}, d={w.d}, causal={w.causal}"
+                      + (f", window={w.window}: the first {w.N} positions" if w.window else "")
+                      + f") of the workload, fp64 forward + analytic backward, {t_total:.1f} s"}
+
+
+def oracle_sample_workload(w):
+    """The part of a workload the CPU oracle times.  Windowed attention is
+    timed on the first min(N, 2W) positions (every row there costs at most W
+    keys, as in the whole sequence); other workloads whole."""
+    if w.window and w.N > 2 * w.window:
+        return w.with_(N=2 * w.window)
+    return w
 
 
 def run_reference(args, w):
@@ -205,7 +219,8 @@ def run_reference(args, w):
         res = cpu_oracle_sample(w, budget_s=0.0, max_heads=w.H // w.Hkv)
         if s >= args.warmup:
             t_steps.append(res)
-    flops_step = attention_flops(w.with_(B=1, H=w.H // w.Hkv, Hkv=1), "fwd_bwd")
+    flops_step = attention_flops(oracle_sample_workload(w).with_(B=1, H=w.H // w.Hkv, Hkv=1),
+                                 "fwd_bwd")
     tflops = statistics.median(r["value"] for r in t_steps)
     ms = flops_step / (tflops * 1e12) * 1e3
     line = {
@@ -267,6 +282,8 @@ def run_native(args, w):
             e[0].record(stream)
         if precise:
             fa.fa_fwd_precise(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+        elif w.window:
+            fa.fa_fwd_window(qd, kd, vd, o, lse, w.window, w.scale, stream)
         else:
             fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
         if timed:
@@ -281,7 +298,10 @@ def run_native(args, w):
             fa.fa_bwd_preprocess(o, dod, lse, work, Hkv, stream)
         if timed:
             e[2].record(stream)
-        fa.fa_bwd_dkdv(qd, kd, vd, dod, dk, dv, work, w.causal, w.scale, stream)
+        if w.window:
+            fa.fa_bwd_dkdv_window(qd, kd, vd, dod, dk, dv, work, w.window, w.scale, stream)
+        else:
+            fa.fa_bwd_dkdv(qd, kd, vd, dod, dk, dv, work, w.causal, w.scale, stream)
         if timed:
             e[3].record(stream)
         fa.fa_bwd_dq_convert(work, dq, Hkv, w.scale, stream)
@@ -382,9 +402,14 @@ def run_native(args, w):
                 dst.copy_(src_, non_blocking=True)
             if precise:
                 fa.fa_fwd_precise(qd, kd, vd, o, lse, w.causal, w.scale, stream)
+            elif w.window:
+                fa.fa_fwd_window(qd, kd, vd, o, lse, w.window, w.scale, stream)
             else:
                 fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
-            if not fwd_only and precise:
+            if not fwd_only and w.window:
+                fa.fa_bwd_window(qd, kd, vd, o, dod, lse, dq, dk, dv, work, w.window, w.scale,
+                                 stream)
+            elif not fwd_only and precise:
                 fa.fa_bwd_precise(qd, kd, vd, o, dod, lse, dq, dk, dv, work, w.causal, w.scale,
                                   stream)
             elif not fwd_only:
@@ -418,12 +443,15 @@ def run_native(args, w):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{w.name}: B={B} H={H} Hkv={Hkv} N={N} d={d} "
-                                   f"causal={w.causal} " + ("fwd" if fwd_only else "fwd+bwd")
+                                   f"causal={w.causal} "
+                                   + (f"window={w.window} " if w.window else "")
+                                   + ("fwd" if fwd_only else "fwd+bwd")
                                    + (" (precise path: fp32 O, two-term P)" if precise else ""),
                        "B": B, "H": H, "Hkv": Hkv, "N": N, "d": d, "causal": w.causal,
                        "flops_per_step": flops_step,
-                       "flop_count": "fwd 4BHN^2d (/2 causal)" + ("" if fwd_only
-                                                                  else ", fwd+bwd x2.5"),
+                       "flop_count": ("fwd 4BHd(NW - W^2/2) (causal window W)" if w.window
+                                      else "fwd 4BHN^2d (/2 causal)")
+                       + ("" if fwd_only else ", fwd+bwd x2.5"),
                        "l2": f"inputs larger than L2: {ws_mb / 2**20:.0f} MiB touched per "
                              f"step vs {L2_BYTES / 2**20:.0f} MiB L2",
                        "parallelism": f"replicas x{ws} (independent batches)"},

@@ -27,7 +27,9 @@ __all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_p
            "fa_bwd_workspace_size", "fa_bwd_precise", "fa_bwd_preprocess",
            "fa_bwd_preprocess_precise", "fa_bwd_dkdv", "fa_bwd_dq_convert",
            "fa_device_status", "fa_device_status_detail", "fa_status_string",
-           "fa_kernel_launches", "fa_watchdog_selftest", "attention", "attention_backward"]
+           "fa_kernel_launches", "fa_watchdog_selftest", "attention", "attention_backward",
+           "fa_fwd_window", "fa_bwd_window", "fa_bwd_dkdv_window", "attention_window",
+           "attention_window_backward"]
 
 
 class FAError(RuntimeError):
@@ -90,6 +92,14 @@ def fa_fwd_precise(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> 
                                 float(scale), _stream(stream)), "fa_fwd_precise")
 
 
+def fa_fwd_window(q, k, v, o, lse, window: int, scale: float, stream=None) -> None:
+    """Causal sliding window: query i attends to keys i - window < j <= i."""
+    B, H, Hkv, N, d = _dims(q, k)
+    _check(lib().fa_fwd_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                               _f32(lse, "lse"), B, H, Hkv, N, d, int(window), float(scale),
+                               _stream(stream)), "fa_fwd_window")
+
+
 def fa_bwd_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
     return int(lib().fa_bwd_workspace_size(B, H, Hkv, N, d))
 
@@ -123,6 +133,17 @@ def fa_bwd_precise(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, s
            "fa_bwd_precise")
 
 
+def fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, workspace, window: int, scale: float,
+                  stream=None) -> None:
+    """Backward of fa_fwd_window."""
+    B, H, Hkv, N, d = _dims(q, k)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                               _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"),
+                               _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d,
+                               int(window), float(scale), _stream(stream)), "fa_bwd_window")
+
+
 def fa_bwd_preprocess(o, dout, lse, workspace, Hkv: int, stream=None) -> None:
     B, H, N, d = o.shape
     wp, wb = _ws(workspace)
@@ -146,6 +167,16 @@ def fa_bwd_dkdv(q, k, v, dout, dk, dv, workspace, causal: bool, scale: float,
     _check(lib().fa_bwd_dkdv(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(dout, "dout"),
                              _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d,
                              int(bool(causal)), float(scale), _stream(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_dkdv_window(q, k, v, dout, dk, dv, workspace, window: int, scale: float,
+                       stream=None) -> None:
+    B, H, Hkv, N, d = _dims(q, k)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_dkdv_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"),
+                                    _bf16(dout, "dout"), _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb,
+                                    B, H, Hkv, N, d, int(window), float(scale), _stream(stream)),
+           "fa_bwd_dkdv_window")
 
 
 def fa_bwd_dq_convert(workspace, dq, Hkv: int, scale: float, stream=None) -> None:
@@ -264,6 +295,31 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, stream=
         o = torch.empty_like(q)
         fa_fwd(q, k, v, o, lse, causal, scale, stream)
     return o, lse
+
+
+def attention_window(q, k, v, window: int, scale: float | None = None, stream=None):
+    """Causal sliding-window attention (query i sees keys i - window < j <= i);
+    returns (o, lse)."""
+    import torch
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    o = torch.empty_like(q)
+    fa_fwd_window(q, k, v, o, lse, window, scale, stream)
+    return o, lse
+
+
+def attention_window_backward(q, k, v, o, lse, dout, window: int, scale: float | None = None,
+                              workspace=None, stream=None):
+    """Returns (dq, dk, dv) for attention_window."""
+    import torch
+    B, H, Hkv, N, d = _dims(q, k)
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(B, H, Hkv, N, d), dtype=torch.uint8,
+                                device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, workspace, window, scale, stream)
+    return dq, dk, dv
 
 
 def attention_backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,

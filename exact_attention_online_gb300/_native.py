@@ -80,6 +80,11 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_fwd.restype = i
     L.fa_fwd_precise.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     L.fa_fwd_precise.restype = i
+    L.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_window.restype = i
+    L.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f,
+                                vp]
+    L.fa_bwd_window.restype = i
     L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     L.fa_bwd_workspace_size.restype = sz
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
@@ -93,6 +98,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_bwd_preprocess_precise.restype = i
     L.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
     L.fa_bwd_dkdv.restype = i
+    L.fa_bwd_dkdv_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
+    L.fa_bwd_dkdv_window.restype = i
     L.fa_bwd_dq_convert.argtypes = [vp, sz, vp, i, i, i, i, i, f, vp]
     L.fa_bwd_dq_convert.restype = i
     L.fa_bwd_static_scratch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
@@ -140,4 +147,5 @@ EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bw
            "fa_bwd_static_scratch", "fa_device_status", "fa_device_status_detail",
            "fa_status_string", "fa_kernel_launches", "fa_watchdog_selftest",
            "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8",
-           "fa_fwd_decode_workspace_size", "fa_fwd_decode"]
+           "fa_fwd_decode_workspace_size", "fa_fwd_decode", "fa_fwd_window", "fa_bwd_window",
+           "fa_bwd_dkdv_window"]

@@ -215,6 +215,20 @@ fa_status fa_fwd_precise(const void* q, const void* k, const void* v, float* o, 
         launch_fwd(s, q, k, v, o, lse, true, g_status_ptr[dev], (cudaStream_t)stream));
 }
 
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int Hkv, int N, int d, int window, float scale,
+                        fa_stream_t stream) {
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(lse)});
+    if (st != FA_OK) return st;
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    const Shape s{B, H, Hkv, N, d, 1, scale, window};
+    return from_cuda(
+        launch_fwd(s, q, k, v, o, lse, false, g_status_ptr[dev], (cudaStream_t)stream));
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d) {
     if (check_shape(B, H, Hkv, N, d) != FA_OK) return 0;
     return bwd_workspace_bytes(Shape{B, H, Hkv, N, d, 0, 1.0f});
@@ -256,10 +270,11 @@ fa_status fa_bwd_preprocess_precise(const float* o, const void* dout, const floa
                                stream);
 }
 
-fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
-                      void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
-                      int N, int d, int causal, float scale, fa_stream_t stream) {
-    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+static fa_status bwd_dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
+                               void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
+                               int H, int Hkv, int N, int d, int causal, float scale, int window,
+                               fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale, window};
     fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
                                 check_ptr(k), check_ptr(v), check_ptr(dout), check_ptr(dk),
                                 check_ptr(dv)});
@@ -269,6 +284,22 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
     if ((st = device_ready(&dev)) != FA_OK) return st;
     return from_cuda(launch_bwd_dkdv(s, q, k, v, dout, dk, dv, bwd_workspace_carve(workspace, s),
                                      g_status_ptr[dev], (cudaStream_t)stream));
+}
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                      void* dv, void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                      int N, int d, int causal, float scale, fa_stream_t stream) {
+    return bwd_dkdv_impl(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d,
+                         causal, scale, 0, stream);
+}
+
+fa_status fa_bwd_dkdv_window(const void* q, const void* k, const void* v, const void* dout,
+                             void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
+                             int H, int Hkv, int N, int d, int window, float scale,
+                             fa_stream_t stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return bwd_dkdv_impl(q, k, v, dout, dk, dv, workspace, workspace_bytes, B, H, Hkv, N, d, 1,
+                         scale, window, stream);
 }
 
 fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void* dq, int B, int H,
@@ -286,8 +317,8 @@ fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void*
 static fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, bool o_f32,
                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
                           void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
-                          int d, int causal, float scale, fa_stream_t stream) {
-    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+                          int d, int causal, float scale, fa_stream_t stream, int window = 0) {
+    const Shape s{B, H, Hkv, N, d, (causal || window > 0) ? 1 : 0, scale, window};
     fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
                                 check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(dout),
                                 check_ptr(lse), check_ptr(dq), check_ptr(dk), check_ptr(dv)});
@@ -317,6 +348,15 @@ fa_status fa_bwd_precise(const void* q, const void* k, const void* v, const floa
                          int d, int causal, float scale, fa_stream_t stream) {
     return bwd_impl(q, k, v, o, true, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H,
                     Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                        int d, int window, float scale, fa_stream_t stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return bwd_impl(q, k, v, o, false, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H,
+                    Hkv, N, d, 1, scale, stream, window);
 }
 
 fa_status fa_device_status(fa_stream_t stream) {

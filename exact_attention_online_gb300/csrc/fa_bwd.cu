@@ -76,6 +76,9 @@ struct BwdCfg {
 
 struct BwdParams {
     int H, Hkv, N, Np, G, causal;
+    // Causal sliding window W: key k is seen by queries k <= i < k + W.
+    // Without a window this holds kNoWindow.
+    int window;
     float scale, scale_log2;
     const float* lse2;
     const float* delta;
@@ -85,7 +88,8 @@ struct BwdParams {
     DeviceStatus* status;
 };
 
-template <int D, bool CAUSAL>
+// WINDOW (with CAUSAL): the causal sliding window of p.window keys.
+template <int D, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -110,8 +114,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int bg = blockIdx.x / n_kblk;           // b * Hkv + g
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int n_qblk = (p.N + BR - 1) / BR;
+    // Query blocks that see some key of the block: rows 128 j .. 128 j + 127
+    // + W - 1 under the causal (windowed) mask.
     const int i_start = CAUSAL ? (jblk * kBN) / BR : 0;
-    const int n_i = n_qblk - i_start;
+    const int i_end = WINDOW ? min(n_qblk, (jblk * kBN + kBN - 1 + (p.window - 1)) / BR + 1)
+                             : n_qblk;
+    const int n_i = i_end - i_start;
     const int n_it = p.G * n_i;                   // (head in group) x (query block)
 
     uint8_t* sK = smem + Cfg::kOffK;
@@ -170,8 +178,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const float* lse_s = sLSE + st * BR;     // -LSE * log2(e)
             const float* del_s = sDel + st * BR;     // -D
             const int q0 = i * BR;
-            const bool need_mask = (CAUSAL && q0 < jblk * kBN + kBN - 1) || (jblk * kBN + kBN > p.N);
-            const int key_lim = CAUSAL ? key - q0 : -1;    // column e visible iff e >= key_lim
+            const bool need_mask = (CAUSAL && (q0 < jblk * kBN + kBN - 1 ||
+                                               (WINDOW && q0 + BR - 1 > jblk * kBN + p.window - 1))) ||
+                                   (jblk * kBN + kBN > p.N);
+            // column e visible iff key_lim <= e <= key_hi
+            const int key_lim = CAUSAL ? key - q0 : -1;
+            const int key_hi = WINDOW ? key + p.window - 1 - q0 : BR;
             const bool key_valid = key < p.N;
             // P^T = 2^(S^T c - LSE log2 e), kept in fp32 for dS; bf16 copy into
             // TMEM over this warp's own S^T columns (already read).  Two
@@ -194,8 +206,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                              x0, x1);
                     float p0 = ex2(x0), p1 = ex2(x1);
                     if (need_mask) {
-                        if (qe < key_lim || !key_valid) p0 = 0.0f;
-                        if (qe + 1 < key_lim || !key_valid) p1 = 0.0f;
+                        if (qe < key_lim || qe > key_hi || !key_valid) p0 = 0.0f;
+                        if (qe + 1 < key_lim || qe + 1 > key_hi || !key_valid) p1 = 0.0f;
                     }
                     pf[ch * 32 + 2 * e2] = p0;
                     pf[ch * 32 + 2 * e2 + 1] = p1;
@@ -680,11 +692,11 @@ int grid_for(long long work_items, int per_block) {
     return (int)blocks;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WINDOW = false>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                           int grid, cudaStream_t stream) {
-    auto kern = fa_bwd_dkdv_kernel<D, CAUSAL>;
+    auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, WINDOW>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -753,6 +765,7 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     p.Np = padded_rows(s.N);
     p.G = s.H / s.Hkv;
     p.causal = s.causal;
+    p.window = s.window > 0 ? s.window : kNoWindow;
     p.scale = s.scale;
     p.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
     p.lse2 = ws.lse2;
@@ -764,6 +777,11 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     const int n_kblk = (s.N + kBN - 1) / kBN;
     const int grid = n_kblk * s.B * s.Hkv;
     count_launch();
+    if (s.window > 0) {   // the causal sliding window
+        if (!s.causal) return cudaErrorInvalidValue;
+        return s.d == 128 ? launch_dkdv_t<128, true, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
+                          : launch_dkdv_t<64, true, true>(tq, tk, tv, tdo, tdq, p, grid, stream);
+    }
     if (s.d == 128)
         return s.causal ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
                         : launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdq, p, grid, stream);

@@ -90,6 +90,9 @@ struct FwdCfg {
 
 struct FwdParams {
     int H, Hkv, N, BH, n_mblk, n_items, causal;
+    // Causal sliding window W: query i sees keys i - W < j <= i.  Without a
+    // window this holds kNoWindow, so large that the lower edge never binds.
+    int window;
     float scale_log2;                 // scale * log2(e)
     void* o;                          // bf16, or fp32 in the precise variant
     float* lse;
@@ -101,9 +104,11 @@ struct FwdParams {
 // cost order, and each CTA takes every gridDim.x-th item).
 struct FwdTile {
     int bh, kv_bh, row_base;
-    int n_kv[kTiles];          // key blocks each query tile needs
+    int lo[kTiles];            // first key block each query tile needs
+    int n_kv[kTiles];          // one past its last key block
 };
 
+template <bool WINDOW>
 __device__ __forceinline__ FwdTile fwd_tile(int item, const FwdParams& p, bool causal) {
     FwdTile w;
     const int mb_rank = item / p.BH;
@@ -114,12 +119,19 @@ __device__ __forceinline__ FwdTile fwd_tile(int item, const FwdParams& p, bool c
     w.row_base = m_blk * (kTiles * kBM);
     const int n_kv_all = (p.N + kBN - 1) / kBN;
 #pragma unroll
-    for (int t = 0; t < kTiles; ++t)
+    for (int t = 0; t < kTiles; ++t) {
         w.n_kv[t] = causal ? min(n_kv_all, 2 * m_blk + t + 1) : n_kv_all;
+        // The tile's first row sees keys from row0 - W + 1 on.  A tile wholly
+        // past N (the second tile of the last pair) keeps one block, which
+        // the masks empty, so that every tile takes at least one block.
+        w.lo[t] = WINDOW ? min(max(0, w.row_base + t * kBM - p.window + 1) / kBN, w.n_kv[t] - 1)
+                         : 0;
+    }
     return w;
 }
 
-template <int D, bool CAUSAL, bool PRECISE>
+// WINDOW (with CAUSAL): the causal sliding window of p.window keys.
+template <int D, bool CAUSAL, bool PRECISE, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -190,13 +202,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bool ok = true;
         int lt = 0;
         for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-            const FwdTile wt = fwd_tile(item, p, CAUSAL);
+            const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
             const int row0 = wt.row_base + t * kBM;
             const int row = row0 + rl;
-            const int n_kv = wt.n_kv[t];
+            // (selects, not a run-time index: the arrays stay in registers)
+            const int lo = t ? wt.lo[1] : wt.lo[0], n_kv = t ? wt.n_kv[1] : wt.n_kv[0];
             float m2 = -CUDART_INF_F;   // running max, log2-scaled
             float l = 0.0f;
-            for (int j = 0; j < n_kv; ++j) {
+            for (int j = lo; j < n_kv; ++j) {
                 if (!fa_wait_warp(&bar_s[t], cs & 1, 30 + t, wc)) { ok = false; break; }
                 ++cs;
                 tc_fence_after();
@@ -218,13 +231,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int e = 0; e < kBN; ++e) sv[e] = __uint_as_float(r[e >> 5][e & 31]);
 
                 const int col0 = j * kBN;
-                const bool need_mask = (CAUSAL && col0 + kBN - 1 > row0) || (col0 + kBN > p.N);
+                const bool need_mask = (CAUSAL && (col0 + kBN - 1 > row0 ||
+                                                   (WINDOW && col0 < row0 + kBM - p.window))) ||
+                                       (col0 + kBN > p.N);
                 if (need_mask) {
                     const int lim_causal = CAUSAL ? row - col0 : kBN;   // keep e <= row - col0
                     const int lim_n = p.N - col0;                        // keep e < N - col0
+                    const int lim_lo = WINDOW ? row - p.window + 1 - col0 : 0;  // keep e >= this
 #pragma unroll
                     for (int e = 0; e < kBN; ++e)
-                        if (e > lim_causal || e >= lim_n) sv[e] = -CUDART_INF_F;
+                        if (e > lim_causal || e >= lim_n || e < lim_lo) sv[e] = -CUDART_INF_F;
                 }
                 // Row max: three-input max, eight independent chains.
                 float mx8[8];
@@ -259,7 +275,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const float m_new = need ? mx2 : m2;
                     alpha = (m_new == m2) ? 1.0f : ex2(m2 - m_new);
                     l *= alpha;
-                    if (!SEP && j > 0) rescale_o(alpha);
+                    if (!SEP && j > lo) rescale_o(alpha);
                     m2 = m_new;
                 }
                 const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
@@ -291,7 +307,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 if (SEP) {
                     // P_t and O_t are free once P_t(j-1) V has completed.
-                    if (j > 0) {
+                    if (j > lo) {
                         if (!fa_wait_warp(&bar_pv[t], cpv & 1, 34 + t, wc)) { ok = false; break; }
                         ++cpv;
                         tc_fence_after();
@@ -318,7 +334,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // P columns the softmax did not wait for the earlier ones; each S
             // MMA was issued only after the P V MMA before it had completed,
             // so those are complete already.
-            if (!SEP) cpv += n_kv - 1;
+            if (!SEP) cpv += n_kv - lo - 1;
             if (!fa_wait_warp(&bar_pv[t], cpv & 1, 34 + t, wc)) { ok = false; break; }
             ++cpv;
             tc_fence_after();
@@ -375,8 +391,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             uint32_t g = 0;              // K blocks loaded so far (ring position)
             bool ok = true;
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-                const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
+                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+                for (int j = wt.lo[0]; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
                     const int s = g % SK;
                     if (g >= (uint32_t)SK && !fa_wait(&bar_k_empty[s], ((g / SK) - 1) & 1, 10, wc)) {
                         ok = false;
@@ -403,7 +419,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int lt = 0, q_loaded = -1;
             bool ok = true;
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-                const FwdTile wt = fwd_tile(item, p, CAUSAL);
+                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
                 for (int t = 0; t < kTiles; ++t) {
                     if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
@@ -413,7 +429,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 if (!ok) break;
                 q_loaded = lt;
-                for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
+                for (int j = wt.lo[0]; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
                     const int s = g % SV;
                     if (g >= (uint32_t)SV && !fa_wait(&bar_v_empty[s], ((g / SV) - 1) & 1, 13, wc)) {
                         ok = false;
@@ -467,20 +483,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 return true;
             };
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-                const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];   // n0 <= n1
-                for (int j = 0; j < n1; ++j) {
-                    const uint32_t gj = g + j, vs = gj % SV;
+                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+                // Key blocks [lo0, n0) for tile 0, [lo1, n1) for tile 1, with
+                // lo0 <= lo1 and n0 <= n1; V_j streams for j in [lo0, n1).
+                const int lo0 = wt.lo[0], lo1 = wt.lo[1], n0 = wt.n_kv[0], n1 = wt.n_kv[1];
+                for (int j = lo0; j < n1; ++j) {
+                    const uint32_t gj = g + (j - lo0), vs = gj % SV;
                     if (!fa_wait(&bar_v[vs], (gj / SV) & 1, 22, wc)) { ok = false; break; }
-                    const bool wait_o = (j == 0 && lt > 0);
-                    if (j < n0 && !pv(std::integral_constant<int, 0>{}, vs, j == 0, wait_o)) {
+                    if (j < n0 && !pv(std::integral_constant<int, 0>{}, vs, j == lo0,
+                                      j == lo0 && lt > 0)) {
                         ok = false;
                         break;
                     }
-                    if (!pv(std::integral_constant<int, 1>{}, vs, j == 0, wait_o)) { ok = false; break; }
+                    if (j >= lo1 && !pv(std::integral_constant<int, 1>{}, vs, j == lo1,
+                                        j == lo1 && lt > 0)) {
+                        ok = false;
+                        break;
+                    }
                     mma_commit(&bar_v_empty[vs]);            // V_j read by both PVs
                 }
-                g += n1;
+                g += n1 - lo0;
             }
             if (!ok) {   // no MMA of this thread may still write TMEM at teardown
                 __shared__ uint64_t bar_drain_pv;
@@ -520,24 +542,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 return true;
             };
             for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-                const FwdTile wt = fwd_tile(item, p, CAUSAL);
-                const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];   // n0 <= n1
+                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+                const int lo0 = wt.lo[0], lo1 = wt.lo[1], n0 = wt.n_kv[0], n1 = wt.n_kv[1];
                 if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc)) {
                     ok = false;
                     break;
                 }
-                for (int j = 0; j < n1; ++j) {
-                    const uint32_t gj = g + j, ks = gj % SK;
+                for (int j = lo0; j < n1; ++j) {
+                    const uint32_t gj = g + (j - lo0), ks = gj % SK;
                     if (!fa_wait(&bar_k[ks], (gj / SK) & 1, 21, wc)) { ok = false; break; }
                     if (j < n0) {
                         if (!s_mma(std::integral_constant<int, 0>{}, ks)) { ok = false; break; }
                         if (j + 1 == n0) mma_commit(&bar_q_free[0]);
                     }
-                    if (!s_mma(std::integral_constant<int, 1>{}, ks)) { ok = false; break; }
-                    if (j + 1 == n1) mma_commit(&bar_q_free[1]);
+                    if (j >= lo1) {
+                        if (!s_mma(std::integral_constant<int, 1>{}, ks)) { ok = false; break; }
+                        if (j + 1 == n1) mma_commit(&bar_q_free[1]);
+                    }
                     mma_commit(&bar_k_empty[ks]);            // K_j read by both S MMAs
                 }
-                g += n1;
+                g += n1 - lo0;
             }
             if (!ok) {
                 __shared__ uint64_t bar_drain;
@@ -558,11 +582,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-template <int D, bool CAUSAL, bool PRECISE>
+template <int D, bool CAUSAL, bool PRECISE, bool WINDOW = false>
 cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdParams& p, int grid,
                          cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, CAUSAL, PRECISE>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, PRECISE, WINDOW>;
     static int configured_device = -1;   // attribute is per device; cheap to repeat
     int dev = 0;
     cudaGetDevice(&dev);
@@ -599,6 +623,7 @@ cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void*
     p.n_mblk = (s.N + kTiles * kBM - 1) / (kTiles * kBM);
     p.n_items = p.n_mblk * p.BH;
     p.causal = s.causal;
+    p.window = s.window > 0 ? s.window : kNoWindow;
     p.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
     p.o = o;
     p.lse = lse;
@@ -609,6 +634,11 @@ cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void*
     const int grid = p.n_items < sms ? p.n_items : sms;
     count_launch();
     const bool c = s.causal != 0;
+    if (s.window > 0) {   // the causal sliding window (bf16 output only)
+        if (!c || precise) return cudaErrorInvalidValue;
+        return s.d == 128 ? launch_fwd_t<128, true, false, true>(s, tq, tk, tv, p, grid, stream)
+                          : launch_fwd_t<64, true, false, true>(s, tq, tk, tv, p, grid, stream);
+    }
     if (s.d == 128) {
         if (precise)
             return c ? launch_fwd_t<128, true, true>(s, tq, tk, tv, p, grid, stream)

@@ -15,7 +15,12 @@ struct Shape {
     int B, H, Hkv, N, d;
     int causal;
     float scale;
+    int window = 0;   // causal sliding window W (query i sees keys i - W < j <= i); 0 = none
 };
+
+// Window value the kernels carry when there is none: the lower edge i - W + 1
+// lies below every key index.
+constexpr int kNoWindow = 1 << 30;
 
 // Rows of every per-head buffer in the backward workspace are padded to this.
 constexpr int kRowPad = 128;

@@ -39,6 +39,7 @@ class Workload:
     k_outlier_gain: float = 20.0
     outlier_frac: float = 0.0
     outlier_mag: float = 30.0
+    window: int = 0            # causal sliding window W (query i sees i - W < j <= i); 0 = none
     passes: tuple = ("fwd", "bwd")
     tags: tuple = field(default_factory=tuple)
 
@@ -72,6 +73,10 @@ WORKLOADS = {
                     outlier_frac=1e-3, passes=("fwd",)),
     "ablation": _cfg(6, "ablation", B=8, H=16, Hkv=16, N=2048, d=128, causal=True,
                      passes=("fwd",)),
+    # Local (sliding-window) attention, the variant the pages name for
+    # Mistral-7B: that model's attention shape (32 query heads, 8 key/value
+    # heads, d = 128) with a 4096-key window over a 16K sequence.
+    "window": _cfg(7, "window", B=1, H=32, Hkv=8, N=16384, d=128, causal=True, window=4096),
 }
 
 

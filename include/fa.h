@@ -98,6 +98,22 @@ FA_API fa_status fa_fwd_precise(const void* q, const void* k, const void* v, flo
                                 float scale, fa_stream_t stream);
 
 /*
+ * Causal sliding-window ("local") forward: query i attends to the `window`
+ * most recent keys, i - window < j <= i (FlashAttention-2 review thread, the
+ * authors' common response, "Collaborations on open source models", names
+ * local attention; the pages do not spell out the mask, and this is the
+ * plain reading: the causal mask with a lower edge).  window >= N is plain
+ * causal attention.  Arguments, layouts, ownership and errors as fa_fwd()
+ * with causal = 1, plus FA_ERR_INVALID_ARG for window < 1.  Key blocks
+ * wholly outside every window of a query tile are neither loaded nor
+ * multiplied, so the cost grows with N * window instead of N^2 / 2.
+ * One launch of the forward kernel.
+ */
+FA_API fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int Hkv, int N, int d, int window, float scale,
+                               fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd() needs: D and a padded copy of LSE
  * (fp32 [B][H][Np]) and the fp32 dQ accumulator ([B][H][Np][d]), where Np is
  * N rounded up to 128.  Returns 0 for arguments fa_bwd() would reject.
@@ -130,6 +146,18 @@ FA_API fa_status fa_bwd_precise(const void* q, const void* k, const void* v, con
                                 fa_stream_t stream);
 
 /*
+ * Backward of fa_fwd_window(): arguments, layouts, workspace and errors as
+ * fa_bwd() with causal = 1, plus FA_ERR_INVALID_ARG for window < 1; lse is the
+ * one fa_fwd_window() wrote.  Each key block is paired only with the query
+ * blocks whose windows reach it.  Three kernel launches.
+ */
+FA_API fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               void* workspace, size_t workspace_bytes,
+                               int B, int H, int Hkv, int N, int d, int window, float scale,
+                               fa_stream_t stream);
+
+/*
  * Backward, stage 1 of 3: D_i = sum_c dO_ic O_ic (fp32), LSE copied into the
  * workspace in base-2 units with padding rows, and the fp32 dQ accumulator
  * zeroed.  One launch.
@@ -155,6 +183,16 @@ FA_API fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const 
                       void* dk, void* dv, void* workspace, size_t workspace_bytes,
                       int B, int H, int Hkv, int N, int d, int causal, float scale,
                       fa_stream_t stream);
+
+/*
+ * Backward stage 2 of fa_bwd_window(): fa_bwd_dkdv() with the causal
+ * sliding-window mask (query i sees keys i - window < j <= i); window < 1 is
+ * FA_ERR_INVALID_ARG.  Stages 1 and 3 do not depend on the mask.  One launch.
+ */
+FA_API fa_status fa_bwd_dkdv_window(const void* q, const void* k, const void* v,
+                                    const void* dout, void* dk, void* dv, void* workspace,
+                                    size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                                    int window, float scale, fa_stream_t stream);
 
 /* Backward, stage 3 of 3: dq = bf16(scale * accumulator).  One launch. */
 FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes, void* dq,

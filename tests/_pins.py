@@ -430,8 +430,33 @@ def pin_sliding_window(mutant=0):
     assert np.allclose(gv, vt.grad.numpy(), rtol=1e-10, atol=1e-12)
 
 
+def pin_window_slice(mutant=0):
+    """Windowed attention of a row depends only on the W positions ending at
+    it: the oracle on the slice [s, e) of the sequence reproduces the forward
+    and dQ of rows i >= s + W - 1 and dK, dV of keys j in [s + W - 1, e - W + 1)
+    of the whole sequence (the reduction the full-size GPU test relies on)."""
+    B, H, Hkv, N, d, scale, W = 1, 2, 1, 61, 8, 0.4, 9
+    q, k, v, do = rand_qkv(B, H, Hkv, N, d, 13, dout=True)
+    fo, fl = oracle.attn_fwd_window(q, k, v, W, scale, mutant)
+    fq, fk, fv, _ = oracle.attn_bwd_window(q, k, v, do, W, scale, mutant)
+    s, e = 17, 49
+    sl = lambda x: np.ascontiguousarray(x[:, :, s:e])
+    so, sl_ = oracle.attn_fwd_window(sl(q), sl(k), sl(v), W, scale, mutant)
+    sq, sk, sv, _ = oracle.attn_bwd_window(sl(q), sl(k), sl(v), sl(do), W, scale, mutant)
+    r0, k1 = W - 1, (e - s) - W + 1
+    close = lambda a, b: np.allclose(a, b, rtol=1e-12, atol=1e-12)
+    assert close(so[:, :, r0:], fo[:, :, s + r0:e]) and close(sl_[:, :, r0:], fl[:, :, s + r0:e])
+    assert close(sq[:, :, r0:], fq[:, :, s + r0:e])
+    assert close(sk[:, :, r0:k1], fk[:, :, s + r0:s + k1])
+    assert close(sv[:, :, r0:k1], fv[:, :, s + r0:s + k1])
+    # The rows before s + W - 1 do change (their windows lose keys): the
+    # slice is exact only where the statement says.
+    assert not close(so[:, :, 0], fo[:, :, s])
+
+
 ALL_PINS = [
     pin_sliding_window,
+    pin_window_slice,
     pin_decode_rows,
     pin_e4m3_definition,
     pin_e4m3_nearest,
