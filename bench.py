@@ -44,10 +44,14 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel source it was taken on.  A source change makes the figure stale and
 # it is then reported as null.
 NCU_TRAFFIC = {
-    # profiles/fa_bwd_dkdv_mha_d64.md: 203.5 MB read + 88.3 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 291.84e6, "src_sha": "b9a8b2f4a0ecb419"},
-    # profiles/fa_fwd_mha_d64.md: 112.8 MB read + 13.1 MB written, one launch
-    ("fa_fwd", "mha_d64"): {"bytes": 125.84e6, "src_sha": "7d54771fdf717a16"},
+    # profiles/launches_mha_d64_fwd_bwd.md capture: 203.5 MB read + 87.6 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 291.06e6, "src_sha": "10a151f2130648b3"},
+    # the same capture: 111.5 MB read + 12.4 MB written, one launch
+    ("fa_fwd", "mha_d64"): {"bytes": 123.92e6, "src_sha": "bd61666491615be6"},
+    # profiles/fa_window_fwd_bwd_window.md: 610.0 MB read + 292.9 MB written
+    ("fa_bwd_dkdv", "window"): {"bytes": 902.86e6, "src_sha": "10a151f2130648b3"},
+    # the same file: 205.6 MB read + 98.5 MB written
+    ("fa_fwd", "window"): {"bytes": 304.13e6, "src_sha": "bd61666491615be6"},
     # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 5.1 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0790e9, "src_sha": "6f9c75dfde0d8a68"},
 }
