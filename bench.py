@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="the FP8 (e4m3) forward on a forward-only d=128 workload")
+    ap.add_argument("--varlen", default=None,
+                    help="packed variable-length workload name (fwd+bwd line of its own)")
     ap.add_argument("--decode", default=None,
                     help="a split-KV decoding workload (decode_gqa, decode_spec4, decode_mha_d64)")
     return ap.parse_args()
@@ -725,12 +727,165 @@ def run_native_decode(args):
         dist.destroy_process_group()
 
 
+def run_native_varlen(args):
+    """Packed variable-length causal training step: fa_fwd_varlen +
+    fa_bwd_varlen on a batch of sequences of mixed lengths.  FLOPs count only
+    the real (unpadded) work, sum over sequences of 4 H d len^2 (/2 causal),
+    x2.5 for forward + backward.  The dominant-kernel roofline is taken on
+    the backward call as a whole (preprocess + dK/dV + dQ convert: the C ABI
+    runs the three as one call), so its `achieved` is a lower bound for the
+    dK/dV kernel alone."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_online_gb300 as fa
+    from exact_attention_online_gb300 import replicas
+    from exact_attention_online_gb300.inputs import VARLEN_WORKLOADS, make_varlen_inputs
+
+    w = VARLEN_WORKLOADS[args.varlen]
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+    peaks = load_peaks()
+    import dataclasses
+    wr = dataclasses.replace(w, seed=w.seed + 7919 * rank)   # each rank its own batch
+    q, k, v, do = make_varlen_inputs(wr)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    cu = w.cu_seqlens().to(dev)
+    ms = w.max_seqlen
+    o = torch.empty_like(qd)
+    lse = torch.empty((w.H, w.total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    work = torch.empty(fa.fa_bwd_varlen_workspace_size(w.B, w.H, w.Hkv, ms, w.d),
+                       dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fwd_ev, bwd_ev = [], []
+
+    def step(timed=False):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if timed else None
+        if timed:
+            e[0].record(stream)
+        fa.fa_fwd_varlen(qd, kd, vd, o, lse, cu, ms, w.causal, w.scale, stream)
+        if timed:
+            e[1].record(stream)
+        fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, work, cu, ms, w.causal, w.scale,
+                         stream)
+        if timed:
+            e[2].record(stream)
+            fwd_ev.append((e[0], e[1]))
+            bwd_ev.append((e[1], e[2]))
+
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if args.steps is None:
+        per = timed(step, 10) / 10
+        args.steps = int(min(20000, max(50, math.ceil(3000.0 / max(per, 1e-3)))))
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    launches0 = fa.fa_kernel_launches()
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        barrier()
+        ms_total = replicas.max_over_ranks(timed(lambda: step(True), args.steps), dev)
+        barrier()
+    launches = fa.fa_kernel_launches() - launches0
+    st = fa.fa_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
+    pairs = sum(n * n / 2.0 if w.causal else float(n) * n for n in w.lens)
+    fwd_flops = 4.0 * w.H * w.d * pairs
+    flops_step = 2.5 * fwd_flops
+    value = flops_step * args.steps * ws / (ms_total * 1e-3) / 1e12
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in bwd_ev)
+    peak = peaks["bf16_tflops_sustained"]
+    kernels = {"fa_fwd_varlen": (fwd_ms, fwd_flops / fwd_ms / 1e9),
+               "fa_bwd_varlen (preprocess + dK/dV + dQ convert)":
+                   (bwd_ms, 2.5 * fwd_flops / bwd_ms / 1e9)}
+    dom = max(kernels, key=lambda n: kernels[n][0])
+    ach = kernels[dom][1]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
+                "other_kernel": {n: {"ms": t, "tflops": f, "frac": f / peak}
+                                 for n, (t, f) in kernels.items() if n != dom}}
+    e2e = None
+    if not args.no_e2e:
+        hin = [t.pin_memory() for t in (q, k, v, do)]
+        hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+
+        def e2e_step():
+            for dst, src in zip((qd, kd, vd, dod), hin):
+                dst.copy_(src, non_blocking=True)
+            fa.fa_fwd_varlen(qd, kd, vd, o, lse, cu, ms, w.causal, w.scale, stream)
+            fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, work, cu, ms, w.causal,
+                             w.scale, stream)
+            for dst, src in zip(hout, (o, lse, dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e = max(3, min(args.steps // 2, 300))
+        e_ms = replicas.max_over_ranks(timed(e2e_step, n_e), dev)
+        e2e = {"value": flops_step * n_e * ws / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
+               "ms_per_step": e_ms / n_e}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{w.name}: {w.B} packed sequences of {min(w.lens)}-"
+                                   f"{max(w.lens)} tokens (total {w.total}), H={w.H} "
+                                   f"Hkv={w.Hkv} d={w.d} causal={w.causal} fwd+bwd",
+                       "lens": list(w.lens), "H": w.H, "Hkv": w.Hkv, "d": w.d,
+                       "causal": w.causal, "flops_per_step": flops_step,
+                       "flop_count": "fwd sum_b 4 H d len_b^2 (/2 causal), fwd+bwd x2.5",
+                       "l2": f"inputs larger than L2: "
+                             f"{sum(t.numel() * t.element_size() for t in (qd, kd, vd, dod, o, dq, dk, dv, work)) / 2**20:.0f}"
+                             f" MiB touched per step vs {L2_BYTES / 2**20:.0f} MiB L2",
+                       "parallelism": f"replicas x{ws} (independent batches)"},
+            "fwd": {"tflops": kernels["fa_fwd_varlen"][1], "ms": fwd_ms},
+            "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
+            "clocks": clk.summary(), "gpu_launches": launches,
+            "launches_per_step": launches / args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     from exact_attention_online_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
     if args.decode and args.impl != "reference":
         run_native_decode(args)
+    elif args.varlen and args.impl != "reference":
+        run_native_varlen(args)
     elif args.impl == "reference":
         run_reference(args, w)
     elif args.fp8:

@@ -29,7 +29,8 @@ __all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_p
            "fa_device_status", "fa_device_status_detail", "fa_status_string",
            "fa_kernel_launches", "fa_watchdog_selftest", "attention", "attention_backward",
            "fa_fwd_window", "fa_bwd_window", "fa_bwd_dkdv_window", "attention_window",
-           "attention_window_backward"]
+           "attention_window_backward", "fa_fwd_varlen", "fa_bwd_varlen",
+           "fa_bwd_varlen_workspace_size", "attention_varlen", "attention_varlen_backward"]
 
 
 class FAError(RuntimeError):
@@ -98,6 +99,49 @@ def fa_fwd_window(q, k, v, o, lse, window: int, scale: float, stream=None) -> No
     _check(lib().fa_fwd_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
                                _f32(lse, "lse"), B, H, Hkv, N, d, int(window), float(scale),
                                _stream(stream)), "fa_fwd_window")
+
+
+def _i32(t, name):
+    import torch
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _varlen_dims(q, k, cu_seqlens):
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("packed q and k must be 3-D [H(kv), total, d]")
+    H, total, d = q.shape
+    if k.shape[1] != total or k.shape[2] != d:
+        raise ValueError(f"q {tuple(q.shape)} and k {tuple(k.shape)} disagree")
+    return cu_seqlens.numel() - 1, H, k.shape[0], total, d
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, scale: float,
+                  stream=None) -> None:
+    """Packed sequences: q, o [H, total, d], k, v [Hkv, total, d], lse [H, total],
+    cu_seqlens int32 [B + 1] on the device."""
+    B, H, Hkv, total, d = _varlen_dims(q, k, cu_seqlens)
+    _check(lib().fa_fwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                               _f32(lse, "lse"), _i32(cu_seqlens, "cu_seqlens"), B,
+                               int(max_seqlen), total, H, Hkv, d, int(bool(causal)),
+                               float(scale), _stream(stream)), "fa_fwd_varlen")
+
+
+def fa_bwd_varlen_workspace_size(B: int, H: int, Hkv: int, max_seqlen: int, d: int) -> int:
+    return int(lib().fa_bwd_varlen_workspace_size(B, H, Hkv, max_seqlen, d))
+
+
+def fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens, max_seqlen: int,
+                  causal: bool, scale: float, stream=None) -> None:
+    B, H, Hkv, total, d = _varlen_dims(q, k, cu_seqlens)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
+                               _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"),
+                               _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb,
+                               _i32(cu_seqlens, "cu_seqlens"), B, int(max_seqlen), total, H, Hkv,
+                               d, int(bool(causal)), float(scale), _stream(stream)),
+           "fa_bwd_varlen")
 
 
 def fa_bwd_workspace_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
@@ -319,6 +363,33 @@ def attention_window_backward(q, k, v, o, lse, dout, window: int, scale: float |
                                 device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, workspace, window, scale, stream)
+    return dq, dk, dv
+
+
+def attention_varlen(q, k, v, cu_seqlens, max_seqlen: int, causal: bool = False,
+                     scale: float | None = None, stream=None):
+    """Packed variable-length sequences; returns (o [H, total, d], lse [H, total])."""
+    import torch
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal, scale, stream)
+    return o, lse
+
+
+def attention_varlen_backward(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int,
+                              causal: bool = False, scale: float | None = None, workspace=None,
+                              stream=None):
+    """Returns (dq, dk, dv) for attention_varlen."""
+    import torch
+    B, H, Hkv, total, d = _varlen_dims(q, k, cu_seqlens)
+    scale = d ** -0.5 if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_varlen_workspace_size(B, H, Hkv, max_seqlen, d),
+                                dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens, max_seqlen, causal,
+                  scale, stream)
     return dq, dk, dv
 
 

@@ -85,6 +85,13 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f,
                                 vp]
     L.fa_bwd_window.restype = i
+    L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_varlen.restype = i
+    L.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i, i]
+    L.fa_bwd_varlen_workspace_size.restype = sz
+    L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, i, i, i, i, i, i,
+                                i, f, vp]
+    L.fa_bwd_varlen.restype = i
     L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i]
     L.fa_bwd_workspace_size.restype = sz
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
@@ -148,4 +155,5 @@ EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bw
            "fa_status_string", "fa_kernel_launches", "fa_watchdog_selftest",
            "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8",
            "fa_fwd_decode_workspace_size", "fa_fwd_decode", "fa_fwd_window", "fa_bwd_window",
-           "fa_bwd_dkdv_window"]
+           "fa_bwd_dkdv_window", "fa_fwd_varlen", "fa_bwd_varlen_workspace_size",
+           "fa_bwd_varlen"]

@@ -359,6 +359,60 @@ fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void*
                     Hkv, N, d, 1, scale, stream, window);
 }
 
+static fa_status check_varlen(const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                              int Hkv, int d) {
+    fa_status st = check_shape(B, H, Hkv, max_seqlen, d);
+    if (st != FA_OK) return st;
+    if (!cu_seqlens || total < 1) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(cu_seqlens) % alignof(int) != 0) return FA_ERR_ALIGNMENT;
+    if ((long long)H * total * d >= (1LL << 31)) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens, int B, int max_seqlen, int total, int H, int Hkv,
+                        int d, int causal, float scale, fa_stream_t stream) {
+    fa_status st = first_error({check_varlen(cu_seqlens, B, max_seqlen, total, H, Hkv, d),
+                                check_scale(scale), check_ptr(q), check_ptr(k), check_ptr(v),
+                                check_ptr(o), check_ptr(lse)});
+    if (st != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    Shape s{B, H, Hkv, max_seqlen, d, causal ? 1 : 0, scale};
+    s.cu_seqlens = cu_seqlens;
+    s.total = total;
+    return from_cuda(
+        launch_fwd(s, q, k, v, o, lse, false, g_status_ptr[dev], (cudaStream_t)stream));
+}
+
+size_t fa_bwd_varlen_workspace_size(int B, int H, int Hkv, int max_seqlen, int d) {
+    return fa_bwd_workspace_size(B, H, Hkv, max_seqlen, d);
+}
+
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes, const int* cu_seqlens, int B,
+                        int max_seqlen, int total, int H, int Hkv, int d, int causal, float scale,
+                        fa_stream_t stream) {
+    Shape s{B, H, Hkv, max_seqlen, d, causal ? 1 : 0, scale};
+    s.cu_seqlens = cu_seqlens;
+    s.total = total;
+    fa_status st = first_error({check_varlen(cu_seqlens, B, max_seqlen, total, H, Hkv, d),
+                                check_scale(scale), check_ptr(q), check_ptr(k), check_ptr(v),
+                                check_ptr(o), check_ptr(dout), check_ptr(lse), check_ptr(dq),
+                                check_ptr(dk), check_ptr(dv)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    const BwdWorkspace ws = bwd_workspace_carve(workspace, s);
+    cudaStream_t cs = (cudaStream_t)stream;
+    cudaError_t e = launch_bwd_preprocess(s, o, false, dout, lse, ws, g_status_ptr[dev], cs);
+    if (e == cudaSuccess) e = launch_bwd_dkdv(s, q, k, v, dout, dk, dv, ws, g_status_ptr[dev], cs);
+    if (e == cudaSuccess) e = launch_bwd_dq_convert(s, ws, dq, cs);
+    return from_cuda(e);
+}
+
 fa_status fa_device_status(fa_stream_t stream) {
     int dev;
     fa_status st = device_ready(&dev);

@@ -76,9 +76,14 @@ struct BwdCfg {
 
 struct BwdParams {
     int H, Hkv, N, Np, G, causal;
+    int rows;                         // rows per head of q, k, v, dk, dv: N, or the packed total
     // Causal sliding window W: key k is seen by queries k <= i < k + W.
     // Without a window this holds kNoWindow.
     int window;
+    // Packed variable-length batches: sequence b is rows cu_seqlens[b] ..
+    // cu_seqlens[b+1] - 1 of every head; N is then the longest sequence and
+    // the workspace keeps N-row (padded) regions per (batch, head).
+    const int* cu_seqlens;
     float scale, scale_log2;
     const float* lse2;
     const float* delta;
@@ -89,7 +94,8 @@ struct BwdParams {
 };
 
 // WINDOW (with CAUSAL): the causal sliding window of p.window keys.
-template <int D, bool CAUSAL, bool WINDOW>
+// VARLEN: packed variable-length sequences (p.cu_seqlens).
+template <int D, bool CAUSAL, bool WINDOW, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -113,7 +119,15 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int jblk = blockIdx.x % n_kblk;
     const int bg = blockIdx.x / n_kblk;           // b * Hkv + g
     const int b = bg / p.Hkv, g = bg % p.Hkv;
-    const int n_qblk = (p.N + BR - 1) / BR;
+    // The sequence: its first row in the tensors and its length.  Dense
+    // batches address rows of head b*H(kv) + h; packed ones rows tok0 + i of
+    // head h.  A key block past the sequence's end has nothing to do (the
+    // whole CTA leaves before any barrier or TMEM is set up).
+    int tok0 = 0;
+    const int seq_len = VARLEN ? packed_seq(p.cu_seqlens, b, p.N, p.rows, tok0) : p.N;
+    if (VARLEN && jblk * kBN >= seq_len) return;
+    const int z_kv = VARLEN ? g : bg;
+    const int n_qblk = (seq_len + BR - 1) / BR;
     // Query blocks that see some key of the block: rows 128 j .. 128 j + 127
     // + W - 1 under the causal (windowed) mask.
     const int i_start = CAUSAL ? (jblk * kBN) / BR : 0;
@@ -180,11 +194,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const int q0 = i * BR;
             const bool need_mask = (CAUSAL && (q0 < jblk * kBN + kBN - 1 ||
                                                (WINDOW && q0 + BR - 1 > jblk * kBN + p.window - 1))) ||
-                                   (jblk * kBN + kBN > p.N);
+                                   (jblk * kBN + kBN > seq_len);
             // column e visible iff key_lim <= e <= key_hi
             const int key_lim = CAUSAL ? key - q0 : -1;
             const int key_hi = WINDOW ? key + p.window - 1 - q0 : BR;
-            const bool key_valid = key < p.N;
+            const bool key_valid = key < seq_len;
             // P^T = 2^(S^T c - LSE log2 e), kept in fp32 for dS; bf16 copy into
             // TMEM over this warp's own S^T columns (already read).  Two
             // columns per paired-fp32 instruction.
@@ -257,8 +271,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // ---------------------------------------------------- dK, dV epilogue
         if (ok && fa_wait_warp(&bar_done, 0, 63, wc)) {
             tc_fence_after();
-            const bool valid = key < p.N;
-            const size_t row = ((size_t)bg * p.N + (valid ? key : 0)) * D;
+            const bool valid = key < seq_len;
+            const size_t row = ((size_t)z_kv * p.rows + tok0 + (valid ? key : 0)) * D;
             const int c_lo = hf * (D / 2);
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
@@ -360,8 +374,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tma_prefetch_desc(&tm_do);
                 mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
                 for (int c = 0; c < D / 64; ++c) {
-                    tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64, jblk * kBN, bg);
-                    tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64, jblk * kBN, bg);
+                    tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64, tok0 + jblk * kBN,
+                                z_kv);
+                    tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64, tok0 + jblk * kBN,
+                                z_kv);
                 }
                 int issued = 0;
                 for (int it = 0; it < n_it; ++it) {
@@ -370,12 +386,13 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const int hq = g * p.G + it / n_i;
                     const int i = i_start + it % n_i;
                     const int bh = b * p.H + hq;
+                    const int z_q = VARLEN ? hq : bh;
                     mbar_arrive_expect_tx(&bar_full[st], Cfg::kStageBytes);
                     for (int c = 0; c < D / 64; ++c) {
                         tma_load_3d(sQ + st * Cfg::kQBytes + c * (BR * 128), &tm_q, &bar_full[st],
-                                    c * 64, i * BR, bh);
+                                    c * 64, tok0 + i * BR, z_q);
                         tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do,
-                                    &bar_full[st], c * 64, i * BR, bh);
+                                    &bar_full[st], c * 64, tok0 + i * BR, z_q);
                     }
                     const size_t stat = (size_t)bh * p.Np + (size_t)i * BR;
                     bulk_load(sLSE + st * BR, p.lse2 + stat, BR * 4, &bar_full[st]);
@@ -591,15 +608,32 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
 }
 
+// Row i of (batch b, head h) in the caller's [.][rows][d] tensors: dense
+// batches keep head b*H + h with rows = N; packed variable-length batches
+// (cu != nullptr) keep head h with rows = the total, sequence b starting at
+// row cu[b].  Returns the sequence length.
+__device__ __forceinline__ int seq_row(const int* __restrict__ cu, long long bh, int H, int N,
+                                       long long rows, long long& base) {
+    if (!cu) {
+        base = bh * N;
+        return N;
+    }
+    const int b = (int)(bh / H), h = (int)(bh % H);
+    int t0;
+    const int len = packed_seq(cu, b, N, rows, t0);
+    base = (long long)h * rows + t0;
+    return len;
+}
+
 // -D_i = -<dO_i, O_i>, -LSE * log2(e) (-inf on padded rows), accumulator = 0.
-// One warp per row, grid-stride over the B*H*Np rows.  O is bf16, or fp32 when
-// it comes from the precise forward.
+// One warp per row, grid-stride over the B*H*Np workspace rows.  O is bf16,
+// or fp32 when it comes from the precise forward.
 template <int D, typename OT>
 __global__ void __launch_bounds__(256)
 fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, float* __restrict__ lse2,
                   float* __restrict__ delta, float* __restrict__ dq_acc, int N, int Np,
-                  long long rows) {
+                  long long rows, const int* __restrict__ cu, int H, long long seq_rows) {
     constexpr int kPer = D / 32;   // elements per lane (2 or 4)
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -607,9 +641,11 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
     for (long long r = wid; r < rows; r += nw) {
         const long long bh = r / Np;
         const int i = (int)(r % Np);
+        long long base;
+        const int len = seq_row(cu, bh, H, N, seq_rows, base);
         float acc = 0.0f;
-        if (i < N) {
-            const long long src = (bh * N + i) * D + lane * kPer;
+        if (i < len) {
+            const long long src = (base + i) * D + lane * kPer;
             float ov[kPer], dv[kPer];
             if (kPer == 4) {
                 const uint2 dd = *reinterpret_cast<const uint2*>(dout + src);
@@ -639,7 +675,7 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
             delta[r] = -acc;
-            lse2[r] = (i < N) ? -lse[bh * N + i] * 1.4426950408889634f : -CUDART_INF_F;
+            lse2[r] = (i < len) ? -lse[base + i] * 1.4426950408889634f : -CUDART_INF_F;
         }
         float4* z = reinterpret_cast<float4*>(dq_acc + r * D);
         for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -669,6 +705,33 @@ fa_bwd_dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restric
     }
 }
 
+// The same for packed variable-length batches: walks the B*H*Np workspace
+// rows and writes the rows inside their sequence.
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_dq_convert_varlen_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                                const int* __restrict__ cu, int H, int N, int Np,
+                                long long seq_rows, float scale, long long n_vec) {
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < n_vec; t += stride) {
+        const long long e = t * 8;                  // element index in the accumulator
+        const long long row = e / D;                // bh * Np + i
+        const int col = (int)(e % D);
+        const long long bh = row / Np;
+        const int i = (int)(row % Np);
+        long long base;
+        if (i >= seq_row(cu, bh, H, N, seq_rows, base)) continue;
+        const float4* src = reinterpret_cast<const float4*>(acc + e);
+        const float4 a = src[0], bb = src[1];
+        uint4 w;
+        w.x = pack_bf16x2(a.x * scale, a.y * scale);
+        w.y = pack_bf16x2(a.z * scale, a.w * scale);
+        w.z = pack_bf16x2(bb.x * scale, bb.y * scale);
+        w.w = pack_bf16x2(bb.z * scale, bb.w * scale);
+        *reinterpret_cast<uint4*>(dq + (base + i) * D + col) = w;
+    }
+}
+
 // Bounded-wait self-test: one CTA waits on an mbarrier nobody completes.
 __global__ void fa_watchdog_kernel(DeviceStatus* status, unsigned long long limit_ns) {
     __shared__ uint64_t bar;
@@ -692,11 +755,11 @@ int grid_for(long long work_items, int per_block) {
     return (int)blocks;
 }
 
-template <int D, bool CAUSAL, bool WINDOW = false>
+template <int D, bool CAUSAL, bool WINDOW = false, bool VARLEN = false>
 cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                           int grid, cudaStream_t stream) {
-    auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, WINDOW>;
+    auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, WINDOW, VARLEN>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -724,6 +787,7 @@ cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, con
     (void)status;
     const int Np = padded_rows(s.N);
     const long long rows = (long long)s.B * s.H * Np;
+    const long long seq_rows = s.cu_seqlens ? s.total : s.N;
     const int grid = grid_for(rows, 8);
     count_launch();
     auto* d_ = static_cast<const __nv_bfloat16*>(dout);
@@ -732,17 +796,21 @@ cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, con
     if (s.d == 128) {
         if (o_f32)
             fa_bwd_pre_kernel<128, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse2, ws.delta,
-                                                                    ws.dq_acc, s.N, Np, rows);
+                                                                    ws.dq_acc, s.N, Np, rows,
+                                                                    s.cu_seqlens, s.H, seq_rows);
         else
             fa_bwd_pre_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows);
+                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows,
+                                                                    s.cu_seqlens, s.H, seq_rows);
     } else {
         if (o_f32)
             fa_bwd_pre_kernel<64, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse2, ws.delta,
-                                                                   ws.dq_acc, s.N, Np, rows);
+                                                                   ws.dq_acc, s.N, Np, rows,
+                                                                    s.cu_seqlens, s.H, seq_rows);
         else
             fa_bwd_pre_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows);
+                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows,
+                                                                    s.cu_seqlens, s.H, seq_rows);
     }
     return cudaGetLastError();
 }
@@ -751,11 +819,14 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
                             const void* dout, void* dk, void* dv, const BwdWorkspace& ws,
                             DeviceStatus* status, cudaStream_t stream) {
     const int br = (s.d == 128) ? BwdCfg<128>::kBR : BwdCfg<64>::kBR;
+    const bool varlen = s.cu_seqlens != nullptr;
+    const int rows = varlen ? s.total : s.N;
+    const int zq = varlen ? s.H : s.B * s.H, zkv = varlen ? s.Hkv : s.B * s.Hkv;
     CUtensorMap tq, tk, tv, tdo, tdq;
-    if (!make_tmap_bf16_3d(&tq, q, s.d, s.N, s.B * s.H, br) ||
-        !make_tmap_bf16_3d(&tdo, dout, s.d, s.N, s.B * s.H, br) ||
-        !make_tmap_bf16_3d(&tk, k, s.d, s.N, s.B * s.Hkv, kBN) ||
-        !make_tmap_bf16_3d(&tv, v, s.d, s.N, s.B * s.Hkv, kBN) ||
+    if (!make_tmap_bf16_3d(&tq, q, s.d, rows, zq, br) ||
+        !make_tmap_bf16_3d(&tdo, dout, s.d, rows, zq, br) ||
+        !make_tmap_bf16_3d(&tk, k, s.d, rows, zkv, kBN) ||
+        !make_tmap_bf16_3d(&tv, v, s.d, rows, zkv, kBN) ||
         !make_tmap_f32_2d(&tdq, ws.dq_acc, s.d, (long long)s.B * s.H * padded_rows(s.N), 32, br))
         return cudaErrorInvalidValue;
     BwdParams p;
@@ -763,6 +834,8 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     p.Hkv = s.Hkv;
     p.N = s.N;
     p.Np = padded_rows(s.N);
+    p.rows = rows;
+    p.cu_seqlens = s.cu_seqlens;
     p.G = s.H / s.Hkv;
     p.causal = s.causal;
     p.window = s.window > 0 ? s.window : kNoWindow;
@@ -777,6 +850,16 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     const int n_kblk = (s.N + kBN - 1) / kBN;
     const int grid = n_kblk * s.B * s.Hkv;
     count_launch();
+    if (varlen) {   // packed variable-length sequences (no window)
+        if (s.window > 0) return cudaErrorInvalidValue;
+        if (s.d == 128)
+            return s.causal
+                       ? launch_dkdv_t<128, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
+                       : launch_dkdv_t<128, false, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream);
+        return s.causal
+                   ? launch_dkdv_t<64, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
+                   : launch_dkdv_t<64, false, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream);
+    }
     if (s.window > 0) {   // the causal sliding window
         if (!s.causal) return cudaErrorInvalidValue;
         return s.d == 128 ? launch_dkdv_t<128, true, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
@@ -791,10 +874,23 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
 
 cudaError_t launch_bwd_dq_convert(const Shape& s, const BwdWorkspace& ws, void* dq,
                                   cudaStream_t stream) {
+    auto* dq_ = static_cast<__nv_bfloat16*>(dq);
+    if (s.cu_seqlens) {
+        const int Np = padded_rows(s.N);
+        const long long nv = (long long)s.B * s.H * Np * s.d / 8;
+        const int g = grid_for(nv, 256);
+        count_launch();
+        if (s.d == 128)
+            fa_bwd_dq_convert_varlen_kernel<128><<<g, 256, 0, stream>>>(
+                ws.dq_acc, dq_, s.cu_seqlens, s.H, s.N, Np, s.total, s.scale, nv);
+        else
+            fa_bwd_dq_convert_varlen_kernel<64><<<g, 256, 0, stream>>>(
+                ws.dq_acc, dq_, s.cu_seqlens, s.H, s.N, Np, s.total, s.scale, nv);
+        return cudaGetLastError();
+    }
     const long long n_vec = (long long)s.B * s.H * s.N * s.d / 8;
     const int grid = grid_for(n_vec, 256);
     count_launch();
-    auto* dq_ = static_cast<__nv_bfloat16*>(dq);
     if (s.d == 128)
         fa_bwd_dq_convert_kernel<128><<<grid, 256, 0, stream>>>(ws.dq_acc, dq_, s.N,
                                                                 padded_rows(s.N), s.scale, n_vec);

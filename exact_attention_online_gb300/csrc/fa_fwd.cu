@@ -93,6 +93,11 @@ struct FwdParams {
     // Causal sliding window W: query i sees keys i - W < j <= i.  Without a
     // window this holds kNoWindow, so large that the lower edge never binds.
     int window;
+    // Packed variable-length batches: sequence b is rows cu_seqlens[b] ..
+    // cu_seqlens[b+1] - 1 of every head ([H][rows][d]); N is then the
+    // longest sequence.  Dense batches: rows = N, cu_seqlens unused.
+    int rows;
+    const int* cu_seqlens;
     float scale_log2;                 // scale * log2(e)
     void* o;                          // bf16, or fp32 in the precise variant
     float* lse;
@@ -103,21 +108,73 @@ struct FwdParams {
 // mask the longest query blocks come first (the tile list is in decreasing
 // cost order, and each CTA takes every gridDim.x-th item).
 struct FwdTile {
-    int bh, kv_bh, row_base;
+    int bh, row_base;
+    int q_z, kv_z;             // head coordinate of the Q / O and K / V tensor maps
+    int tok0, len;             // first row of the sequence in its head, its length
     int lo[kTiles];            // first key block each query tile needs
     int n_kv[kTiles];          // one past its last key block
 };
 
-template <bool WINDOW>
+__device__ __forceinline__ int fwd_m_blk(int item, const FwdParams& p, bool causal) {
+    const int mb_rank = item / p.BH;
+    return causal ? (p.n_mblk - 1 - mb_rank) : mb_rank;
+}
+
+// The work items of this CTA, the same sequence for every role.  Items are
+// ranked in decreasing cost (under the causal mask) and dealt out in rounds
+// of gridDim.x, the order of the CTAs reversed every other round ("snake"),
+// so that the sum of costs per CTA evens out (CPU model of the bench
+// workloads: 0.98-1.00 of the mean load per CTA, against 0.88-0.94 for
+// plain round robin).  With variable lengths the ranks count only the items
+// that have rows (query-block pairs past a sequence's end are passed over):
+// a cursor walks the (level, sequence) list forward, ranks only grow.
+template <bool VARLEN>
+struct FwdSched {
+    int round = 0;
+    int mb = 0, b = 0, base = 0;   // cursor: level, sequence, rank of (b, head 0)
+
+    __device__ __forceinline__ int next(const FwdParams& p, bool causal) {
+        const int G = gridDim.x, c = blockIdx.x;
+        const int t = round * G + ((round & 1) ? G - 1 - c : c);   // rank
+        ++round;
+        if (!VARLEN) return t < p.n_items ? t : p.n_items;
+        const int B = p.BH / p.H;
+        while (mb < p.n_mblk) {
+            if (b >= B) {
+                ++mb;
+                b = 0;
+                continue;
+            }
+            int t0;
+            const int len = packed_seq(p.cu_seqlens, b, p.N, p.rows, t0);
+            if (fwd_m_blk(mb * p.BH, p, causal) * (kTiles * kBM) < len) {
+                if (t < base + p.H) return mb * p.BH + b * p.H + (t - base);
+                base += p.H;
+            }
+            ++b;
+        }
+        return p.n_items;
+    }
+};
+
+template <bool WINDOW, bool VARLEN>
 __device__ __forceinline__ FwdTile fwd_tile(int item, const FwdParams& p, bool causal) {
     FwdTile w;
-    const int mb_rank = item / p.BH;
     w.bh = item % p.BH;
-    const int m_blk = causal ? (p.n_mblk - 1 - mb_rank) : mb_rank;
+    const int m_blk = fwd_m_blk(item, p, causal);
     const int b = w.bh / p.H, h = w.bh % p.H;
-    w.kv_bh = b * p.Hkv + h / (p.H / p.Hkv);
+    if (VARLEN) {
+        w.len = packed_seq(p.cu_seqlens, b, p.N, p.rows, w.tok0);
+        w.q_z = h;
+        w.kv_z = h / (p.H / p.Hkv);
+    } else {
+        w.tok0 = 0;
+        w.len = p.N;
+        w.q_z = w.bh;
+        w.kv_z = b * p.Hkv + h / (p.H / p.Hkv);
+    }
     w.row_base = m_blk * (kTiles * kBM);
-    const int n_kv_all = (p.N + kBN - 1) / kBN;
+    const int n_kv_all = (w.len + kBN - 1) / kBN;
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) {
         w.n_kv[t] = causal ? min(n_kv_all, 2 * m_blk + t + 1) : n_kv_all;
@@ -131,7 +188,8 @@ __device__ __forceinline__ FwdTile fwd_tile(int item, const FwdParams& p, bool c
 }
 
 // WINDOW (with CAUSAL): the causal sliding window of p.window keys.
-template <int D, bool CAUSAL, bool PRECISE, bool WINDOW>
+// VARLEN: packed variable-length sequences (p.cu_seqlens).
+template <int D, bool CAUSAL, bool PRECISE, bool WINDOW, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -201,8 +259,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         uint32_t cpv = 0;                        // P_t V completions seen (separate P)
         bool ok = true;
         int lt = 0;
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-            const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+        FwdSched<VARLEN> sch;
+        for (int item = sch.next(p, CAUSAL); ok && item < p.n_items;
+             item = sch.next(p, CAUSAL), ++lt) {
+            const FwdTile wt = fwd_tile<WINDOW, VARLEN>(item, p, CAUSAL);
             const int row0 = wt.row_base + t * kBM;
             const int row = row0 + rl;
             // (selects, not a run-time index: the arrays stay in registers)
@@ -233,10 +293,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int col0 = j * kBN;
                 const bool need_mask = (CAUSAL && (col0 + kBN - 1 > row0 ||
                                                    (WINDOW && col0 < row0 + kBM - p.window))) ||
-                                       (col0 + kBN > p.N);
+                                       (col0 + kBN > wt.len);
                 if (need_mask) {
                     const int lim_causal = CAUSAL ? row - col0 : kBN;   // keep e <= row - col0
-                    const int lim_n = p.N - col0;                        // keep e < N - col0
+                    const int lim_n = wt.len - col0;                     // keep e < N - col0
                     const int lim_lo = WINDOW ? row - p.window + 1 - col0 : 0;  // keep e >= this
 #pragma unroll
                     for (int e = 0; e < kBN; ++e)
@@ -346,9 +406,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             for (int c0 = 1; c0 < D / 32; ++c0) asm volatile("" : FA_R32(ov[c0]) : : "memory");
             tc_fence_before();
             mbar_arrive(&bar_o_free[t]);
-            const bool valid = row < p.N;
+            const bool valid = row < wt.len;
             const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-            const size_t orow = ((size_t)wt.bh * p.N + (valid ? row : 0)) * D;
+            const size_t orow = ((size_t)wt.q_z * p.rows + wt.tok0 + (valid ? row : 0)) * D;
             if (valid) {
 #pragma unroll
                 for (int c0 = 0; c0 < D / 32; ++c0) {
@@ -379,7 +439,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         }
                     }
                 }
-                p.lse[(size_t)wt.bh * p.N + row] =
+                p.lse[(size_t)wt.q_z * p.rows + wt.tok0 + row] =
                     (l > 0.0f) ? (m2 + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
             }
         }
@@ -390,8 +450,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tma_prefetch_desc(&tm_k);
             uint32_t g = 0;              // K blocks loaded so far (ring position)
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+            FwdSched<VARLEN> sch;
+            for (int item = sch.next(p, CAUSAL); ok && item < p.n_items;
+                 item = sch.next(p, CAUSAL)) {
+                const FwdTile wt = fwd_tile<WINDOW, VARLEN>(item, p, CAUSAL);
                 for (int j = wt.lo[0]; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
                     const int s = g % SK;
                     if (g >= (uint32_t)SK && !fa_wait(&bar_k_empty[s], ((g / SK) - 1) & 1, 10, wc)) {
@@ -401,7 +463,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     mbar_arrive_expect_tx(&bar_k[s], Cfg::kTileBytes);
                     for (int c = 0; c < Cfg::kChunks; ++c)
                         tma_load_3d(sK + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_k, &bar_k[s],
-                                    c * 64, j * kBN, wt.kv_bh);
+                                    c * 64, wt.tok0 + j * kBN, wt.kv_z);
                 }
             }
             if (abort_sh) {   // drain the copies still in flight (bounded)
@@ -418,14 +480,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             uint32_t g = 0;
             int lt = 0, q_loaded = -1;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+            FwdSched<VARLEN> sch;
+            for (int item = sch.next(p, CAUSAL); ok && item < p.n_items;
+                 item = sch.next(p, CAUSAL), ++lt) {
+                const FwdTile wt = fwd_tile<WINDOW, VARLEN>(item, p, CAUSAL);
                 for (int t = 0; t < kTiles; ++t) {
                     if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
                     for (int c = 0; c < Cfg::kChunks; ++c)
                         tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
-                                    &bar_q[t], c * 64, wt.row_base + t * kBM, wt.bh);
+                                    &bar_q[t], c * 64, wt.tok0 + wt.row_base + t * kBM, wt.q_z);
                 }
                 if (!ok) break;
                 q_loaded = lt;
@@ -438,7 +502,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     mbar_arrive_expect_tx(&bar_v[s], Cfg::kTileBytes);
                     for (int c = 0; c < Cfg::kChunks; ++c)
                         tma_load_3d(sV + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_v, &bar_v[s],
-                                    c * 64, j * kBN, wt.kv_bh);
+                                    c * 64, wt.tok0 + j * kBN, wt.kv_z);
                 }
             }
             if (abort_sh) {   // drain the copies still in flight (bounded)
@@ -482,8 +546,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 mma_commit(&bar_pv[T]);
                 return true;
             };
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+            FwdSched<VARLEN> sch;
+            for (int item = sch.next(p, CAUSAL); ok && item < p.n_items;
+                 item = sch.next(p, CAUSAL), ++lt) {
+                const FwdTile wt = fwd_tile<WINDOW, VARLEN>(item, p, CAUSAL);
                 // Key blocks [lo0, n0) for tile 0, [lo1, n1) for tile 1, with
                 // lo0 <= lo1 and n0 <= n1; V_j streams for j in [lo0, n1).
                 const int lo0 = wt.lo[0], lo1 = wt.lo[1], n0 = wt.n_kv[0], n1 = wt.n_kv[1];
@@ -541,8 +607,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 mma_commit(&bar_s[T]);
                 return true;
             };
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
-                const FwdTile wt = fwd_tile<WINDOW>(item, p, CAUSAL);
+            FwdSched<VARLEN> sch;
+            for (int item = sch.next(p, CAUSAL); ok && item < p.n_items;
+                 item = sch.next(p, CAUSAL), ++lt) {
+                const FwdTile wt = fwd_tile<WINDOW, VARLEN>(item, p, CAUSAL);
                 const int lo0 = wt.lo[0], lo1 = wt.lo[1], n0 = wt.n_kv[0], n1 = wt.n_kv[1];
                 if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc)) {
                     ok = false;
@@ -582,11 +650,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-template <int D, bool CAUSAL, bool PRECISE, bool WINDOW = false>
+template <int D, bool CAUSAL, bool PRECISE, bool WINDOW = false, bool VARLEN = false>
 cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const FwdParams& p, int grid,
                          cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, CAUSAL, PRECISE, WINDOW>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, PRECISE, WINDOW, VARLEN>;
     static int configured_device = -1;   // attribute is per device; cheap to repeat
     int dev = 0;
     cudaGetDevice(&dev);
@@ -610,15 +678,21 @@ cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& tq, const CUtensorMa
 
 cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void* v, void* o,
                        float* lse, bool precise, DeviceStatus* status, cudaStream_t stream) {
+    // Dense: maps {d, N, B*H(kv)}.  Packed variable lengths: {d, total, H(kv)},
+    // a sequence's rows addressed from its first row.
+    const bool varlen = s.cu_seqlens != nullptr;
+    const int rows = varlen ? s.total : s.N;
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bf16_3d(&tq, q, s.d, s.N, s.B * s.H, kBM) ||
-        !make_tmap_bf16_3d(&tk, k, s.d, s.N, s.B * s.Hkv, kBN) ||
-        !make_tmap_bf16_3d(&tv, v, s.d, s.N, s.B * s.Hkv, kBN))
+    if (!make_tmap_bf16_3d(&tq, q, s.d, rows, varlen ? s.H : s.B * s.H, kBM) ||
+        !make_tmap_bf16_3d(&tk, k, s.d, rows, varlen ? s.Hkv : s.B * s.Hkv, kBN) ||
+        !make_tmap_bf16_3d(&tv, v, s.d, rows, varlen ? s.Hkv : s.B * s.Hkv, kBN))
         return cudaErrorInvalidValue;
     FwdParams p;
     p.H = s.H;
     p.Hkv = s.Hkv;
     p.N = s.N;
+    p.rows = rows;
+    p.cu_seqlens = s.cu_seqlens;
     p.BH = s.B * s.H;
     p.n_mblk = (s.N + kTiles * kBM - 1) / (kTiles * kBM);
     p.n_items = p.n_mblk * p.BH;
@@ -634,6 +708,14 @@ cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void*
     const int grid = p.n_items < sms ? p.n_items : sms;
     count_launch();
     const bool c = s.causal != 0;
+    if (varlen) {   // packed variable-length sequences (bf16 output, no window)
+        if (precise || s.window > 0) return cudaErrorInvalidValue;
+        if (s.d == 128)
+            return c ? launch_fwd_t<128, true, false, false, true>(s, tq, tk, tv, p, grid, stream)
+                     : launch_fwd_t<128, false, false, false, true>(s, tq, tk, tv, p, grid, stream);
+        return c ? launch_fwd_t<64, true, false, false, true>(s, tq, tk, tv, p, grid, stream)
+                 : launch_fwd_t<64, false, false, false, true>(s, tq, tk, tv, p, grid, stream);
+    }
     if (s.window > 0) {   // the causal sliding window (bf16 output only)
         if (!c || precise) return cudaErrorInvalidValue;
         return s.d == 128 ? launch_fwd_t<128, true, false, true>(s, tq, tk, tv, p, grid, stream)

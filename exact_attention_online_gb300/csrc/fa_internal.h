@@ -16,7 +16,25 @@ struct Shape {
     int causal;
     float scale;
     int window = 0;   // causal sliding window W (query i sees keys i - W < j <= i); 0 = none
+    // Packed variable-length batches: device array of B + 1 row offsets and
+    // the total row count; N is then the longest sequence.  nullptr = dense.
+    const int* cu_seqlens = nullptr;
+    int total = 0;
 };
+
+// Rows [t0, t0 + len) of sequence b of a packed variable-length batch (cu =
+// the B + 1 row offsets), clamped to the tensor's rows and to the longest
+// sequence N: whatever the offsets hold, every access stays in bounds.
+__device__ __forceinline__ int packed_seq(const int* __restrict__ cu, int b, int N,
+                                          long long rows, int& t0) {
+    long long a = __ldg(cu + b), e = __ldg(cu + b + 1);
+    a = a < 0 ? 0 : (a > rows ? rows : a);
+    e = e > rows ? rows : e;
+    long long len = e - a;
+    len = len < 0 ? 0 : (len > N ? N : len);
+    t0 = (int)a;
+    return (int)len;
+}
 
 // Window value the kernels carry when there is none: the lower edge i - W + 1
 // lies below every key index.

@@ -161,3 +161,67 @@ def make_decode_inputs(w: DecodeWorkload):
     k = torch.randn((w.B, w.Hkv, w.Nk, w.d), generator=gen, dtype=torch.float32)
     v = torch.randn((w.B, w.Hkv, w.Nk, w.d), generator=gen, dtype=torch.float32)
     return tuple(t.to(torch.bfloat16) for t in (q, k, v))
+
+
+# ------------------------------------------------------------ packed batches
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """B sequences of different lengths packed without padding: q, dO
+    [H][total][d], k, v [Hkv][total][d], sequence b at rows cu[b] .. cu[b+1] - 1."""
+    name: str
+    lens: tuple
+    H: int
+    Hkv: int
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def B(self) -> int:
+        return len(self.lens)
+
+    @property
+    def total(self) -> int:
+        return int(sum(self.lens))
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(max(self.lens))
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def cu_seqlens(self) -> torch.Tensor:
+        cu = [0]
+        for n in self.lens:
+            cu.append(cu[-1] + int(n))
+        return torch.tensor(cu, dtype=torch.int32)
+
+
+def varlen_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
+    """n lengths drawn uniformly from [lo, hi] by a torch.Generator seeded
+    with `seed` (the mix of a packed training batch)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    return tuple(int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen))
+
+
+# A packed causal training batch: 16 sequences of 128 to 4096 tokens (about
+# 33K tokens), the GPT-style head shape of the long workloads (16 heads,
+# d = 128).
+VARLEN_WORKLOADS = {
+    "varlen": VarlenWorkload("varlen", lens=varlen_lengths(16, 128, 4096, 1208), H=16, Hkv=16,
+                             d=128, causal=True, seed=1008),
+}
+
+
+def make_varlen_inputs(w: VarlenWorkload):
+    """(q, k, v, dout) as CPU bf16 tensors in the packed layout: one
+    torch.Generator seeded with w.seed, N(0, 1) fp32 draws in the order Q, K,
+    V, dO, rounded to bf16 (round to nearest even)."""
+    gen = torch.Generator().manual_seed(int(w.seed))
+    q = torch.randn((w.H, w.total, w.d), generator=gen, dtype=torch.float32)
+    k = torch.randn((w.Hkv, w.total, w.d), generator=gen, dtype=torch.float32)
+    v = torch.randn((w.Hkv, w.total, w.d), generator=gen, dtype=torch.float32)
+    dout = torch.randn((w.H, w.total, w.d), generator=gen, dtype=torch.float32)
+    return tuple(t.to(torch.bfloat16) for t in (q, k, v, dout))

@@ -114,6 +114,48 @@ FA_API fa_status fa_fwd_window(const void* q, const void* k, const void* v, void
                                fa_stream_t stream);
 
 /*
+ * Packed variable-length batch forward ("varlen"): B sequences of different
+ * lengths, concatenated without padding (FlashAttention-2 review thread, the
+ * authors' answer "FA2 with variable sequence lengths": the lengths come as
+ * an array; here as their running sums, so each sequence's first row needs
+ * no scan).
+ * Sequence b occupies rows cu_seqlens[b] .. cu_seqlens[b+1] - 1 of every
+ * head; attention (with the causal mask when causal != 0) runs inside each
+ * sequence only.
+ *   q, o: bf16 [H][total][d];  k, v: bf16 [Hkv][total][d];  lse: fp32 [H][total].
+ *   cu_seqlens: DEVICE int32 [B + 1], 0 = cu[0] <= cu[1] <= ... <= cu[B] = total,
+ *     each length <= max_seqlen (read by the kernels; owned by the caller).
+ *   max_seqlen: the longest sequence (sizes the work decomposition).
+ * Offsets outside these rules give unspecified results but no access
+ * outside the tensors: the kernels clamp each sequence to [0, total) and to
+ * max_seqlen.  Errors as fa_fwd(), plus FA_ERR_INVALID_ARG for a null
+ * cu_seqlens or total < 1.  bf16 output; no sliding window.
+ * One launch of the forward kernel.
+ */
+FA_API fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                               const int* cu_seqlens, int B, int max_seqlen, int total, int H,
+                               int Hkv, int d, int causal, float scale, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd_varlen() needs: that of fa_bwd() for B
+ * sequences of max_seqlen rows (the workspace keeps a padded max_seqlen-row
+ * region per sequence and head).
+ */
+FA_API size_t fa_bwd_varlen_workspace_size(int B, int H, int Hkv, int max_seqlen, int d);
+
+/*
+ * Backward of fa_fwd_varlen(): layouts as there (dq like q; dk, dv like k),
+ * lse as fa_fwd_varlen() wrote it, workspace as in fa_bwd() (>=
+ * fa_bwd_varlen_workspace_size bytes).  Errors as fa_bwd() and
+ * fa_fwd_varlen().  Three kernel launches.
+ */
+FA_API fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               void* workspace, size_t workspace_bytes, const int* cu_seqlens,
+                               int B, int max_seqlen, int total, int H, int Hkv, int d,
+                               int causal, float scale, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd() needs: D and a padded copy of LSE
  * (fp32 [B][H][Np]) and the fp32 dQ accumulator ([B][H][Np][d]), where Np is
  * N rounded up to 128.  Returns 0 for arguments fa_bwd() would reject.

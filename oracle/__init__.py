@@ -14,6 +14,9 @@ Functions (NumPy float64 in, NumPy float64 out; layouts as in the C file):
                       (FlashAttention-2 answer on non-matmul FLOPs).
     attn_fwd_window / attn_bwd_window
                       causal sliding window: query i sees keys i - W < j <= i.
+    attn_fwd_varlen / attn_bwd_varlen
+                      packed variable-length sequences ([H][T][d], offsets
+                      cu_seqlens), each sequence its own attention problem.
     attn_fwd_decode   fewer query rows than keys (the decoding setting), the
                       queries being the last positions (bottom-right causal).
     attn_bwd          analytic gradients dQ, dK, dV and D = rowsum(dO * O).
@@ -226,6 +229,52 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float, mutant: int = 0):
                                       _ptr(dk), _ptr(dv), _ptr(D), B, H, Hkv, N, d,
                                       int(causal), float(scale))
     _check(rc, "oracle_attn_bwd")
+    return dq, dk, dv, D
+
+
+# ------------------------------------------------------------------ varlen
+# Packed variable-length batches (FlashAttention-2 review thread, the
+# authors' answer "FA2 with variable sequence lengths": sequences concatenated
+# without padding, their lengths in an array).  Layout q [H][T][d], k, v
+# [Hkv][T][d]; sequence b is rows cu[b] .. cu[b+1] - 1.  Each sequence is an
+# independent attention problem, so it is cut out and handed to attn_fwd /
+# attn_bwd.  Mutant 17 (a planted mistake for the pins) lets each sequence
+# run one row into the next.
+
+def _varlen_spans(cu, T, mutant):
+    cu = [int(x) for x in np.asarray(cu).ravel()]
+    if cu[0] != 0 or cu[-1] != T or any(b < a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must rise from 0 to the packed row count")
+    for a, e in zip(cu, cu[1:]):
+        if e > a:
+            yield a, (min(e + 1, T) if mutant == 17 else e), e
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens, causal: bool, scale: float, mutant: int = 0):
+    """Returns (O [H][T][d], LSE [H][T])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    H, T, d = q.shape
+    o = np.zeros_like(q)
+    lse = np.zeros((H, T))
+    for a, e, keep in _varlen_spans(cu_seqlens, T, mutant):
+        ob, lb = attn_fwd(q[None, :, a:e], k[None, :, a:e], v[None, :, a:e], causal, scale,
+                          mutant=mutant)
+        o[:, a:keep] = ob[0, :, :keep - a]
+        lse[:, a:keep] = lb[0, :, :keep - a]
+    return o, lse
+
+
+def attn_bwd_varlen(q, k, v, dout, cu_seqlens, causal: bool, scale: float, mutant: int = 0):
+    """Returns (dQ, dK, dV, D) in the packed layout."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    H, T, d = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    D = np.zeros((H, T))
+    for a, e, keep in _varlen_spans(cu_seqlens, T, mutant):
+        g = attn_bwd(q[None, :, a:e], k[None, :, a:e], v[None, :, a:e], dout[None, :, a:e],
+                     causal, scale, mutant=mutant)
+        for dst, src in zip((dq, dk, dv, D), g):
+            dst[:, a:keep] = src[0, :, :keep - a]
     return dq, dk, dv, D
 
 

@@ -454,7 +454,51 @@ def pin_window_slice(mutant=0):
     assert not close(so[:, :, 0], fo[:, :, s])
 
 
+def pin_varlen(mutant=0):
+    """Packed variable-length batches: with equal lengths the packed result is
+    the dense batched one (forward and gradients, both masks); with ragged
+    lengths (an empty and a one-row sequence among them) a torch fp64
+    softmax over the whole packed row with a block-diagonal (and causal) mask,
+    and its autograd, agree."""
+    close = lambda a, b: np.allclose(a, b, rtol=1e-10, atol=1e-12)
+    B, H, Hkv, N, d, scale = 3, 4, 2, 13, 8, 0.3
+    q, k, v, do = rand_qkv(B, H, Hkv, N, d, 14, dout=True)
+    pack = lambda x: np.ascontiguousarray(
+        x.transpose(1, 0, *range(2, x.ndim)).reshape(x.shape[1], B * N, *x.shape[3:]))
+    cu = np.arange(B + 1) * N
+    for causal in (False, True):
+        o, l = oracle.attn_fwd(q, k, v, causal, scale)
+        ov, lv = oracle.attn_fwd_varlen(pack(q), pack(k), pack(v), cu, causal, scale, mutant)
+        assert close(ov, pack(o)) and close(lv, pack(l[..., None])[..., 0])
+        g = oracle.attn_bwd(q, k, v, do, causal, scale)
+        gv = oracle.attn_bwd_varlen(pack(q), pack(k), pack(v), pack(do), cu, causal, scale, mutant)
+        for a_, b_ in zip(gv[:3], g[:3]):
+            assert close(a_, pack(b_))
+    lens = [5, 0, 1, 17, 9]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, G = int(cu[-1]), H // Hkv
+    rng = np.random.default_rng(15)
+    qp, dop = rng.standard_normal((H, T, d)), rng.standard_normal((H, T, d))
+    kp, vp = rng.standard_normal((Hkv, T, d)), rng.standard_normal((Hkv, T, d))
+    seq = np.repeat(np.arange(len(lens)), lens)
+    same = torch.tensor(seq[:, None] == seq[None, :])
+    for causal in (False, True):
+        allowed = same & torch.tril(torch.ones(T, T, dtype=torch.bool)) if causal else same
+        qt, kt, vt = (torch.tensor(x, requires_grad=True) for x in (qp, kp, vp))
+        ke, ve = kt.repeat_interleave(G, dim=0), vt.repeat_interleave(G, dim=0)
+        sc = (qt @ ke.transpose(-1, -2) * scale).masked_fill(~allowed, float("-inf"))
+        out = torch.softmax(sc, -1) @ ve
+        lse = torch.logsumexp(sc, -1)
+        (out * torch.tensor(dop)).sum().backward()
+        ov, lv = oracle.attn_fwd_varlen(qp, kp, vp, cu, causal, scale, mutant)
+        assert close(ov, out.detach().numpy()) and close(lv, lse.detach().numpy())
+        gq, gk, gv, _ = oracle.attn_bwd_varlen(qp, kp, vp, dop, cu, causal, scale, mutant)
+        assert close(gq, qt.grad.numpy()) and close(gk, kt.grad.numpy())
+        assert close(gv, vt.grad.numpy())
+
+
 ALL_PINS = [
+    pin_varlen,
     pin_sliding_window,
     pin_window_slice,
     pin_decode_rows,

@@ -23,6 +23,7 @@ MUTANTS = {
     14: "V codes not transposed",
     15: "decoding queries aligned top-left instead of bottom-right",
     16: "sliding window one key too wide",
+    17: "packed sequences run one row into the next",
 }
 
 
