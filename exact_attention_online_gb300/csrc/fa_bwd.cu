@@ -65,10 +65,16 @@ struct BwdCfg {
     static constexpr int kOffDS = kOffDO + 2 * kQBytes;
     static constexpr int kOffStage = kOffDS + kDSBytes;       // 2 x fp32 dQ staging tile
     static constexpr int kStageTileBytes = kBR * D * 4;        // 32 KB for both head dims
-    static constexpr int kOffStat = kOffStage + 2 * kStageTileBytes;   // lse2[2][BR], delta[2][BR]
-    static constexpr int kSmemBytes = kOffStat + 4 * kBR * 4;
+    // The K = 16 extension operands (unswizzled core matrices, 32 bytes a
+    // row): the constant A tile for the 128 key rows, and per stage the -LSE
+    // and -D tables of the BR query rows.
+    static constexpr int kOnesBytes = kBN * 32;
+    static constexpr int kExtBytes = kBR * 32;
+    static constexpr int kOffOnes = kOffStage + 2 * kStageTileBytes;
+    static constexpr int kOffExt = kOffOnes + kOnesBytes;     // [2 stages][lse, d]
+    static constexpr int kSmemBytes = kOffExt + 4 * kExtBytes;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;
-    static constexpr int kStageBytes = 2 * kQBytes + 2 * kBR * 4;
+    static constexpr int kStageBytes = 2 * kQBytes + 2 * kExtBytes;
     // TMEM columns
     static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + kBR,
                               kColDQ = 2 * D + 2 * kBR;
@@ -85,8 +91,8 @@ struct BwdParams {
     // the workspace keeps N-row (padded) regions per (batch, head).
     const int* cu_seqlens;
     float scale, scale_log2;
-    const float* lse2;
-    const float* delta;
+    const uint16_t* lse_ext;          // workspace tables (fa_internal.h)
+    const uint16_t* d_ext;
     float* dq_acc;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
@@ -147,8 +153,34 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint8_t* sDO = smem + Cfg::kOffDO;
     uint8_t* sDS = smem + Cfg::kOffDS;
     float* sStage = reinterpret_cast<float*>(smem + Cfg::kOffStage);   // [2][BR*D] fp32
-    float* sLSE = reinterpret_cast<float*>(smem + Cfg::kOffStat);      // [2][BR]
-    float* sDel = sLSE + 2 * BR;                                        // [2][BR]
+    uint8_t* sOnes = smem + Cfg::kOffOnes;
+    uint8_t* sExt = smem + Cfg::kOffExt;      // stage st: lse at 2 st, d at 2 st + 1
+
+    // The constant A operand of the extension MMAs, 128 key rows x 16
+    // columns: cols 0-8 hold 1/c as three bf16 terms (h h h m m m l l l),
+    // against the B columns (x_h x_m x_l) x 3 of -LSE log2(e), so that the
+    // nine products sum to (-LSE log2 e) / c; cols 9-11 hold 1 against the
+    // three terms of -D; the rest 0.  One 16-byte piece per compute thread.
+    if (threadIdx.x < kBN * 32 / 16) {
+        const float inv = 1.0f / p.scale_log2;
+        const float ih = bf16_round(inv), im = bf16_round(inv - ih),
+                    il = bf16_round(inv - ih - im);
+        const int kc = (threadIdx.x >> 3) & 1;   // K half of this core-matrix row
+        uint4 w;
+        if (kc == 0) {
+            w.x = pack_bf16x2(ih, ih);
+            w.y = pack_bf16x2(ih, im);
+            w.z = pack_bf16x2(im, im);
+            w.w = pack_bf16x2(il, il);
+        } else {
+            w.x = pack_bf16x2(il, 1.0f);
+            w.y = pack_bf16x2(1.0f, 1.0f);
+            w.z = 0u;
+            w.w = 0u;
+        }
+        *reinterpret_cast<uint4*>(sOnes + threadIdx.x * 16) = w;
+        fence_proxy_async_smem();
+    }
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
@@ -194,8 +226,6 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             if (!fa_wait_warp(&bar_full[st], (it >> 1) & 1, 60, wc) ||
                 !fa_wait_warp(&bar_s, it & 1, 61, wc)) { ok = false; break; }
             tc_fence_after();
-            const float* lse_s = sLSE + st * BR;     // -LSE * log2(e)
-            const float* del_s = sDel + st * BR;     // -D
             const int q0 = i * BR;
             const bool need_mask = (CAUSAL && (q0 < jblk * kBN + kBN - 1 ||
                                                (WINDOW && q0 + BR - 1 > jblk * kBN + p.window - 1))) ||
@@ -204,9 +234,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const int key_lim = CAUSAL ? key - q0 : -1;
             const int key_hi = WINDOW ? key + p.window - 1 - q0 : BR;
             const bool key_valid = key < seq_len;
-            // P^T = 2^(S^T c - LSE log2 e), kept in fp32 for dS; bf16 copy into
-            // TMEM over this warp's own S^T columns (already read).  Two
-            // columns per paired-fp32 instruction.
+            // P^T = 2^(S'^T c) with S'^T = S^T - LSE log2(e) / c from the
+            // tensor core, kept in fp32 for dS; bf16 copy into TMEM over this
+            // warp's own S^T columns (already read).  Two columns per
+            // paired-fp32 instruction.
             float pf[HALF];
             const uint64_t c2 = f2(c, c);
 #pragma unroll
@@ -218,10 +249,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 #pragma unroll
                 for (int e2 = 0; e2 < 16; ++e2) {
                     const int qe = cb + ch * 32 + 2 * e2;
-                    const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(lse_s + qe);
                     float x0, x1;
-                    f2_split(f2_fma(f2(__uint_as_float(sr[2 * e2]), __uint_as_float(sr[2 * e2 + 1])),
-                                    c2, nl2),
+                    f2_split(f2_mul(f2(__uint_as_float(sr[2 * e2]), __uint_as_float(sr[2 * e2 + 1])),
+                                    c2),
                              x0, x1);
                     float p0 = ex2(x0), p1 = ex2(x1);
                     if (need_mask) {
@@ -238,7 +268,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before();
             mbar_arrive(&bar_p);
 
-            // dS^T = P^T o (dP^T - D) -> bf16, swizzled [key][query] tile in smem.
+            // dS^T = P^T o (dP^T - D) -> bf16, swizzled [key][query] tile in
+            // smem; dP^T - D comes from the tensor core.
             if (!fa_wait_warp(&bar_dp, it & 1, 62, wc)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
@@ -249,13 +280,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 uint32_t dsk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int qe = cb + ch * 32 + 2 * e;
-                    const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(del_s + qe);
                     float d0, d1;
                     f2_split(f2_mul(f2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]),
-                                    f2_add(f2(__uint_as_float(dpr[2 * e]),
-                                              __uint_as_float(dpr[2 * e + 1])),
-                                           nd2)),
+                                    f2(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1]))),
                              d0, d1);
                     dsk[e] = pack_bf16x2(d0, d1);
                 }
@@ -399,9 +426,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do,
                                     &bar_full[st], c * 64, tok0 + i * BR, z_q);
                     }
-                    const size_t stat = (size_t)bh * p.Np + (size_t)i * BR;
-                    bulk_load(sLSE + st * BR, p.lse2 + stat, BR * 4, &bar_full[st]);
-                    bulk_load(sDel + st * BR, p.delta + stat, BR * 4, &bar_full[st]);
+                    const size_t xrow = (size_t)bh * p.Np + (size_t)i * BR;
+                    bulk_load(sExt + (2 * st) * Cfg::kExtBytes, p.lse_ext + xrow * kExtCols,
+                              Cfg::kExtBytes, &bar_full[st]);
+                    bulk_load(sExt + (2 * st + 1) * Cfg::kExtBytes, p.d_ext + xrow * kExtCols,
+                              Cfg::kExtBytes, &bar_full[st]);
                     issued = it + 1;
                 }
                 if (abort_sh) {
@@ -423,20 +452,26 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 // Descriptors are built once per operand tile and stepped by
                 // constants, keeping the issuing thread's work between MMAs small.
                 const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
-                auto issue_s = [&](int st) {      // S^T = K_j Q_i^T
+                const uint32_t sext = smem_u32(sExt);
+                const uint64_t onesd = sdesc_plain(smem_u32(sOnes), 128, 256);
+                auto issue_s = [&](int st) {      // S^T = K_j Q_i^T - LSE log2(e) / c
                     const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
                                qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                    mma_ss(tmem + Cfg::kColS, onesd, sdesc_plain(sext + 2 * st * Cfg::kExtBytes,
+                                                                 128, 256), id_s, 1u);
                     mma_commit(&bar_s);
                 };
-                auto issue_dp = [&](int st) {     // dP^T = V_j dO_i^T
+                auto issue_dp = [&](int st) {     // dP^T - D = V_j dO_i^T - D
                     const uint64_t dod = sdesc_sw128(sdo + st * Cfg::kQBytes, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss(tmem + Cfg::kColDP, vd + kmajor_step(kk, kBN * 128),
                                dod + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                    mma_ss(tmem + Cfg::kColDP, onesd,
+                           sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s, 1u);
                     mma_commit(&bar_dp);
                 };
                 bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
@@ -512,22 +547,28 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
                            sdo = smem_u32(sDO), sds = smem_u32(sDS);
             const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
+            const uint32_t sext = smem_u32(sExt);
+            const uint64_t onesd = sdesc_plain(smem_u32(sOnes), 128, 256);
             const bool half_a = (warp == kMmaWarp);
             const bool half_b = (warp == kMma2Warp);
-            auto issue_s = [&](int st) {      // S^T = K_j Q_i^T
+            auto issue_s = [&](int st) {      // S^T = K_j Q_i^T - LSE log2(e) / c
                 const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
                            qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                mma_ss(tmem + Cfg::kColS, onesd, sdesc_plain(sext + 2 * st * Cfg::kExtBytes, 128,
+                                                             256), id_s, 1u);
                 mma_commit(&bar_s);
             };
-            auto issue_dp = [&](int st) {     // dP^T = V_j dO_i^T
+            auto issue_dp = [&](int st) {     // dP^T - D = V_j dO_i^T - D
                 const uint64_t dod = sdesc_sw128(sdo + st * Cfg::kQBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + Cfg::kColDP, vd + kmajor_step(kk, kBN * 128),
                            dod + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                mma_ss(tmem + Cfg::kColDP, onesd,
+                       sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s, 1u);
                 mma_commit(&bar_dp);
             };
             bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
@@ -630,60 +671,90 @@ __device__ __forceinline__ int seq_row(const int* __restrict__ cu, long long bh,
     return len;
 }
 
-// -D_i = -<dO_i, O_i>, -LSE * log2(e) (-inf on padded rows), accumulator = 0.
-// One warp per row, grid-stride over the B*H*Np workspace rows.  O is bf16,
-// or fp32 when it comes from the precise forward.
+// Per workspace row (b, h, i < Np): the two K = 16 extension tables of the
+// dK/dV kernel and a zeroed dQ accumulator row.  x = -LSE log2(e) (padded
+// rows: -1e30, so that P = 0 there) and y = -D = -<dO_i, O_i> are each split
+// into three bf16 terms (h + m + l holds x to about 24 bits):
+//   lse_ext row: cols 0-8 = x_h x_m x_l x_h x_m x_l x_h x_m x_l, 9-15 = 0
+//   d_ext row:   cols 9-11 = y_h y_m y_l, the rest 0
+// stored as unswizzled K-major core matrices (row group g = r / 8, K half kc:
+// 16 bytes at ((2 g + kc) * 8 + r % 8) * 16).  D / 8 lanes per row (16-byte
+// loads), 256 / D rows per warp, grid-stride over the B*H*Np rows.  O is
+// bf16, or fp32 when it comes from the precise forward.
 template <int D, typename OT>
 __global__ void __launch_bounds__(256)
 fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                  const float* __restrict__ lse, float* __restrict__ lse2,
-                  float* __restrict__ delta, float* __restrict__ dq_acc, int N, int Np,
+                  const float* __restrict__ lse, uint16_t* __restrict__ lse_ext,
+                  uint16_t* __restrict__ d_ext, float* __restrict__ dq_acc, int N, int Np,
                   long long rows, const int* __restrict__ cu, int H, long long seq_rows) {
-    constexpr int kPer = D / 32;   // elements per lane (2 or 4)
-    const int lane = threadIdx.x & 31;
+    constexpr int LPR = D / 8;          // lanes per row, 8 elements each
+    constexpr int RPW = 32 / LPR;       // rows per warp
+    const int lane = threadIdx.x & 31, sub = lane / LPR, sl = lane % LPR;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    for (long long r = wid; r < rows; r += nw) {
+    for (long long r0 = wid * RPW; r0 < rows; r0 += nw * RPW) {
+        const long long r = r0 + sub;
+        const bool in = r < rows;
         const long long bh = r / Np;
         const int i = (int)(r % Np);
-        long long base;
-        const int len = seq_row(cu, bh, H, N, seq_rows, base);
+        long long base = 0;
+        const int len = in ? seq_row(cu, bh, H, N, seq_rows, base) : 0;
+        const bool valid = in && i < len;
+        float x = -1e30f;
+        if (valid) x = -lse[base + i] * 1.4426950408889634f;
         float acc = 0.0f;
-        if (i < len) {
-            const long long src = (base + i) * D + lane * kPer;
-            float ov[kPer], dv[kPer];
-            if (kPer == 4) {
-                const uint2 dd = *reinterpret_cast<const uint2*>(dout + src);
-                const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dd);
-                const float2 a = __bfloat1622float2(d2[0]), c2 = __bfloat1622float2(d2[1]);
-                dv[0] = a.x; dv[1] = a.y; dv[kPer - 2] = c2.x; dv[kPer - 1] = c2.y;
-            } else {
-                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + src));
-                dv[0] = a.x; dv[kPer - 1] = a.y;
-            }
+        if (valid) {
+            const long long src = (base + i) * D + sl * 8;
+            const uint4 dd = *reinterpret_cast<const uint4*>(dout + src);
+            const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dd);
+            float ov[8];
             if constexpr (sizeof(OT) == 4) {
-#pragma unroll
-                for (int t = 0; t < kPer; ++t) ov[t] = reinterpret_cast<const float*>(o)[src + t];
-            } else if (kPer == 4) {
-                const uint2 oo = *reinterpret_cast<const uint2*>(o + src);
-                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&oo);
-                const float2 a = __bfloat1622float2(o2[0]), c2 = __bfloat1622float2(o2[1]);
-                ov[0] = a.x; ov[1] = a.y; ov[kPer - 2] = c2.x; ov[kPer - 1] = c2.y;
+                const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o) + src);
+                const float4 b = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o) + src + 4);
+                ov[0] = a.x; ov[1] = a.y; ov[2] = a.z; ov[3] = a.w;
+                ov[4] = b.x; ov[5] = b.y; ov[6] = b.z; ov[7] = b.w;
             } else {
-                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + src));
-                ov[0] = a.x; ov[kPer - 1] = a.y;
+                const uint4 oo = *reinterpret_cast<const uint4*>(o + src);
+                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&oo);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 f = __bfloat1622float2(o2[t]);
+                    ov[2 * t] = f.x;
+                    ov[2 * t + 1] = f.y;
+                }
             }
 #pragma unroll
-            for (int t = 0; t < kPer; ++t) acc = fmaf(ov[t], dv[t], acc);
+            for (int t = 0; t < 4; ++t) {
+                const float2 f = __bfloat1622float2(d2[t]);
+                acc = fmaf(ov[2 * t], f.x, acc);
+                acc = fmaf(ov[2 * t + 1], f.y, acc);
+            }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            delta[r] = -acc;
-            lse2[r] = (i < len) ? -lse[base + i] * 1.4426950408889634f : -CUDART_INF_F;
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (in && sl < 2) {
+            // lane 0 of the row: the lse_ext row, lane 1: the d_ext row
+            const float v = (sl == 0) ? x : -acc;
+            const float h = bf16_round(v), m = bf16_round(v - h), l = bf16_round(v - h - m);
+            uint4 w0, w1;
+            if (sl == 0) {
+                w0 = make_uint4(pack_bf16x2(h, m), pack_bf16x2(l, h), pack_bf16x2(m, l),
+                                pack_bf16x2(h, m));
+                w1 = make_uint4(pack_bf16x2(l, 0.0f), 0u, 0u, 0u);
+            } else {
+                w0 = make_uint4(0u, 0u, 0u, 0u);
+                w1 = make_uint4(pack_bf16x2(0.0f, h), pack_bf16x2(m, l), 0u, 0u);
+            }
+            uint16_t* row = (sl == 0 ? lse_ext : d_ext) +
+                            ((r >> 3) * 2 * 8 + (r & 7)) * 8;   // (2 g + 0) * 64 + (r % 8) * 8
+            *reinterpret_cast<uint4*>(row) = w0;
+            *reinterpret_cast<uint4*>(row + 64) = w1;            // K half 1: + 8 rows x 8
         }
-        float4* z = reinterpret_cast<float4*>(dq_acc + r * D);
-        for (int e = lane; e < D / 4; e += 32) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in) {
+            float4* z = reinterpret_cast<float4*>(dq_acc + r * D) + sl * 2;
+            z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+            z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 }
 
@@ -793,28 +864,28 @@ cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, con
     const int Np = padded_rows(s.N);
     const long long rows = (long long)s.B * s.H * Np;
     const long long seq_rows = s.cu_seqlens ? s.total : s.N;
-    const int grid = grid_for(rows, 8);
+    const int grid = grid_for(rows, 8 * (256 / s.d));   // 8 warps a block, 256/d rows a warp
     count_launch();
     auto* d_ = static_cast<const __nv_bfloat16*>(dout);
     auto* ob = static_cast<const __nv_bfloat16*>(o);
     auto* of = static_cast<const float*>(o);
     if (s.d == 128) {
         if (o_f32)
-            fa_bwd_pre_kernel<128, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse2, ws.delta,
+            fa_bwd_pre_kernel<128, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse_ext, ws.d_ext,
                                                                     ws.dq_acc, s.N, Np, rows,
                                                                     s.cu_seqlens, s.H, seq_rows);
         else
             fa_bwd_pre_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows,
+                ob, d_, lse, ws.lse_ext, ws.d_ext, ws.dq_acc, s.N, Np, rows,
                                                                     s.cu_seqlens, s.H, seq_rows);
     } else {
         if (o_f32)
-            fa_bwd_pre_kernel<64, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse2, ws.delta,
+            fa_bwd_pre_kernel<64, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse_ext, ws.d_ext,
                                                                    ws.dq_acc, s.N, Np, rows,
                                                                     s.cu_seqlens, s.H, seq_rows);
         else
             fa_bwd_pre_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-                ob, d_, lse, ws.lse2, ws.delta, ws.dq_acc, s.N, Np, rows,
+                ob, d_, lse, ws.lse_ext, ws.d_ext, ws.dq_acc, s.N, Np, rows,
                                                                     s.cu_seqlens, s.H, seq_rows);
     }
     return cudaGetLastError();
@@ -846,8 +917,8 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     p.window = s.window > 0 ? s.window : kNoWindow;
     p.scale = s.scale;
     p.scale_log2 = (float)((double)s.scale * 1.4426950408889634);
-    p.lse2 = ws.lse2;
-    p.delta = ws.delta;
+    p.lse_ext = ws.lse_ext;
+    p.d_ext = ws.d_ext;
     p.dq_acc = ws.dq_acc;
     p.dk = static_cast<__nv_bfloat16*>(dk);
     p.dv = static_cast<__nv_bfloat16*>(dv);

@@ -44,13 +44,18 @@ constexpr int kNoWindow = 1 << 30;
 constexpr int kRowPad = 128;
 inline int padded_rows(int N) { return (N + kRowPad - 1) / kRowPad * kRowPad; }
 
-// Backward workspace: [lse2 fp32 B*H*Np][D fp32 B*H*Np][dQacc fp32 B*H*Np*d],
-// each region 256-byte aligned.
+// Backward workspace: [lse_ext bf16 B*H*Np x 16][d_ext bf16 B*H*Np x 16]
+// [dQacc fp32 B*H*Np*d], each region 256-byte aligned.  The two ext tables
+// are the B operands of the K = 16 MMAs that add -LSE (scaled) to S^T and -D
+// to dP^T inside the tensor core: per row 16 bf16 columns, stored as
+// 8-row x 16-byte core matrices (row group g, K half kc at (2 g + kc) * 128
+// bytes), the layout of an unswizzled K-major MMA operand.
 struct BwdWorkspace {
-    float* lse2;   // -LSE * log2(e), padded rows = -inf
-    float* delta;  // -D = -rowsum(dO * O), padded rows = 0
-    float* dq_acc; // fp32 accumulator of dQ / scale
+    uint16_t* lse_ext;  // cols 0-8: -LSE log2(e) as three bf16 terms, three times
+    uint16_t* d_ext;    // cols 9-11: -D = -rowsum(dO o O) as three bf16 terms
+    float* dq_acc;      // fp32 accumulator of dQ / scale
 };
+constexpr int kExtCols = 16;   // bf16 columns per row of an ext table
 size_t bwd_workspace_bytes(const Shape& s);
 BwdWorkspace bwd_workspace_carve(void* base, const Shape& s);
 

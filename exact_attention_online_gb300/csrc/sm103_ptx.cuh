@@ -236,6 +236,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Shared-memory matrix descriptor, no swizzle (layout type 0): 8-row x
+// 16-byte core matrices stored whole (row r at +16 r); lbo = byte distance
+// between core matrices adjacent along K, sbo = between 8-row groups along M/N.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // Offset, in the descriptor's 16-byte address units, of 16-element K step kk
 // of a K-major 128B-swizzled tile whose 64-element chunks lie chunk_bytes
 // apart.  A descriptor for step kk is the step-0 descriptor plus this value:
@@ -388,6 +400,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// x rounded to bf16 (nearest even), returned as fp32.
+__device__ __forceinline__ float bf16_round(float x) {
+    return __uint_as_float(pack_bf16x2(x, 0.0f) << 16);
 }
 
 // Two fp32 values -> two e4m3 codes (round to nearest even, saturating at

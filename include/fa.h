@@ -156,9 +156,10 @@ FA_API fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, cons
                                int causal, float scale, fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd() needs: D and a padded copy of LSE
- * (fp32 [B][H][Np]) and the fp32 dQ accumulator ([B][H][Np][d]), where Np is
- * N rounded up to 128.  Returns 0 for arguments fa_bwd() would reject.
+ * Bytes of device workspace fa_bwd() needs: -LSE and -D as 16-column bf16
+ * tables ([B][H][Np][16] each, the operands of the small MMAs that fold them
+ * into S and dP) and the fp32 dQ accumulator ([B][H][Np][d]), where Np is N
+ * rounded up to 128.  Returns 0 for arguments fa_bwd() would reject.
  */
 FA_API size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
 
@@ -200,9 +201,9 @@ FA_API fa_status fa_bwd_window(const void* q, const void* k, const void* v, cons
                                fa_stream_t stream);
 
 /*
- * Backward, stage 1 of 3: D_i = sum_c dO_ic O_ic (fp32), LSE copied into the
- * workspace in base-2 units with padding rows, and the fp32 dQ accumulator
- * zeroed.  One launch.
+ * Backward, stage 1 of 3: D_i = sum_c dO_ic O_ic (fp32); -D and -LSE (base-2
+ * units, padding rows that give P = 0) written into the workspace tables as
+ * three bf16 terms each; the fp32 dQ accumulator zeroed.  One launch.
  */
 FA_API fa_status fa_bwd_preprocess(const void* o, const void* dout, const float* lse,
                             void* workspace, size_t workspace_bytes,
