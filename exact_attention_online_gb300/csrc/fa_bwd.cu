@@ -120,15 +120,20 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const WaitCtx wc{p.status, &abort_sh};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // (batch, kv head, key block j), key-block-major: the CTAs go out in
-    // blockIdx order, so under the causal mask the longest ones (small j,
-    // every query block after them) start first and the shortest fill the
-    // tail (a CPU model of the bench workloads puts the busiest SM within
-    // 1-2 % of the mean instead of 7-14 %).
+    // (batch, kv head, key block j).  The CTAs go out in blockIdx order.
+    // Dense causal batches: key-block-major, so that the longest CTAs (small
+    // j, every query block after them) start first and the shortest fill the
+    // tail (a CPU model of the bench workloads puts the busiest SM within 1-2 %
+    // of the mean instead of 7-14 %; measured: dK/dV +2 % to +13 %).
+    // Otherwise head-major: without the mask every CTA costs the same and
+    // the CTAs that run at the same time share Q and dO in L2 (key-block-major
+    // measured 12 % slower there), and with packed sequences of different
+    // lengths j does not rank the cost (measured 12 % slower).
+    constexpr bool kKeyMajor = CAUSAL && !VARLEN;
     const int n_kblk = (p.N + kBN - 1) / kBN;
     const int n_bg = gridDim.x / n_kblk;          // B * Hkv
-    const int jblk = blockIdx.x / n_bg;
-    const int bg = blockIdx.x % n_bg;             // b * Hkv + g
+    const int jblk = kKeyMajor ? blockIdx.x / n_bg : blockIdx.x % n_kblk;
+    const int bg = kKeyMajor ? blockIdx.x % n_bg : blockIdx.x / n_kblk;   // b * Hkv + g
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     // The sequence: its first row in the tensors and its length.  Dense
     // batches address rows of head b*H(kv) + h; packed ones rows tok0 + i of
