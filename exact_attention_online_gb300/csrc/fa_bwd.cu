@@ -83,6 +83,7 @@ struct BwdCfg {
 struct BwdParams {
     int H, Hkv, N, Np, G, causal;
     int rows;                         // rows per head of q, k, v, dk, dv: N, or the packed total
+    int chunk;                        // key/value heads per key-block-major chunk (causal)
     // Causal sliding window W: key k is seen by queries k <= i < k + W.
     // Without a window this holds kNoWindow.
     int window;
@@ -129,11 +130,22 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // the CTAs that run at the same time share Q and dO in L2 (key-block-major
     // measured 12 % slower there), and with packed sequences of different
     // lengths j does not rank the cost (measured 12 % slower).
+    // Key-block-major runs over chunks of p.chunk heads at a time, sized so
+    // that a chunk's Q, dO and dQ accumulator stay in L2 while its key blocks
+    // re-read them.
     constexpr bool kKeyMajor = CAUSAL && !VARLEN;
     const int n_kblk = (p.N + kBN - 1) / kBN;
     const int n_bg = gridDim.x / n_kblk;          // B * Hkv
-    const int jblk = kKeyMajor ? blockIdx.x / n_bg : blockIdx.x % n_kblk;
-    const int bg = kKeyMajor ? blockIdx.x % n_bg : blockIdx.x / n_kblk;   // b * Hkv + g
+    int jblk, bg;                                 // bg = b * Hkv + g
+    if (kKeyMajor) {
+        const int chunk = blockIdx.x / (p.chunk * n_kblk), loc = blockIdx.x % (p.chunk * n_kblk);
+        const int width = min(p.chunk, n_bg - chunk * p.chunk);
+        jblk = loc / width;
+        bg = chunk * p.chunk + loc % width;
+    } else {
+        jblk = blockIdx.x % n_kblk;
+        bg = blockIdx.x / n_kblk;
+    }
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     // The sequence: its first row in the tensors and its length.  Dense
     // batches address rows of head b*H(kv) + h; packed ones rows tok0 + i of
@@ -918,6 +930,21 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     p.rows = rows;
     p.cu_seqlens = s.cu_seqlens;
     p.G = s.H / s.Hkv;
+    // Chunk size: what fits a 64 MB L2 budget of Q, dO (bf16) and dQ
+    // accumulator (fp32) rows, 8 G N d bytes per key/value head, but at least
+    // a quarter of the heads: with many small chunks the heavy CTAs of the last
+    // one start late and the balance is lost (CPU model: gqa 0.88 of the mean
+    // load at 3 heads a chunk, 0.98 at 8).
+    {
+        const long long n_bg = (long long)s.B * s.Hkv;
+        const long long per = 8LL * p.G * s.N * s.d;
+        long long c = (64LL << 20) / (per > 0 ? per : 1);
+        c = c > (n_bg + 3) / 4 ? c : (n_bg + 3) / 4;
+        // A window bounds every key block's query range, so the working set
+        // of all heads at once is small: one chunk (measured 1 % faster).
+        if (s.window > 0) c = n_bg;
+        p.chunk = (int)(c < 1 ? 1 : (c > n_bg ? n_bg : c));
+    }
     p.causal = s.causal;
     p.window = s.window > 0 ? s.window : kNoWindow;
     p.scale = s.scale;
