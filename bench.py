@@ -432,11 +432,81 @@ def run_native(args, w):
             e2e_step()
         b.record(stream)
         barrier()
+        serial_ms = replicas.max_over_ranks(a.elapsed_time(b), dev)
+
+        # The same steps pipelined as a training loop would run them: three
+        # streams (host->device, compute, device->host) and two slots of
+        # device buffers, so that the copies of step k+1's inputs and of step
+        # k-1's outputs overlap the kernels of step k.  Every step still copies
+        # all of its inputs in and all of its outputs out.
+        dev_in = [[qd, kd, vd, dod], [torch.empty_like(t) for t in (qd, kd, vd, dod)]]
+        dev_out = [[o, lse, dq, dk, dv], [torch.empty_like(t) for t in (o, lse, dq, dk, dv)]]
+        host_in = [hq, hk, hv, hdo]
+        n_in = 3 if fwd_only else 4
+        n_out = len(outs_h)
+        # one copy stream each way (two each way measured slower)
+        s_in = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        ev = {k_: [torch.cuda.Event(), torch.cuda.Event()] for k_ in ("in", "comp", "out")}
+
+        def compute(slot):
+            q_, k_, v_, do_ = dev_in[slot]
+            o_, l_, dq_, dk_, dv_ = dev_out[slot]
+            if precise:
+                fa.fa_fwd_precise(q_, k_, v_, o_, l_, w.causal, w.scale, stream)
+            elif w.window:
+                fa.fa_fwd_window(q_, k_, v_, o_, l_, w.window, w.scale, stream)
+            else:
+                fa.fa_fwd(q_, k_, v_, o_, l_, w.causal, w.scale, stream)
+            if not fwd_only and w.window:
+                fa.fa_bwd_window(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.window, w.scale,
+                                 stream)
+            elif not fwd_only and precise:
+                fa.fa_bwd_precise(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.causal,
+                                  w.scale, stream)
+            elif not fwd_only:
+                fa.fa_bwd(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.causal, w.scale, stream)
+
+        def pipelined(n):
+            for k_ in range(n):
+                sl = k_ % 2
+                with torch.cuda.stream(s_in):
+                    if k_ >= 2:
+                        s_in.wait_event(ev["comp"][sl])     # step k-2 done with these inputs
+                    for dst, src_ in zip(dev_in[sl][:n_in], host_in[:n_in]):
+                        dst.copy_(src_, non_blocking=True)
+                    ev["in"][sl].record(s_in)
+                stream.wait_event(ev["in"][sl])
+                if k_ >= 2:
+                    stream.wait_event(ev["out"][sl])        # step k-2's outputs copied out
+                compute(sl)
+                ev["comp"][sl].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev["comp"][sl])
+                    for dst, src_ in zip(outs_h, dev_out[sl][:n_out]):
+                        dst.copy_(src_, non_blocking=True)
+                    ev["out"][sl].record(s_out)
+
+        pipelined(2)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_in)
+        pipelined(e2e_steps)
+        b.record(s_out)
+        barrier()
         e_ms = replicas.max_over_ranks(a.elapsed_time(b), dev)
+        st = fa.fa_device_status(stream)
+        if st != 0:
+            raise RuntimeError(f"device status after e2e steps: {fa.fa_status_string(st)}")
         e2e = {"value": replicas.whole_job_rate(flops_step, e2e_steps, ws, e_ms) / 1e12,
                "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / e2e_steps}
+               "ms_per_step": e_ms / e2e_steps,
+               "pipelined": "inputs of step k+1 copied in and outputs of step k-1 copied out "
+                            "while step k computes (three streams, two device buffer slots)",
+               "serial_value": replicas.whole_job_rate(flops_step, e2e_steps, ws,
+                                                       serial_ms) / 1e12,
+               "serial_ms_per_step": serial_ms / e2e_steps}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
