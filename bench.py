@@ -44,14 +44,14 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel source it was taken on.  A source change makes the figure stale and
 # it is then reported as null.
 NCU_TRAFFIC = {
-    # profiles/launches_mha_d64_fwd_bwd.md capture: 203.5 MB read + 87.6 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 291.06e6, "src_sha": "10a151f2130648b3"},
-    # the same capture: 111.5 MB read + 12.4 MB written, one launch
-    ("fa_fwd", "mha_d64"): {"bytes": 123.92e6, "src_sha": "bd61666491615be6"},
-    # profiles/fa_window_fwd_bwd_window.md: 610.0 MB read + 292.9 MB written
-    ("fa_bwd_dkdv", "window"): {"bytes": 902.86e6, "src_sha": "10a151f2130648b3"},
-    # the same file: 205.6 MB read + 98.5 MB written
-    ("fa_fwd", "window"): {"bytes": 304.13e6, "src_sha": "bd61666491615be6"},
+    # profiles/fa_bwd_dkdv_mha_d64.md: 239.6 MB read + 107.8 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 347.39e6, "src_sha": "2295e403134c24cc"},
+    # profiles/launches_mha_d64_fwd_bwd.md: 113.8 MB read + 13.3 MB written, one launch
+    ("fa_fwd", "mha_d64"): {"bytes": 127.10e6, "src_sha": "d1d60eb3316b9335"},
+    # profiles/fa_window_fwd_bwd_window.md: 1388.2 MB read + 645.8 MB written
+    ("fa_bwd_dkdv", "window"): {"bytes": 2034.00e6, "src_sha": "2295e403134c24cc"},
+    # the same file: 205.7 MB read + 97.9 MB written
+    ("fa_fwd", "window"): {"bytes": 303.62e6, "src_sha": "d1d60eb3316b9335"},
     # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 5.1 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0790e9, "src_sha": "6f9c75dfde0d8a68"},
 }
