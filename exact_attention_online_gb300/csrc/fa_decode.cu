@@ -7,24 +7,23 @@
 // sees key j iff j <= r + Nk - Nq (bottom-right alignment; the forward's
 // j <= i when Nq == Nk).
 //
-// The work is bandwidth-bound (every key and value row is read once and used
-// for only R = G * Nq query rows, G = H / Hkv), so it runs on the CUDA cores:
-//   split kernel   one CTA per (batch, kv head, key split): one producer warp
-//                  streams the split's contiguous K and V rows, 64 keys per
-//                  tile, into a 96 KB shared-memory ring by bulk copies (two
-//                  CTAs per SM for up to 8 rows); eight compute warps, per tile:
-//                  (1) warp w scores keys w, w + 8, ...: lane l holds head-dim
-//                  elements [EPL l, EPL l + EPL) of K and of the q rows
-//                  (registers), and a key's R partial dot products are summed
-//                  over the lanes by a reduce-scatter butterfly; (2) one warp
-//                  per row updates the running max m and sum l over the tile
-//                  (online softmax, base 2) and turns the scores into p;
-//                  (3) thread t owns four columns (t % (d/4)) and every
-//                  (256 / (d/4))-th key of the tile, and accumulates all R
-//                  output rows over its keys after scaling them by
-//                  2^(m_old - m_new).  At the end of the split the key groups'
-//                  sums are added through shared memory, and the split writes
-//                  o / l (fp32) and its LSE.
+// Every key and value row is read once and used for only R = G * Nq query
+// rows (G = H / Hkv), so the work is bandwidth-bound; the arithmetic still
+// goes to the tensor core, which leaves the CUDA cores only the softmax:
+//   split kernel   one CTA (three warps) per (batch, kv head, key split).  The
+//                  R query rows of the group sit in the first rows of a
+//                  128-row Q tile (the rest zero) and the split's keys stream
+//                  through a TMA ring in tiles of 128:
+//                    S_t = Q K_t^T   (SS MMA, M = N = 128, two TMEM buffers)
+//                    O  += P_t V_t   (TS MMA, P over the first half of S_t)
+//                  so the tensor core does 128 / R times the useful work and
+//                  still idles most of the time (a 64 KB tile takes about
+//                  3000 cycles of one SM's share of HBM bandwidth, its MMAs
+//                  about 700).  Warp 0 holds rows 0-31 of S and runs the
+//                  online softmax (base 2, conditional rescale of O in TMEM)
+//                  for the rows below R; warp 1 loads; warp 2 issues the
+//                  MMAs (S one tile ahead of P V).  The split writes o / l
+//                  (fp32) and its LSE.
 //   combine kernel one warp per output row: LSE = log sum_s exp(LSE_s),
 //                  O = sum_s exp(LSE_s - LSE) O_s, bf16.
 #include <cuda_bf16.h>
@@ -36,16 +35,14 @@
 namespace fa {
 namespace {
 
-constexpr int kTileKeys = 64;         // keys per tile
-constexpr int kThreads = 256;         // compute threads; one more warp produces
-constexpr int kMaxRows = kDecodeMaxRows;   // G * Nq
+constexpr int kTileKeys = 128;        // keys per tile (the MMA's N)
+constexpr int kThreads = 96;          // softmax warp, producer warp, MMA warp
+constexpr int kQRows = 16;            // query rows loaded (R <= 16), rest of the tile zero
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kRescale = 8.0f;      // log2 units, as in the forward
 
 struct DecodeParams {
-    const __nv_bfloat16* q;   // [B][H][Nq][d]
-    const __nv_bfloat16* k;   // [B][Hkv][Nk][d]
-    const __nv_bfloat16* v;
     float* o_part;            // [B][H][Nq][n_split][d]
     float* lse_part;          // [B][H][Nq][n_split], natural log
     int H, Hkv, Nq, Nk, G, R, n_split, keys_per_split, causal;
@@ -53,264 +50,262 @@ struct DecodeParams {
     DeviceStatus* status;
 };
 
-// K/V ring depth: 3 stages of 32 KB at d = 128, 6 of 16 KB at d = 64 (96 KB,
-// so two CTAs fit on an SM when their registers allow).
+// K/V ring: 3 stages of 64 KB (K and V tiles) at d = 128, 6 of 32 KB at d = 64;
+// with the 16 or 32 KB Q tile one CTA fills an SM's shared memory.
 template <int D>
 __host__ __device__ constexpr int decode_stages() { return D == 128 ? 3 : 6; }
 template <int D>
-__host__ __device__ constexpr int decode_smem_bytes() { return decode_stages<D>() * 2 * kTileKeys * D * 2; }
+__host__ __device__ constexpr int decode_tile_bytes() { return kTileKeys * D * 2; }
+template <int D>
+__host__ __device__ constexpr int decode_smem_bytes() {
+    return 128 * D * 2 + decode_stages<D>() * 2 * decode_tile_bytes<D>() + 1024;
+}
 
-template <int D, int RP>
-__global__ void __launch_bounds__(kThreads + 32, 1)
-fa_decode_split_kernel(const DecodeParams p) {
-    constexpr int EPL = D / 32;               // head-dim elements per lane in (1)
-    constexpr int CG = D / 4;                 // column groups of four
-    constexpr int KG = kThreads / CG;         // key groups: 8 at d = 128, 16 at d = 64
-    constexpr int KPT = kTileKeys / KG;       // keys of a tile per thread in (3)
-    constexpr int KV_BYTES = kTileKeys * D * 2;
-    constexpr int kStages = decode_stages<D>();
-    extern __shared__ __align__(128) uint8_t dsm[];
-    uint8_t* sK = dsm;                                   // [kStages][T][D] bf16
-    uint8_t* sV = dsm + kStages * KV_BYTES;              // [kStages][T][D] bf16
-    __shared__ __align__(16) float q_s[kMaxRows][D];     // q * scale * log2(e)
-    __shared__ __align__(16) float p_s[kMaxRows][kTileKeys];
-    __shared__ float alpha_s[kMaxRows], l_s[kMaxRows], m_s[kMaxRows];
-    __shared__ uint64_t bar_full[kStages], bar_empty[kStages];
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+    constexpr int S = decode_stages<D>();
+    constexpr int TB = decode_tile_bytes<D>();
+    constexpr int kChunkBytes = 128 * 128;        // 64 columns x 128 rows, one SW128 chunk
+    constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+    extern __shared__ uint8_t dsm_raw[];
+    uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = dsm;                            // 128 x D, rows >= kQRows zero
+    uint8_t* sK = dsm + 128 * D * 2;              // [S] tiles
+    uint8_t* sV = sK + S * TB;                    // [S] tiles
+    __shared__ uint64_t bar_q, bar_k[S], bar_k_empty[S], bar_v[S], bar_v_empty[S];
+    // S_t, P_t and P_t V_t signal barrier t & 1 (completion k of barrier b
+    // is tile b + 2k): a waiter for tile t never finds tile t + 2 complete
+    __shared__ uint64_t bar_s[2], bar_p[2], bar_pv[2];
+    __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     const WaitCtx wc{p.status, &abort_sh};
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
     const int split = blockIdx.x % p.n_split;
-    const int bg = blockIdx.x / p.n_split;                  // b * Hkv + g
+    const int bg = blockIdx.x / p.n_split;        // b * Hkv + g
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int j_begin = split * p.keys_per_split;
     const int j_end = min(p.Nk, j_begin + p.keys_per_split);
-    const int n_tiles = (j_end - j_begin + kTileKeys - 1) / kTileKeys;
-    const int R = p.R;
-    const __nv_bfloat16* kh = p.k + (size_t)bg * p.Nk * D;
-    const __nv_bfloat16* vh = p.v + (size_t)bg * p.Nk * D;
+    const int n_tiles = (j_end - j_begin + kTileKeys - 1) / kTileKeys;   // >= 1 by the plan
 
-    if (tid == 0) {
+    // The Q tile's rows past the loaded ones are MMA rows whose results nobody
+    // reads; they are zeroed so that they hold plain numbers.
+    for (int e = threadIdx.x; e < 128 * D * 2 / 16; e += kThreads)
+        reinterpret_cast<uint4*>(sQ)[e] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    if (threadIdx.x == 0) {
         abort_sh = 0;
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bar_full[s], 1);
-            mbar_init(&bar_empty[s], kThreads);
+        mbar_init(&bar_q, 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&bar_k[s], 1);
+            mbar_init(&bar_k_empty[s], 1);
+            mbar_init(&bar_v[s], 1);
+            mbar_init(&bar_v_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bar_s[t], 1);
+            mbar_init(&bar_p[t], 32);
+            mbar_init(&bar_pv[t], 1);
         }
         fence_mbar_init();
     }
-    // q rows of the group: row r = hl * Nq + qi reads head g * G + hl.
-    for (int e = tid; e < R * D; e += kThreads + 32) {
-        const int r = e / D, c = e % D;
-        const int hl = r / p.Nq, qi = r % p.Nq;
-        const size_t src = (((size_t)b * p.H + g * p.G + hl) * p.Nq + qi) * D + c;
-        q_s[r][c] = __bfloat162float(p.q[src]) * p.scale_log2;
+    if (warp == 2) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
 
-    if (warp == kThreads / 32) {
-        // ------------------------------------------------------ producer
-        // K and V tiles are contiguous rows: one bulk copy each per tile.
+    if (warp == 1) {
+        // -------------------------------------------------------- producer
         if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(&bar_q, kQRows * 128 * (D / 64));
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_3d(sQ + c * kChunkBytes, &tm_q, &bar_q, c * 64, bg * p.R, 0);
             int issued = 0;
             for (int t = 0; t < n_tiles; ++t, ++issued) {
-                const int s = t % kStages;
-                if (t >= kStages && !fa_wait(&bar_empty[s], ((t / kStages) - 1) & 1, 80, wc)) break;
+                const int s = t % S;
                 const int j0 = j_begin + t * kTileKeys;
-                const uint32_t bytes = (uint32_t)min(kTileKeys, j_end - j0) * D * 2;
-                mbar_arrive_expect_tx(&bar_full[s], 2 * bytes);
-                bulk_load(sK + s * KV_BYTES, kh + (size_t)j0 * D, bytes, &bar_full[s]);
-                bulk_load(sV + s * KV_BYTES, vh + (size_t)j0 * D, bytes, &bar_full[s]);
+                if (t >= S && !fa_wait(&bar_k_empty[s], ((t / S) - 1) & 1, 80, wc)) break;
+                mbar_arrive_expect_tx(&bar_k[s], TB);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(sK + s * TB + c * kChunkBytes, &tm_k, &bar_k[s], c * 64, j0, bg);
+                if (t >= S && !fa_wait(&bar_v_empty[s], ((t / S) - 1) & 1, 81, wc)) break;
+                mbar_arrive_expect_tx(&bar_v[s], TB);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(sV + s * TB + c * kChunkBytes, &tm_v, &bar_v[s], c * 64, j0, bg);
             }
-            if (abort_sh) {   // copies still in flight (bounded)
+            if (abort_sh) {   // drain the copies still in flight (bounded)
                 const WaitCtx dc{p.status, nullptr};
-                for (int t = max(0, issued - kStages); t < issued; ++t)
-                    fa_wait(&bar_full[t % kStages], (t / kStages) & 1, 81, dc);
+                fa_wait(&bar_q, 0, 82, dc);
+                for (int t = max(0, issued - S); t < issued; ++t) {
+                    fa_wait(&bar_k[t % S], (t / S) & 1, 82, dc);
+                    fa_wait(&bar_v[t % S], (t / S) & 1, 82, dc);
+                }
             }
         }
         __syncwarp();
-        return;   // the compute threads use named barrier 1 below, not __syncthreads
-    }
-
-    // ---------------------------------------------------------- compute
-    float q_reg[RP][EPL];                     // this lane's slice of every q row
+    } else if (warp == 2) {
+        // ---------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, kTileKeys, false, false);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+            const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
+            const uint64_t qd = sdesc_sw128(sq, 16, 1024);
+            bool ok = fa_wait(&bar_q, 0, 83, wc);
+            tc_fence_after();
+            auto pv = [&](int u) -> bool {   // O += P_u V_u
+                const int s = u % S;
+                if (!fa_wait(&bar_p[u & 1], (u >> 1) & 1, 84, wc) ||
+                    !fa_wait(&bar_v[s], (u / S) & 1, 85, wc))
+                    return false;
+                tc_fence_after();
+                const uint32_t col_p = (u & 1) ? kColS1 : kColS0;
+                const uint64_t vd = sdesc_sw128(sv + s * TB, kChunkBytes, 1024);
 #pragma unroll
-    for (int r = 0; r < RP; ++r)
+                for (int kk = 0; kk < kTileKeys / 16; ++kk)
+                    mma_ts(tmem + kColO, tmem + col_p + kk * 8, vd + mnmajor_step(kk), idesc_o,
+                           (u > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bar_pv[u & 1]);
+                mma_commit(&bar_v_empty[s]);
+                return true;
+            };
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                const int s = t % S;
+                if (!fa_wait(&bar_k[s], (t / S) & 1, 86, wc)) { ok = false; break; }
+                tc_fence_after();
+                // S_t over P_{t-2}: in issue order after P_{t-2} V, which read it
+                const uint32_t col_s = (t & 1) ? kColS1 : kColS0;
+                const uint64_t kd = sdesc_sw128(sk + s * TB, 16, 1024);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) q_reg[r][e] = (r < R) ? q_s[r][lane * EPL + e] : 0.0f;
-    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.0f, 0.0f};
-    const int cg = tid % CG, kg = tid / CG;
-    float acc[RP][4];
-#pragma unroll
-    for (int r = 0; r < RP; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.0f;
-    const int shift = p.Nk - p.Nq;            // query row qi sees keys j <= qi + shift
-    bool ok = true;
-
-    for (int t = 0; ok && t < n_tiles; ++t) {
-        const int s = t % kStages;
-        // every compute thread waits (bounded); all of them stop if any gave up
-        const bool got = fa_wait(&bar_full[s], (t / kStages) & 1, 82, wc);
-        if (named_bar_or(1, kThreads, !got)) { ok = false; break; }
-        const int t0 = j_begin + t * kTileKeys;
-        const int nk = min(kTileKeys, j_end - t0);
-        const uint8_t* kt = sK + s * KV_BYTES;
-        const uint8_t* vt = sV + s * KV_BYTES;
-        // (1) scores: warp w takes keys w, w + 8, ...; lane l holds head-dim
-        // elements [EPL l, EPL l + EPL) of K (one conflict-free shared-memory
-        // read per key) and of the RP q rows (registers); the RP partial dot
-        // products are summed over the 32 lanes by a reduce-scatter butterfly
-        // (RP - 1 + 5 - log2 RP shuffles per key), after which lanes with
-        // l % (32 / RP) == 0 hold the score of row l / (32 / RP).
-#pragma unroll
-        for (int key = warp; key < kTileKeys; key += kThreads / 32) {
-            float vals[RP];
-            if (key < nk) {
-                float kf[EPL];
-                if (EPL == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(kt + (size_t)key * D * 2 + lane * 8);
-                    kf[0] = __uint_as_float(w.x << 16);
-                    kf[1] = __uint_as_float(w.x & 0xffff0000u);
-                    kf[EPL > 2 ? 2 : 0] = __uint_as_float(w.y << 16);
-                    kf[EPL > 2 ? 3 : 1] = __uint_as_float(w.y & 0xffff0000u);
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + (size_t)key * D * 2 + lane * 4);
-                    kf[0] = __uint_as_float(w << 16);
-                    kf[1] = __uint_as_float(w & 0xffff0000u);
-                }
-#pragma unroll
-                for (int r = 0; r < RP; ++r) {
-                    float a = 0.0f;
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) a = fmaf(q_reg[r][e], kf[e], a);
-                    vals[r] = a;
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < RP; ++r) vals[r] = 0.0f;
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + col_s, qd + kmajor_step(kk, kChunkBytes),
+                           kd + kmajor_step(kk, kChunkBytes), idesc_s, kk > 0);
+                mma_commit(&bar_s[t & 1]);
+                mma_commit(&bar_k_empty[s]);
+                if (t > 0 && !pv(t - 1)) { ok = false; break; }
             }
-            // reduce-scatter: at each step a lane keeps half of its rows and
-            // adds the partner's copy of them
-#pragma unroll
-            for (int cnt = RP, o = 16; cnt > 1; cnt >>= 1, o >>= 1) {
-                const bool upper = (lane & o) != 0;
-#pragma unroll
-                for (int i2 = 0; i2 < cnt / 2; ++i2) {
-                    const float send = upper ? vals[i2] : vals[i2 + cnt / 2];
-                    const float keep = upper ? vals[i2 + cnt / 2] : vals[i2];
-                    vals[i2] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
-            }
-#pragma unroll
-            for (int o = 16 / RP; o > 0; o >>= 1) vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], o);
-            const int span = 32 / RP;
-            if ((lane % span) == 0) {
-                const int r = lane / span;
-                if (r < R) {
-                    const int j = t0 + key;
-                    const bool vis = key < nk && (!p.causal || j <= r % p.Nq + shift);
-                    p_s[r][key] = vis ? vals[0] : -CUDART_INF_F;
-                }
+            if (ok) ok = pv(n_tiles - 1);
+            if (!ok) {   // no MMA of this thread may still write TMEM at teardown
+                __shared__ uint64_t bar_drain;
+                mbar_init(&bar_drain, 1);
+                fence_mbar_init();
+                mma_commit(&bar_drain);
+                fa_wait(&bar_drain, 0, 87, WaitCtx{p.status, nullptr});
             }
         }
-        named_bar_sync(1, kThreads);
-        // (2) one warp per row: tile max, running max and sum, p in place
+        __syncwarp();
+    } else {
+        // ------------------------------------------- softmax (rows = lanes)
+        const int r = lane;                       // query row of the group
+        const bool row_ok = r < p.R;
+        const int last_vis = p.causal ? (r % p.Nq) + (p.Nk - p.Nq) : p.Nk - 1;
+        const float c = p.scale_log2;
+        float m2 = -CUDART_INF_F, l = 0.0f;
+        bool ok = true;
+        for (int t = 0; t < n_tiles; ++t) {
+            if (!fa_wait_warp(&bar_s[t & 1], (t >> 1) & 1, 88, wc)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t col_s = (t & 1) ? kColS1 : kColS0;
+            uint32_t sr[4][32];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = warp + 8 * i;
-            if (r < R) {
-                float sv[kTileKeys / 32];
-                float mx = -CUDART_INF_F;
+            for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(tmem + col_s + q4 * 32, sr[q4]);
+            tmem_ld_wait(sr[0]);
 #pragma unroll
-                for (int e = 0; e < kTileKeys / 32; ++e) {
-                    sv[e] = p_s[r][lane + 32 * e];
-                    mx = fmaxf(mx, sv[e]);
-                }
+            for (int q4 = 1; q4 < 4; ++q4) asm volatile("" : FA_R32(sr[q4]) : : "memory");
+            // visible keys of the tile for this row: j0 + e <= lim
+            const int j0 = j_begin + t * kTileKeys;
+            const int lim = min(last_vis, j_end - 1) - j0;   // keep e <= lim
+            float x[kTileKeys];
+            float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1)
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float m_new = fmaxf(m_run[i], mx);
-                // no visible key so far: keep everything at zero
-                const float alpha = (m_new == -CUDART_INF_F) ? 1.0f : exp2f(m_run[i] - m_new);
-                float sum = 0.0f;
-#pragma unroll
-                for (int e = 0; e < kTileKeys / 32; ++e) {
-                    const float pe = (m_new == -CUDART_INF_F) ? 0.0f : exp2f(sv[e] - m_new);
-                    p_s[r][lane + 32 * e] = pe;
-                    sum += pe;
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                l_run[i] = l_run[i] * alpha + sum;
-                m_run[i] = m_new;
-                if (lane == 0) alpha_s[r] = alpha;
+            for (int e = 0; e < kTileKeys; ++e) {
+                x[e] = (e <= lim) ? __uint_as_float(sr[e >> 5][e & 31]) * c : -CUDART_INF_F;
+                mx = fmaxf(mx, x[e]);
             }
-        }
-        named_bar_sync(1, kThreads);
-        // (3) O rows += p V over this thread's keys of the tile (rows of V in
-        // shared memory, a warp reading one contiguous row segment)
+            const bool need = row_ok && mx > m2 + kRescale;
+            float alpha = 1.0f;
+            if (__any_sync(0xffffffffu, need)) {
+                const float m_new = need ? mx : m2;
+                alpha = (m_new == m2) ? 1.0f : ex2(m2 - m_new);
+                m2 = m_new;
+                // O holds P V of the earlier tiles: rescale it once the last
+                // of those P V MMAs (and so every earlier one) has completed
+                if (t > 0) {
+                    if (!fa_wait_warp(&bar_pv[(t - 1) & 1], ((t - 1) >> 1) & 1, 89, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll
-        for (int r = 0; r < RP; ++r) {
-            if (r < R) {
-                const float a = alpha_s[r];
-                acc[r][0] *= a;
-                acc[r][1] *= a;
-                acc[r][2] *= a;
-                acc[r][3] *= a;
-            }
-        }
-#pragma unroll 4
-        for (int i = 0; i < KPT; ++i) {
-            const int jj = kg + KG * i;
-            if (jj < nk) {
-                const uint2 w = *reinterpret_cast<const uint2*>(vt + (size_t)jj * D * 2 + cg * 8);
-                const float v0 = __uint_as_float(w.x << 16), v1 = __uint_as_float(w.x & 0xffff0000u);
-                const float v2 = __uint_as_float(w.y << 16), v3 = __uint_as_float(w.y & 0xffff0000u);
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32(tmem + kColO + c0, ov);
+                        tmem_ld_wait(ov);
 #pragma unroll
-                for (int r = 0; r < RP; ++r) {
-                    if (r < R) {
-                        const float pe = p_s[r][jj];
-                        acc[r][0] = fmaf(pe, v0, acc[r][0]);
-                        acc[r][1] = fmaf(pe, v1, acc[r][1]);
-                        acc[r][2] = fmaf(pe, v2, acc[r][2]);
-                        acc[r][3] = fmaf(pe, v3, acc[r][3]);
+                        for (int e = 0; e < 32; ++e)
+                            ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                        tmem_st32(tmem + kColO + c0, ov);
                     }
                 }
+                l *= alpha;
             }
-        }
-        mbar_arrive(&bar_empty[s]);           // K and V of this stage are no longer read
-        named_bar_sync(1, kThreads);          // p_s and alpha_s are rewritten next tile
-    }
-    if (!ok) return;
-
-    // split outputs: O_s = o / l, LSE_s = ln2 (m + log2 l); -inf and zeros
-    // when no key of the split is visible to the row.  The key groups' partial
-    // sums meet in shared memory (p_s is free now), one row at a time.
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int r = warp + 8 * i;
-        if (r < R && lane == 0) {
-            l_s[r] = l_run[i];
-            m_s[r] = m_run[i];
-        }
-    }
-    float* red = &p_s[0][0];                  // [KG][D] floats: KG * D <= 16 * T
-#pragma unroll
-    for (int r = 0; r < RP; ++r) {
-        if (r >= R) break;                    // uniform across the compute threads
-        named_bar_sync(1, kThreads);
-        *reinterpret_cast<float4*>(red + kg * D + 4 * cg) =
-            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-        named_bar_sync(1, kThreads);
-        if (tid < D) {
+            const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
+            uint32_t pk[2][32];
             float sum = 0.0f;
 #pragma unroll
-            for (int k2 = 0; k2 < KG; ++k2) sum += red[k2 * D + tid];
-            const int hl = r / p.Nq, qi = r % p.Nq;
-            const size_t row = ((size_t)b * p.H + g * p.G + hl) * p.Nq + qi;
-            const float l = l_s[r];
-            p.o_part[(row * p.n_split + split) * D + tid] = (l > 0.0f) ? sum / l : 0.0f;
-            if (tid == 0)
-                p.lse_part[row * p.n_split + split] =
-                    (l > 0.0f) ? (m_s[r] + log2f(l)) * kLn2 : -CUDART_INF_F;
+            for (int e2 = 0; e2 < kTileKeys / 2; ++e2) {
+                const float p0 = ex2(x[2 * e2] - m_use), p1 = ex2(x[2 * e2 + 1] - m_use);
+                sum += p0 + p1;
+                pk[e2 >> 5][e2 & 31] = pack_bf16x2(p0, p1);
+            }
+            l += sum;
+            tmem_st32(tmem + col_s, pk[0]);
+            tmem_st32(tmem + col_s + 32, pk[1]);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bar_p[t & 1]);
         }
+        if (ok && fa_wait_warp(&bar_pv[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, 90, wc)) {
+            tc_fence_after();
+            // split outputs: O_s = o / l, LSE_s = ln2 (m + log2 l); zeros and
+            // -inf when no key of the split is visible to the row
+            const int hl = r / max(p.Nq, 1), qi = r % max(p.Nq, 1);
+            const size_t row = ((size_t)b * p.H + g * p.G + hl) * p.Nq + qi;
+            const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tmem_ld32(tmem + kColO + c0, ov);
+                tmem_ld_wait(ov);
+                if (row_ok) {
+                    float4* dst = reinterpret_cast<float4*>(
+                        p.o_part + (row * p.n_split + split) * D + c0);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        dst[q4] = make_float4(__uint_as_float(ov[4 * q4]) * inv,
+                                              __uint_as_float(ov[4 * q4 + 1]) * inv,
+                                              __uint_as_float(ov[4 * q4 + 2]) * inv,
+                                              __uint_as_float(ov[4 * q4 + 3]) * inv);
+                }
+            }
+            if (row_ok)
+                p.lse_part[row * p.n_split + split] =
+                    (l > 0.0f) ? (m2 + log2f(l)) * kLn2 : -CUDART_INF_F;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -351,14 +346,14 @@ fa_decode_combine_kernel(const float* __restrict__ o_part, const float* __restri
 
 }  // namespace
 
-// Split policy: with its 96 KB K/V ring the split kernel fits two CTAs per SM
-// for up to 8 rows per kv group (one for 16, by registers), so the number of
-// CTAs, B * Hkv * n_split, is chosen for the fullest waves of that many
-// slots on a 152-SM part among n_split in [ceil(slots / (B Hkv)),
-// 4 ceil(slots / (B Hkv))], each split a whole number of 64-key tiles.  The
-// target is fixed, so the workspace size does not depend on the device.
+// Split policy: one CTA per SM (the K/V ring fills shared memory), so the
+// number of CTAs, B * Hkv * n_split, is chosen for the fullest waves of 152
+// among n_split in [ceil(152 / (B Hkv)), 4 ceil(152 / (B Hkv))], each split a
+// whole number of 128-key tiles.  The target is fixed, so the workspace size
+// does not depend on the device.
 void decode_split_plan(int B, int Hkv, int R, int Nk, int* n_split, int* keys_per_split) {
-    const int kSms = R <= 8 ? 2 * 152 : 152;
+    (void)R;
+    const int kSms = 152;
     const int tiles = (Nk + kTileKeys - 1) / kTileKeys;
     const long long groups = (long long)B * Hkv;
     int lo = (int)((kSms + groups - 1) / groups);
@@ -391,9 +386,10 @@ size_t decode_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d) {
     return o_bytes + rows * ns * 4;
 }
 
-template <int D, int RP>
-static cudaError_t launch_split(const DecodeParams& p, long long blocks, cudaStream_t stream) {
-    auto kern = fa_decode_split_kernel<D, RP>;
+template <int D>
+static cudaError_t launch_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const DecodeParams& p, long long blocks, cudaStream_t stream) {
+    auto kern = fa_decode_split_kernel<D>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -403,7 +399,7 @@ static cudaError_t launch_split(const DecodeParams& p, long long blocks, cudaStr
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    kern<<<(unsigned)blocks, kThreads + 32, decode_smem_bytes<D>(), stream>>>(p);
+    kern<<<(unsigned)blocks, kThreads, decode_smem_bytes<D>(), stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -415,9 +411,14 @@ cudaError_t launch_fwd_decode(const void* q, const void* k, const void* v, void*
     int ns, kps;
     decode_split_plan(B, Hkv, (H / Hkv) * Nq, Nk, &ns, &kps);
     const size_t rows = (size_t)B * H * Nq;
-    p.q = static_cast<const __nv_bfloat16*>(q);
-    p.k = static_cast<const __nv_bfloat16*>(k);
-    p.v = static_cast<const __nv_bfloat16*>(v);
+    // q as one column of rows: the group (b, g) is rows (b Hkv + g) R ...
+    // (heads of a group are adjacent); 16 rows are loaded, rows past R are
+    // never read back.  K and V: {d, Nk, B Hkv}, 128-key tiles.
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_bf16_3d(&tq, q, d, (int)rows, 1, kQRows) ||
+        !make_tmap_bf16_3d(&tk, k, d, Nk, B * Hkv, kTileKeys) ||
+        !make_tmap_bf16_3d(&tv, v, d, Nk, B * Hkv, kTileKeys))
+        return cudaErrorInvalidValue;
     p.o_part = static_cast<float*>(workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                           (rows * ns * d * 4 + 255) / 256 * 256);
@@ -435,21 +436,8 @@ cudaError_t launch_fwd_decode(const void* q, const void* k, const void* v, void*
     const long long blocks = (long long)B * Hkv * ns;
     if (blocks > 0x7fffffffLL || rows * 32 / 256 + 1 > 0x7fffffffULL) return cudaErrorInvalidValue;
     count_launch();
-    // rows padded to a power of two: 1, 2, 4, 8 or 16
-    const int R = p.R;
-    cudaError_t e;
-    if (d == 128)
-        e = R <= 1 ? launch_split<128, 1>(p, blocks, stream)
-          : R <= 2 ? launch_split<128, 2>(p, blocks, stream)
-          : R <= 4 ? launch_split<128, 4>(p, blocks, stream)
-          : R <= 8 ? launch_split<128, 8>(p, blocks, stream)
-                   : launch_split<128, 16>(p, blocks, stream);
-    else
-        e = R <= 1 ? launch_split<64, 1>(p, blocks, stream)
-          : R <= 2 ? launch_split<64, 2>(p, blocks, stream)
-          : R <= 4 ? launch_split<64, 4>(p, blocks, stream)
-          : R <= 8 ? launch_split<64, 8>(p, blocks, stream)
-                   : launch_split<64, 16>(p, blocks, stream);
+    cudaError_t e = d == 128 ? launch_split<128>(tq, tk, tv, p, blocks, stream)
+                             : launch_split<64>(tq, tk, tv, p, blocks, stream);
     if (e != cudaSuccess) return e;
     count_launch();
     const unsigned cblocks = (unsigned)((rows * 32 + 255) / 256);
