@@ -50,10 +50,14 @@ struct DecodeParams {
     DeviceStatus* status;
 };
 
-// K/V ring: 3 stages of 64 KB (K and V tiles) at d = 128, 6 of 32 KB at d = 64;
-// with the 16 or 32 KB Q tile one CTA fills an SM's shared memory.
+// d = 128: a K/V ring of 3 stages of 64 KB (K and V tiles) and two S buffers
+// in TMEM (512 columns with O): one CTA fills an SM.  d = 64: 2 stages of
+// 32 KB and one S buffer (256 columns), so that two CTAs share an SM and
+// each one's MMA and softmax chain hides behind the other's loads.
 template <int D>
-__host__ __device__ constexpr int decode_stages() { return D == 128 ? 3 : 6; }
+__host__ __device__ constexpr int decode_stages() { return D == 128 ? 3 : 2; }
+template <int D>
+__host__ __device__ constexpr int decode_ctas_per_sm() { return D == 128 ? 1 : 2; }
 template <int D>
 __host__ __device__ constexpr int decode_tile_bytes() { return kTileKeys * D * 2; }
 template <int D>
@@ -68,7 +72,9 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     constexpr int S = decode_stages<D>();
     constexpr int TB = decode_tile_bytes<D>();
     constexpr int kChunkBytes = 128 * 128;        // 64 columns x 128 rows, one SW128 chunk
-    constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+    constexpr bool kTwoS = (D == 128);            // two S buffers (else S_t+1 after P_t V)
+    constexpr uint32_t kColS0 = 0, kColS1 = kTwoS ? 128 : 0, kColO = kTwoS ? 256 : 128;
+    constexpr uint32_t kTmemCols = kTwoS ? 512 : 256;
     extern __shared__ uint8_t dsm_raw[];
     uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -113,7 +119,7 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         fence_mbar_init();
     }
     if (warp == 2) {
-        tmem_alloc(&tmem_base_sh, 512);
+        tmem_alloc(&tmem_base_sh, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -181,7 +187,8 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 const int s = t % S;
                 if (!fa_wait(&bar_k[s], (t / S) & 1, 86, wc)) { ok = false; break; }
                 tc_fence_after();
-                // S_t over P_{t-2}: in issue order after P_{t-2} V, which read it
+                // S_t over P_{t-2} (P_{t-1} with one buffer): in issue order
+                // after the P V MMA that read it
                 const uint32_t col_s = (t & 1) ? kColS1 : kColS0;
                 const uint64_t kd = sdesc_sw128(sk + s * TB, 16, 1024);
 #pragma unroll
@@ -190,9 +197,14 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                            kd + kmajor_step(kk, kChunkBytes), idesc_s, kk > 0);
                 mma_commit(&bar_s[t & 1]);
                 mma_commit(&bar_k_empty[s]);
-                if (t > 0 && !pv(t - 1)) { ok = false; break; }
+                if (kTwoS) {
+                    if (t > 0 && !pv(t - 1)) { ok = false; break; }
+                } else if (!pv(t)) {   // one S buffer: P_t V before S_t+1 overwrites P_t
+                    ok = false;
+                    break;
+                }
             }
-            if (ok) ok = pv(n_tiles - 1);
+            if (kTwoS && ok) ok = pv(n_tiles - 1);
             if (!ok) {   // no MMA of this thread may still write TMEM at teardown
                 __shared__ uint64_t bar_drain;
                 mbar_init(&bar_drain, 1);
@@ -305,7 +317,7 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     __syncthreads();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -346,14 +358,13 @@ fa_decode_combine_kernel(const float* __restrict__ o_part, const float* __restri
 
 }  // namespace
 
-// Split policy: one CTA per SM (the K/V ring fills shared memory), so the
-// number of CTAs, B * Hkv * n_split, is chosen for the fullest waves of 152
-// among n_split in [ceil(152 / (B Hkv)), 4 ceil(152 / (B Hkv))], each split a
+// Split policy: the number of CTAs, B * Hkv * n_split, is chosen for the
+// fullest waves of 152 x (CTAs per SM: 1 at d = 128, 2 at d = 64) among
+// n_split in [ceil(slots / (B Hkv)), 4 ceil(slots / (B Hkv))], each split a
 // whole number of 128-key tiles.  The target is fixed, so the workspace size
 // does not depend on the device.
-void decode_split_plan(int B, int Hkv, int R, int Nk, int* n_split, int* keys_per_split) {
-    (void)R;
-    const int kSms = 152;
+void decode_split_plan(int B, int Hkv, int Nk, int d, int* n_split, int* keys_per_split) {
+    const int kSms = 152 * (d == 128 ? decode_ctas_per_sm<128>() : decode_ctas_per_sm<64>());
     const int tiles = (Nk + kTileKeys - 1) / kTileKeys;
     const long long groups = (long long)B * Hkv;
     int lo = (int)((kSms + groups - 1) / groups);
@@ -380,7 +391,7 @@ void decode_split_plan(int B, int Hkv, int R, int Nk, int* n_split, int* keys_pe
 
 size_t decode_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d) {
     int ns, kps;
-    decode_split_plan(B, Hkv, (H / Hkv) * Nq, Nk, &ns, &kps);
+    decode_split_plan(B, Hkv, Nk, d, &ns, &kps);
     const size_t rows = (size_t)B * H * Nq;
     const size_t o_bytes = (rows * ns * d * 4 + 255) / 256 * 256;
     return o_bytes + rows * ns * 4;
@@ -409,7 +420,7 @@ cudaError_t launch_fwd_decode(const void* q, const void* k, const void* v, void*
                               cudaStream_t stream) {
     DecodeParams p;
     int ns, kps;
-    decode_split_plan(B, Hkv, (H / Hkv) * Nq, Nk, &ns, &kps);
+    decode_split_plan(B, Hkv, Nk, d, &ns, &kps);
     const size_t rows = (size_t)B * H * Nq;
     // q as one column of rows: the group (b, g) is rows (b Hkv + g) R ...
     // (heads of a group are adjacent); 16 rows are loaded, rows past R are

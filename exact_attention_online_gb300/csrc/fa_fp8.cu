@@ -69,6 +69,14 @@ struct Tile {
     int n_kv[kTiles];
 };
 
+// Item of this CTA in round rd: the cost-ranked items are dealt in rounds of
+// gridDim.x with the order of the CTAs reversed every other round, which
+// evens out the causal costs per CTA (as in the bf16 forward).
+__device__ __forceinline__ int snake_item(int rd) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return rd * G + ((rd & 1) ? G - 1 - c : c);
+}
+
 __device__ __forceinline__ Tile fp8_tile(int item, const Fp8Params& p, bool causal) {
     Tile w;
     const int mb_rank = item / p.BH;
@@ -146,7 +154,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         uint32_t cs = 0;
         bool ok = true;
         int lt = 0;
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+        for (int rd = 0, item = snake_item(0); ok && item < p.n_items;
+             item = snake_item(++rd), ++lt) {
             const Tile wt = fp8_tile(item, p, CAUSAL);
             const int row0 = wt.row_base + t * kBM;
             const int row = row0 + rl;
@@ -283,7 +292,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_prefetch_desc(&tm_k);
             uint32_t g = 0;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            for (int rd = 0, item = snake_item(0); ok && item < p.n_items;
+                 item = snake_item(++rd)) {
                 const Tile wt = fp8_tile(item, p, CAUSAL);
                 for (int j = 0; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
                     const int s = g % SK;
@@ -307,7 +317,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             uint32_t g = 0;
             int lt = 0, q_loaded = -1;
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+            for (int rd = 0, item = snake_item(0); ok && item < p.n_items;
+                 item = snake_item(++rd), ++lt) {
                 const Tile wt = fp8_tile(item, p, CAUSAL);
                 for (int t = 0; t < kTiles; ++t) {
                     if (lt > 0 && !fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc)) { ok = false; break; }
@@ -361,7 +372,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (last) mma_commit(&bar_o[T]);
                 return true;
             };
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+            for (int rd = 0, item = snake_item(0); ok && item < p.n_items;
+                 item = snake_item(++rd), ++lt) {
                 const Tile wt = fp8_tile(item, p, CAUSAL);
                 const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];
                 for (int j = 0; j < n1; ++j) {
@@ -412,7 +424,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 mma_commit(&bar_s[T]);
                 return true;
             };
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++lt) {
+            for (int rd = 0, item = snake_item(0); ok && item < p.n_items;
+                 item = snake_item(++rd), ++lt) {
                 const Tile wt = fp8_tile(item, p, CAUSAL);
                 const int n0 = wt.n_kv[0], n1 = wt.n_kv[1];
                 if (!fa_wait(&bar_q[0], lt & 1, 20, wc) || !fa_wait(&bar_q[1], lt & 1, 20, wc)) {

@@ -111,7 +111,7 @@ cudaError_t launch_fwd_fp8(const Shape& s, const Fp8Buffer& buf, void* o, float*
 // Split-KV decoding forward (fa_decode.cu).  Workspace: fp32 partial outputs
 // [B][H][Nq][n_split][d] (256-byte aligned end), then fp32 partial LSEs
 // [B][H][Nq][n_split]; n_split from decode_split_plan().
-void decode_split_plan(int B, int Hkv, int R, int Nk, int* n_split, int* keys_per_split);
+void decode_split_plan(int B, int Hkv, int Nk, int d, int* n_split, int* keys_per_split);
 size_t decode_workspace_bytes(int B, int H, int Hkv, int Nq, int Nk, int d);
 cudaError_t launch_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                               void* workspace, int B, int H, int Hkv, int Nq, int Nk, int d,
