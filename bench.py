@@ -52,8 +52,10 @@ NCU_TRAFFIC = {
     ("fa_bwd_dkdv", "window"): {"bytes": 2034.00e6, "src_sha": "2295e403134c24cc"},
     # the same file: 205.7 MB read + 97.9 MB written
     ("fa_fwd", "window"): {"bytes": 303.62e6, "src_sha": "d1d60eb3316b9335"},
-    # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 5.1 MB written, one launch
-    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0790e9, "src_sha": "6f9c75dfde0d8a68"},
+    # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 4.3 MB written, one launch
+    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0782e9, "src_sha": "737ec0dc1b9c060c"},
+    # profiles/fa_fwd_fp8_long16k.md: 165.5 MB read + 35.8 MB written, one launch
+    ("fa_fwd_fp8", "long16k"): {"bytes": 201.27e6, "src_sha": "89e534af2f8dc9c0"},
 }
 
 
@@ -622,8 +624,10 @@ def run_native_fp8(args, w):
     with_quant = flops_step / ((fwd_ms + q_ms) * 1e-3) / 1e12
     # e4m3 dense peak: the measured bf16 figure times the nominal fp8/bf16 ratio (2).
     peak = 2.0 * peaks["bf16_tflops_sustained"]
+    tr = NCU_TRAFFIC.get(("fa_fwd_fp8", w.name))
+    fp8_traffic = tr["bytes"] if tr and tr["src_sha"] == kernel_source_hash("fa_fp8.cu") else None
     roofline = {"bound": "tensor", "kernel": "fa_fwd_fp8", "achieved": value / ws, "peak": peak,
-                "unit": "TFLOP/s", "frac": value / ws / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": value / ws / peak, "traffic": fp8_traffic,
                 "peak_kind": f"2 x bf16_tflops_sustained ({peaks['source']}), nominal fp8:bf16 ratio"}
     e2e = None
     if not args.no_e2e:
