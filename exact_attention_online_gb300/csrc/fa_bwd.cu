@@ -46,10 +46,11 @@ constexpr int kMma2Warp = 10;    // dK, dQ and dP^T MMAs
 constexpr int kReadoutWarp0 = 12;
 constexpr int kReadoutThreads = 128;
 // Register split (setmaxnreg) of the 512 x 128 launch registers:
-// 256 x 160 + 128 x 96 + 128 x 96 = 65536.
-constexpr int kRegsCompute = 160;
+// 256 x 152 + 128 x 96 + 128 x 112 = 65536.  With 112 for the control warps
+// (producer, MMA issuers) no role spills; 96 left the MMA issuers spilling.
+constexpr int kRegsCompute = 152;
 constexpr int kRegsReadout = 96;
-constexpr int kRegsControl = 96;
+constexpr int kRegsControl = 112;
 constexpr int kRegsNeeded = 256 * kRegsCompute + 128 * kRegsReadout + 128 * kRegsControl;
 
 template <int D>
