@@ -40,8 +40,10 @@ constexpr int kProducerWarp = 8;    // K tiles
 constexpr int kMmaWarp = 9;         // S MMA issuer; allocates TMEM
 constexpr int kVProducerWarp = 10;  // V and Q tiles
 constexpr int kPvWarp = 11;         // P V MMA issuer
-constexpr int kRegsControl = 88;
-constexpr int kRegsSoftmax = 208;
+// 128 x 72 + 256 x 216 = 64512 = 384 x 168: no role spills (the softmax
+// warps did at 208).
+constexpr int kRegsControl = 72;
+constexpr int kRegsSoftmax = 216;
 constexpr int kRegsNeeded = 128 * kRegsControl + 256 * kRegsSoftmax;
 constexpr int kStagesK = 4, kStagesV = 3;
 constexpr int kTileBytes = 128 * 128;             // every tile: 128 rows x 128 bytes
