@@ -45,18 +45,18 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel source it was taken on.  A source change makes the figure stale and
 # it is then reported as null.
 NCU_TRAFFIC = {
-    # profiles/fa_bwd_dkdv_mha_d64.md: 239.6 MB read + 107.8 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 347.39e6, "src_sha": "2295e403134c24cc"},
-    # profiles/launches_mha_d64_fwd_bwd.md: 113.8 MB read + 13.3 MB written, one launch
-    ("fa_fwd", "mha_d64"): {"bytes": 127.10e6, "src_sha": "d1d60eb3316b9335"},
-    # profiles/fa_window_fwd_bwd_window.md: 1388.2 MB read + 645.8 MB written
-    ("fa_bwd_dkdv", "window"): {"bytes": 2034.00e6, "src_sha": "2295e403134c24cc"},
-    # the same file: 205.7 MB read + 97.9 MB written
-    ("fa_fwd", "window"): {"bytes": 303.62e6, "src_sha": "d1d60eb3316b9335"},
+    # profiles/fa_bwd_dkdv_mha_d64.md: 236.6 MB read + 101.8 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 338.44e6, "src_sha": "a69917941837eba2"},
+    # profiles/launches_mha_d64_fwd_bwd.md: 110.3 MB read + 12.7 MB written, one launch
+    ("fa_fwd", "mha_d64"): {"bytes": 123.07e6, "src_sha": "9edd374358a89cb8"},
+    # profiles/fa_window_fwd_bwd_window.md: 1385.7 MB read + 641.4 MB written
+    ("fa_bwd_dkdv", "window"): {"bytes": 2027.09e6, "src_sha": "a69917941837eba2"},
+    # the same file: 205.0 MB read + 97.9 MB written
+    ("fa_fwd", "window"): {"bytes": 302.90e6, "src_sha": "9edd374358a89cb8"},
     # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 4.3 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0782e9, "src_sha": "737ec0dc1b9c060c"},
-    # profiles/fa_fwd_fp8_long16k.md: 165.5 MB read + 35.8 MB written, one launch
-    ("fa_fwd_fp8", "long16k"): {"bytes": 201.27e6, "src_sha": "89e534af2f8dc9c0"},
+    # profiles/fa_fwd_fp8_long16k.md: 166.0 MB read + 33.8 MB written, one launch
+    ("fa_fwd_fp8", "long16k"): {"bytes": 199.78e6, "src_sha": "9cc4f81f16caefe2"},
 }
 
 
