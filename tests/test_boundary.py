@@ -123,3 +123,68 @@ def test_python_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fa_fwd(q, q, q, q, torch.zeros(1, 1, 8), False, 0.125, stream=0)
+
+
+def test_window_entry_points_validate(L):
+    """window < 1 and the shape rules of fa_fwd / fa_bwd, before any launch."""
+    before = fa.fa_kernel_launches()
+    for w in (0, -3):
+        assert L.fa_fwd_window(A, A, A, A, A, 1, 2, 1, 128, 64, w, 0.125, None) == \
+            fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_window(A, A, A, A, A, 1, 2, 1, 128, 96, 16, 0.125, None) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert L.fa_fwd_window(A, A, A, MIS, A, 1, 2, 1, 128, 64, 16, 0.125, None) == \
+        fa.FA_ERR_ALIGNMENT
+    ws = L.fa_bwd_workspace_size(1, 2, 1, 128, 64)
+    assert L.fa_bwd_window(A, A, A, A, A, A, A, A, A, A, ws, 1, 2, 1, 128, 64, 0, 0.125,
+                           None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_bwd_window(A, A, A, A, A, A, A, A, A, A, 16, 1, 2, 1, 128, 64, 8, 0.125,
+                           None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_bwd_dkdv_window(A, A, A, A, A, A, A, ws, 1, 2, 1, 128, 64, 0, 0.125,
+                                None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_kernel_launches() == before
+
+
+def test_varlen_entry_points_validate(L):
+    """Packed batches: a null offsets array, total < 1, a misaligned offsets
+    pointer and the shape rules, before any launch."""
+    before = fa.fa_kernel_launches()
+    f = lambda cu, B, ms, total, d=64: L.fa_fwd_varlen(A, A, A, A, A, cu, B, ms, total, 2, 1, d,
+                                                       1, 0.125, None)
+    assert f(None, 2, 128, 200) == fa.FA_ERR_INVALID_ARG
+    assert f(A, 2, 128, 0) == fa.FA_ERR_INVALID_ARG
+    assert f(A + 2, 2, 128, 200) == fa.FA_ERR_ALIGNMENT
+    assert f(A, 2, 128, 200, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert f(A, 0, 128, 200) == fa.FA_ERR_INVALID_ARG
+    ws = L.fa_bwd_varlen_workspace_size(2, 2, 1, 128, 64)
+    assert ws == L.fa_bwd_workspace_size(2, 2, 1, 128, 64)
+    assert L.fa_bwd_varlen(A, A, A, A, A, A, A, A, A, A, 16, A, 2, 128, 200, 2, 1, 64, 1, 0.125,
+                           None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_kernel_launches() == before
+
+
+def test_decode_entry_points_validate(L):
+    """Decoding: more query rows than keys, more than 16 rows per kv group, an
+    unsupported head dim and a short workspace, before any launch."""
+    before = fa.fa_kernel_launches()
+    assert L.fa_fwd_decode_workspace_size(1, 4, 1, 8, 4, 64) == 0        # Nq > Nk
+    assert L.fa_fwd_decode_workspace_size(1, 32, 1, 1, 1024, 64) == 0    # G * Nq = 32 > 16
+    assert L.fa_fwd_decode_workspace_size(1, 4, 1, 1, 1024, 96) == 0     # d = 96
+    ws = L.fa_fwd_decode_workspace_size(2, 8, 2, 1, 4096, 128)
+    assert ws > 0
+    d = lambda wsb, Nq=1, Nk=4096: L.fa_fwd_decode(A, A, A, A, A, A, wsb, 2, 8, 2, Nq, Nk, 128, 1,
+                                                   0.088, None)
+    assert d(ws, Nq=8, Nk=4) != fa.FA_OK
+    assert d(16) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_kernel_launches() == before
+
+
+def test_fp8_entry_points_validate(L):
+    """FP8: d = 64 is not supported and a short buffer is rejected."""
+    before = fa.fa_kernel_launches()
+    assert L.fa_fp8_buffer_size(1, 2, 1, 256, 64) == 0
+    n = L.fa_fp8_buffer_size(1, 2, 1, 256, 128)
+    assert n > 0
+    assert L.fa_fp8_quantize(A, A, A, A, 16, 1, 2, 1, 256, 128, None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_fwd_fp8(A, 16, A, A, 1, 2, 1, 256, 128, 1, 0.088, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_kernel_launches() == before
