@@ -45,12 +45,12 @@ L2_BYTES = 129 * 1024 * 1024
 # kernel source it was taken on.  A source change makes the figure stale and
 # it is then reported as null.
 NCU_TRAFFIC = {
-    # profiles/fa_bwd_dkdv_mha_d64.md: 236.6 MB read + 101.8 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 338.44e6, "src_sha": "a69917941837eba2"},
+    # profiles/fa_bwd_dkdv_mha_d64.md: 237.5 MB read + 103.6 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 341.09e6, "src_sha": "e9d1140dc8699988"},
     # profiles/launches_mha_d64_fwd_bwd.md: 110.3 MB read + 12.7 MB written, one launch
     ("fa_fwd", "mha_d64"): {"bytes": 123.07e6, "src_sha": "9edd374358a89cb8"},
-    # profiles/fa_window_fwd_bwd_window.md: 1385.7 MB read + 641.4 MB written
-    ("fa_bwd_dkdv", "window"): {"bytes": 2027.09e6, "src_sha": "a69917941837eba2"},
+    # profiles/fa_window_fwd_bwd_window.md: 1385.7 MB read + 641.3 MB written
+    ("fa_bwd_dkdv", "window"): {"bytes": 2026.96e6, "src_sha": "e9d1140dc8699988"},
     # the same file: 205.0 MB read + 97.9 MB written
     ("fa_fwd", "window"): {"bytes": 302.90e6, "src_sha": "9edd374358a89cb8"},
     # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 4.3 MB written, one launch

@@ -110,7 +110,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
     using Cfg = BwdCfg<D>;
     constexpr int BR = Cfg::kBR;
-    constexpr bool kTwoIssuers = (D == 128);
+    // Two MMA-issuing threads at d = 128 and without the mask (d = 64: +8 %);
+    // one for causal d = 64 (two measured 3 % slower there).
+    constexpr bool kTwoIssuers = (D == 128) || !CAUSAL;
     constexpr int HALF = BR / 2;                  // query columns per compute warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -555,10 +557,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             // completion also tells the compute warps that dS^T may be
             // overwritten).  An MMA issue blocks while the tensor pipe is busy
             // and each barrier wait and commit of an issuing thread costs on
-            // the order of a hundred cycles; at d = 128 the halves go to two
-            // threads (warps kMmaWarp and kMma2Warp) so that one's waits overlap
-            // the other's MMAs.  At d = 64 the halves hardly overlap in time and
-            // one thread issues both, in the order A, B.
+            // the order of a hundred cycles; at d = 128, and at d = 64 without
+            // the mask, the halves go to two threads (warps kMmaWarp and
+            // kMma2Warp) so that one's waits overlap the other's MMAs.  For
+            // causal d = 64 one thread issues both, in the order A, B.
             constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
             constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
             constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
