@@ -543,12 +543,36 @@ def run_native(args, w):
             "fwd_bwd_alg_tflops": None if fwd_only else
             attention_flops(w, "fwd_bwd_alg") * args.steps * ws / (ms_total * 1e-3) / 1e12,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "exp_unit": exp_unit_line(w, kernels, clk.summary()),
             "clocks": clk.summary(), "gpu_launches": launches,
             "launches_per_step": launches / args.steps,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+# The second bound of the forward and backward kernels: one ex2 per score.
+# Its peak is derived from a microbenchmark on GB300 (ex2.approx.ftz.f32 at a
+# quarter of the FFMA rate: 32 lanes a clock per SM) times 152 SMs and the SM
+# clock sampled during the timed region.
+EX2_LANES_PER_CLK_SM = 32
+N_SMS = 152
+
+
+def exp_unit_line(w, kernels, clocks):
+    from exact_attention_online_gb300.measure import visible_pairs
+    mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    peak = EX2_LANES_PER_CLK_SM * N_SMS * mhz * 1e6
+    exps = float(w.B) * w.H * visible_pairs(w.N, w.causal, getattr(w, "window", 0))
+    out = {"exps_per_launch": exps, "peak_per_s": peak,
+           "peak_kind": "32 lanes/clk/SM (microbenchmark) x 152 SMs x sampled SM clock"}
+    for name, (key, mult) in (("fwd", ("fa_fwd", 1.0)), ("dkdv", ("fa_bwd_dkdv", 1.0))):
+        k = kernels.get(key)
+        if k:
+            rate = exps * mult / (k["ms"] * 1e-3)
+            out[name] = {"per_s": rate, "frac": rate / peak}
+    return out
 
 
 def run_native_fp8(args, w):
