@@ -53,6 +53,14 @@ NCU_TRAFFIC = {
     ("fa_bwd_dkdv", "window"): {"bytes": 2026.96e6, "src_sha": "e9d1140dc8699988"},
     # the same file: 205.0 MB read + 97.9 MB written
     ("fa_fwd", "window"): {"bytes": 302.90e6, "src_sha": "9edd374358a89cb8"},
+    # profiles/fa_fwd_bwd_d128_gpt_long_gqa.md: 427.9 MB read + 224.6 MB written
+    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 652.53e6, "src_sha": "e9d1140dc8699988"},
+    # the same file: 534.0 MB read + 46.4 MB written
+    ("fa_fwd", "gpt_long"): {"bytes": 580.44e6, "src_sha": "9edd374358a89cb8"},
+    # the same file: 771.6 MB read + 347.6 MB written
+    ("fa_bwd_dkdv", "gqa"): {"bytes": 1119.17e6, "src_sha": "e9d1140dc8699988"},
+    # the same file: 298.1 MB read + 216.1 MB written (fp32 O, precise path)
+    ("fa_fwd", "gqa"): {"bytes": 514.19e6, "src_sha": "9edd374358a89cb8"},
     # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 4.3 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0782e9, "src_sha": "737ec0dc1b9c060c"},
     # profiles/fa_fwd_fp8_long16k.md: 166.0 MB read + 33.8 MB written, one launch
