@@ -30,7 +30,9 @@ __all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_p
            "fa_kernel_launches", "fa_watchdog_selftest", "attention", "attention_backward",
            "fa_fwd_window", "fa_bwd_window", "fa_bwd_dkdv_window", "attention_window",
            "attention_window_backward", "fa_fwd_varlen", "fa_bwd_varlen",
-           "fa_bwd_varlen_workspace_size", "attention_varlen", "attention_varlen_backward"]
+           "fa_bwd_varlen_workspace_size", "attention_varlen", "attention_varlen_backward",
+           "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8", "attention_fp8",
+           "fa_fwd_decode_workspace_size", "fa_fwd_decode", "attention_decode"]
 
 
 class FAError(RuntimeError):
@@ -55,18 +57,25 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _bf16(t, name):
-    import torch
-    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA bfloat16 tensor")
+def _ptr(t, name, dtype, shape):
+    """Device pointer of t after checking its shape (the C entry points see
+    only pointers, so a short buffer would be read or written past its end),
+    dtype, device and contiguity."""
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {str(dtype)[6:]} tensor")
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _f32(t, name):
+def _bf16(t, name, shape=None):
     import torch
-    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA float32 tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return _ptr(t, name, torch.bfloat16, shape)
+
+
+def _f32(t, name, shape=None):
+    import torch
+    return _ptr(t, name, torch.float32, shape)
 
 
 def _dims(q, k):
@@ -78,34 +87,41 @@ def _dims(q, k):
     return B, H, k.shape[1], N, d
 
 
+def _shapes(B, H, Hkv, N, d):
+    """Shapes of the query-side tensors (q, o, dout, dq), the key-side tensors
+    (k, v, dk, dv) and lse: [B, H, N, d], [B, Hkv, N, d], [B, H, N]."""
+    return (B, H, N, d), (B, Hkv, N, d), (B, H, N)
+
+
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     B, H, Hkv, N, d = _dims(q, k)
-    _check(lib().fa_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
-                        _f32(lse, "lse"), B, H, Hkv, N, d, int(bool(causal)), float(scale),
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
+    _check(lib().fa_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _bf16(o, "o", qs),
+                        _f32(lse, "lse", ls), B, H, Hkv, N, d, int(bool(causal)), float(scale),
                         _stream(stream)), "fa_fwd")
 
 
 def fa_fwd_precise(q, k, v, o, lse, causal: bool, scale: float, stream=None) -> None:
     """o: fp32 [B, H, N, d]."""
     B, H, Hkv, N, d = _dims(q, k)
-    _check(lib().fa_fwd_precise(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _f32(o, "o"),
-                                _f32(lse, "lse"), B, H, Hkv, N, d, int(bool(causal)),
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
+    _check(lib().fa_fwd_precise(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _f32(o, "o", qs),
+                                _f32(lse, "lse", ls), B, H, Hkv, N, d, int(bool(causal)),
                                 float(scale), _stream(stream)), "fa_fwd_precise")
 
 
 def fa_fwd_window(q, k, v, o, lse, window: int, scale: float, stream=None) -> None:
     """Causal sliding window: query i attends to keys i - window < j <= i."""
     B, H, Hkv, N, d = _dims(q, k)
-    _check(lib().fa_fwd_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
-                               _f32(lse, "lse"), B, H, Hkv, N, d, int(window), float(scale),
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
+    _check(lib().fa_fwd_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _bf16(o, "o", qs),
+                               _f32(lse, "lse", ls), B, H, Hkv, N, d, int(window), float(scale),
                                _stream(stream)), "fa_fwd_window")
 
 
-def _i32(t, name):
+def _i32(t, name, shape=None):
     import torch
-    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return _ptr(t, name, torch.int32, shape)
 
 
 def _varlen_dims(q, k, cu_seqlens):
@@ -114,6 +130,8 @@ def _varlen_dims(q, k, cu_seqlens):
     H, total, d = q.shape
     if k.shape[1] != total or k.shape[2] != d:
         raise ValueError(f"q {tuple(q.shape)} and k {tuple(k.shape)} disagree")
+    if cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be 1-D [B + 1]")
     return cu_seqlens.numel() - 1, H, k.shape[0], total, d
 
 
@@ -122,8 +140,9 @@ def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, sc
     """Packed sequences: q, o [H, total, d], k, v [Hkv, total, d], lse [H, total],
     cu_seqlens int32 [B + 1] on the device."""
     B, H, Hkv, total, d = _varlen_dims(q, k, cu_seqlens)
-    _check(lib().fa_fwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
-                               _f32(lse, "lse"), _i32(cu_seqlens, "cu_seqlens"), B,
+    qs, ks = (H, total, d), (Hkv, total, d)
+    _check(lib().fa_fwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _bf16(o, "o", qs),
+                               _f32(lse, "lse", (H, total)), _i32(cu_seqlens, "cu_seqlens"), B,
                                int(max_seqlen), total, H, Hkv, d, int(bool(causal)),
                                float(scale), _stream(stream)), "fa_fwd_varlen")
 
@@ -135,10 +154,12 @@ def fa_bwd_varlen_workspace_size(B: int, H: int, Hkv: int, max_seqlen: int, d: i
 def fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, cu_seqlens, max_seqlen: int,
                   causal: bool, scale: float, stream=None) -> None:
     B, H, Hkv, total, d = _varlen_dims(q, k, cu_seqlens)
+    qs, ks = (H, total, d), (Hkv, total, d)
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
-                               _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"),
-                               _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb,
+    _check(lib().fa_bwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _bf16(o, "o", qs),
+                               _bf16(dout, "dout", qs), _f32(lse, "lse", (H, total)),
+                               _bf16(dq, "dq", qs), _bf16(dk, "dk", ks), _bf16(dv, "dv", ks),
+                               wp, wb,
                                _i32(cu_seqlens, "cu_seqlens"), B, int(max_seqlen), total, H, Hkv,
                                d, int(bool(causal)), float(scale), _stream(stream)),
            "fa_bwd_varlen")
@@ -158,10 +179,12 @@ def _ws(workspace):
 def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, scale: float,
            stream=None) -> None:
     B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
-                        _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"), _bf16(dk, "dk"),
-                        _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d, int(bool(causal)),
+    _check(lib().fa_bwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _bf16(o, "o", qs),
+                        _bf16(dout, "dout", qs), _f32(lse, "lse", ls), _bf16(dq, "dq", qs),
+                        _bf16(dk, "dk", ks), _bf16(dv, "dv", ks), wp, wb, B, H, Hkv, N, d,
+                        int(bool(causal)),
                         float(scale), _stream(stream)), "fa_bwd")
 
 
@@ -169,10 +192,11 @@ def fa_bwd_precise(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, s
                    stream=None) -> None:
     """o: the fp32 output of fa_fwd_precise."""
     B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd_precise(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _f32(o, "o"),
-                                _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"),
-                                _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d,
+    _check(lib().fa_bwd_precise(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _f32(o, "o", qs),
+                                _bf16(dout, "dout", qs), _f32(lse, "lse", ls), _bf16(dq, "dq", qs),
+                                _bf16(dk, "dk", ks), _bf16(dv, "dv", ks), wp, wb, B, H, Hkv, N, d,
                                 int(bool(causal)), float(scale), _stream(stream)),
            "fa_bwd_precise")
 
@@ -181,25 +205,34 @@ def fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, workspace, window: int, sca
                   stream=None) -> None:
     """Backward of fa_fwd_window."""
     B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
-                               _bf16(dout, "dout"), _f32(lse, "lse"), _bf16(dq, "dq"),
-                               _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d,
+    _check(lib().fa_bwd_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), _bf16(o, "o", qs),
+                               _bf16(dout, "dout", qs), _f32(lse, "lse", ls), _bf16(dq, "dq", qs),
+                               _bf16(dk, "dk", ks), _bf16(dv, "dv", ks), wp, wb, B, H, Hkv, N, d,
                                int(window), float(scale), _stream(stream)), "fa_bwd_window")
 
 
+def _dims_of(t, name):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be 4-D [B, H, N, d]")
+    return tuple(t.shape)
+
+
 def fa_bwd_preprocess(o, dout, lse, workspace, Hkv: int, stream=None) -> None:
-    B, H, N, d = o.shape
+    B, H, N, d = _dims_of(o, "o")
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd_preprocess(_bf16(o, "o"), _bf16(dout, "dout"), _f32(lse, "lse"), wp, wb,
+    _check(lib().fa_bwd_preprocess(_bf16(o, "o"), _bf16(dout, "dout", (B, H, N, d)),
+                                   _f32(lse, "lse", (B, H, N)), wp, wb,
                                    B, H, Hkv, N, d, _stream(stream)), "fa_bwd_preprocess")
 
 
 def fa_bwd_preprocess_precise(o, dout, lse, workspace, Hkv: int, stream=None) -> None:
     """o: the fp32 output of fa_fwd_precise."""
-    B, H, N, d = o.shape
+    B, H, N, d = _dims_of(o, "o")
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd_preprocess_precise(_f32(o, "o"), _bf16(dout, "dout"), _f32(lse, "lse"),
+    _check(lib().fa_bwd_preprocess_precise(_f32(o, "o"), _bf16(dout, "dout", (B, H, N, d)),
+                                           _f32(lse, "lse", (B, H, N)),
                                            wp, wb, B, H, Hkv, N, d, _stream(stream)),
            "fa_bwd_preprocess_precise")
 
@@ -207,24 +240,28 @@ def fa_bwd_preprocess_precise(o, dout, lse, workspace, Hkv: int, stream=None) ->
 def fa_bwd_dkdv(q, k, v, dout, dk, dv, workspace, causal: bool, scale: float,
                 stream=None) -> None:
     B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, _ = _shapes(B, H, Hkv, N, d)
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd_dkdv(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(dout, "dout"),
-                             _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb, B, H, Hkv, N, d,
+    _check(lib().fa_bwd_dkdv(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks),
+                             _bf16(dout, "dout", qs), _bf16(dk, "dk", ks), _bf16(dv, "dv", ks),
+                             wp, wb, B, H, Hkv, N, d,
                              int(bool(causal)), float(scale), _stream(stream)), "fa_bwd_dkdv")
 
 
 def fa_bwd_dkdv_window(q, k, v, dout, dk, dv, workspace, window: int, scale: float,
                        stream=None) -> None:
     B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, _ = _shapes(B, H, Hkv, N, d)
     wp, wb = _ws(workspace)
-    _check(lib().fa_bwd_dkdv_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"),
-                                    _bf16(dout, "dout"), _bf16(dk, "dk"), _bf16(dv, "dv"), wp, wb,
+    _check(lib().fa_bwd_dkdv_window(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks),
+                                    _bf16(dout, "dout", qs), _bf16(dk, "dk", ks),
+                                    _bf16(dv, "dv", ks), wp, wb,
                                     B, H, Hkv, N, d, int(window), float(scale), _stream(stream)),
            "fa_bwd_dkdv_window")
 
 
 def fa_bwd_dq_convert(workspace, dq, Hkv: int, scale: float, stream=None) -> None:
-    B, H, N, d = dq.shape
+    B, H, N, d = _dims_of(dq, "dq")
     wp, wb = _ws(workspace)
     _check(lib().fa_bwd_dq_convert(wp, wb, _bf16(dq, "dq"), B, H, Hkv, N, d, float(scale),
                                    _stream(stream)), "fa_bwd_dq_convert")
@@ -258,17 +295,16 @@ def fa_fp8_quantize(q, k, v, fp8_buf, stream=None) -> None:
     """fp8_buf: a contiguous CUDA tensor of at least fa_fp8_buffer_size() bytes."""
     B, H, Hkv, N, d = _dims(q, k)
     bp, bb = _ws(fp8_buf)
-    _check(lib().fa_fp8_quantize(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), bp, bb,
+    _check(lib().fa_fp8_quantize(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", (B, Hkv, N, d)),
+                                 bp, bb,
                                  B, H, Hkv, N, d, _stream(stream)), "fa_fp8_quantize")
 
 
 def fa_fwd_fp8(fp8_buf, o, lse, Hkv: int, causal: bool, scale: float, stream=None) -> None:
     """o: bf16 [B, H, N, d] (its shape gives B, H, N, d), lse: fp32 [B, H, N]."""
-    if o.dim() != 4:
-        raise ValueError("o must be 4-D [B, H, N, d]")
-    B, H, N, d = o.shape
+    B, H, N, d = _dims_of(o, "o")
     bp, bb = _ws(fp8_buf)
-    _check(lib().fa_fwd_fp8(bp, bb, _bf16(o, "o"), _f32(lse, "lse"), B, H, Hkv, N, d,
+    _check(lib().fa_fwd_fp8(bp, bb, _bf16(o, "o"), _f32(lse, "lse", (B, H, N)), B, H, Hkv, N, d,
                             int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_fp8")
 
 
@@ -302,8 +338,9 @@ def fa_fwd_decode(q, k, v, o, lse, workspace, causal: bool, scale: float, stream
     if k.shape[0] != B or k.shape[3] != d or v.shape != k.shape:
         raise ValueError(f"q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)} disagree")
     wp, wb = _ws(workspace)
-    _check(lib().fa_fwd_decode(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"),
-                               _f32(lse, "lse"), wp, wb, B, H, Hkv, Nq, Nk, d,
+    _check(lib().fa_fwd_decode(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"),
+                               _bf16(o, "o", (B, H, Nq, d)), _f32(lse, "lse", (B, H, Nq)),
+                               wp, wb, B, H, Hkv, Nq, Nk, d,
                                int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_decode")
 
 

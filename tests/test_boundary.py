@@ -188,3 +188,118 @@ def test_fp8_entry_points_validate(L):
     assert L.fa_fp8_quantize(A, A, A, A, 16, 1, 2, 1, 256, 128, None) == fa.FA_ERR_WORKSPACE
     assert L.fa_fwd_fp8(A, 16, A, A, 1, 2, 1, 256, 128, 1, 0.088, None) == fa.FA_ERR_WORKSPACE
     assert fa.fa_kernel_launches() == before
+
+
+class FakeCuda:
+    """Stands in for a contiguous CUDA tensor of a given shape and dtype: the
+    binding reads only these attributes before it calls the library, and the
+    library rejects its null pointer before any launch."""
+
+    def __init__(self, shape, dtype):
+        import torch
+        self.shape, self.dtype, self.is_cuda = torch.Size(shape), dtype, True
+        self._esize = torch.empty(0, dtype=dtype).element_size()
+
+    def dim(self):
+        return len(self.shape)
+
+    def numel(self):
+        n = 1
+        for x in self.shape:
+            n *= x
+        return n
+
+    def element_size(self):
+        return self._esize
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return 0
+
+
+def test_python_binding_checks_every_tensor_shape():
+    """The C entry points see only pointers, so the binding checks the shape of
+    every tensor against the one q and k imply before anything reaches the
+    library."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    T = FakeCuda
+    q, k = T((1, 4, 8, 64), bf), T((1, 2, 8, 64), bf)
+    lse, ws = T((1, 4, 8), f32), T((16,), torch.uint8)
+    short_k, short_lse = T((1, 2, 7, 64), bf), T((1, 4, 7), f32)
+    cases = [
+        ("v", lambda: fa.fa_fwd(q, k, short_k, q, lse, True, 0.125, stream=0)),
+        ("o", lambda: fa.fa_fwd(q, k, k, k, lse, True, 0.125, stream=0)),
+        ("lse", lambda: fa.fa_fwd(q, k, k, q, short_lse, True, 0.125, stream=0)),
+        ("o", lambda: fa.fa_fwd_precise(q, k, k, T((1, 4, 8, 32), f32), lse, True, 0.125,
+                                        stream=0)),
+        ("lse", lambda: fa.fa_fwd_window(q, k, k, q, short_lse, 4, 0.125, stream=0)),
+        ("dout", lambda: fa.fa_bwd(q, k, k, q, k, lse, q, k, k, ws, True, 0.125, stream=0)),
+        ("dq", lambda: fa.fa_bwd(q, k, k, q, q, lse, k, k, k, ws, True, 0.125, stream=0)),
+        ("dk", lambda: fa.fa_bwd_window(q, k, k, q, q, lse, q, q, k, ws, 4, 0.125, stream=0)),
+        ("dv", lambda: fa.fa_bwd_dkdv(q, k, k, q, k, short_k, ws, True, 0.125, stream=0)),
+        ("dout", lambda: fa.fa_bwd_preprocess(q, k, lse, ws, 2, stream=0)),
+        ("lse", lambda: fa.fa_fwd_fp8(ws, q, short_lse, 2, True, 0.125, stream=0)),
+        ("v", lambda: fa.fa_fp8_quantize(q, k, short_k, ws, stream=0)),
+        ("o", lambda: fa.fa_fwd_decode(q, k, k, T((1, 4, 1, 64), bf), lse, ws, True, 0.125,
+                                       stream=0)),
+    ]
+    for name, call in cases:
+        with pytest.raises(ValueError, match=rf"^{name} has shape"):
+            call()
+    # the same tensors with the right shapes pass the binding and reach the
+    # library, which rejects the null pointers before any launch
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fwd(q, k, k, q, lse, True, 0.125, stream=0)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG
+    # packed layout: [H, total, d] and [H, total]
+    pq, pk, cu = T((4, 10, 64), bf), T((2, 10, 64), bf), T((3,), torch.int32)
+    with pytest.raises(ValueError, match=r"^lse has shape"):
+        fa.fa_fwd_varlen(pq, pk, pk, pq, T((4, 9), f32), cu, 6, True, 0.125, stream=0)
+    with pytest.raises(ValueError, match=r"^dk has shape"):
+        fa.fa_bwd_varlen(pq, pk, pk, pq, pq, T((4, 10), f32), pq, pq, pk, ws, cu, 6, True,
+                         0.125, stream=0)
+    with pytest.raises(ValueError, match=r"cu_seqlens must be 1-D"):
+        fa.fa_fwd_varlen(pq, pk, pk, pq, T((4, 10), f32), T((1, 3), torch.int32), 6, True,
+                         0.125, stream=0)
+
+
+def test_python_binding_accepts_consistent_shapes():
+    """Every wrapper, given tensors of the shapes its documentation states, passes
+    the binding's checks and reaches the library (which rejects the null
+    pointers of the stand-ins before any launch)."""
+    import torch
+    bf, f32, u8, i32 = torch.bfloat16, torch.float32, torch.uint8, torch.int32
+    T = FakeCuda
+    B, H, Hkv, N, d = 2, 4, 2, 8, 64
+    q, k, lse = T((B, H, N, d), bf), T((B, Hkv, N, d), bf), T((B, H, N), f32)
+    o32, ws = T((B, H, N, d), f32), T((1 << 20,), u8)
+    pq, pk, plse = T((H, 20, d), bf), T((Hkv, 20, d), bf), T((H, 20), f32)
+    cu = T((B + 1,), i32)
+    dq, dlse = T((B, H, 1, d), bf), T((B, H, 1), f32)
+    calls = [
+        lambda: fa.fa_fwd(q, k, k, q, lse, True, 0.125, stream=0),
+        lambda: fa.fa_fwd_precise(q, k, k, o32, lse, True, 0.125, stream=0),
+        lambda: fa.fa_fwd_window(q, k, k, q, lse, 4, 0.125, stream=0),
+        lambda: fa.fa_bwd(q, k, k, q, q, lse, q, k, k, ws, True, 0.125, stream=0),
+        lambda: fa.fa_bwd_precise(q, k, k, o32, q, lse, q, k, k, ws, True, 0.125, stream=0),
+        lambda: fa.fa_bwd_window(q, k, k, q, q, lse, q, k, k, ws, 4, 0.125, stream=0),
+        lambda: fa.fa_bwd_preprocess(q, q, lse, ws, Hkv, stream=0),
+        lambda: fa.fa_bwd_preprocess_precise(o32, q, lse, ws, Hkv, stream=0),
+        lambda: fa.fa_bwd_dkdv(q, k, k, q, k, k, ws, True, 0.125, stream=0),
+        lambda: fa.fa_bwd_dkdv_window(q, k, k, q, k, k, ws, 4, 0.125, stream=0),
+        lambda: fa.fa_bwd_dq_convert(ws, q, Hkv, 0.125, stream=0),
+        lambda: fa.fa_fwd_varlen(pq, pk, pk, pq, plse, cu, 12, True, 0.125, stream=0),
+        lambda: fa.fa_bwd_varlen(pq, pk, pk, pq, pq, plse, pq, pk, pk, ws, cu, 12, True, 0.125,
+                                 stream=0),
+        lambda: fa.fa_fp8_quantize(T((B, H, N, 128), bf), T((B, Hkv, N, 128), bf),
+                                   T((B, Hkv, N, 128), bf), ws, stream=0),
+        lambda: fa.fa_fwd_fp8(ws, T((B, H, N, 128), bf), lse, Hkv, True, 0.125, stream=0),
+        lambda: fa.fa_fwd_decode(dq, k, k, dq, dlse, ws, True, 0.125, stream=0),
+    ]
+    for i, call in enumerate(calls):
+        with pytest.raises(fa.FAError) as e:
+            call()
+        assert e.value.status == fa.FA_ERR_INVALID_ARG, i
