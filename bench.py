@@ -10,10 +10,20 @@ fa_bwd_dq_convert, all on the current CUDA stream.  FLOPs per step use the
 headline count: forward 4*B*H*N^2*d (halved under the causal mask) and
 forward+backward 2.5x that.
 
-Default workload: B=8, H=16, N=2048, d=64, causal, bf16 (the multi-head
-workload of the pages' setting).  Under torchrun every rank runs the same
-per-GPU workload on its own GPU (independent batches, no data-path
+Default workload: gpt_long, B=2, H=16, N=8192, d=128, causal, bf16, forward +
+backward (the long-sequence GPT-style workload, the head dimension and mask on
+which the throughput target is stated).  Under torchrun every rank runs the
+same per-GPU workload on its own GPU (independent batches, no data-path
 collective): weak scaling, value = all ranks' FLOPs / max-over-ranks time.
+
+Timing: W warm-up steps, then an untimed, labelled clock soak of the same step
+(--soak seconds, default 3) so that clocks and power settle under load and the
+clock samplers see the GPU busy, then exactly K timed steps with no events
+between kernels (the headline), then a separate instrumented loop that times
+each kernel of the step with CUDA events.  nvidia-smi is sampled every 200 ms
+from the start of the soak to the end of the timed region, and an in-process
+read-only NVML poller samples the SM clock and the clock-event reasons every
+few milliseconds inside the timed region itself.
 
 --impl reference times the fp64 CPU oracle (the only other implementation of
 this path) on a bounded sample of the same workload on the host cores; rank 0
@@ -40,30 +50,29 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 
 # DRAM traffic of the dominant kernel from one ncu capture (dram__bytes_read.sum
-# + dram__bytes_write.sum, per launch, scaled to the benchmark workload as
-# described in profiles/), keyed by workload, together with the sha256 of the
-# kernel source it was taken on.  A source change makes the figure stale and
-# it is then reported as null.
+# + dram__bytes_write.sum, one launch of the workload), keyed by kernel and
+# workload, together with the sha256 of the kernel source it was taken on.  A
+# source change makes the figure stale and it is then reported as null.
 NCU_TRAFFIC = {
-    # profiles/fa_bwd_dkdv_mha_d64.md: 237.5 MB read + 103.6 MB written, one launch
+    # 237.5 MB read + 103.6 MB written, one launch
     ("fa_bwd_dkdv", "mha_d64"): {"bytes": 341.09e6, "src_sha": "e9d1140dc8699988"},
-    # profiles/launches_mha_d64_fwd_bwd.md: 110.3 MB read + 12.7 MB written, one launch
+    # 110.3 MB read + 12.7 MB written, one launch
     ("fa_fwd", "mha_d64"): {"bytes": 123.07e6, "src_sha": "9edd374358a89cb8"},
-    # profiles/fa_window_fwd_bwd_window.md: 1385.7 MB read + 641.3 MB written
+    # 1385.7 MB read + 641.3 MB written
     ("fa_bwd_dkdv", "window"): {"bytes": 2026.96e6, "src_sha": "e9d1140dc8699988"},
-    # the same file: 205.0 MB read + 97.9 MB written
+    # 205.0 MB read + 97.9 MB written
     ("fa_fwd", "window"): {"bytes": 302.90e6, "src_sha": "9edd374358a89cb8"},
-    # profiles/fa_fwd_bwd_d128_gpt_long_gqa.md: 427.9 MB read + 224.6 MB written
+    # 427.9 MB read + 224.6 MB written
     ("fa_bwd_dkdv", "gpt_long"): {"bytes": 652.53e6, "src_sha": "e9d1140dc8699988"},
-    # the same file: 534.0 MB read + 46.4 MB written
+    # 534.0 MB read + 46.4 MB written
     ("fa_fwd", "gpt_long"): {"bytes": 580.44e6, "src_sha": "9edd374358a89cb8"},
-    # the same file: 771.6 MB read + 347.6 MB written
+    # 771.6 MB read + 347.6 MB written
     ("fa_bwd_dkdv", "gqa"): {"bytes": 1119.17e6, "src_sha": "e9d1140dc8699988"},
-    # the same file: 298.1 MB read + 216.1 MB written (fp32 O, precise path)
+    # 298.1 MB read + 216.1 MB written (fp32 O, precise path)
     ("fa_fwd", "gqa"): {"bytes": 514.19e6, "src_sha": "9edd374358a89cb8"},
-    # profiles/fa_decode_split_decode_gqa.md: 1.0739 GB read + 4.3 MB written, one launch
+    # 1.0739 GB read + 4.3 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0782e9, "src_sha": "737ec0dc1b9c060c"},
-    # profiles/fa_fwd_fp8_long16k.md: 166.0 MB read + 33.8 MB written, one launch
+    # 166.0 MB read + 33.8 MB written, one launch
     ("fa_fwd_fp8", "long16k"): {"bytes": 199.78e6, "src_sha": "9cc4f81f16caefe2"},
 }
 
@@ -74,7 +83,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: enough for about 3 s of timed work)")
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="mha_d64")
+    ap.add_argument("--workload", default="gpt_long")
+    ap.add_argument("--soak", type=float, default=3.0,
+                    help="seconds of untimed steps between the warm-up and the timed region "
+                         "(clocks and power settle; the samplers see the GPU under load)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -105,7 +117,8 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling (every 200 ms) over the clock soak
+    and the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -158,6 +171,190 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[0] for r in rows),
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
                 "samples": len(rows)}
+
+
+# Clock-event reason bits of NVML's public API (nvmlClocksEventReason*).
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def nvml_reason_names(mask: int) -> list:
+    """Names of the throttle reasons set in an NVML clock-event reason mask."""
+    return sorted(name for bit, name in NVML_REASONS.items() if mask & bit)
+
+
+class NvmlPoller:
+    """Read-only, in-process clock queries through NVML (libnvidia-ml, loaded
+    with ctypes): a thread reads the SM clock, the maximum SM clock and the
+    clock-event reasons every `period_s`, and `mark()` brackets the timed
+    region.  Nothing here changes a GPU setting.  `lib` may be a stand-in
+    object with the same functions (tests)."""
+
+    def __init__(self, uuid, index: int, period_s: float = 0.002, lib=None):
+        import threading
+        self.samples = []            # (host time, sm_mhz, max_mhz, reason mask)
+        self.t_start = self.t_end = None
+        self.error = None
+        self._stop = threading.Event()
+        self._thread = None
+        self.period = period_s
+        self.dev = None
+        try:
+            self.L = lib if lib is not None else self._load()
+            self.dev = self._handle(uuid, index)
+        except Exception as e:      # no NVML on this host: reported, not fatal
+            self.error = f"{type(e).__name__}: {e}"
+
+    @staticmethod
+    def _load():
+        import ctypes
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        return L
+
+    def _handle(self, uuid, index):
+        import ctypes
+        h = ctypes.c_void_p()
+        if uuid and self.L.nvmlDeviceGetHandleByUUID(str(uuid).encode(), ctypes.byref(h)) == 0:
+            return h
+        if self.L.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) == 0:
+            return h
+        raise RuntimeError("no NVML handle for the device")
+
+    def _reasons_fn(self):
+        # the current name, or the older name of the same call on older drivers
+        fn = getattr(self.L, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        return fn if fn is not None else self.L.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def read(self):
+        import ctypes
+        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.L.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(sm)) != 0:   # NVML_CLOCK_SM
+            return None
+        self.L.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))
+        self._reasons_fn()(self.dev, ctypes.byref(rs))
+        return (time.perf_counter(), float(sm.value), float(mx.value), int(rs.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                s = self.read()
+            except Exception as e:
+                self.error = f"{type(e).__name__}: {e}"
+                return
+            if s is not None:
+                self.samples.append(s)
+            self._stop.wait(self.period)
+
+    def __enter__(self):
+        import threading
+        if self.dev is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def mark(self, start: bool):
+        """Host time of the start (after the opening barrier) or the end (after
+        the closing synchronize) of the timed region, with a read taken there."""
+        t = time.perf_counter()
+        if start:
+            self.t_start = t
+        if self.dev is not None:
+            try:
+                s = self.read()
+            except Exception:
+                s = None
+            if s is not None:
+                self.samples.append(s)
+        if not start:
+            self.t_end = time.perf_counter()
+
+    def summary(self) -> dict:
+        if self.dev is None:
+            return {"samples": 0, "error": self.error}
+        inside = [s for s in list(self.samples)
+                  if self.t_start is not None and self.t_end is not None
+                  and self.t_start <= s[0] <= self.t_end]
+        if not inside:
+            return {"samples": 0, "error": self.error}
+        mask = 0
+        for s in inside:
+            mask |= s[3]
+        return {"samples": len(inside), "sm_mhz": statistics.median(s[1] for s in inside),
+                "sm_mhz_min": min(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "at_start_mhz": inside[0][1], "at_end_mhz": inside[-1][1],
+                "reasons": nvml_reason_names(mask), "period_ms": self.period * 1e3}
+
+
+def clocks_record(smi: dict, poll: dict, soak_s: float) -> dict:
+    """The line's clock record: the nvidia-smi samples (clock soak and timed
+    region, every 200 ms) and the in-process NVML reads inside the timed
+    region.  sm_mhz is the timed region's median when it has reads, else the
+    nvidia-smi median."""
+    out = dict(smi)
+    out["source"] = "nvidia-smi every 200 ms over the clock soak and the timed region"
+    out["soak_s"] = soak_s
+    out["timed_region"] = poll
+    if poll.get("samples"):
+        out["sm_mhz"] = poll["sm_mhz"]
+        out["sm_max_mhz"] = max(poll["sm_max_mhz"], smi.get("sm_max_mhz") or 0.0)
+        out["reasons"] = sorted((set(smi.get("reasons", [])) - {"no samples",
+                                                                 "nvidia-smi unavailable"})
+                                | set(poll["reasons"]))
+        out["source"] = ("sm_mhz: median of in-process NVML reads inside the timed region; "
+                         "samples and reasons also from nvidia-smi every 200 ms over the clock "
+                         "soak and the timed region")
+    return out
+
+
+def choose_peak(peaks: dict, timed_s: float):
+    """Roofline denominator: the burst figure (a cuBLAS burst) when the timed
+    region is short, the sustained one (seconds back to back under the power
+    cap) once the timed region lasts a second or more."""
+    if timed_s < 1.0:
+        return peaks["bf16_tflops"], (f"bf16_tflops burst ({peaks['source']}; timed region "
+                                      f"{timed_s:.3f} s < 1 s)")
+    return peaks["bf16_tflops_sustained"], (f"bf16_tflops_sustained ({peaks['source']}; "
+                                            f"timed region {timed_s:.1f} s)")
+
+
+def soak_and_time(torch, fa, dev, stream, fn, steps: int, per_ms: float, soak_s: float,
+                  barrier):
+    """The measured region every line shares: an untimed clock soak of about
+    `soak_s` seconds of `fn` back to back, a barrier, exactly `steps` calls of
+    `fn` between two CUDA events on `stream`, a barrier.  nvidia-smi samples
+    the soak and the timed region; an in-process NVML poller reads the clocks
+    inside the timed region.  Returns (elapsed ms, clock record, launches in
+    the timed region, soak calls)."""
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None and not str(uuid).startswith("GPU-"):
+        uuid = f"GPU-{uuid}"
+    gpu_index = dev.index if dev.index is not None else 0
+    n_soak = int(math.ceil(soak_s * 1e3 / max(per_ms, 1e-3))) if soak_s > 0 else 0
+    with ClockSampler(gpu_index) as clk, NvmlPoller(uuid, gpu_index) as poll:
+        for _ in range(n_soak):
+            fn()
+        barrier()
+        launches0 = fa.fa_kernel_launches()
+        poll.mark(True)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            fn()
+        t1.record(stream)
+        barrier()
+        poll.mark(False)
+        launches = fa.fa_kernel_launches() - launches0
+    return (t0.elapsed_time(t1), clocks_record(clk.summary(), poll.summary(), soak_s),
+            launches, n_soak)
 
 
 def kernel_source_hash(name: str) -> str:
@@ -293,54 +490,50 @@ def run_native(args, w):
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    fwd_ev, dkdv_ev = [], []
-
-    def step(timed: bool):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
-        if timed:
-            e[0].record(stream)
+    # The step's kernels in order; `ev` (instrumented loop only) receives an
+    # event after each kernel so that each kernel's own time can be read.
+    def step(ev=None):
         if precise:
             fa.fa_fwd_precise(qd, kd, vd, o, lse, w.causal, w.scale, stream)
         elif w.window:
             fa.fa_fwd_window(qd, kd, vd, o, lse, w.window, w.scale, stream)
         else:
             fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
-        if timed:
-            e[1].record(stream)
+        if ev is not None:
+            ev[1].record(stream)
         if fwd_only:
-            if timed:
-                fwd_ev.append((e[0], e[1]))
             return
         if precise:
             fa.fa_bwd_preprocess_precise(o, dod, lse, work, Hkv, stream)
         else:
             fa.fa_bwd_preprocess(o, dod, lse, work, Hkv, stream)
-        if timed:
-            e[2].record(stream)
+        if ev is not None:
+            ev[2].record(stream)
         if w.window:
             fa.fa_bwd_dkdv_window(qd, kd, vd, dod, dk, dv, work, w.window, w.scale, stream)
         else:
             fa.fa_bwd_dkdv(qd, kd, vd, dod, dk, dv, work, w.causal, w.scale, stream)
-        if timed:
-            e[3].record(stream)
+        if ev is not None:
+            ev[3].record(stream)
         fa.fa_bwd_dq_convert(work, dq, Hkv, w.scale, stream)
-        if timed:
-            fwd_ev.append((e[0], e[1]))
-            dkdv_ev.append((e[2], e[3]))
+        if ev is not None:
+            ev[4].record(stream)
 
-    for _ in range(args.warmup):
-        step(False)
-    torch.cuda.synchronize()
-    if args.steps is None:
-        # Calibrate K so the timed region lasts about 3 s (clock sampling
-        # needs several 200 ms samples); the same K is then timed exactly.
+    def timed(fn, n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(10):
-            step(False)
+        for _ in range(n):
+            fn()
         b.record(stream)
         torch.cuda.synchronize()
-        per = a.elapsed_time(b) / 10
+        return a.elapsed_time(b)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    per = timed(step, 3) / 3                  # untimed estimate of one step
+    if args.steps is None:
+        # K for about 3 s of timed work; the same K is then timed exactly.
         n_steps = int(min(20000, max(50, math.ceil(3000.0 / max(per, 1e-3)))))
         if ws > 1:
             kt = torch.tensor([n_steps], device=dev)
@@ -356,32 +549,36 @@ def run_native(args, w):
             dist.barrier()
         torch.cuda.synchronize()
 
-    launches0 = fa.fa_kernel_launches()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        barrier()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
-            step(True)
-        t1.record(stream)
-        barrier()
-    launches = fa.fa_kernel_launches() - launches0
+    ms_local, clocks, launches, n_soak = soak_and_time(torch, fa, dev, stream, step, args.steps,
+                                                       per, args.soak, barrier)
     st = fa.fa_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
-    ms_total = replicas.max_over_ranks(t0.elapsed_time(t1), dev)
+    ms_total = replicas.max_over_ranks(ms_local, dev)
     ms_step = ms_total / args.steps
     flops_step = attention_flops(w, "fwd" if fwd_only else "fwd_bwd")
     value = replicas.whole_job_rate(flops_step, args.steps, ws, ms_total) / 1e12
 
-    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_ev)
-    dkdv_ms = statistics.mean(a.elapsed_time(b) for a, b in dkdv_ev) if dkdv_ev else 0.0
+    # Per-kernel times from a separate, instrumented loop (events between the
+    # kernels of every step), run right after the timed region.
+    n_inst = max(3, min(args.steps, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_inst)]
+    for e in evs:
+        e[0].record(stream)
+        step(e)
+    torch.cuda.synchronize()
+    names = ["fa_fwd"] if fwd_only else ["fa_fwd", "fa_bwd_preprocess", "fa_bwd_dkdv",
+                                         "fa_bwd_dq_convert"]
+    kern_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+               for i, n in enumerate(names)}
+    inst_ms = statistics.mean(e[0].elapsed_time(e[len(names)]) for e in evs)
+    fwd_ms = kern_ms["fa_fwd"]
+    dkdv_ms = kern_ms.get("fa_bwd_dkdv", 0.0)
     fwd_flops = attention_flops(w, "fwd")
     # Algorithmic work of the dK/dV kernel: the five backward matmuls
     # (S^T, dP^T, dV, dK, dQ), 2*N^2*d each per head, halved when causal.
     dkdv_flops = fwd_flops * 2.5
-    peak = peaks["bf16_tflops_sustained"]
+    peak, peak_kind = choose_peak(peaks, ms_total * 1e-3)
     kernels = {"fa_fwd": {"ms": fwd_ms, "tflops": fwd_flops / fwd_ms / 1e9}}
     if not fwd_only:
         kernels["fa_bwd_dkdv"] = {"ms": dkdv_ms, "tflops": dkdv_flops / dkdv_ms / 1e9}
@@ -392,8 +589,14 @@ def run_native(args, w):
     ach = kernels[dom]["tflops"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
-                "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
+                "peak_kind": peak_kind,
                 "frac_of_burst_peak": ach / peaks["bf16_tflops"],
+                "frac_of_sustained_peak": ach / peaks["bf16_tflops_sustained"],
+                "kernel_times": {"source": f"separate instrumented loop of {n_inst} steps "
+                                           f"(events between kernels), after the timed region",
+                                 "ms_per_step_instrumented": inst_ms,
+                                 "ms": kern_ms,
+                                 "share": {n: t / inst_ms for n, t in kern_ms.items()}},
                 "other_kernel": {n: {"ms": kernels[n]["ms"], "tflops": kernels[n]["tflops"],
                                      "frac": kernels[n]["tflops"] / peak}
                                  for n in kernels if n != dom}}
@@ -544,16 +747,19 @@ def run_native(args, w):
                        "l2": f"inputs larger than L2: {ws_mb / 2**20:.0f} MiB touched per "
                              f"step vs {L2_BYTES / 2**20:.0f} MiB L2",
                        "parallelism": f"replicas x{ws} (independent batches)"},
-            "pct_of_bf16_peak": {"sustained": value / ws / peak,
+            "pct_of_bf16_peak": {"sustained": value / ws / peaks["bf16_tflops_sustained"],
                                  "burst": value / ws / peaks["bf16_tflops"],
+                                 "headline": value / ws / peak, "headline_peak": peak_kind,
                                  "source": peaks["source"]},
             "fwd": {"tflops": kernels["fa_fwd"]["tflops"], "ms": fwd_ms},
             "fwd_bwd_alg_tflops": None if fwd_only else
             attention_flops(w, "fwd_bwd_alg") * args.steps * ws / (ms_total * 1e-3) / 1e12,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "exp_unit": exp_unit_line(w, kernels, clk.summary()),
-            "clocks": clk.summary(), "gpu_launches": launches,
+            "exp_unit": exp_unit_line(w, kernels, clocks),
+            "clocks": clocks, "gpu_launches": launches,
             "launches_per_step": launches / args.steps,
+            "clock_soak": {"steps": n_soak, "seconds_requested": args.soak,
+                           "note": "untimed steps between the warm-up and the timed region"},
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -641,12 +847,10 @@ def run_native_fp8(args, w):
             dist.barrier()
         torch.cuda.synchronize()
 
-    launches0 = fa.fa_kernel_launches()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        barrier()
-        ms_total = replicas.max_over_ranks(timed(fwd, args.steps), dev)
-        barrier()
-    launches = fa.fa_kernel_launches() - launches0
+    per = timed(fwd, 3) / 3
+    ms_local, clocks, launches, n_soak = soak_and_time(torch, fa, dev, stream, fwd, args.steps,
+                                                       per, args.soak, barrier)
+    ms_total = replicas.max_over_ranks(ms_local, dev)
     st = fa.fa_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
@@ -702,7 +906,8 @@ def run_native_fp8(args, w):
                        "parallelism": f"replicas x{ws} (independent batches)"},
             "with_quantize": {"tflops": with_quant, "quantize_ms": q_ms},
             "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
-            "clocks": clk.summary(), "gpu_launches": launches,
+            "clocks": clocks, "clock_soak": {"steps": n_soak, "seconds_requested": args.soak},
+            "gpu_launches": launches,
             "launches_per_step": launches / args.steps,
         }
         print(json.dumps(line), flush=True)
@@ -771,12 +976,10 @@ def run_native_decode(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    launches0 = fa.fa_kernel_launches()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        barrier()
-        ms_total = replicas.max_over_ranks(timed(step, args.steps), dev)
-        barrier()
-    launches = fa.fa_kernel_launches() - launches0
+    per = timed(step, 3) / 3
+    ms_local, clocks, launches, n_soak = soak_and_time(torch, fa, dev, stream, step, args.steps,
+                                                       per, args.soak, barrier)
+    ms_total = replicas.max_over_ranks(ms_local, dev)
     st = fa.fa_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
@@ -828,7 +1031,8 @@ def run_native_decode(args):
                        "parallelism": f"replicas x{ws} (independent batches)"},
             "tflops": flops * args.steps * ws / (ms_total * 1e-3) / 1e12,
             "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
-            "clocks": clk.summary(), "gpu_launches": launches,
+            "clocks": clocks, "clock_soak": {"steps": n_soak, "seconds_requested": args.soak},
+            "gpu_launches": launches,
             "launches_per_step": launches / args.steps,
         }
         print(json.dumps(line), flush=True)
@@ -872,21 +1076,14 @@ def run_native_varlen(args):
     work = torch.empty(fa.fa_bwd_varlen_workspace_size(w.B, w.H, w.Hkv, ms, w.d),
                        dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    fwd_ev, bwd_ev = [], []
-
-    def step(timed=False):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)] if timed else None
-        if timed:
-            e[0].record(stream)
+    def step(e=None):
         fa.fa_fwd_varlen(qd, kd, vd, o, lse, cu, ms, w.causal, w.scale, stream)
-        if timed:
+        if e is not None:
             e[1].record(stream)
         fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, dq, dk, dv, work, cu, ms, w.causal, w.scale,
                          stream)
-        if timed:
+        if e is not None:
             e[2].record(stream)
-            fwd_ev.append((e[0], e[1]))
-            bwd_ev.append((e[1], e[2]))
 
     def timed(fn, n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -912,12 +1109,19 @@ def run_native_varlen(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    launches0 = fa.fa_kernel_launches()
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        barrier()
-        ms_total = replicas.max_over_ranks(timed(lambda: step(True), args.steps), dev)
-        barrier()
-    launches = fa.fa_kernel_launches() - launches0
+    per = timed(step, 3) / 3
+    ms_local, clocks, launches, n_soak = soak_and_time(torch, fa, dev, stream, step, args.steps,
+                                                       per, args.soak, barrier)
+    ms_total = replicas.max_over_ranks(ms_local, dev)
+    # per-call times from a separate instrumented loop
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+           for _ in range(max(3, min(args.steps, 50)))]
+    for e in evs:
+        e[0].record(stream)
+        step(e)
+    torch.cuda.synchronize()
+    fwd_ev = [(e[0], e[1]) for e in evs]
+    bwd_ev = [(e[1], e[2]) for e in evs]
     st = fa.fa_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status after timed steps: {fa.fa_status_string(st)}")
@@ -979,7 +1183,8 @@ def run_native_varlen(args):
                        "parallelism": f"replicas x{ws} (independent batches)"},
             "fwd": {"tflops": kernels["fa_fwd_varlen"][1], "ms": fwd_ms},
             "roofline": roofline, "cpu_baseline": None, "e2e": e2e,
-            "clocks": clk.summary(), "gpu_launches": launches,
+            "clocks": clocks, "clock_soak": {"steps": n_soak, "seconds_requested": args.soak},
+            "gpu_launches": launches,
             "launches_per_step": launches / args.steps,
         }
         print(json.dumps(line), flush=True)

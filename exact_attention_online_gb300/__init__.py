@@ -50,21 +50,45 @@ def _check(status: int, where: str) -> None:
         raise FAError(status, where)
 
 
+def _current_index() -> int:
+    """Index of the current CUDA device: every pointer the library receives
+    must be memory of this device (its kernels and tensor maps are built
+    there)."""
+    import torch
+    try:
+        return torch.cuda.current_device()
+    except Exception:   # no CUDA runtime in this process: the library rejects the call
+        return 0
+
+
+def _on_current_device(t, name) -> None:
+    dev = getattr(t, "device", None)
+    idx = getattr(dev, "index", None)
+    cur = _current_index()
+    if idx is not None and idx != cur:
+        raise ValueError(f"{name} is on cuda:{idx} but the current device is cuda:{cur}")
+
+
 def _stream(stream):
     import torch
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    if hasattr(stream, "cuda_stream"):
+        _on_current_device(stream, "stream")
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
 
 
 def _ptr(t, name, dtype, shape):
     """Device pointer of t after checking its shape (the C entry points see
     only pointers, so a short buffer would be read or written past its end),
-    dtype, device and contiguity."""
+    dtype, contiguity and device: a CUDA tensor of the current device, so that
+    every operand of a call shares one device."""
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA {str(dtype)[6:]} tensor")
+    _on_current_device(t, name)
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -173,6 +197,7 @@ def _ws(workspace):
     import torch
     if not workspace.is_cuda or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
+    _on_current_device(workspace, "workspace")
     return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
 
 

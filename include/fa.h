@@ -44,6 +44,12 @@
  *     that ran out) are recorded in a device status word that
  *     fa_device_status() reads.
  *   - Outputs may not alias inputs.  The library is thread-safe.
+ *   - The library caches, per device, the device addresses of its own
+ *     device variables (the status word, the fixed scratch array of
+ *     fa_bwd_static_scratch) from the first call on that device.  Do not use
+ *     it across a cudaDeviceReset() (or any teardown of the device's primary
+ *     context) in the same process: the cached addresses would then point
+ *     into memory that no longer belongs to the library.
  */
 #ifndef FA_H_
 #define FA_H_

@@ -33,7 +33,7 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
-    assert d["config"]["workload"].startswith("mha_d64")
+    assert d["config"]["workload"].startswith("gpt_long")
 
 
 def test_reference_arm_other_ranks_are_silent():

@@ -195,9 +195,10 @@ class FakeCuda:
     binding reads only these attributes before it calls the library, and the
     library rejects its null pointer before any launch."""
 
-    def __init__(self, shape, dtype):
+    def __init__(self, shape, dtype, index=0):
         import torch
         self.shape, self.dtype, self.is_cuda = torch.Size(shape), dtype, True
+        self.device = torch.device("cuda", index)
         self._esize = torch.empty(0, dtype=dtype).element_size()
 
     def dim(self):
@@ -303,3 +304,32 @@ def test_python_binding_accepts_consistent_shapes():
         with pytest.raises(fa.FAError) as e:
             call()
         assert e.value.status == fa.FA_ERR_INVALID_ARG, i
+
+
+def test_python_binding_rejects_tensors_of_another_device():
+    """Every pointer must be memory of the current device: an operand (or the
+    workspace, or the FP8 buffer) on another GPU is rejected before any
+    library call, so no kernel or tensor map is built over another GPU's
+    memory."""
+    import torch
+    bf, f32, u8 = torch.bfloat16, torch.float32, torch.uint8
+    T = FakeCuda
+    B, H, Hkv, N, d = 1, 4, 2, 8, 64
+    q, k, lse, ws = T((B, H, N, d), bf), T((B, Hkv, N, d), bf), T((B, H, N), f32), T((64,), u8)
+    other = lambda shape, dt: T(shape, dt, index=1)
+    before = fa.fa_kernel_launches()
+    cases = [
+        ("q", lambda: fa.fa_fwd(other(q.shape, bf), k, k, q, lse, True, 0.125, stream=0)),
+        ("v", lambda: fa.fa_fwd(q, k, other(k.shape, bf), q, lse, True, 0.125, stream=0)),
+        ("lse", lambda: fa.fa_fwd(q, k, k, q, other(lse.shape, f32), True, 0.125, stream=0)),
+        ("workspace", lambda: fa.fa_bwd(q, k, k, q, q, lse, q, k, k, other((64,), u8), True,
+                                        0.125, stream=0)),
+        ("dk", lambda: fa.fa_bwd_dkdv(q, k, k, q, other(k.shape, bf), k, ws, True, 0.125,
+                                      stream=0)),
+        ("workspace", lambda: fa.fa_fwd_fp8(other((64,), u8), T((B, H, N, 128), bf), lse, Hkv,
+                                            True, 0.125, stream=0)),
+    ]
+    for name, call in cases:
+        with pytest.raises(ValueError, match=rf"^{name} is on cuda:1 but the current device"):
+            call()
+    assert fa.fa_kernel_launches() == before

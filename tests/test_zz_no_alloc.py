@@ -58,21 +58,40 @@ def test_sizes_beyond_the_array_are_rejected():
 def test_static_scratch_matches_fa_bwd_on_two_calls_in_a_row():
     """Two calls in a row (different shapes, so the second sees what the first
     left in the shared array) give fa_bwd's dQ, dK, dV within the gradient
-    tolerance of the parity tests."""
+    tolerance of the parity tests.  Each call launches exactly its three
+    kernels and leaves device memory as it was: neither PyTorch's reserve nor
+    the driver's free bytes move (measured after a first round of both shapes,
+    so that the lazy loading of the kernels' code is not counted)."""
     L = _lib()
     dev = torch.device("cuda:0")
     cases = [
         Workload(name="noalloc_a", B=1, H=4, Hkv=2, N=333, d=128, causal=True, seed=71),
         Workload(name="noalloc_b", B=2, H=2, Hkv=2, N=512, d=64, causal=False, seed=72),
     ]
+    prepared = []
     for w in cases:
         assert L.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d) <= SCRATCH_BYTES
         q, k, v, do = (t.to(dev) for t in make_inputs(w))
         o, lse = fa.attention(q, k, v, causal=w.causal, scale=w.scale)
         ref = fa.attention_backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale)
         out = [torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)]
+        prepared.append((w, q, k, v, o, do, lse, ref, out))
+    torch.cuda.synchronize()
+    for w, q, k, v, o, do, lse, ref, out in prepared:          # warm-up round
+        assert _call(L, w, q, k, v, o, do, lse, *out) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == fa.FA_OK
+    for w, q, k, v, o, do, lse, ref, out in prepared:          # checked round
+        for t in out:
+            t.fill_(float("nan"))
+        torch.cuda.synchronize()
+        reserved, (free, _) = torch.cuda.memory_reserved(dev), torch.cuda.mem_get_info(dev)
+        launches = fa.fa_kernel_launches()
         assert _call(L, w, q, k, v, o, do, lse, *out) == fa.FA_OK
         torch.cuda.synchronize()
+        assert fa.fa_kernel_launches() - launches == 3, w.name
+        assert torch.cuda.memory_reserved(dev) == reserved, w.name
+        assert torch.cuda.mem_get_info(dev)[0] == free, w.name
         assert fa.fa_device_status() == fa.FA_OK
         for name, a, b in zip(("dq", "dk", "dv"), out, ref):
             assert torch.isfinite(a.float()).all(), name
