@@ -3,10 +3,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl reference]
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-fa_fwd (online-softmax forward), fa_bwd_preprocess (D, lse2, zeroed dQ
-accumulator), fa_bwd_dkdv (recompute, dK/dV, dQ reduction) and
-fa_bwd_dq_convert, all on the current CUDA stream.  FLOPs per step use the
+One step = one pass of the whole hot path over one batch of synthetic input,
+as a training step makes it: fa_fwd_train (the online-softmax forward, whose
+epilogue also writes the backward's -LSE table and zeroes its dQ accumulator)
+then fa_bwd_train (D = rowsum(dO o O), the dK/dV kernel with the dQ reduction,
+the dQ conversion), four kernel launches on the current CUDA stream.  The sliding-window line runs fa_fwd_window + fa_bwd_window.  FLOPs per step use the
 headline count: forward 4*B*H*N^2*d (halved under the causal mask) and
 forward+backward 2.5x that.
 
@@ -490,34 +491,53 @@ def run_native(args, w):
     work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    # The step's kernels in order; `ev` (instrumented loop only) receives an
-    # event after each kernel so that each kernel's own time can be read.
-    def step(ev=None):
-        if precise:
-            fa.fa_fwd_precise(qd, kd, vd, o, lse, w.causal, w.scale, stream)
-        elif w.window:
-            fa.fa_fwd_window(qd, kd, vd, o, lse, w.window, w.scale, stream)
-        else:
-            fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        if fwd_only:
-            return
-        if precise:
-            fa.fa_bwd_preprocess_precise(o, dod, lse, work, Hkv, stream)
-        else:
-            fa.fa_bwd_preprocess(o, dod, lse, work, Hkv, stream)
-        if ev is not None:
-            ev[2].record(stream)
+    # One training step through the public calls: the training forward (it
+    # also prepares the backward's workspace) and its backward; the sliding
+    # window keeps fa_fwd_window + fa_bwd_window.  step_inst() runs the same
+    # kernels through the stage entry points with an event after each, for
+    # per-kernel times (instrumented loop only).
+    def run_step(q_, k_, v_, do_, o_, l_, dq_, dk_, dv_):
         if w.window:
+            fa.fa_fwd_window(q_, k_, v_, o_, l_, w.window, w.scale, stream)
+            if not fwd_only:
+                fa.fa_bwd_window(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.window, w.scale,
+                                 stream)
+            return
+        if fwd_only:
+            if precise:
+                fa.fa_fwd_precise(q_, k_, v_, o_, l_, w.causal, w.scale, stream)
+            else:
+                fa.fa_fwd(q_, k_, v_, o_, l_, w.causal, w.scale, stream)
+            return
+        fa.fa_fwd_train(q_, k_, v_, o_, l_, work, w.causal, w.scale, stream)
+        fa.fa_bwd_train(q_, k_, v_, o_, do_, dq_, dk_, dv_, work, w.causal, w.scale, stream)
+
+    def step():
+        run_step(qd, kd, vd, dod, o, lse, dq, dk, dv)
+
+    def step_inst(ev):
+        if fwd_only:
+            step()
+            ev[1].record(stream)
+            return
+        if w.window:
+            fa.fa_fwd_window(qd, kd, vd, o, lse, w.window, w.scale, stream)
+            ev[1].record(stream)
+            fa.fa_bwd_preprocess(o, dod, lse, work, Hkv, stream)
+            ev[2].record(stream)
             fa.fa_bwd_dkdv_window(qd, kd, vd, dod, dk, dv, work, w.window, w.scale, stream)
-        else:
-            fa.fa_bwd_dkdv(qd, kd, vd, dod, dk, dv, work, w.causal, w.scale, stream)
-        if ev is not None:
             ev[3].record(stream)
-        fa.fa_bwd_dq_convert(work, dq, Hkv, w.scale, stream)
-        if ev is not None:
+            fa.fa_bwd_dq_convert(work, dq, Hkv, w.scale, stream)
             ev[4].record(stream)
+            return
+        fa.fa_fwd_train(qd, kd, vd, o, lse, work, w.causal, w.scale, stream)
+        ev[1].record(stream)
+        fa.fa_bwd_preprocess_train(o, dod, work, Hkv, stream)
+        ev[2].record(stream)
+        fa.fa_bwd_dkdv(qd, kd, vd, dod, dk, dv, work, w.causal, w.scale, stream)
+        ev[3].record(stream)
+        fa.fa_bwd_dq_convert(work, dq, Hkv, w.scale, stream)
+        ev[4].record(stream)
 
     def timed(fn, n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -565,10 +585,12 @@ def run_native(args, w):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_inst)]
     for e in evs:
         e[0].record(stream)
-        step(e)
+        step_inst(e)
     torch.cuda.synchronize()
-    names = ["fa_fwd"] if fwd_only else ["fa_fwd", "fa_bwd_preprocess", "fa_bwd_dkdv",
-                                         "fa_bwd_dq_convert"]
+    if fwd_only:
+        names = ["fa_fwd"]
+    else:
+        names = ["fa_fwd", "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert"]
     kern_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
                for i, n in enumerate(names)}
     inst_ms = statistics.mean(e[0].elapsed_time(e[len(names)]) for e in evs)
@@ -594,6 +616,9 @@ def run_native(args, w):
                 "frac_of_sustained_peak": ach / peaks["bf16_tflops_sustained"],
                 "kernel_times": {"source": f"separate instrumented loop of {n_inst} steps "
                                            f"(events between kernels), after the timed region",
+                                 "kernels": ("fa_fwd = fa_fwd_train (forward + backward "
+                                             "workspace), fa_bwd_preprocess = -D only"
+                                             if not (fwd_only or w.window) else "as named"),
                                  "ms_per_step_instrumented": inst_ms,
                                  "ms": kern_ms,
                                  "share": {n: t / inst_ms for n, t in kern_ms.items()}},
@@ -622,20 +647,7 @@ def run_native(args, w):
                 ((qd, hq), (kd, hk), (vd, hv), (dod, hdo))
             for dst, src_ in ins:
                 dst.copy_(src_, non_blocking=True)
-            if precise:
-                fa.fa_fwd_precise(qd, kd, vd, o, lse, w.causal, w.scale, stream)
-            elif w.window:
-                fa.fa_fwd_window(qd, kd, vd, o, lse, w.window, w.scale, stream)
-            else:
-                fa.fa_fwd(qd, kd, vd, o, lse, w.causal, w.scale, stream)
-            if not fwd_only and w.window:
-                fa.fa_bwd_window(qd, kd, vd, o, dod, lse, dq, dk, dv, work, w.window, w.scale,
-                                 stream)
-            elif not fwd_only and precise:
-                fa.fa_bwd_precise(qd, kd, vd, o, dod, lse, dq, dk, dv, work, w.causal, w.scale,
-                                  stream)
-            elif not fwd_only:
-                fa.fa_bwd(qd, kd, vd, o, dod, lse, dq, dk, dv, work, w.causal, w.scale, stream)
+            step()
             for dst, src_ in zip(outs_h, (o, lse, dq, dk, dv)):
                 dst.copy_(src_, non_blocking=True)
 
@@ -666,22 +678,7 @@ def run_native(args, w):
         ev = {k_: [torch.cuda.Event(), torch.cuda.Event()] for k_ in ("in", "comp", "out")}
 
         def compute(slot):
-            q_, k_, v_, do_ = dev_in[slot]
-            o_, l_, dq_, dk_, dv_ = dev_out[slot]
-            if precise:
-                fa.fa_fwd_precise(q_, k_, v_, o_, l_, w.causal, w.scale, stream)
-            elif w.window:
-                fa.fa_fwd_window(q_, k_, v_, o_, l_, w.window, w.scale, stream)
-            else:
-                fa.fa_fwd(q_, k_, v_, o_, l_, w.causal, w.scale, stream)
-            if not fwd_only and w.window:
-                fa.fa_bwd_window(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.window, w.scale,
-                                 stream)
-            elif not fwd_only and precise:
-                fa.fa_bwd_precise(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.causal,
-                                  w.scale, stream)
-            elif not fwd_only:
-                fa.fa_bwd(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.causal, w.scale, stream)
+            run_step(*dev_in[slot], *dev_out[slot])
 
         def pipelined(n):
             for k_ in range(n):

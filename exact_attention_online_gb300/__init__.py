@@ -32,7 +32,8 @@ __all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_p
            "attention_window_backward", "fa_fwd_varlen", "fa_bwd_varlen",
            "fa_bwd_varlen_workspace_size", "attention_varlen", "attention_varlen_backward",
            "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8", "attention_fp8",
-           "fa_fwd_decode_workspace_size", "fa_fwd_decode", "attention_decode"]
+           "fa_fwd_decode_workspace_size", "fa_fwd_decode", "attention_decode",
+           "fa_fwd_train", "fa_bwd_train", "fa_bwd_preprocess_train"]
 
 
 class FAError(RuntimeError):
@@ -224,6 +225,55 @@ def fa_bwd_precise(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal: bool, s
                                 _bf16(dk, "dk", ks), _bf16(dv, "dv", ks), wp, wb, B, H, Hkv, N, d,
                                 int(bool(causal)), float(scale), _stream(stream)),
            "fa_bwd_precise")
+
+
+def fa_fwd_train(q, k, v, o, lse, workspace, causal: bool, scale: float, stream=None) -> None:
+    """fa_fwd, plus the backward's workspace prepared for fa_bwd_train; o is
+    bf16, or fp32 (the precise forward)."""
+    B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
+    wp, wb = _ws(workspace)
+    import torch
+    if o.dtype == torch.float32:
+        fn, op, name = lib().fa_fwd_train_precise, _f32(o, "o", qs), "fa_fwd_train_precise"
+    else:
+        fn, op, name = lib().fa_fwd_train, _bf16(o, "o", qs), "fa_fwd_train"
+    _check(fn(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), op, _f32(lse, "lse", ls), wp, wb,
+              B, H, Hkv, N, d, int(bool(causal)), float(scale), _stream(stream)), name)
+
+
+def fa_bwd_train(q, k, v, o, dout, dq, dk, dv, workspace, causal: bool, scale: float,
+                 stream=None) -> None:
+    """The backward of fa_fwd_train, on the workspace it prepared; o is bf16 or
+    fp32 as that forward wrote it."""
+    B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
+    wp, wb = _ws(workspace)
+    import torch
+    if o.dtype == torch.float32:
+        fn, op, name = lib().fa_bwd_train_precise, _f32(o, "o", qs), "fa_bwd_train_precise"
+    else:
+        fn, op, name = lib().fa_bwd_train, _bf16(o, "o", qs), "fa_bwd_train"
+    _check(fn(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), op, _bf16(dout, "dout", qs),
+              _bf16(dq, "dq", qs), _bf16(dk, "dk", ks), _bf16(dv, "dv", ks), wp, wb,
+              B, H, Hkv, N, d, int(bool(causal)), float(scale), _stream(stream)), name)
+
+
+def fa_bwd_preprocess_train(o, dout, workspace, Hkv: int, stream=None) -> None:
+    """Stage 1 of fa_bwd_train: -D into the workspace fa_fwd_train prepared (o
+    bf16, or fp32 from the precise forward)."""
+    import torch
+    if o.dim() != 4:
+        raise ValueError("o must be 4-D [B, H, N, d]")
+    B, H, N, d = o.shape
+    wp, wb = _ws(workspace)
+    if o.dtype == torch.float32:
+        fn, op, name = (lib().fa_bwd_preprocess_train_precise, _f32(o, "o"),
+                        "fa_bwd_preprocess_train_precise")
+    else:
+        fn, op, name = lib().fa_bwd_preprocess_train, _bf16(o, "o"), "fa_bwd_preprocess_train"
+    _check(fn(op, _bf16(dout, "dout", (B, H, N, d)), wp, wb, B, H, int(Hkv), N, d,
+              _stream(stream)), name)
 
 
 def fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, workspace, window: int, scale: float,

@@ -99,6 +99,20 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_bwd_precise.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f,
                                  vp]
     L.fa_bwd_precise.restype = i
+    # training pair: forward that prepares the backward's workspace, and that backward
+    L.fa_fwd_train.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_train.restype = i
+    L.fa_fwd_train_precise.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_train_precise.restype = i
+    L.fa_bwd_train.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
+    L.fa_bwd_train.restype = i
+    L.fa_bwd_train_precise.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i,
+                                       f, vp]
+    L.fa_bwd_train_precise.restype = i
+    L.fa_bwd_preprocess_train.argtypes = [vp, vp, vp, sz, i, i, i, i, i, vp]
+    L.fa_bwd_preprocess_train.restype = i
+    L.fa_bwd_preprocess_train_precise.argtypes = [vp, vp, vp, sz, i, i, i, i, i, vp]
+    L.fa_bwd_preprocess_train_precise.restype = i
     L.fa_bwd_preprocess.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
     L.fa_bwd_preprocess.restype = i
     L.fa_bwd_preprocess_precise.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
@@ -156,4 +170,5 @@ EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bw
            "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8",
            "fa_fwd_decode_workspace_size", "fa_fwd_decode", "fa_fwd_window", "fa_bwd_window",
            "fa_bwd_dkdv_window", "fa_fwd_varlen", "fa_bwd_varlen_workspace_size",
-           "fa_bwd_varlen"]
+           "fa_bwd_varlen", "fa_fwd_train", "fa_fwd_train_precise", "fa_bwd_train",
+           "fa_bwd_train_precise", "fa_bwd_preprocess_train", "fa_bwd_preprocess_train_precise"]

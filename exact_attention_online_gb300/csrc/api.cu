@@ -359,6 +359,102 @@ fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void*
                     Hkv, N, d, 1, scale, stream, window);
 }
 
+static fa_status fwd_train_impl(const void* q, const void* k, const void* v, void* o,
+                                bool precise, float* lse, void* workspace,
+                                size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                                int causal, float scale, fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(lse)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    const BwdWorkspace ws = bwd_workspace_carve(workspace, s);
+    return from_cuda(launch_fwd(s, q, k, v, o, lse, precise, g_status_ptr[dev],
+                                (cudaStream_t)stream, &ws));
+}
+
+fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, float* lse,
+                       void* workspace, size_t workspace_bytes, int B, int H, int Hkv, int N,
+                       int d, int causal, float scale, fa_stream_t stream) {
+    return fwd_train_impl(q, k, v, o, false, lse, workspace, workspace_bytes, B, H, Hkv, N, d,
+                          causal, scale, stream);
+}
+
+fa_status fa_fwd_train_precise(const void* q, const void* k, const void* v, float* o,
+                               float* lse, void* workspace, size_t workspace_bytes, int B,
+                               int H, int Hkv, int N, int d, int causal, float scale,
+                               fa_stream_t stream) {
+    return fwd_train_impl(q, k, v, o, true, lse, workspace, workspace_bytes, B, H, Hkv, N, d,
+                          causal, scale, stream);
+}
+
+static fa_status bwd_train_impl(const void* q, const void* k, const void* v, const void* o,
+                                bool o_f32, const void* dout, void* dq, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                                int N, int d, int causal, float scale, fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(dout),
+                                check_ptr(dq), check_ptr(dk), check_ptr(dv)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    const BwdWorkspace ws = bwd_workspace_carve(workspace, s);
+    cudaStream_t cs = (cudaStream_t)stream;
+    // -D only (the training forward wrote the -LSE table and zeroed the
+    // accumulator), then dK/dV and the dQ conversion.
+    cudaError_t e = launch_bwd_preprocess(s, o, o_f32, dout, nullptr, ws, g_status_ptr[dev], cs,
+                                          /*full=*/false);
+    if (e == cudaSuccess) e = launch_bwd_dkdv(s, q, k, v, dout, dk, dv, ws, g_status_ptr[dev], cs);
+    if (e == cudaSuccess) e = launch_bwd_dq_convert(s, ws, dq, cs);
+    return from_cuda(e);
+}
+
+fa_status fa_bwd_train(const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, int B, int H, int Hkv, int N, int d, int causal,
+                       float scale, fa_stream_t stream) {
+    return bwd_train_impl(q, k, v, o, false, dout, dq, dk, dv, workspace, workspace_bytes, B, H,
+                          Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_bwd_train_precise(const void* q, const void* k, const void* v, const float* o,
+                               const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                               size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                               int causal, float scale, fa_stream_t stream) {
+    return bwd_train_impl(q, k, v, o, true, dout, dq, dk, dv, workspace, workspace_bytes, B, H,
+                          Hkv, N, d, causal, scale, stream);
+}
+
+static fa_status pre_train_impl(const void* o, bool o_f32, const void* dout, void* workspace,
+                                size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                                fa_stream_t stream) {
+    const Shape s{B, H, Hkv, N, d, 0, 1.0f};
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_ptr(o), check_ptr(dout)});
+    if (st != FA_OK) return st;
+    if ((st = check_workspace(workspace, workspace_bytes, s)) != FA_OK) return st;
+    int dev;
+    if ((st = device_ready(&dev)) != FA_OK) return st;
+    return from_cuda(launch_bwd_preprocess(s, o, o_f32, dout, nullptr,
+                                           bwd_workspace_carve(workspace, s), g_status_ptr[dev],
+                                           (cudaStream_t)stream, /*full=*/false));
+}
+
+fa_status fa_bwd_preprocess_train(const void* o, const void* dout, void* workspace,
+                                  size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                                  fa_stream_t stream) {
+    return pre_train_impl(o, false, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream);
+}
+
+fa_status fa_bwd_preprocess_train_precise(const float* o, const void* dout, void* workspace,
+                                          size_t workspace_bytes, int B, int H, int Hkv, int N,
+                                          int d, fa_stream_t stream) {
+    return pre_train_impl(o, true, dout, workspace, workspace_bytes, B, H, Hkv, N, d, stream);
+}
+
 static fa_status check_varlen(const int* cu_seqlens, int B, int max_seqlen, int total, int H,
                               int Hkv, int d) {
     fa_status st = check_shape(B, H, Hkv, max_seqlen, d);

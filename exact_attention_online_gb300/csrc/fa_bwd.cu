@@ -19,7 +19,9 @@
 //               the fp32 accumulator by one bulk (d=128) or tensor (d=64)
 //               reduce per query block (FlashAttention-2 review 2: the
 //               query-derivative update is shared between the workers of one
-//               query block).
+//               query block).  At d=128 K_j is also copied into tensor memory
+//               once per CTA (the last 64 columns), so S^T = K_j Q_i^T is a TS
+//               MMA that reads only Q_i from shared memory.
 //   dq_convert  dQ = bf16(scale * accumulator).
 //
 // Roles in dkdv: warps 0-7 compute (one key row per thread, two warps per row
@@ -79,6 +81,11 @@ struct BwdCfg {
     // TMEM columns
     static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D, kColDP = 2 * D + kBR,
                               kColDQ = 2 * D + 2 * kBR;
+    // d = 128: K_j as bf16 pairs (128 key lanes x 64 columns) in the last 64
+    // columns, the A operand of S^T = K_j Q_i^T read from tensor memory
+    // instead of shared memory.
+    static constexpr uint32_t kColKT = kColDQ + 64;
+    static constexpr bool kKInTmem = (D == 128);
 };
 
 struct BwdParams {
@@ -118,7 +125,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_kv, bar_full[2], bar_empty[2], bar_s, bar_dp, bar_p, bar_ds,
-        bar_dq_full, bar_dq_free, bar_done;
+        bar_dq_full, bar_dq_free, bar_done, bar_ktm;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     const WaitCtx wc{p.status, &abort_sh};
@@ -216,6 +223,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(&bar_dq_full, 1);
         mbar_init(&bar_dq_free, kReadoutThreads);
         mbar_init(&bar_done, kTwoIssuers ? 2 : 1);   // one arrival per MMA issuer
+        mbar_init(&bar_ktm, kComputeThreads);        // K_j copied into tensor memory
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -240,11 +248,34 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int cb = hf * HALF;                    // first query column of this warp
         const float c = p.scale_log2;
         bool ok = n_it > 0;
+        if (Cfg::kKInTmem && ok) {
+            // K_j -> tensor memory: this thread's key row, the 64 head-dim
+            // columns of its half (one 128-byte swizzled row of chunk hf),
+            // as 32 bf16 pairs; the S^T MMAs take it from there.
+            if (!fa_wait_warp(&bar_kv, 0, 64, wc)) {
+                ok = false;
+            } else {
+                const uint8_t* rowp = sK + hf * (kBN * 128) + rl * 128;
+                uint32_t kw[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((u ^ (rl & 7)) * 16));
+                    kw[4 * u + 0] = x.x;
+                    kw[4 * u + 1] = x.y;
+                    kw[4 * u + 2] = x.z;
+                    kw[4 * u + 3] = x.w;
+                }
+                tmem_st32(lane_addr + Cfg::kColKT + hf * 32, kw);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bar_ktm);
+            }
+        }
         for (int it = 0; ok && it < n_it; ++it) {
-            const int st = it & 1;
             const int i = i_start + it % n_i;
-            if (!fa_wait_warp(&bar_full[st], (it >> 1) & 1, 60, wc) ||
-                !fa_wait_warp(&bar_s, it & 1, 61, wc)) { ok = false; break; }
+            // (no wait for the Q_i / dO_i stage: these warps read neither, and
+            // S^T(i) completing implies the stage has landed)
+            if (!fa_wait_warp(&bar_s, it & 1, 61, wc)) { ok = false; break; }
             tc_fence_after();
             const int q0 = i * BR;
             const bool need_mask = (CAUSAL && (q0 < jblk * kBN + kBN - 1 ||
@@ -369,7 +400,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             const int hq = g * p.G + it / n_i;
             const int i = i_start + it % n_i;
             const int bh = b * p.H + hq;
-            if (!fa_wait_warp(&bar_dq_full, it & 1, 70, wc)) { ok = false; break; }
+            // The four read-out warps leave together (they meet at named
+            // barriers below), so a failed wait in one of them stops all.
+            const bool w_ok = fa_wait_warp(&bar_dq_full, it & 1, 70, wc);
+            if (named_bar_or(1, kReadoutThreads, !w_ok)) { ok = false; break; }
             tc_fence_after();
             uint32_t r0[32], r1[32];
             tmem_ld32(lane_addr + Cfg::kColDQ, r0);
@@ -477,9 +511,14 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 auto issue_s = [&](int st) {      // S^T = K_j Q_i^T - LSE log2(e) / c
                     const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
-                               qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        if constexpr (Cfg::kKInTmem)
+                            mma_ts(tmem + Cfg::kColS, tmem + Cfg::kColKT + kk * 8,
+                                   qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                        else
+                            mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
+                                   qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                    }
                     mma_ss(tmem + Cfg::kColS, onesd, sdesc_plain(sext + 2 * st * Cfg::kExtBytes,
                                                                  128, 256), id_s, 1u);
                     mma_commit(&bar_s);
@@ -494,7 +533,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                            sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s, 1u);
                     mma_commit(&bar_dp);
                 };
-                bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
+                bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc) &&
+                          (!Cfg::kKInTmem || fa_wait(&bar_ktm, 0, 57, wc));
                 if (ok) {
                     tc_fence_after();
                     issue_s(0);
@@ -574,9 +614,15 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             auto issue_s = [&](int st) {      // S^T = K_j Q_i^T - LSE log2(e) / c
                 const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
-                           qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    // S^T: A = K_j from tensor memory at d = 128, else shared memory
+                    if constexpr (Cfg::kKInTmem)
+                        mma_ts(tmem + Cfg::kColS, tmem + Cfg::kColKT + kk * 8,
+                               qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                    else
+                        mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
+                               qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                }
                 mma_ss(tmem + Cfg::kColS, onesd, sdesc_plain(sext + 2 * st * Cfg::kExtBytes, 128,
                                                              256), id_s, 1u);
                 mma_commit(&bar_s);
@@ -591,7 +637,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                        sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s, 1u);
                 mma_commit(&bar_dp);
             };
-            bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc);
+            bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc) &&
+                      (!(Cfg::kKInTmem && half_a) || fa_wait(&bar_ktm, 0, 57, wc));
             if (ok) {
                 tc_fence_after();
                 if (half_a) issue_s(0);
@@ -700,8 +747,10 @@ __device__ __forceinline__ int seq_row(const int* __restrict__ cu, long long bh,
 // stored as unswizzled K-major core matrices (row group g = r / 8, K half kc:
 // 16 bytes at ((2 g + kc) * 8 + r % 8) * 16).  D / 8 lanes per row (16-byte
 // loads), 256 / D rows per warp, grid-stride over the B*H*Np rows.  O is
-// bf16, or fp32 when it comes from the precise forward.
-template <int D, typename OT>
+// bf16, or fp32 when it comes from the precise forward.  FULL = false (after
+// a training forward, which wrote the -LSE table and zeroed the accumulator):
+// the -D table only.
+template <int D, typename OT, bool FULL>
 __global__ void __launch_bounds__(256)
 fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, uint16_t* __restrict__ lse_ext,
@@ -721,7 +770,7 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
         const int len = in ? seq_row(cu, bh, H, N, seq_rows, base) : 0;
         const bool valid = in && i < len;
         float x = -1e30f;
-        if (valid) x = -lse[base + i] * 1.4426950408889634f;
+        if (FULL && valid) x = -lse[base + i] * 1.4426950408889634f;
         float acc = 0.0f;
         if (valid) {
             const long long src = (base + i) * D + sl * 8;
@@ -752,25 +801,17 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
         }
 #pragma unroll
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (in && sl < 2) {
-            // lane 0 of the row: the lse_ext row, lane 1: the d_ext row
-            const float v = (sl == 0) ? x : -acc;
+        if (in && sl == 0 && FULL) write_lse_ext_row(lse_ext, r, x);   // lane 0: -LSE row
+        if (in && sl == 1) {
+            // lane 1 of the row: the d_ext row, -D in columns 9-11
+            const float v = -acc;
             const float h = bf16_round(v), m = bf16_round(v - h), l = bf16_round(v - h - m);
-            uint4 w0, w1;
-            if (sl == 0) {
-                w0 = make_uint4(pack_bf16x2(h, m), pack_bf16x2(l, h), pack_bf16x2(m, l),
-                                pack_bf16x2(h, m));
-                w1 = make_uint4(pack_bf16x2(l, 0.0f), 0u, 0u, 0u);
-            } else {
-                w0 = make_uint4(0u, 0u, 0u, 0u);
-                w1 = make_uint4(pack_bf16x2(0.0f, h), pack_bf16x2(m, l), 0u, 0u);
-            }
-            uint16_t* row = (sl == 0 ? lse_ext : d_ext) +
-                            ((r >> 3) * 2 * 8 + (r & 7)) * 8;   // (2 g + 0) * 64 + (r % 8) * 8
-            *reinterpret_cast<uint4*>(row) = w0;
-            *reinterpret_cast<uint4*>(row + 64) = w1;            // K half 1: + 8 rows x 8
+            uint16_t* row = d_ext + ((r >> 3) * 2 * 8 + (r & 7)) * 8;   // (2 g) * 64 + (r % 8) * 8
+            *reinterpret_cast<uint4*>(row) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(row + 64) =                       // K half 1: + 8 rows x 8
+                make_uint4(pack_bf16x2(0.0f, h), pack_bf16x2(m, l), 0u, 0u);
         }
-        if (in) {
+        if (FULL && in) {
             float4* z = reinterpret_cast<float4*>(dq_acc + r * D) + sl * 2;
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -879,7 +920,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 
 cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, const void* dout,
                                   const float* lse, const BwdWorkspace& ws, DeviceStatus* status,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, bool full) {
     (void)status;
     const int Np = padded_rows(s.N);
     const long long rows = (long long)s.B * s.H * Np;
@@ -887,28 +928,25 @@ cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, con
     const int grid = grid_for(rows, 8 * (256 / s.d));   // 8 warps a block, 256/d rows a warp
     count_launch();
     auto* d_ = static_cast<const __nv_bfloat16*>(dout);
+    auto go = [&](auto kern, auto* o_) {
+        kern<<<grid, 256, 0, stream>>>(o_, d_, lse, ws.lse_ext, ws.d_ext, ws.dq_acc, s.N, Np, rows,
+                                       s.cu_seqlens, s.H, seq_rows);
+        return cudaGetLastError();
+    };
     auto* ob = static_cast<const __nv_bfloat16*>(o);
     auto* of = static_cast<const float*>(o);
     if (s.d == 128) {
         if (o_f32)
-            fa_bwd_pre_kernel<128, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse_ext, ws.d_ext,
-                                                                    ws.dq_acc, s.N, Np, rows,
-                                                                    s.cu_seqlens, s.H, seq_rows);
-        else
-            fa_bwd_pre_kernel<128, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-                ob, d_, lse, ws.lse_ext, ws.d_ext, ws.dq_acc, s.N, Np, rows,
-                                                                    s.cu_seqlens, s.H, seq_rows);
-    } else {
-        if (o_f32)
-            fa_bwd_pre_kernel<64, float><<<grid, 256, 0, stream>>>(of, d_, lse, ws.lse_ext, ws.d_ext,
-                                                                   ws.dq_acc, s.N, Np, rows,
-                                                                    s.cu_seqlens, s.H, seq_rows);
-        else
-            fa_bwd_pre_kernel<64, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-                ob, d_, lse, ws.lse_ext, ws.d_ext, ws.dq_acc, s.N, Np, rows,
-                                                                    s.cu_seqlens, s.H, seq_rows);
+            return full ? go(fa_bwd_pre_kernel<128, float, true>, of)
+                        : go(fa_bwd_pre_kernel<128, float, false>, of);
+        return full ? go(fa_bwd_pre_kernel<128, __nv_bfloat16, true>, ob)
+                    : go(fa_bwd_pre_kernel<128, __nv_bfloat16, false>, ob);
     }
-    return cudaGetLastError();
+    if (o_f32)
+        return full ? go(fa_bwd_pre_kernel<64, float, true>, of)
+                    : go(fa_bwd_pre_kernel<64, float, false>, of);
+    return full ? go(fa_bwd_pre_kernel<64, __nv_bfloat16, true>, ob)
+                : go(fa_bwd_pre_kernel<64, __nv_bfloat16, false>, ob);
 }
 
 cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const void* v,

@@ -103,6 +103,12 @@ struct FwdParams {
     void* o;                          // bf16, or fp32 in the precise variant
     float* lse;
     DeviceStatus* status;
+    // Training forward (dense batches): the backward workspace rows this
+    // forward prepares, Np (= N rounded up to 128) rows per (batch, head):
+    // the -LSE table row and a zeroed dQ accumulator row.  nullptr = none.
+    uint16_t* lse_ext;
+    float* dq_acc;
+    int Np;
 };
 
 // Work item (query-block pair, batch*head) -> coordinates.  Under the causal
@@ -443,6 +449,23 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 p.lse[(size_t)wt.q_z * p.rows + wt.tok0 + row] =
                     (l > 0.0f) ? (m2 + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
             }
+            if (p.lse_ext != nullptr && row0 < p.Np) {
+                // Training forward: this tile's rows of the backward workspace
+                // (a tile lies wholly below Np or wholly past it: both are
+                // multiples of 128).  The -LSE row as the preprocess would
+                // write it from the stored LSE (padding rows past N get -1e30,
+                // so P = 0 there), and the tile's 128 fp32 dQ accumulator rows
+                // zeroed, contiguous in memory: consecutive threads write
+                // consecutive 16-byte pieces, so each warp store is coalesced.
+                const long long r0 = (long long)wt.bh * p.Np + row0;
+                const float lse_row =
+                    (l > 0.0f) ? (m2 + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+                write_lse_ext_row(p.lse_ext, r0 + rl,
+                                  valid ? -lse_row * 1.4426950408889634f : -1e30f);
+                float4* z = reinterpret_cast<float4*>(p.dq_acc + r0 * D);
+#pragma unroll
+                for (int c4 = 0; c4 < D / 4; ++c4) z[c4 * kBM + rl] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
@@ -678,7 +701,8 @@ cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& tq, const CUtensorMa
 }  // namespace
 
 cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void* v, void* o,
-                       float* lse, bool precise, DeviceStatus* status, cudaStream_t stream) {
+                       float* lse, bool precise, DeviceStatus* status, cudaStream_t stream,
+                       const BwdWorkspace* train_ws) {
     // Dense: maps {d, N, B*H(kv)}.  Packed variable lengths: {d, total, H(kv)},
     // a sequence's rows addressed from its first row.
     const bool varlen = s.cu_seqlens != nullptr;
@@ -703,6 +727,14 @@ cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void*
     p.o = o;
     p.lse = lse;
     p.status = status;
+    p.lse_ext = nullptr;
+    p.dq_acc = nullptr;
+    p.Np = padded_rows(s.N);
+    if (train_ws) {   // dense batches only (packed ones keep the plain preprocess)
+        if (varlen) return cudaErrorInvalidValue;
+        p.lse_ext = train_ws->lse_ext;
+        p.dq_acc = train_ws->dq_acc;
+    }
     // Persistent: one CTA per SM (at most one work item per CTA when there
     // are fewer items than SMs).
     const int sms = device_sm_count() > 0 ? device_sm_count() : 148;

@@ -1,5 +1,5 @@
-// Internal launch interface between the C ABI (api.cu) and the kernel files.
-// Plain C++ (no CUDA device code), so every translation unit can include it.
+// Internal launch interface between the C ABI (api.cu) and the kernel files,
+// plus the few device helpers that two kernel files share.
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -56,15 +56,30 @@ struct BwdWorkspace {
     float* dq_acc;      // fp32 accumulator of dQ / scale
 };
 constexpr int kExtCols = 16;   // bf16 columns per row of an ext table
+
+// One row of the -LSE table: x = -LSE log2(e) (or -1e30 on a padded row)
+// split into three bf16 terms h + m + l (about 24 bits of x), written three
+// times into columns 0-8 of workspace row r; columns 9-15 are zero.
+__device__ __forceinline__ void write_lse_ext_row(uint16_t* lse_ext, long long r, float x) {
+    const float h = bf16_round(x), m = bf16_round(x - h), l = bf16_round(x - h - m);
+    uint16_t* row = lse_ext + ((r >> 3) * 2 * 8 + (r & 7)) * 8;   // (2 g + 0) * 64 + (r % 8) * 8
+    *reinterpret_cast<uint4*>(row) =
+        make_uint4(pack_bf16x2(h, m), pack_bf16x2(l, h), pack_bf16x2(m, l), pack_bf16x2(h, m));
+    *reinterpret_cast<uint4*>(row + 64) = make_uint4(pack_bf16x2(l, 0.0f), 0u, 0u, 0u);
+}
 size_t bwd_workspace_bytes(const Shape& s);
 BwdWorkspace bwd_workspace_carve(void* base, const Shape& s);
 
 // Launchers (return a cudaError_t from the launch).
+// launch_fwd: train_ws non-null = training forward, which also writes the
+// -LSE table and zeroes the dQ accumulator of that backward workspace.
 cudaError_t launch_fwd(const Shape& s, const void* q, const void* k, const void* v, void* o,
-                       float* lse, bool precise, DeviceStatus* status, cudaStream_t stream);
+                       float* lse, bool precise, DeviceStatus* status, cudaStream_t stream,
+                       const BwdWorkspace* train_ws = nullptr);
+// full = false: only -D (the rest was prepared by the training forward).
 cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, const void* dout,
                                   const float* lse, const BwdWorkspace& ws,
-                                  DeviceStatus* status, cudaStream_t stream);
+                                  DeviceStatus* status, cudaStream_t stream, bool full = true);
 cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const void* v,
                             const void* dout, void* dk, void* dv, const BwdWorkspace& ws,
                             DeviceStatus* status, cudaStream_t stream);

@@ -249,6 +249,57 @@ FA_API fa_status fa_bwd_dq_convert(const void* workspace, size_t workspace_bytes
                             fa_stream_t stream);
 
 /*
+ * Training pair: a forward that also prepares its backward, and that
+ * backward.  The backward of this library starts with a pass that writes a
+ * -LSE table and zeroes the fp32 dQ accumulator in the workspace (stage 1);
+ * a training step runs the forward and the backward back to back, and
+ * fa_fwd_train writes those rows from its own epilogue, where LSE is
+ * computed, so the backward's first pass only computes D = rowsum(dO o O).
+ * Splitting stage 1 this way is this library's; the pages describe the
+ * backward's inputs (O, dO, LSE), not this schedule.
+ *
+ * fa_fwd_train: fa_fwd() (same arguments, outputs and errors), plus
+ * `workspace` (>= fa_bwd_workspace_size(B, H, Hkv, N, d) bytes, 16-byte
+ * aligned, owned by the caller) prepared for fa_bwd_train().  One launch.
+ * fa_bwd_train: the backward of that forward.  q, k, v, o, dout as in
+ * fa_bwd(); the workspace must be the one the last fa_fwd_train() with the
+ * same shapes prepared, unchanged since (no lse argument: its -LSE table is
+ * in the workspace).  Same results as fa_bwd() on the lse that forward wrote.
+ * Three launches.  The _precise forms take and give the fp32 o of
+ * fa_fwd_precise().
+ */
+FA_API fa_status fa_fwd_train(const void* q, const void* k, const void* v, void* o, float* lse,
+                              void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                              int N, int d, int causal, float scale, fa_stream_t stream);
+FA_API fa_status fa_fwd_train_precise(const void* q, const void* k, const void* v, float* o,
+                                      float* lse, void* workspace, size_t workspace_bytes,
+                                      int B, int H, int Hkv, int N, int d, int causal,
+                                      float scale, fa_stream_t stream);
+FA_API fa_status fa_bwd_train(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                              int causal, float scale, fa_stream_t stream);
+FA_API fa_status fa_bwd_train_precise(const void* q, const void* k, const void* v,
+                                      const float* o, const void* dout, void* dq, void* dk,
+                                      void* dv, void* workspace, size_t workspace_bytes, int B,
+                                      int H, int Hkv, int N, int d, int causal, float scale,
+                                      fa_stream_t stream);
+
+/*
+ * Stage 1 of fa_bwd_train(), for callers that time or interleave the stages:
+ * -D into the workspace a training forward prepared (one launch; _precise:
+ * fp32 o).  fa_bwd_train() is fa_bwd_preprocess_train() + fa_bwd_dkdv() +
+ * fa_bwd_dq_convert().
+ */
+FA_API fa_status fa_bwd_preprocess_train(const void* o, const void* dout, void* workspace,
+                                         size_t workspace_bytes, int B, int H, int Hkv, int N,
+                                         int d, fa_stream_t stream);
+FA_API fa_status fa_bwd_preprocess_train_precise(const float* o, const void* dout,
+                                                 void* workspace, size_t workspace_bytes, int B,
+                                                 int H, int Hkv, int N, int d,
+                                                 fa_stream_t stream);
+
+/*
  * Backward without a workspace argument, for callers that cannot allocate
  * device memory (a runtime that owns all device memory in a fixed pool, a
  * latency-critical loop that must not risk the synchronisation cudaMalloc can

@@ -118,6 +118,26 @@ def test_stage_entry_points_validate(L):
         fa.FA_ERR_INVALID_ARG
 
 
+def test_training_entry_points_validate(L):
+    """The training pair and its stages reject bad arguments before any launch."""
+    before = fa.fa_kernel_launches()
+    ws = L.fa_bwd_workspace_size(1, 2, 1, 128, 64)
+    args = (1, 2, 1, 128, 64, 1, 0.125, None)
+    assert L.fa_fwd_train(A, A, A, A, A, A, 8, *args) == fa.FA_ERR_WORKSPACE
+    assert L.fa_fwd_train(A, A, A, A, 0, A, ws, *args) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_train_precise(A, A, A, MIS, A, A, ws, *args) == fa.FA_ERR_ALIGNMENT
+    assert L.fa_fwd_train(A, A, A, A, A, A, ws, 1, 2, 1, 128, 80, 1, 0.125, None) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert L.fa_bwd_train(A, A, A, A, A, A, A, A, 0, ws, *args) == fa.FA_ERR_WORKSPACE
+    assert L.fa_bwd_train(A, A, A, A, A, 0, A, A, A, ws, *args) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_bwd_train_precise(A, A, A, A, A, A, A, A, A, ws, 1, 2, 1, 128, 64, 1,
+                                  float("inf"), None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_bwd_preprocess_train(A, A, A, 8, 1, 2, 1, 128, 64, None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_bwd_preprocess_train_precise(0, A, A, ws, 1, 2, 1, 128, 64, None) == \
+        fa.FA_ERR_INVALID_ARG
+    assert fa.fa_kernel_launches() == before
+
+
 def test_python_binding_rejects_cpu_tensors():
     import torch
     q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)

@@ -1,13 +1,14 @@
-"""Backward parity: fa_bwd (preprocess, dK/dV kernel with dQ reduction, dQ
-conversion) on the GPU's own O and LSE, against the fp64 oracle's analytic
-gradients on the same seeded bf16 inputs.  dQ, dK, dV relative Frobenius error
-<= 2e-2 each."""
+"""Backward parity: fa_bwd (the preprocess, the dK/dV kernel with the dQ
+reduction, the dQ conversion) on the GPU's own O and LSE, and the
+training pair fa_fwd_train + fa_bwd_train, against the fp64 oracle on the same
+seeded bf16 inputs.  dQ, dK, dV relative Frobenius error <= 2e-2 each; O and
+LSE as in the forward tests."""
 import numpy as np
 import pytest
 import torch
 
 import exact_attention_online_gb300 as fa
-from _gpu import GRAD_REL_FRO, check_bwd_groups, f64, run_bwd, run_fwd, stress
+from _gpu import GRAD_REL_FRO, check_bwd_groups, check_fwd_heads, f64, run_bwd, run_fwd, stress
 from exact_attention_online_gb300.inputs import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -96,3 +97,109 @@ def test_bwd_full_size(name):
         assert torch.isfinite(t.float()).all()
     groups = [(0, 0)] if w.N >= 8192 else [(0, 0), (w.B - 1, w.Hkv - 1)]
     check_bwd_groups(q, k, v, do, dq, dk, dv, w.causal, w.scale, groups)
+
+
+def run_train_pair(w, q, k, v, do, precise):
+    """fa_fwd_train then fa_bwd_train on a workspace filled with NaN bytes first,
+    so that anything the training forward fails to prepare shows."""
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    ws = torch.full((fa.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d),), 0xFF,
+                    dtype=torch.uint8, device=dev)
+    o = torch.empty(qd.shape, dtype=torch.float32 if precise else torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    fa.fa_fwd_train(qd, kd, vd, o, lse, ws, w.causal, w.scale)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    fa.fa_bwd_train(qd, kd, vd, o, dod, dq, dk, dv, ws, w.causal, w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    return o.cpu(), lse.cpu(), dq.cpu(), dk.cpu(), dv.cpu()
+
+
+@pytest.mark.parametrize("precise", [False, True], ids=["bf16out", "precise"])
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_train_pair_small_full(w, precise):
+    """fa_fwd_train + fa_bwd_train: the same O, LSE and gradients as the oracle
+    (every head, every row)."""
+    q, k, v, do = make_inputs(w)
+    o, lse, dq, dk, dv = run_train_pair(w, q, k, v, do, precise)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    check_fwd_heads(q, k, v, o, lse, w.causal, w.scale, heads,
+                    bf16_bound=stress(w) and not precise)
+    groups = [(b, g) for b in range(w.B) for g in range(w.Hkv)]
+    check_bwd_groups(q, k, v, do, dq, dk, dv, w.causal, w.scale, groups)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_train_forward_prepares_the_workspace(d):
+    """The -LSE table fa_fwd_train writes is bit-identical to the one the
+    preprocess writes from the stored LSE (padding rows included), and the
+    dQ accumulator it leaves is all zeros."""
+    w = small("prep", 2, 3, 1, 300, d, True, 54)
+    q, k, v, do = make_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    n = fa.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d)
+    ws1 = torch.full((n,), 0xFF, dtype=torch.uint8, device=dev)
+    ws2 = torch.full((n,), 0x7F, dtype=torch.uint8, device=dev)
+    o, lse = torch.empty_like(qd), torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    fa.fa_fwd_train(qd, kd, vd, o, lse, ws1, True, w.scale)
+    fa.fa_bwd_preprocess(o, dod, lse, ws2, w.Hkv)
+    torch.cuda.synchronize()
+    rows = w.B * w.H * ((w.N + 127) // 128 * 128)
+    a256 = lambda x: (x + 255) // 256 * 256
+    ext = rows * 16 * 2
+    assert torch.equal(ws1[:ext], ws2[:ext])
+    acc0 = 2 * a256(ext)
+    acc = ws1[acc0:acc0 + rows * d * 4].view(torch.float32)
+    assert torch.count_nonzero(acc).item() == 0
+
+
+TRAIN_FULL = ["gpt_long", "gqa"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", TRAIN_FULL)
+def test_train_pair_full_size(name):
+    """The training pair the benchmark times, at full size (the stress workload
+    through the precise forms): O and LSE of sampled heads, and the gradients
+    of the first key/value group in full, against the oracle."""
+    w = WORKLOADS[name]
+    q, k, v, do = make_inputs(w)
+    o, lse, dq, dk, dv = run_train_pair(w, q, k, v, do, precise=stress(w))
+    for t in (o, dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    rows = list(range(0, w.N, 97)) + [w.N - 1]
+    check_fwd_heads(q, k, v, o, lse, w.causal, w.scale, [(0, 0), (w.B - 1, w.H - 1)],
+                    rows=rows)
+    check_bwd_groups(q, k, v, do, dq, dk, dv, w.causal, w.scale, [(0, 0)])
+
+
+def test_train_stages_equal_train_call():
+    """fa_bwd_train equals fa_bwd_preprocess_train + fa_bwd_dkdv +
+    fa_bwd_dq_convert, and both equal fa_bwd on the same forward (dK, dV
+    bit-equal; dQ up to the order of the fp32 reductions)."""
+    w = small("tstages", 2, 4, 2, 300, 128, True, 55)
+    q, k, v, do = make_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    n = fa.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d)
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    o, lse = torch.empty_like(qd), torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    outs = []
+    for staged in (False, True):
+        fa.fa_fwd_train(qd, kd, vd, o, lse, ws, True, w.scale)
+        g = [torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)]
+        if staged:
+            fa.fa_bwd_preprocess_train(o, dod, ws, w.Hkv)
+            fa.fa_bwd_dkdv(qd, kd, vd, dod, g[1], g[2], ws, True, w.scale)
+            fa.fa_bwd_dq_convert(ws, g[0], w.Hkv, w.scale)
+        else:
+            fa.fa_bwd_train(qd, kd, vd, o, dod, *g, ws, True, w.scale)
+        outs.append(g)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    ref = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=True, scale=w.scale)
+    for dq_, dk_, dv_ in outs:
+        assert torch.equal(dk_, ref[1]) and torch.equal(dv_, ref[2])
+        assert (dq_.float() - ref[0].float()).abs().max() <= 1e-2 * ref[0].float().abs().max()
