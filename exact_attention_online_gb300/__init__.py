@@ -366,25 +366,29 @@ def fa_fp8_buffer_size(B: int, H: int, Hkv: int, N: int, d: int) -> int:
     return int(lib().fa_fp8_buffer_size(B, H, Hkv, N, d))
 
 
-def fa_fp8_quantize(q, k, v, fp8_buf, stream=None) -> None:
-    """fp8_buf: a contiguous CUDA tensor of at least fa_fp8_buffer_size() bytes."""
+def fa_fp8_quantize(v, fp8_buf, H: int, stream=None) -> None:
+    """e4m3 codes (transposed) and block scales of v [B, Hkv, N, d] into fp8_buf,
+    a contiguous CUDA tensor of at least fa_fp8_buffer_size() bytes; H is the
+    number of query heads (checked against Hkv)."""
+    B, Hkv, N, d = _dims_of(v, "v")
+    bp, bb = _ws(fp8_buf)
+    _check(lib().fa_fp8_quantize(_bf16(v, "v"), bp, bb, B, int(H), Hkv, N, d, _stream(stream)),
+           "fa_fp8_quantize")
+
+
+def fa_fwd_fp8(q, k, fp8_buf, o, lse, causal: bool, scale: float, stream=None) -> None:
+    """S from the bf16 q, k; P V in e4m3 with V from fp8_buf; o: bf16 [B, H, N, d],
+    lse: fp32 [B, H, N]."""
     B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
     bp, bb = _ws(fp8_buf)
-    _check(lib().fa_fp8_quantize(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", (B, Hkv, N, d)),
-                                 bp, bb,
-                                 B, H, Hkv, N, d, _stream(stream)), "fa_fp8_quantize")
-
-
-def fa_fwd_fp8(fp8_buf, o, lse, Hkv: int, causal: bool, scale: float, stream=None) -> None:
-    """o: bf16 [B, H, N, d] (its shape gives B, H, N, d), lse: fp32 [B, H, N]."""
-    B, H, N, d = _dims_of(o, "o")
-    bp, bb = _ws(fp8_buf)
-    _check(lib().fa_fwd_fp8(bp, bb, _bf16(o, "o"), _f32(lse, "lse", (B, H, N)), B, H, Hkv, N, d,
-                            int(bool(causal)), float(scale), _stream(stream)), "fa_fwd_fp8")
+    _check(lib().fa_fwd_fp8(_bf16(q, "q"), _bf16(k, "k"), bp, bb, _bf16(o, "o", qs),
+                            _f32(lse, "lse", ls), B, H, Hkv, N, d, int(bool(causal)),
+                            float(scale), _stream(stream)), "fa_fwd_fp8")
 
 
 def attention_fp8(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """FP8 forward: quantize (into a new buffer) and attend; returns (O, LSE, buffer)."""
+    """FP8 forward: quantize V (into a new buffer) and attend; returns (O, LSE, buffer)."""
     import torch
     B, H, Hkv, N, d = _dims(q, k)
     if scale is None:
@@ -395,8 +399,8 @@ def attention_fp8(q, k, v, causal: bool = False, scale: float | None = None, str
     buf = torch.empty(n, dtype=torch.uint8, device=q.device)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fp8_quantize(q, k, v, buf, stream)
-    fa_fwd_fp8(buf, o, lse, Hkv, causal, scale, stream)
+    fa_fp8_quantize(v, buf, H, stream)
+    fa_fwd_fp8(q, k, buf, o, lse, causal, scale, stream)
     return o, lse, buf
 
 

@@ -138,9 +138,9 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_watchdog_selftest.restype = i
     L.fa_fp8_buffer_size.argtypes = [i, i, i, i, i]
     L.fa_fp8_buffer_size.restype = sz
-    L.fa_fp8_quantize.argtypes = [vp, vp, vp, vp, sz, i, i, i, i, i, vp]
+    L.fa_fp8_quantize.argtypes = [vp, vp, sz, i, i, i, i, i, vp]
     L.fa_fp8_quantize.restype = i
-    L.fa_fwd_fp8.argtypes = [vp, sz, vp, vp, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_fp8.argtypes = [vp, vp, vp, sz, vp, vp, i, i, i, i, i, i, f, vp]
     L.fa_fwd_fp8.restype = i
     L.fa_fwd_decode_workspace_size.argtypes = [i, i, i, i, i, i]
     L.fa_fwd_decode_workspace_size.restype = sz

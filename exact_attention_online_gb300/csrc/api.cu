@@ -567,33 +567,31 @@ static fa_status check_fp8_buffer(const void* buf, size_t bytes, const Shape& s)
     return FA_OK;
 }
 
-fa_status fa_fp8_quantize(const void* q, const void* k, const void* v, void* fp8_buf,
-                          size_t fp8_buf_bytes, int B, int H, int Hkv, int N, int d,
-                          fa_stream_t stream) {
-    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_ptr(q), check_ptr(k),
-                                check_ptr(v)});
+fa_status fa_fp8_quantize(const void* v, void* fp8_buf, size_t fp8_buf_bytes, int B, int H,
+                          int Hkv, int N, int d, fa_stream_t stream) {
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_ptr(v)});
     if (st != FA_OK) return st;
     if (d != 128) return FA_ERR_UNSUPPORTED;
     const Shape s{B, H, Hkv, N, d, 0, 1.0f};
     if ((st = check_fp8_buffer(fp8_buf, fp8_buf_bytes, s)) != FA_OK) return st;
     int dev;
     if ((st = device_ready(&dev)) != FA_OK) return st;
-    return from_cuda(launch_fp8_quantize(s, q, k, v, fp8_buffer_carve(fp8_buf, s),
-                                         (cudaStream_t)stream));
+    return from_cuda(launch_fp8_quantize(s, v, fp8_buffer_carve(fp8_buf, s), (cudaStream_t)stream));
 }
 
-fa_status fa_fwd_fp8(const void* fp8_buf, size_t fp8_buf_bytes, void* o, float* lse, int B, int H,
-                     int Hkv, int N, int d, int causal, float scale, fa_stream_t stream) {
-    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(o),
-                                check_ptr(lse)});
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* fp8_buf, size_t fp8_buf_bytes,
+                     void* o, float* lse, int B, int H, int Hkv, int N, int d, int causal,
+                     float scale, fa_stream_t stream) {
+    fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
+                                check_ptr(k), check_ptr(o), check_ptr(lse)});
     if (st != FA_OK) return st;
     if (d != 128) return FA_ERR_UNSUPPORTED;
     const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
     if ((st = check_fp8_buffer(fp8_buf, fp8_buf_bytes, s)) != FA_OK) return st;
     int dev;
     if ((st = device_ready(&dev)) != FA_OK) return st;
-    return from_cuda(launch_fwd_fp8(s, fp8_buffer_carve(const_cast<void*>(fp8_buf), s), o, lse,
-                                    g_status_ptr[dev], (cudaStream_t)stream));
+    return from_cuda(launch_fwd_fp8(s, q, k, fp8_buffer_carve(const_cast<void*>(fp8_buf), s), o,
+                                    lse, g_status_ptr[dev], (cudaStream_t)stream));
 }
 
 static fa_status check_decode_shape(int B, int H, int Hkv, int Nq, int Nk, int d) {

@@ -103,25 +103,20 @@ bool make_tmap_f32_2d(CUtensorMap* map, const void* base, int inner, long long r
 // 128-byte swizzle (inner and rows multiples of 128).
 bool make_tmap_u8_3d(CUtensorMap* map, const void* base, int inner, int rows, int outer);
 
-// FP8 buffer: e4m3 codes of Q [B*H][Np][d], K [B*Hkv][Np][d], V transposed
-// [B*Hkv][d][Np], then fp32 block scales of Q [B*H][Np/128], K and V
-// [B*Hkv][Np/128], and the largest V scale of each kv head [B*Hkv]; each
-// region 256-byte aligned.
+// FP8 buffer: e4m3 codes of V transposed [B*Hkv][d][Np], then fp32 block
+// scales of V [B*Hkv][Np/128] and the largest V scale of each kv head
+// [B*Hkv]; each region 256-byte aligned.
 struct Fp8Buffer {
-    uint8_t* q8;
-    uint8_t* k8;
     uint8_t* v8t;
-    float* sq;
-    float* sk;
     float* sv;
     float* svmax;
 };
 size_t fp8_buffer_bytes(const Shape& s);
 Fp8Buffer fp8_buffer_carve(void* base, const Shape& s);
-cudaError_t launch_fp8_quantize(const Shape& s, const void* q, const void* k, const void* v,
-                                const Fp8Buffer& buf, cudaStream_t stream);
-cudaError_t launch_fwd_fp8(const Shape& s, const Fp8Buffer& buf, void* o, float* lse,
-                           DeviceStatus* status, cudaStream_t stream);
+cudaError_t launch_fp8_quantize(const Shape& s, const void* v, const Fp8Buffer& buf,
+                                cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const Shape& s, const void* q, const void* k, const Fp8Buffer& buf,
+                           void* o, float* lse, DeviceStatus* status, cudaStream_t stream);
 
 // Split-KV decoding forward (fa_decode.cu).  Workspace: fp32 partial outputs
 // [B][H][Nq][n_split][d] (256-byte aligned end), then fp32 partial LSEs

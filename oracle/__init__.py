@@ -25,7 +25,10 @@ Functions (NumPy float64 in, NumPy float64 out; layouts as in the C file):
     fp8_quantize      per-(batch, head, 128-row block) quantisation of Q, K, V
                       with scale amax / 448 (FlashAttention-3 summary, "block
                       quantization"; the granularity is this repository's
-                      reading), V also transposed.
+                      reading), V also transposed; fp8_quantize_v for V alone,
+                      fp8_dequantize(_v) for the values the codes stand for.
+    incoherent_rotate x times diag(signs) Hd / sqrt(d), the reading of the
+                      FlashAttention-3 summary's "incoherent processing".
 """
 from __future__ import annotations
 
@@ -89,6 +92,8 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_e4m3_decode.restype = ctypes.c_double
     lib.oracle_fp8_quant_block.argtypes = [fp, i, i, ll, u8p, ll, u8p, ll, fp]
     lib.oracle_fp8_quant_block.restype = i
+    lib.oracle_hadamard_rotate.argtypes = [dp, i, i, ctypes.POINTER(ctypes.c_byte), dp]
+    lib.oracle_hadamard_rotate.restype = i
     return lib
 
 
@@ -344,6 +349,40 @@ def fp8_quantize(q, k, v, mutant: int = 0) -> dict:
     v8t, sv = _quant_blocks(v.reshape(B * Hkv, N, d), True, mutant)
     return {"q8": q8, "k8": k8, "v8t": v8t, "sq": sq, "sk": sk, "sv": sv,
             "svmax": sv.max(axis=1).astype(np.float32)}
+
+
+def fp8_quantize_v(v, mutant: int = 0) -> dict:
+    """Block quantisation of bf16 V [B,Hkv,N,d] alone (the operand the FP8
+    forward takes in e4m3): v8t [B*Hkv][d][Np], sv [B*Hkv][nblk], svmax."""
+    v = np.asarray(v, dtype=np.float32)
+    B, Hkv, N, d = v.shape
+    v8t, sv = _quant_blocks(v.reshape(B * Hkv, N, d), True, mutant)
+    return {"v8t": v8t, "sv": sv, "svmax": sv.max(axis=1).astype(np.float32)}
+
+
+def fp8_dequantize_v(qd: dict, B: int, Hkv: int, N: int, d: int) -> np.ndarray:
+    """The values V's codes stand for (codes times block scales), float64
+    [B,Hkv,N,d]."""
+    vals = np.swapaxes(e4m3_decode_table()[qd["v8t"]], 1, 2)
+    s = np.repeat(qd["sv"].astype(np.float64), FP8_BLOCK, axis=1)[:, :, None]
+    return (vals * s)[:, :N, :].reshape(B, Hkv, N, d)
+
+
+def incoherent_rotate(x, signs, mutant: int = 0) -> np.ndarray:
+    """x [..., d] times M = diag(signs) Hd / sqrt(d) (incoherent processing of
+    Q and K: scores unchanged, large entries spread over the channels); d a
+    power of two, signs a sequence of d values +-1."""
+    x = _f64(x)
+    d = x.shape[-1]
+    sg = np.ascontiguousarray(np.asarray(signs, dtype=np.int8))
+    if sg.shape != (d,) or not np.all(np.abs(sg) == 1):
+        raise ValueError("signs must be d values of +-1")
+    flat = np.ascontiguousarray(x.reshape(-1, d))
+    out = np.empty_like(flat)
+    _check(load(mutant).oracle_hadamard_rotate(
+        _ptr(flat), flat.shape[0], d, sg.ctypes.data_as(ctypes.POINTER(ctypes.c_byte)),
+        _ptr(out)), "oracle_hadamard_rotate")
+    return out.reshape(x.shape)
 
 
 def fp8_dequantize(qd: dict, B: int, H: int, Hkv: int, N: int, d: int):

@@ -489,6 +489,35 @@ int oracle_fp8_quant_block(const float* x, int rows, int cols, long long ld,
 }
 
 /*
+ * Incoherent processing (FlashAttention-3 summary, abstract: FP8 "with block
+ * quantization and incoherent processing"; the pages do not define it, and
+ * this is the reading from its name): multiply Q and K by one random
+ * orthogonal matrix M, Q -> Q M and K -> K M, which leaves every score
+ * (Q M)(K M)^T = Q K^T unchanged while spreading a large entry of a row over
+ * all d channels.  M = diag(signs) Hd / sqrt(d), Hd the Sylvester Hadamard
+ * matrix, entry (c, j) = (-1)^popcount(c & j), d a power of two, signs +-1.
+ * x and out are rows x d, row-major (out may not alias x).
+ */
+int oracle_hadamard_rotate(const double* x, int rows, int d, const signed char* signs,
+                           double* out) {
+    if (!x || !out || !signs || rows < 0 || d < 1 || (d & (d - 1)) != 0) return ORACLE_EINVAL;
+    const double norm = MUT(18) ? 1.0 : 1.0 / sqrt((double)d);   /* 18: not normalised */
+    for (int r = 0; r < rows; ++r) {
+        const double* xr = x + (size_t)r * d;
+        double* orow = out + (size_t)r * d;
+        for (int j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) {
+                const double h = (__builtin_popcount((unsigned)(c & j)) & 1) ? -1.0 : 1.0;
+                acc += xr[c] * signs[c] * h;
+            }
+            orow[j] = acc * norm;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/*
  * Attention forward with fewer queries than keys, as in decoding with a cache
  * of Nk keys (the decoding setting of the FlashAttention blog and FA2 review
  * thread: few new query rows against a long key/value sequence).  q is

@@ -362,6 +362,35 @@ def pin_fp8_block_quant(mutant=0):
     assert qd["svmax"][0] == np.float32(40.0 / 448.0)
     plain = oracle.fp8_quantize(v.reshape(1, 1, N, d), v, v, mutant)["q8"]
     assert np.array_equal(np.swapaxes(qd["v8t"], 1, 2), plain)
+    # V alone (the operand the FP8 forward quantises): the same codes and
+    # scales, and the values they stand for within half a step of V
+    qv = oracle.fp8_quantize_v(v, mutant)
+    assert np.array_equal(qv["v8t"], qd["v8t"]) and np.array_equal(qv["sv"], qd["sv"])
+    back = oracle.fp8_dequantize_v(qv, B, Hkv, N, d)
+    svr = np.repeat(qv["sv"][0].astype(np.float64), 128)[:N, None]
+    assert np.all(np.abs(v[0, 0] - back[0, 0]) <=
+                  np.maximum(2.0 ** -4 * np.abs(v[0, 0]), 2.0 ** -10 * svr) + 1e-30)
+
+
+def pin_incoherent_rotation(mutant=0):
+    """The rotation of incoherent processing (reading of the FlashAttention-3
+    summary's abstract): M = diag(signs) Hd / sqrt(d).  d = 2 and d = 4 against
+    the textbook Hadamard matrices written out by hand; M orthogonal at
+    d = 128; rotating Q and K by the same M leaves attention unchanged."""
+    r2 = 1.0 / math.sqrt(2.0)
+    got = oracle.incoherent_rotate(np.array([[3.0, 5.0]]), [1, -1], mutant)
+    assert np.allclose(got, [[(3.0 - 5.0) * r2, (3.0 + 5.0) * r2]], rtol=0, atol=1e-14)
+    h4 = 0.5 * np.array([[1, 1, 1, 1], [1, -1, 1, -1], [1, 1, -1, -1], [1, -1, -1, 1]], float)
+    assert np.array_equal(oracle.incoherent_rotate(np.eye(4), [1, 1, 1, 1], mutant), h4)
+    rng = np.random.default_rng(11)
+    signs = rng.choice([-1, 1], 128)
+    m = oracle.incoherent_rotate(np.eye(128), signs, mutant)
+    assert np.abs(m @ m.T - np.eye(128)).max() <= 1e-12
+    q, k, v = rand_qkv(1, 2, 1, 96, 128, 12)
+    o, lse = oracle.attn_fwd(q, k, v, True, 0.088)
+    ro, rl = oracle.attn_fwd(oracle.incoherent_rotate(q, signs, mutant),
+                             oracle.incoherent_rotate(k, signs, mutant), v, True, 0.088)
+    assert np.abs(ro - o).max() <= 1e-12 and np.abs(rl - lse).max() <= 1e-12
 
 
 def pin_decode_rows(mutant=0):
@@ -505,6 +534,7 @@ ALL_PINS = [
     pin_e4m3_definition,
     pin_e4m3_nearest,
     pin_fp8_block_quant,
+    pin_incoherent_rotation,
     pin_rows_sum_to_one, pin_torch_library, pin_online_matches_three_pass,
     pin_identical_keys, pin_one_hot, pin_causal_row0_and_single_key,
     pin_shift_invariance, pin_golden_closed_form, pin_finite_differences,

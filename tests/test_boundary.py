@@ -205,8 +205,16 @@ def test_fp8_entry_points_validate(L):
     assert L.fa_fp8_buffer_size(1, 2, 1, 256, 64) == 0
     n = L.fa_fp8_buffer_size(1, 2, 1, 256, 128)
     assert n > 0
-    assert L.fa_fp8_quantize(A, A, A, A, 16, 1, 2, 1, 256, 128, None) == fa.FA_ERR_WORKSPACE
-    assert L.fa_fwd_fp8(A, 16, A, A, 1, 2, 1, 256, 128, 1, 0.088, None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_fp8_quantize(A, A, 16, 1, 2, 1, 256, 128, None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_fp8_quantize(0, A, n, 1, 2, 1, 256, 128, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_fp8(A, A, A, 16, A, A, 1, 2, 1, 256, 128, 1, 0.088, None) == \
+        fa.FA_ERR_WORKSPACE
+    assert L.fa_fwd_fp8(A, 0, A, n, A, A, 1, 2, 1, 256, 128, 1, 0.088, None) == \
+        fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_fp8(A, A, MIS, n, A, A, 1, 2, 1, 256, 128, 1, 0.088, None) == \
+        fa.FA_ERR_ALIGNMENT
+    # the buffer holds V only: its size depends on B, Hkv, N, not on H
+    assert L.fa_fp8_buffer_size(1, 8, 1, 256, 128) == n
     assert fa.fa_kernel_launches() == before
 
 
@@ -262,8 +270,8 @@ def test_python_binding_checks_every_tensor_shape():
         ("dk", lambda: fa.fa_bwd_window(q, k, k, q, q, lse, q, q, k, ws, 4, 0.125, stream=0)),
         ("dv", lambda: fa.fa_bwd_dkdv(q, k, k, q, k, short_k, ws, True, 0.125, stream=0)),
         ("dout", lambda: fa.fa_bwd_preprocess(q, k, lse, ws, 2, stream=0)),
-        ("lse", lambda: fa.fa_fwd_fp8(ws, q, short_lse, 2, True, 0.125, stream=0)),
-        ("v", lambda: fa.fa_fp8_quantize(q, k, short_k, ws, stream=0)),
+        ("lse", lambda: fa.fa_fwd_fp8(q, k, ws, q, short_lse, True, 0.125, stream=0)),
+        ("o", lambda: fa.fa_fwd_fp8(q, k, ws, k, lse, True, 0.125, stream=0)),
         ("o", lambda: fa.fa_fwd_decode(q, k, k, T((1, 4, 1, 64), bf), lse, ws, True, 0.125,
                                        stream=0)),
     ]
@@ -315,9 +323,9 @@ def test_python_binding_accepts_consistent_shapes():
         lambda: fa.fa_fwd_varlen(pq, pk, pk, pq, plse, cu, 12, True, 0.125, stream=0),
         lambda: fa.fa_bwd_varlen(pq, pk, pk, pq, pq, plse, pq, pk, pk, ws, cu, 12, True, 0.125,
                                  stream=0),
-        lambda: fa.fa_fp8_quantize(T((B, H, N, 128), bf), T((B, Hkv, N, 128), bf),
-                                   T((B, Hkv, N, 128), bf), ws, stream=0),
-        lambda: fa.fa_fwd_fp8(ws, T((B, H, N, 128), bf), lse, Hkv, True, 0.125, stream=0),
+        lambda: fa.fa_fp8_quantize(T((B, Hkv, N, 128), bf), ws, H, stream=0),
+        lambda: fa.fa_fwd_fp8(T((B, H, N, 128), bf), T((B, Hkv, N, 128), bf), ws,
+                              T((B, H, N, 128), bf), lse, True, 0.125, stream=0),
         lambda: fa.fa_fwd_decode(dq, k, k, dq, dlse, ws, True, 0.125, stream=0),
     ]
     for i, call in enumerate(calls):
@@ -346,7 +354,8 @@ def test_python_binding_rejects_tensors_of_another_device():
                                         0.125, stream=0)),
         ("dk", lambda: fa.fa_bwd_dkdv(q, k, k, q, other(k.shape, bf), k, ws, True, 0.125,
                                       stream=0)),
-        ("workspace", lambda: fa.fa_fwd_fp8(other((64,), u8), T((B, H, N, 128), bf), lse, Hkv,
+        ("workspace", lambda: fa.fa_fwd_fp8(T((B, H, N, 128), bf), T((B, Hkv, N, 128), bf),
+                                            other((64,), u8), T((B, H, N, 128), bf), lse,
                                             True, 0.125, stream=0)),
     ]
     for name, call in cases:

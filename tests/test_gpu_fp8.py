@@ -1,37 +1,29 @@
-"""FP8 (e4m3) forward on the GPU, through the C ABI.
+"""FP8 (e4m3) forward on the GPU, through the C ABI: S = Q K^T from the bf16
+inputs, P and V in e4m3 (the placement tests/test_fp8_error_model.py derives).
 
-- fa_fp8_quantize against the oracle's quantiser: every code byte and every
-  block scale bit-exact (integer/byte work).
-- fa_fwd_fp8 against the fp64 oracle run on the dequantised inputs (codes
-  times block scales): the problem the kernel computes, so only its own
-  rounding remains (P in e4m3, fp32 accumulation): O relative RMS,
-  sqrt(mean((o - ref)^2)) / sqrt(mean(ref^2)), <= 3e-2, LSE max abs <= 1e-3.
-- fa_fwd_fp8 against the fp64 oracle on the unquantised bf16 inputs.  The
-  target for this is a relative RMS of 5e-2, and block-quantised e4m3 does NOT
-  reach it on these inputs: each of Q, K, V and P rounded to e4m3's 3 mantissa
-  bits adds about 2-2.7 % relative RMS to O on N(0,1) data (measured 0.052 on
-  the 128- and 600-row cases), and the outlier workloads reach 0.077-0.086,
-  where the outliers set the block scales.  The test bounds the measured error
-  at 0.10 (END_TO_END_BOUND) so that a regression shows, and does not claim
-  the target.
+- fa_fp8_quantize against the oracle's quantiser of V: every code byte and
+  every block scale bit-exact (integer/byte work).
+- fa_fwd_fp8 against the fp64 oracle on the unquantised bf16 inputs: O's
+  relative RMS error sqrt(mean((o - ref)^2)) / sqrt(mean(ref^2)) <= 5e-2, the
+  bar for an FP8 forward; LSE max abs <= 1e-3 (LSE depends on S alone, which
+  is computed as in the bf16 forward).
+- fa_fwd_fp8 against the fp64 oracle on the unquantised Q, K and the values
+  V's codes stand for: what remains is the kernel's own rounding of P to e4m3
+  (about 2.7 % RMS per element) and of O to bf16: relative RMS <= 3e-2.
 """
-import math
-
 import numpy as np
 import pytest
 import torch
 
 import exact_attention_online_gb300 as fa
 import oracle
-from _gpu import f64
+from _gpu import LSE_MAX_ABS, f64
 from exact_attention_online_gb300.inputs import WORKLOADS, Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-FP8_O_REL_RMS_TARGET = 5e-2   # against the unquantised inputs: not met (see above)
-END_TO_END_BOUND = 0.10       # the measured quantisation error, with margin
-FP8_O_REL_RMS_DEQ = 3e-2      # against the dequantised inputs
-FP8_LSE_MAX_ABS_DEQ = 1e-3
+FP8_O_REL_RMS = 5e-2          # against the unquantised inputs
+FP8_O_REL_RMS_DEQ_V = 3e-2    # against the unquantised Q, K and the dequantised V
 
 
 def rel_rms(a, ref):
@@ -53,19 +45,18 @@ CASES = [
 ]
 
 
-def quantize_gpu(q, k, v):
-    B, H, N, d = q.shape
-    Hkv = k.shape[1]
+def quantize_gpu(v, H):
+    B, Hkv, N, d = v.shape
     n = fa.fa_fp8_buffer_size(B, H, Hkv, N, d)
     assert n > 0
     buf = torch.zeros(n, dtype=torch.uint8, device="cuda")
-    fa.fa_fp8_quantize(q.cuda(), k.cuda(), v.cuda(), buf)
+    fa.fa_fp8_quantize(v.cuda(), buf, H)
     torch.cuda.synchronize()
     assert fa.fa_device_status() == 0
     return buf
 
 
-def carve(buf, B, H, Hkv, N, d):
+def carve(buf, B, Hkv, N, d):
     """Views of the documented buffer layout (fa.h), on the host."""
     Np = (N + 127) // 128 * 128
     nblk = Np // 128
@@ -73,11 +64,7 @@ def carve(buf, B, H, Hkv, N, d):
     h = buf.cpu().numpy()
     off = 0
     out = {}
-    for name, count, dt, shape in (("q8", B * H * Np * d, np.uint8, (B * H, Np, d)),
-                                   ("k8", B * Hkv * Np * d, np.uint8, (B * Hkv, Np, d)),
-                                   ("v8t", B * Hkv * Np * d, np.uint8, (B * Hkv, d, Np)),
-                                   ("sq", B * H * nblk, np.float32, (B * H, nblk)),
-                                   ("sk", B * Hkv * nblk, np.float32, (B * Hkv, nblk)),
+    for name, count, dt, shape in (("v8t", B * Hkv * Np * d, np.uint8, (B * Hkv, d, Np)),
                                    ("sv", B * Hkv * nblk, np.float32, (B * Hkv, nblk)),
                                    ("svmax", B * Hkv, np.float32, (B * Hkv,))):
         nbytes = count * np.dtype(dt).itemsize
@@ -88,10 +75,10 @@ def carve(buf, B, H, Hkv, N, d):
 
 @pytest.mark.parametrize("w", CASES[:3] + CASES[5:], ids=lambda w: w.name)
 def test_fp8_quantize_bit_exact(w):
-    q, k, v, _ = make_inputs(w)
-    got = carve(quantize_gpu(q, k, v), w.B, w.H, w.Hkv, w.N, w.d)
-    want = oracle.fp8_quantize(q.float().numpy(), k.float().numpy(), v.float().numpy())
-    for name in ("q8", "k8", "v8t", "sq", "sk", "sv", "svmax"):
+    _, _, v, _ = make_inputs(w)
+    got = carve(quantize_gpu(v, w.H), w.B, w.Hkv, w.N, w.d)
+    want = oracle.fp8_quantize_v(v.float().numpy())
+    for name in ("v8t", "sv", "svmax"):
         g, r = got[name], want[name]
         if g.dtype == np.float32:
             assert np.array_equal(g.view(np.uint32), r.view(np.uint32)), name
@@ -104,22 +91,21 @@ def test_fp8_quantize_zero_block_and_saturation():
     """An all-zero block gets scale 1 and zero codes; an element at the block
     amax encodes to +-448 exactly."""
     w = small("zero", 1, 1, 1, 256, False, 308)
-    q, k, v, _ = make_inputs(w)
-    q[0, 0, :128] = 0
+    _, _, v, _ = make_inputs(w)
+    v[0, 0, :128] = 0
     v[0, 0, 200, 5] = -64.0
-    got = carve(quantize_gpu(q, k, v), 1, 1, 1, 256, 128)
-    assert got["sq"][0, 0] == 1.0 and not got["q8"][0, :128].any()
+    got = carve(quantize_gpu(v, 1), 1, 1, 256, 128)
+    assert got["sv"][0, 0] == 1.0 and not got["v8t"][0, :, :128].any()
     assert got["v8t"][0, 5, 200] == 0xFE
     assert got["sv"][0, 1] == np.float32(np.float32(64.0) / np.float32(448.0))
 
 
 def run_fp8(q, k, v, causal, scale):
     B, H, N, d = q.shape
-    Hkv = k.shape[1]
-    buf = quantize_gpu(q, k, v)
+    buf = quantize_gpu(v, H)
     o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
-    fa.fa_fwd_fp8(buf, o, lse, Hkv, causal, scale)
+    fa.fa_fwd_fp8(q.cuda(), k.cuda(), buf, o, lse, causal, scale)
     torch.cuda.synchronize()
     assert fa.fa_device_status() == 0
     return buf, o.cpu(), lse.cpu()
@@ -128,24 +114,22 @@ def run_fp8(q, k, v, causal, scale):
 def check_heads(w, q, k, v, buf, o, lse, heads):
     d = w.d
     G = w.H // w.Hkv
-    qd = carve(buf, w.B, w.H, w.Hkv, w.N, d)
-    deq = oracle.fp8_dequantize(qd, w.B, w.H, w.Hkv, w.N, d)
-    worst = {"rel_rms": 0.0, "rel_rms_deq": 0.0, "lse_deq": 0.0}
+    v_deq = oracle.fp8_dequantize_v(carve(buf, w.B, w.Hkv, w.N, d), w.B, w.Hkv, w.N, d)
+    worst = {"rel_rms": 0.0, "rel_rms_deq_v": 0.0, "lse": 0.0}
     for (b, h) in heads:
         g = h // G
-        ref_o, _ = oracle.attn_fwd(f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, g:g + 1]),
-                                   f64(v[b:b + 1, g:g + 1]), w.causal, w.scale)
-        dq_o, dq_l = oracle.attn_fwd(deq[0][b:b + 1, h:h + 1], deq[1][b:b + 1, g:g + 1],
-                                     deq[2][b:b + 1, g:g + 1], w.causal, w.scale)
+        qh, kh = f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, g:g + 1])
+        ref_o, ref_l = oracle.attn_fwd(qh, kh, f64(v[b:b + 1, g:g + 1]), w.causal, w.scale)
+        dq_o, _ = oracle.attn_fwd(qh, kh, v_deq[b:b + 1, g:g + 1], w.causal, w.scale)
         go = f64(o[b, h])
         assert np.isfinite(go).all()
         worst["rel_rms"] = max(worst["rel_rms"], rel_rms(go, ref_o[0, 0]))
-        worst["rel_rms_deq"] = max(worst["rel_rms_deq"], rel_rms(go, dq_o[0, 0]))
-        worst["lse_deq"] = max(worst["lse_deq"],
-                               float(np.abs(lse[b, h].double().numpy() - dq_l[0, 0]).max()))
-    assert worst["rel_rms_deq"] <= FP8_O_REL_RMS_DEQ, worst
-    assert worst["lse_deq"] <= FP8_LSE_MAX_ABS_DEQ, worst
-    assert worst["rel_rms"] <= END_TO_END_BOUND, worst
+        worst["rel_rms_deq_v"] = max(worst["rel_rms_deq_v"], rel_rms(go, dq_o[0, 0]))
+        worst["lse"] = max(worst["lse"],
+                           float(np.abs(lse[b, h].double().numpy() - ref_l[0, 0]).max()))
+    assert worst["rel_rms"] <= FP8_O_REL_RMS, worst
+    assert worst["rel_rms_deq_v"] <= FP8_O_REL_RMS_DEQ_V, worst
+    assert worst["lse"] <= LSE_MAX_ABS, worst
     return worst
 
 
@@ -158,15 +142,15 @@ def test_fp8_fwd_small(w):
 
 
 def test_fp8_entry_points_reject():
-    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
     assert fa.fa_fp8_buffer_size(1, 1, 1, 128, 64) == 0
     buf = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FAError) as e:
-        fa.fa_fp8_quantize(q, q, q, buf)
+        fa.fa_fp8_quantize(v, buf, 1)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
-    q = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros((1, 1, 128, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fa.FAError) as e:
-        fa.fa_fp8_quantize(q, q, q, buf[:1024])
+        fa.fa_fp8_quantize(v, buf[:1024], 1)
     assert e.value.status == fa.FA_ERR_WORKSPACE
 
 

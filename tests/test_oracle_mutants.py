@@ -24,6 +24,7 @@ MUTANTS = {
     15: "decoding queries aligned top-left instead of bottom-right",
     16: "sliding window one key too wide",
     17: "packed sequences run one row into the next",
+    18: "incoherent rotation not normalised by sqrt(d)",
 }
 
 
