@@ -63,18 +63,18 @@ NCU_TRAFFIC = {
     ("fa_bwd_dkdv", "window"): {"bytes": 2026.96e6, "src_sha": "e9d1140dc8699988"},
     # 205.0 MB read + 97.9 MB written
     ("fa_fwd", "window"): {"bytes": 302.90e6, "src_sha": "9edd374358a89cb8"},
-    # 427.9 MB read + 224.6 MB written
-    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 652.53e6, "src_sha": "e9d1140dc8699988"},
-    # 534.0 MB read + 46.4 MB written
-    ("fa_fwd", "gpt_long"): {"bytes": 580.44e6, "src_sha": "9edd374358a89cb8"},
-    # 771.6 MB read + 347.6 MB written
-    ("fa_bwd_dkdv", "gqa"): {"bytes": 1119.17e6, "src_sha": "e9d1140dc8699988"},
-    # 298.1 MB read + 216.1 MB written (fp32 O, precise path)
-    ("fa_fwd", "gqa"): {"bytes": 514.19e6, "src_sha": "9edd374358a89cb8"},
+    # 427.2 MB read + 223.4 MB written, one launch
+    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 650.63e6, "src_sha": "4080affbf37cc299"},
+    # 559.5 MB read + 160.2 MB written (training forward), one launch
+    ("fa_fwd", "gpt_long"): {"bytes": 719.71e6, "src_sha": "393e55eb0670981c"},
+    # 768.8 MB read + 345.9 MB written, one launch
+    ("fa_bwd_dkdv", "gqa"): {"bytes": 1114.67e6, "src_sha": "4080affbf37cc299"},
+    # 406.4 MB read + 495.8 MB written (training forward, fp32 O), one launch
+    ("fa_fwd", "gqa"): {"bytes": 902.19e6, "src_sha": "393e55eb0670981c"},
     # 1.0739 GB read + 4.3 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0782e9, "src_sha": "737ec0dc1b9c060c"},
-    # 166.0 MB read + 33.8 MB written, one launch
-    ("fa_fwd_fp8", "long16k"): {"bytes": 199.78e6, "src_sha": "9cc4f81f16caefe2"},
+    # 386.7 MB read + 43.7 MB written, one launch
+    ("fa_fwd_fp8", "long16k"): {"bytes": 430.44e6, "src_sha": "7bf0ac776fe40c35"},
 }
 
 
