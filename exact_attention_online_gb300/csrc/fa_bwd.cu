@@ -108,6 +108,85 @@ struct BwdParams {
     DeviceStatus* status;
 };
 
+// What one dK/dV CTA works on: (batch, kv head, key block j) and the range of
+// query blocks (of br rows) that see some key of the block.  The CTAs go out
+// in blockIdx order.  Dense causal batches: key-block-major, so that the
+// longest CTAs (small j, every query block after them) start first and the
+// shortest fill the tail (a CPU model of the bench workloads puts the busiest
+// SM within 1-2 % of the mean instead of 7-14 %; measured: dK/dV +2 % to
+// +13 %).  Otherwise head-major: without the mask every CTA costs the same and
+// the CTAs that run at the same time share Q and dO in L2 (key-block-major
+// measured 12 % slower there), and with packed sequences of different lengths
+// j does not rank the cost (measured 12 % slower).  Key-block-major runs over
+// chunks of p.chunk heads at a time, sized so that a chunk's Q, dO and dQ
+// accumulator stay in L2 while its key blocks re-read them.
+struct BwdCta {
+    int jblk, b, g, bg, tok0, seq_len, z_kv, i_start, n_i, n_it;
+    bool idle;   // a key block past its packed sequence's end: nothing to do
+};
+template <bool CAUSAL, bool WINDOW, bool VARLEN>
+__device__ __forceinline__ BwdCta bwd_cta(const BwdParams& p, int br) {
+    BwdCta c;
+    constexpr bool kKeyMajor = CAUSAL && !VARLEN;
+    const int n_kblk = (p.N + kBN - 1) / kBN;
+    const int n_bg = gridDim.x / n_kblk;          // B * Hkv
+    if (kKeyMajor) {
+        const int chunk = blockIdx.x / (p.chunk * n_kblk), loc = blockIdx.x % (p.chunk * n_kblk);
+        const int width = min(p.chunk, n_bg - chunk * p.chunk);
+        c.jblk = loc / width;
+        c.bg = chunk * p.chunk + loc % width;
+    } else {
+        c.jblk = blockIdx.x % n_kblk;
+        c.bg = blockIdx.x / n_kblk;
+    }
+    c.b = c.bg / p.Hkv;
+    c.g = c.bg % p.Hkv;
+    // The sequence: its first row in the tensors and its length.  Dense
+    // batches address rows of head b*H(kv) + h; packed ones rows tok0 + i of
+    // head h.
+    c.tok0 = 0;
+    c.seq_len = VARLEN ? packed_seq(p.cu_seqlens, c.b, p.N, p.rows, c.tok0) : p.N;
+    c.idle = VARLEN && c.jblk * kBN >= c.seq_len;
+    c.z_kv = VARLEN ? c.g : c.bg;
+    const int n_qblk = (c.seq_len + br - 1) / br;
+    // Query blocks that see some key of the block: rows 128 j .. 128 j + 127
+    // + W - 1 under the causal (windowed) mask.
+    c.i_start = CAUSAL ? (c.jblk * kBN) / br : 0;
+    const int i_end = WINDOW ? min(n_qblk, (c.jblk * kBN + kBN - 1 + (p.window - 1)) / br + 1)
+                             : n_qblk;
+    c.n_i = i_end - c.i_start;
+    c.n_it = p.G * c.n_i;                         // (head in group) x (query block)
+    return c;
+}
+
+// The constant A operand of the extension MMAs, 128 key rows x 16 columns:
+// cols 0-8 hold 1/c as three bf16 terms (h h h m m m l l l), against the B
+// columns (x_h x_m x_l) x 3 of -LSE log2(e), so that the nine products sum to
+// (-LSE log2 e) / c; cols 9-11 hold 1 against the three terms of -D; the rest
+// 0.  One 16-byte piece per thread of the first 256.
+__device__ __forceinline__ void bwd_fill_ones(uint8_t* sOnes, float scale_log2) {
+    if (threadIdx.x < kBN * 32 / 16) {
+        const float inv = 1.0f / scale_log2;
+        const float ih = bf16_round(inv), im = bf16_round(inv - ih),
+                    il = bf16_round(inv - ih - im);
+        const int kc = (threadIdx.x >> 3) & 1;   // K half of this core-matrix row
+        uint4 w;
+        if (kc == 0) {
+            w.x = pack_bf16x2(ih, ih);
+            w.y = pack_bf16x2(ih, im);
+            w.z = pack_bf16x2(im, im);
+            w.w = pack_bf16x2(il, il);
+        } else {
+            w.x = pack_bf16x2(il, 1.0f);
+            w.y = pack_bf16x2(1.0f, 1.0f);
+            w.z = 0u;
+            w.w = 0u;
+        }
+        *reinterpret_cast<uint4*>(sOnes + threadIdx.x * 16) = w;
+        fence_proxy_async_smem();
+    }
+}
+
 // WINDOW (with CAUSAL): the causal sliding window of p.window keys.
 // VARLEN: packed variable-length sequences (p.cu_seqlens).
 template <int D, bool CAUSAL, bool WINDOW, bool VARLEN>
@@ -131,48 +210,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const WaitCtx wc{p.status, &abort_sh};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // (batch, kv head, key block j).  The CTAs go out in blockIdx order.
-    // Dense causal batches: key-block-major, so that the longest CTAs (small
-    // j, every query block after them) start first and the shortest fill the
-    // tail (a CPU model of the bench workloads puts the busiest SM within 1-2 %
-    // of the mean instead of 7-14 %; measured: dK/dV +2 % to +13 %).
-    // Otherwise head-major: without the mask every CTA costs the same and
-    // the CTAs that run at the same time share Q and dO in L2 (key-block-major
-    // measured 12 % slower there), and with packed sequences of different
-    // lengths j does not rank the cost (measured 12 % slower).
-    // Key-block-major runs over chunks of p.chunk heads at a time, sized so
-    // that a chunk's Q, dO and dQ accumulator stay in L2 while its key blocks
-    // re-read them.
-    constexpr bool kKeyMajor = CAUSAL && !VARLEN;
-    const int n_kblk = (p.N + kBN - 1) / kBN;
-    const int n_bg = gridDim.x / n_kblk;          // B * Hkv
-    int jblk, bg;                                 // bg = b * Hkv + g
-    if (kKeyMajor) {
-        const int chunk = blockIdx.x / (p.chunk * n_kblk), loc = blockIdx.x % (p.chunk * n_kblk);
-        const int width = min(p.chunk, n_bg - chunk * p.chunk);
-        jblk = loc / width;
-        bg = chunk * p.chunk + loc % width;
-    } else {
-        jblk = blockIdx.x % n_kblk;
-        bg = blockIdx.x / n_kblk;
-    }
-    const int b = bg / p.Hkv, g = bg % p.Hkv;
-    // The sequence: its first row in the tensors and its length.  Dense
-    // batches address rows of head b*H(kv) + h; packed ones rows tok0 + i of
-    // head h.  A key block past the sequence's end has nothing to do (the
-    // whole CTA leaves before any barrier or TMEM is set up).
-    int tok0 = 0;
-    const int seq_len = VARLEN ? packed_seq(p.cu_seqlens, b, p.N, p.rows, tok0) : p.N;
-    if (VARLEN && jblk * kBN >= seq_len) return;
-    const int z_kv = VARLEN ? g : bg;
-    const int n_qblk = (seq_len + BR - 1) / BR;
-    // Query blocks that see some key of the block: rows 128 j .. 128 j + 127
-    // + W - 1 under the causal (windowed) mask.
-    const int i_start = CAUSAL ? (jblk * kBN) / BR : 0;
-    const int i_end = WINDOW ? min(n_qblk, (jblk * kBN + kBN - 1 + (p.window - 1)) / BR + 1)
-                             : n_qblk;
-    const int n_i = i_end - i_start;
-    const int n_it = p.G * n_i;                   // (head in group) x (query block)
+    const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR);
+    if (cta.idle) return;   // the whole CTA leaves before any barrier or TMEM is set up
+    const int jblk = cta.jblk, b = cta.b, g = cta.g, tok0 = cta.tok0, seq_len = cta.seq_len;
+    const int z_kv = cta.z_kv, i_start = cta.i_start, n_i = cta.n_i, n_it = cta.n_it;
 
     uint8_t* sK = smem + Cfg::kOffK;
     uint8_t* sV = smem + Cfg::kOffV;
@@ -183,31 +224,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint8_t* sOnes = smem + Cfg::kOffOnes;
     uint8_t* sExt = smem + Cfg::kOffExt;      // stage st: lse at 2 st, d at 2 st + 1
 
-    // The constant A operand of the extension MMAs, 128 key rows x 16
-    // columns: cols 0-8 hold 1/c as three bf16 terms (h h h m m m l l l),
-    // against the B columns (x_h x_m x_l) x 3 of -LSE log2(e), so that the
-    // nine products sum to (-LSE log2 e) / c; cols 9-11 hold 1 against the
-    // three terms of -D; the rest 0.  One 16-byte piece per compute thread.
-    if (threadIdx.x < kBN * 32 / 16) {
-        const float inv = 1.0f / p.scale_log2;
-        const float ih = bf16_round(inv), im = bf16_round(inv - ih),
-                    il = bf16_round(inv - ih - im);
-        const int kc = (threadIdx.x >> 3) & 1;   // K half of this core-matrix row
-        uint4 w;
-        if (kc == 0) {
-            w.x = pack_bf16x2(ih, ih);
-            w.y = pack_bf16x2(ih, im);
-            w.z = pack_bf16x2(im, im);
-            w.w = pack_bf16x2(il, il);
-        } else {
-            w.x = pack_bf16x2(il, 1.0f);
-            w.y = pack_bf16x2(1.0f, 1.0f);
-            w.z = 0u;
-            w.w = 0u;
-        }
-        *reinterpret_cast<uint4*>(sOnes + threadIdx.x * 16) = w;
-        fence_proxy_async_smem();
-    }
+    bwd_fill_ones(sOnes, p.scale_log2);
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
