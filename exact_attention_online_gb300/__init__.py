@@ -33,7 +33,7 @@ __all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_p
            "fa_bwd_varlen_workspace_size", "attention_varlen", "attention_varlen_backward",
            "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8", "attention_fp8",
            "fa_fwd_decode_workspace_size", "fa_fwd_decode", "attention_decode",
-           "fa_fwd_train", "fa_bwd_train", "fa_bwd_preprocess_train"]
+           "fa_fwd_train", "fa_bwd_train", "fa_bwd_preprocess_train", "fa_exp2_check"]
 
 
 class FAError(RuntimeError):
@@ -257,6 +257,14 @@ def fa_bwd_train(q, k, v, o, dout, dq, dk, dv, workspace, causal: bool, scale: f
     _check(fn(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks), op, _bf16(dout, "dout", qs),
               _bf16(dq, "dq", qs), _bf16(dk, "dk", ks), _bf16(dv, "dv", ks), wp, wb,
               B, H, Hkv, N, d, int(bool(causal)), float(scale), _stream(stream)), name)
+
+
+def fa_exp2_check(x, y_fma, y_ex2, stream=None) -> None:
+    """2^x on the FMA pipe (y_fma) and from ex2.approx (y_ex2) for fp32 CUDA x."""
+    n = x.numel()
+    _check(lib().fa_exp2_check(_f32(x, "x"), _f32(y_fma, "y_fma", tuple(x.shape)),
+                               _f32(y_ex2, "y_ex2", tuple(x.shape)), n, _stream(stream)),
+           "fa_exp2_check")
 
 
 def fa_bwd_preprocess_train(o, dout, workspace, Hkv: int, stream=None) -> None:

@@ -540,6 +540,14 @@ fa_status fa_watchdog_selftest(long long timeout_ns, fa_stream_t stream) {
     return from_cuda(launch_watchdog_selftest(timeout_ns, g_status_ptr[dev], (cudaStream_t)stream));
 }
 
+fa_status fa_exp2_check(const float* x, float* y_fma, float* y_ex2, int n, fa_stream_t stream) {
+    if (n < 1 || !x || !y_fma || !y_ex2) return FA_ERR_INVALID_ARG;
+    int dev;
+    fa_status st = device_ready(&dev);
+    if (st != FA_OK) return st;
+    return from_cuda(launch_exp2_check(x, y_fma, y_ex2, n, (cudaStream_t)stream));
+}
+
 const char* fa_status_string(fa_status s) {
     switch (s) {
         case FA_OK: return "FA_OK";

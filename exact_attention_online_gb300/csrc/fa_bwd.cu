@@ -900,6 +900,22 @@ __global__ void fa_watchdog_kernel(DeviceStatus* status, unsigned long long limi
     __syncthreads();
 }
 
+// exp2 on the FMA pipe and on the exponential unit, side by side (diagnostic).
+__global__ void fa_exp2_check_kernel(const float* __restrict__ x, float* __restrict__ y_fma,
+                                     float* __restrict__ y_ex2, int n) {
+    const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i >= n) return;
+    const float a = x[i], b = (i + 1 < n) ? x[i + 1] : 0.0f;
+    float r0, r1;
+    f2_split(exp2_fma2(f2(a, b)), r0, r1);
+    y_fma[i] = r0;
+    y_ex2[i] = ex2(a);
+    if (i + 1 < n) {
+        y_fma[i + 1] = r1;
+        y_ex2[i + 1] = ex2(b);
+    }
+}
+
 int grid_for(long long work_items, int per_block) {
     const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
     long long blocks = (work_items + per_block - 1) / per_block;
@@ -1063,6 +1079,14 @@ cudaError_t launch_bwd_dq_convert(const Shape& s, const BwdWorkspace& ws, void* 
     else
         fa_bwd_dq_convert_kernel<64><<<grid, 256, 0, stream>>>(ws.dq_acc, dq_, s.N,
                                                                padded_rows(s.N), s.scale, n_vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_exp2_check(const float* x, float* y_fma, float* y_ex2, int n,
+                              cudaStream_t stream) {
+    count_launch();
+    const int pairs = (n + 1) / 2;
+    fa_exp2_check_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y_fma, y_ex2, n);
     return cudaGetLastError();
 }
 

@@ -67,6 +67,16 @@ constexpr int kRegsControl = 72;
 constexpr int kRegsSoftmax = 216;
 constexpr int kRegsNeeded = 128 * kRegsControl + 256 * kRegsSoftmax;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+// One pair in every kExp2FmaEvery of a row's exps is computed on the FMA pipe
+// (exp2_fma2) instead of the exponential unit, 0 = none.  Measured on the
+// forward alone: d = 128 one pair in 8: +1.8 % (one in 16 +0.6 %, one in 4
+// -4.6 %); d = 64, where the softmax is bound by instruction issue rather than
+// by the exponential unit: one in 16 -4 %, one in 8 -6.5 %.
+template <int D, bool PRECISE>
+struct Exp2FmaEvery {
+    static constexpr int value = (D == 128 && !PRECISE) ? 8 : 0;
+    static constexpr int mod = value > 0 ? value : 1;
+};
 
 template <int D>
 struct FwdCfg {
@@ -210,6 +220,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_pv[kTiles], bar_o_free[kTiles];
     __shared__ uint64_t bar_s_free[kTiles];   // separate-P form only
     constexpr bool SEP = (D == 64) && !PRECISE;
+    constexpr int kExp2FmaEvery = Exp2FmaEvery<D, PRECISE>::value;
+    constexpr int kExp2FmaMod = Exp2FmaEvery<D, PRECISE>::mod;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     const WaitCtx wc{p.status, &abort_sh};
@@ -357,9 +369,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                     for (int e2 = 0; e2 < 32; ++e2) {
                         const int e = hh * 64 + 2 * e2;
-                        float x0, x1;
-                        f2_split(f2_fma(f2(sv[e], sv[e + 1]), c2, negm2), x0, x1);
-                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        float p0, p1;
+                        if (kExp2FmaEvery > 0 && e2 % kExp2FmaMod == kExp2FmaMod - 1) {
+                            // this pair on the FMA pipe (exp2_fma2), the rest
+                            // on the exponential unit
+                            f2_split(exp2_fma2(f2_fma(f2(sv[e], sv[e + 1]), c2, negm2)), p0, p1);
+                        } else {
+                            float x0, x1;
+                            f2_split(f2_fma(f2(sv[e], sv[e + 1]), c2, negm2), x0, x1);
+                            p0 = ex2(x0);
+                            p1 = ex2(x1);
+                        }
                         acc2[e2 & 3] = f2_add(acc2[e2 & 3], f2(p0, p1));
                         pk[hh][e2] = pack_bf16x2(p0, p1);
                         if (PRECISE) {

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "exp2_poly.h"
 #include "fa.h"
 #include "sm103_ptx.cuh"
 
@@ -35,6 +36,33 @@ __device__ __forceinline__ int packed_seq(const int* __restrict__ cu, int b, int
     t0 = (int)a;
     return (int)len;
 }
+
+// 2^x for two fp32 values on the FMA pipe instead of the exponential unit:
+// x = n + f with n = rint(x), from the fp32 rounding of x + 1.5 * 2^23 (exact
+// for |x| < 2^22), and f = x - n in [-1/2, 1/2], also exact; 2^f by the
+// minimax polynomial of exp2_poly.h (Horner, paired FMAs); 2^n by adding n to
+// the exponent field (t = x + 1.5 * 2^23 holds 2^22 + n in its mantissa, so
+// bits(t) << 23 is n << 23 modulo 2^32).  x is clamped below at -126, so
+// -inf (a masked score) gives a value under 2^-126, which the softmax's bf16
+// P and fp32 sums treat as zero.  Relative error at most kExp2PolyMaxRelErr
+// for results in the normal range.
+__device__ __forceinline__ uint64_t exp2_fma2(uint64_t x2) {
+    float x0, x1;
+    f2_split(x2, x0, x1);
+    const uint64_t x = f2(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
+    const uint64_t magic = f2(12582912.0f, 12582912.0f);
+    const uint64_t t = f2_add(x, magic);
+    const uint64_t f = f2_sub(x, f2_sub(t, magic));
+    uint64_t p = f2_fma(f2(kExp2C3, kExp2C3), f, f2(kExp2C2, kExp2C2));
+    p = f2_fma(p, f, f2(kExp2C1, kExp2C1));
+    p = f2_fma(p, f, f2(kExp2C0, kExp2C0));
+    float t0, t1, p0, p1;
+    f2_split(t, t0, t1);
+    f2_split(p, p0, p1);
+    return f2(__uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23)),
+              __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23)));
+}
+static_assert(kExp2PolyDegree == 3, "exp2_fma2 evaluates a cubic");
 
 // Window value the kernels carry when there is none: the lower edge i - W + 1
 // lies below every key index.
@@ -87,6 +115,9 @@ cudaError_t launch_bwd_dq_convert(const Shape& s, const BwdWorkspace& ws, void* 
                                   cudaStream_t stream);
 cudaError_t launch_watchdog_selftest(long long timeout_ns, DeviceStatus* status,
                                      cudaStream_t stream);
+// Evaluates exp2_fma2 and ex2.approx.ftz.f32 on n inputs (diagnostic).
+cudaError_t launch_exp2_check(const float* x, float* y_fma, float* y_ex2, int n,
+                              cudaStream_t stream);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
 // Builds a 3-D map over a bf16 tensor [outer][rows][d] with a {64, box_rows, 1}

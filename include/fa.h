@@ -429,6 +429,20 @@ FA_API long long fa_kernel_launches(void);
  */
 FA_API fa_status fa_watchdog_selftest(long long timeout_ns, fa_stream_t stream);
 
+/*
+ * Diagnostic of the exponential used when part of a softmax row's exps run on
+ * the FMA pipe instead of the exponential unit (the pages' argument that every
+ * non-matmul cycle counts, FlashAttention-2 review thread, author answer on
+ * non-matmul FLOPs, applied to the GPU's second bottleneck): for n device
+ * floats x, writes y_fma = 2^x computed as 2^rint(x) * p(x - rint(x)), p the
+ * fp32 minimax cubic fitted by csrc/fit_exp2_poly.py (relative error at most
+ * 7.5e-5 in the normal range, x clamped below at -126), and y_ex2 = 2^x from
+ * ex2.approx.ftz.f32.  Device pointers; one launch; FA_ERR_INVALID_ARG for
+ * n < 1 or a null pointer.
+ */
+FA_API fa_status fa_exp2_check(const float* x, float* y_fma, float* y_ex2, int n,
+                               fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
