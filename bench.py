@@ -55,22 +55,22 @@ L2_BYTES = 129 * 1024 * 1024
 # workload, together with the sha256 of the kernel source it was taken on.  A
 # source change makes the figure stale and it is then reported as null.
 NCU_TRAFFIC = {
-    # 237.5 MB read + 103.6 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 341.09e6, "src_sha": "e9d1140dc8699988"},
-    # 110.3 MB read + 12.7 MB written, one launch
-    ("fa_fwd", "mha_d64"): {"bytes": 123.07e6, "src_sha": "9edd374358a89cb8"},
-    # 1385.7 MB read + 641.3 MB written
-    ("fa_bwd_dkdv", "window"): {"bytes": 2026.96e6, "src_sha": "e9d1140dc8699988"},
-    # 205.0 MB read + 97.9 MB written
-    ("fa_fwd", "window"): {"bytes": 302.90e6, "src_sha": "9edd374358a89cb8"},
-    # 427.2 MB read + 223.4 MB written, one launch
-    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 650.63e6, "src_sha": "4080affbf37cc299"},
-    # 559.5 MB read + 160.2 MB written (training forward), one launch
-    ("fa_fwd", "gpt_long"): {"bytes": 719.71e6, "src_sha": "393e55eb0670981c"},
-    # 768.8 MB read + 345.9 MB written, one launch
-    ("fa_bwd_dkdv", "gqa"): {"bytes": 1114.67e6, "src_sha": "4080affbf37cc299"},
-    # 406.4 MB read + 495.8 MB written (training forward, fp32 O), one launch
-    ("fa_fwd", "gqa"): {"bytes": 902.19e6, "src_sha": "393e55eb0670981c"},
+    # 236.5 MB read + 99.4 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 335.90e6, "src_sha": "8b297de3a9a409ec"},
+    # 133.1 MB read + 58.9 MB written (training forward), one launch
+    ("fa_fwd", "mha_d64"): {"bytes": 192.05e6, "src_sha": "4ea3adf4eb4f28a7"},
+    # 1385.3 MB read + 637.6 MB written, one launch
+    ("fa_bwd_dkdv", "window"): {"bytes": 2022.89e6, "src_sha": "8b297de3a9a409ec"},
+    # 204.7 MB read + 98.0 MB written, one launch
+    ("fa_fwd", "window"): {"bytes": 302.66e6, "src_sha": "4ea3adf4eb4f28a7"},
+    # 426.9 MB read + 223.8 MB written, one launch
+    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 650.68e6, "src_sha": "8b297de3a9a409ec"},
+    # 559.2 MB read + 160.2 MB written (training forward), one launch
+    ("fa_fwd", "gpt_long"): {"bytes": 719.39e6, "src_sha": "4ea3adf4eb4f28a7"},
+    # 771.2 MB read + 347.9 MB written, one launch
+    ("fa_bwd_dkdv", "gqa"): {"bytes": 1119.02e6, "src_sha": "8b297de3a9a409ec"},
+    # 409.2 MB read + 496.3 MB written (training forward, fp32 O), one launch
+    ("fa_fwd", "gqa"): {"bytes": 905.51e6, "src_sha": "4ea3adf4eb4f28a7"},
     # 1.0739 GB read + 4.3 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0782e9, "src_sha": "737ec0dc1b9c060c"},
     # 386.7 MB read + 43.7 MB written, one launch
