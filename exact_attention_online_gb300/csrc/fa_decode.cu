@@ -236,12 +236,25 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             const int j0 = j_begin + t * kTileKeys;
             const int lim = min(last_vis, j_end - 1) - j0;   // keep e <= lim
             float x[kTileKeys];
-            float mx = -CUDART_INF_F;
 #pragma unroll
-            for (int e = 0; e < kTileKeys; ++e) {
-                x[e] = (e <= lim) ? __uint_as_float(sr[e >> 5][e & 31]) * c : -CUDART_INF_F;
-                mx = fmaxf(mx, x[e]);
+            for (int e = 0; e < kTileKeys; ++e) x[e] = __uint_as_float(sr[e >> 5][e & 31]);
+            if (lim < kTileKeys - 1) {
+#pragma unroll
+                for (int e = 0; e < kTileKeys; ++e)
+                    if (e > lim) x[e] = -CUDART_INF_F;
             }
+            // Row max of the raw scores in eight independent chains of
+            // three-input maxima, then scaled (c > 0): a short dependency
+            // chain where a single running max would be 128 deep.
+            float mx8[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(x[2 * u], x[2 * u + 1]);
+#pragma unroll
+            for (int e = 16; e < kTileKeys; e += 16)
+#pragma unroll
+                for (int u = 0; u < 8; ++u) mx8[u] = fmax3(mx8[u], x[e + 2 * u], x[e + 2 * u + 1]);
+            const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                                   fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7])) * c;
             const bool need = row_ok && mx > m2 + kRescale;
             float alpha = 1.0f;
             if (__any_sync(0xffffffffu, need)) {
@@ -270,15 +283,24 @@ fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                 l *= alpha;
             }
             const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
+            // p = 2^(s c - m): the exponent argument two lanes per paired
+            // FMA, the row sum in four paired accumulators.
+            const uint64_t c2 = f2(c, c), negm2 = f2(-m_use, -m_use);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pk[2][32];
-            float sum = 0.0f;
 #pragma unroll
             for (int e2 = 0; e2 < kTileKeys / 2; ++e2) {
-                const float p0 = ex2(x[2 * e2] - m_use), p1 = ex2(x[2 * e2 + 1] - m_use);
-                sum += p0 + p1;
+                float a0, a1;
+                f2_split(f2_fma(f2(x[2 * e2], x[2 * e2 + 1]), c2, negm2), a0, a1);
+                const float p0 = ex2(a0), p1 = ex2(a1);
+                acc2[e2 & 3] = f2_add(acc2[e2 & 3], f2(p0, p1));
                 pk[e2 >> 5][e2 & 31] = pack_bf16x2(p0, p1);
             }
-            l += sum;
+            {
+                float a0, a1;
+                f2_split(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), a0, a1);
+                l += a0 + a1;
+            }
             tmem_st32(tmem + col_s, pk[0]);
             tmem_st32(tmem + col_s + 32, pk[1]);
             tmem_st_wait();
@@ -340,15 +362,26 @@ fa_decode_combine_kernel(const float* __restrict__ o_part, const float* __restri
     for (int c = 0; c < D / 32; ++c) acc[c] = 0.0f;
     float wsum = 0.0f;
     if (mx != -CUDART_INF_F) {
-        for (int s = 0; s < n_split; ++s) {
-            const float ls = lp[s];
-            if (ls == -CUDART_INF_F) continue;
-            const float w = expf(ls - mx);
+        // 32 splits at a time: lane k computes the weight of split base + k
+        // (0 for a split that saw no key: its partial O is zero), then every
+        // lane adds its columns of each split's partial O, the loads of
+        // different splits independent of one another.
+        for (int base = 0; base < n_split; base += 32) {
+            const int sl = base + lane;
+            const float ls = sl < n_split ? lp[sl] : -CUDART_INF_F;
+            const float w = (ls == -CUDART_INF_F) ? 0.0f : expf(ls - mx);
             wsum += w;
-            const float* os = o_part + (row * n_split + s) * D;
+            const int cnt = min(32, n_split - base);
+            const float* os = o_part + (row * n_split + base) * D + lane;
+#pragma unroll 4
+            for (int k = 0; k < cnt; ++k) {
+                const float wk = __shfl_sync(0xffffffffu, w, k);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(w, os[lane + 32 * c], acc[c]);
+                for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(wk, os[k * D + 32 * c], acc[c]);
+            }
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     }
     const float inv = (wsum > 0.0f) ? 1.0f / wsum : 0.0f;
 #pragma unroll
