@@ -71,8 +71,10 @@ NCU_TRAFFIC = {
     ("fa_bwd_dkdv", "gqa"): {"bytes": 1119.02e6, "src_sha": "8b297de3a9a409ec"},
     # 409.2 MB read + 496.3 MB written (training forward, fp32 O), one launch
     ("fa_fwd", "gqa"): {"bytes": 905.51e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 1.0739 GB read + 4.3 MB written, one launch
-    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0782e9, "src_sha": "737ec0dc1b9c060c"},
+    # 1.0739 GB read + 4.1 MB written, one launch
+    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0780e9, "src_sha": "3b872653e5a67590"},
+    # 537.0 MB read + 3.3 MB written, one launch
+    ("fa_decode_split", "decode_mha_d64"): {"bytes": 540.29e6, "src_sha": "3b872653e5a67590"},
     # 386.7 MB read + 43.7 MB written, one launch
     ("fa_fwd_fp8", "long16k"): {"bytes": 430.44e6, "src_sha": "7bf0ac776fe40c35"},
 }
