@@ -353,8 +353,19 @@ fa_decode_combine_kernel(const float* __restrict__ o_part, const float* __restri
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     const float* lp = lse_part + row * n_split;
-    float mx = -CUDART_INF_F;
-    for (int s = lane; s < n_split; s += 32) mx = fmaxf(mx, lp[s]);
+    const float* os = o_part + row * n_split * D + lane;
+    // The partial O of the first kPre splits is loaded together with the
+    // LSEs (one memory round trip when n_split <= kPre, the usual case);
+    // rows past n_split read as zero and get weight zero.
+    constexpr int kPre = 8;
+    float pre[kPre][D / 32];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k)
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) pre[k][c] = (k < n_split) ? os[k * D + 32 * c] : 0.0f;
+    const float l0 = lane < n_split ? lp[lane] : -CUDART_INF_F;
+    float mx = l0;
+    for (int s = lane + 32; s < n_split; s += 32) mx = fmaxf(mx, lp[s]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     float acc[D / 32];
@@ -368,16 +379,26 @@ fa_decode_combine_kernel(const float* __restrict__ o_part, const float* __restri
         // different splits independent of one another.
         for (int base = 0; base < n_split; base += 32) {
             const int sl = base + lane;
-            const float ls = sl < n_split ? lp[sl] : -CUDART_INF_F;
+            const float ls = (base == 0) ? l0 : (sl < n_split ? lp[sl] : -CUDART_INF_F);
             const float w = (ls == -CUDART_INF_F) ? 0.0f : expf(ls - mx);
             wsum += w;
             const int cnt = min(32, n_split - base);
-            const float* os = o_part + (row * n_split + base) * D + lane;
+            int k = 0;
+            if (base == 0) {
+#pragma unroll
+                for (int kp = 0; kp < kPre; ++kp) {
+                    const float wk = __shfl_sync(0xffffffffu, w, kp);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(wk, pre[kp][c], acc[c]);
+                }
+                k = kPre;
+            }
 #pragma unroll 4
-            for (int k = 0; k < cnt; ++k) {
+            for (; k < cnt; ++k) {
                 const float wk = __shfl_sync(0xffffffffu, w, k);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) acc[c] = fmaf(wk, os[k * D + 32 * c], acc[c]);
+                for (int c = 0; c < D / 32; ++c)
+                    acc[c] = fmaf(wk, os[(base + k) * D + 32 * c], acc[c]);
             }
         }
 #pragma unroll
