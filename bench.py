@@ -71,10 +71,10 @@ NCU_TRAFFIC = {
     ("fa_bwd_dkdv", "gqa"): {"bytes": 1119.02e6, "src_sha": "8b297de3a9a409ec"},
     # 409.2 MB read + 496.3 MB written (training forward, fp32 O), one launch
     ("fa_fwd", "gqa"): {"bytes": 905.51e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 1.0739 GB read + 4.1 MB written, one launch
-    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0780e9, "src_sha": "3b872653e5a67590"},
-    # 537.0 MB read + 3.3 MB written, one launch
-    ("fa_decode_split", "decode_mha_d64"): {"bytes": 540.29e6, "src_sha": "3b872653e5a67590"},
+    # 1.0739 GB read + 3.6 MB written, one launch
+    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0775e9, "src_sha": "38a45fea4cd86473"},
+    # 537.0 MB read + 3.4 MB written, one launch
+    ("fa_decode_split", "decode_mha_d64"): {"bytes": 540.33e6, "src_sha": "38a45fea4cd86473"},
     # 386.7 MB read + 43.7 MB written, one launch
     ("fa_fwd_fp8", "long16k"): {"bytes": 430.44e6, "src_sha": "7bf0ac776fe40c35"},
 }
@@ -628,6 +628,10 @@ def run_native(args, w):
                                      "frac": kernels[n]["tflops"] / peak}
                                  for n in kernels if n != dom}}
 
+    # The exponential unit's rate, measured after the timed region (the exp
+    # roofline of the line's exp_unit entry).
+    ex2 = measure_ex2_rate(torch, fa, dev, stream, clocks)
+
     # End to end through the public API with pinned host buffers: H2D of the
     # step's inputs, fa_fwd + fa_bwd, D2H of every output, inside the timing.
     e2e = None
@@ -754,7 +758,7 @@ def run_native(args, w):
             "fwd_bwd_alg_tflops": None if fwd_only else
             attention_flops(w, "fwd_bwd_alg") * args.steps * ws / (ms_total * 1e-3) / 1e12,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "exp_unit": exp_unit_line(w, kernels, clocks),
+            "exp_unit": exp_unit_line(w, kernels, ex2),
             "clocks": clocks, "gpu_launches": launches,
             "launches_per_step": launches / args.steps,
             "clock_soak": {"steps": n_soak, "seconds_requested": args.soak,
@@ -766,20 +770,43 @@ def run_native(args, w):
 
 
 # The second bound of the forward and backward kernels: one ex2 per score.
-# Its peak is derived from a microbenchmark on GB300 (ex2.approx.ftz.f32 at a
-# quarter of the FFMA rate: 32 lanes a clock per SM) times 152 SMs and the SM
-# clock sampled during the timed region.
-EX2_LANES_PER_CLK_SM = 32
-N_SMS = 152
-
-
-def exp_unit_line(w, kernels, clocks):
-    from exact_attention_online_gb300.measure import visible_pairs
+# Its peak is measured live, after the timed region, by the library's
+# exponential-unit microbenchmark (fa_ex2_rate: eight independent
+# ex2.approx.ftz.f32 chains per thread, eight 256-thread blocks an SM).
+def measure_ex2_rate(torch, fa, dev, stream, clocks):
+    """Best of five launches of fa_ex2_rate over the whole GPU: exps per
+    second, and per SM per clock at the SM clock sampled in the timed region."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = sms * 8, 2048
+    out = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    for _ in range(2):
+        fa.fa_ex2_rate(out, blocks, iters, stream)
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fa.fa_ex2_rate(out, blocks, iters, stream)
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    vals = out.float()
+    if not bool(torch.isfinite(vals).all()) or float(vals.min()) < 4.0 or float(vals.max()) > 8.0:
+        raise RuntimeError("fa_ex2_rate: chain values outside [4, 8]")
+    exps = float(blocks) * 256 * 8 * iters
+    per_s = exps / (best * 1e-3)
     mhz = (clocks or {}).get("sm_mhz") or 2070.0
-    peak = EX2_LANES_PER_CLK_SM * N_SMS * mhz * 1e6
+    return {"per_s": per_s, "ms": best, "exps": exps, "sms": sms,
+            "lanes_per_clk_sm": per_s / sms / (mhz * 1e6), "at_sm_mhz": mhz}
+
+
+def exp_unit_line(w, kernels, ex2):
+    from exact_attention_online_gb300.measure import visible_pairs
+    peak = ex2["per_s"]
     exps = float(w.B) * w.H * visible_pairs(w.N, w.causal, getattr(w, "window", 0))
     out = {"exps_per_launch": exps, "peak_per_s": peak,
-           "peak_kind": "32 lanes/clk/SM (microbenchmark) x 152 SMs x sampled SM clock"}
+           "peak_kind": (f"measured live: fa_ex2_rate over {ex2['sms']} SMs, "
+                         f"{ex2['lanes_per_clk_sm']:.1f} exps/clk/SM at {ex2['at_sm_mhz']:.0f} MHz")}
     for name, (key, mult) in (("fwd", ("fa_fwd", 1.0)), ("dkdv", ("fa_bwd_dkdv", 1.0))):
         k = kernels.get(key)
         if k:

@@ -33,7 +33,8 @@ __all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_p
            "fa_bwd_varlen_workspace_size", "attention_varlen", "attention_varlen_backward",
            "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8", "attention_fp8",
            "fa_fwd_decode_workspace_size", "fa_fwd_decode", "attention_decode",
-           "fa_fwd_train", "fa_bwd_train", "fa_bwd_preprocess_train", "fa_exp2_check"]
+           "fa_fwd_train", "fa_bwd_train", "fa_bwd_preprocess_train", "fa_exp2_check",
+           "fa_ex2_rate"]
 
 
 class FAError(RuntimeError):
@@ -265,6 +266,15 @@ def fa_exp2_check(x, y_fma, y_ex2, stream=None) -> None:
     _check(lib().fa_exp2_check(_f32(x, "x"), _f32(y_fma, "y_fma", tuple(x.shape)),
                                _f32(y_ex2, "y_ex2", tuple(x.shape)), n, _stream(stream)),
            "fa_exp2_check")
+
+
+def fa_ex2_rate(out, blocks: int, iters: int, stream=None) -> None:
+    """One launch of the exponential-unit microbenchmark: blocks x 256 threads,
+    8 x iters ex2.approx each; out is an fp32 CUDA tensor of blocks x 256."""
+    if out.numel() < int(blocks) * 256:
+        raise ValueError(f"out must hold blocks x 256 = {int(blocks) * 256} floats")
+    _check(lib().fa_ex2_rate(_f32(out, "out"), int(blocks), int(iters), _stream(stream)),
+           "fa_ex2_rate")
 
 
 def fa_bwd_preprocess_train(o, dout, workspace, Hkv: int, stream=None) -> None:

@@ -19,7 +19,8 @@ OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libfa.so")
 
-SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_fp8.cu", "fa_decode.cu"]
+SOURCES = ["api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_noalloc.cu", "fa_fp8.cu", "fa_decode.cu",
+           "fa_diag.cu"]
 HEADERS = ["sm103_ptx.cuh", "fa_internal.h", "exp2_poly.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -111,6 +112,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_bwd_train_precise.restype = i
     L.fa_exp2_check.argtypes = [vp, vp, vp, i, vp]
     L.fa_exp2_check.restype = i
+    L.fa_ex2_rate.argtypes = [vp, i, i, vp]
+    L.fa_ex2_rate.restype = i
     L.fa_bwd_preprocess_train.argtypes = [vp, vp, vp, sz, i, i, i, i, i, vp]
     L.fa_bwd_preprocess_train.restype = i
     L.fa_bwd_preprocess_train_precise.argtypes = [vp, vp, vp, sz, i, i, i, i, i, vp]
@@ -173,4 +176,5 @@ EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bw
            "fa_fwd_decode_workspace_size", "fa_fwd_decode", "fa_fwd_window", "fa_bwd_window",
            "fa_bwd_dkdv_window", "fa_fwd_varlen", "fa_bwd_varlen_workspace_size",
            "fa_bwd_varlen", "fa_fwd_train", "fa_fwd_train_precise", "fa_bwd_train",
-           "fa_bwd_train_precise", "fa_bwd_preprocess_train", "fa_bwd_preprocess_train_precise", "fa_exp2_check"]
+           "fa_bwd_train_precise", "fa_bwd_preprocess_train", "fa_bwd_preprocess_train_precise", "fa_exp2_check",
+           "fa_ex2_rate"]

@@ -548,6 +548,15 @@ fa_status fa_exp2_check(const float* x, float* y_fma, float* y_ex2, int n, fa_st
     return from_cuda(launch_exp2_check(x, y_fma, y_ex2, n, (cudaStream_t)stream));
 }
 
+fa_status fa_ex2_rate(float* out, int blocks, int iters, fa_stream_t stream) {
+    if (!out || blocks < 1 || iters < 1 || blocks > (1 << 20) || iters > (1 << 24))
+        return FA_ERR_INVALID_ARG;
+    int dev;
+    fa_status st = device_ready(&dev);
+    if (st != FA_OK) return st;
+    return from_cuda(launch_ex2_rate(out, blocks, iters, (cudaStream_t)stream));
+}
+
 const char* fa_status_string(fa_status s) {
     switch (s) {
         case FA_OK: return "FA_OK";

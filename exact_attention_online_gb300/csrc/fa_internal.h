@@ -118,6 +118,9 @@ cudaError_t launch_watchdog_selftest(long long timeout_ns, DeviceStatus* status,
 // Evaluates exp2_fma2 and ex2.approx.ftz.f32 on n inputs (diagnostic).
 cudaError_t launch_exp2_check(const float* x, float* y_fma, float* y_ex2, int n,
                               cudaStream_t stream);
+// Exponential-unit throughput microbenchmark (diagnostic): blocks x 256
+// threads, each 8 x iters ex2.approx; out holds blocks x 256 floats.
+cudaError_t launch_ex2_rate(float* out, int blocks, int iters, cudaStream_t stream);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
 // Builds a 3-D map over a bf16 tensor [outer][rows][d] with a {64, box_rows, 1}

@@ -443,6 +443,20 @@ FA_API fa_status fa_watchdog_selftest(long long timeout_ns, fa_stream_t stream);
 FA_API fa_status fa_exp2_check(const float* x, float* y_fma, float* y_ex2, int n,
                                fa_stream_t stream);
 
+/*
+ * Throughput microbenchmark of the exponential unit, the second bound of the
+ * attention kernels after the tensor core (one 2^x per score element; the
+ * FlashAttention-2 review thread, author answer on non-matmul FLOPs): `blocks`
+ * CTAs of 256 threads, each thread running eight independent chains
+ * x <- 2^(-x) of ex2.approx.ftz.f32 for `iters` rounds, so one launch
+ * evaluates blocks * 256 * 8 * iters exps; `out` (device, blocks * 256 floats,
+ * owned by the caller) receives each thread's sum of its eight final values
+ * (each in [1/2, 1]).  Time the launch on `stream` to get the unit's rate.
+ * FA_ERR_INVALID_ARG for a null pointer, blocks outside [1, 2^20] or iters
+ * outside [1, 2^24].
+ */
+FA_API fa_status fa_ex2_rate(float* out, int blocks, int iters, fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

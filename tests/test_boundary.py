@@ -362,3 +362,15 @@ def test_python_binding_rejects_tensors_of_another_device():
         with pytest.raises(ValueError, match=rf"^{name} is on cuda:1 but the current device"):
             call()
     assert fa.fa_kernel_launches() == before
+
+
+def test_ex2_rate_validates(L):
+    """The exponential-unit microbenchmark rejects a null output and block or
+    round counts out of range before any launch."""
+    before = fa.fa_kernel_launches()
+    assert L.fa_ex2_rate(None, 8, 16, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_rate(A, 0, 16, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_rate(A, 8, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_rate(A, (1 << 20) + 1, 16, None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_ex2_rate(A, 8, (1 << 24) + 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_kernel_launches() == before

@@ -76,3 +76,25 @@ def test_device_exp2_within_bound():
     fa.fa_exp2_check(m, yf, ye)
     torch.cuda.synchronize()
     assert (yf.abs() < 2.0 ** -125).all()
+
+
+@pytest.mark.gpu
+def test_device_ex2_rate_chains_reach_the_fixed_point():
+    """fa_ex2_rate iterates x <- 2^(-x), a contraction (|slope| = ln 2 * 2^-x
+    <= 0.6 on [1/2, 1]) whose fixed point x* solves x = 2^-x; after 64 rounds
+    each thread's sum of its eight chains is 8 x* to within the exponential's
+    error, and no lane is left unwritten."""
+    import torch
+    import exact_attention_online_gb300 as fa
+    xs = 0.5
+    for _ in range(200):
+        xs = 2.0 ** -xs
+    assert abs(xs - 2.0 ** -xs) < 1e-15
+    blocks = 12
+    out = torch.full((blocks * 256,), float("nan"), dtype=torch.float32, device="cuda")
+    fa.fa_ex2_rate(out, blocks, 64)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert np.abs(got - 8.0 * xs).max() <= 1e-4, np.abs(got - 8.0 * xs).max()
