@@ -755,8 +755,10 @@ __device__ __forceinline__ int seq_row(const int* __restrict__ cu, long long bh,
     return len;
 }
 
-// Per workspace row (b, h, i < Np): the two K = 16 extension tables of the
-// dK/dV kernel and a zeroed dQ accumulator row.  x = -LSE log2(e) (padded
+// Per workspace row (b, h, i) that the dK/dV kernel reads (i below the
+// sequence's length rounded up to 128: every one of the Np rows of a dense
+// batch): the two K = 16 extension tables of the dK/dV kernel and a zeroed dQ
+// accumulator row.  x = -LSE log2(e) (padded
 // rows: -1e30, so that P = 0 there) and y = -D = -<dO_i, O_i> are each split
 // into three bf16 terms (h + m + l holds x to about 24 bits):
 //   lse_ext row: cols 0-8 = x_h x_m x_l x_h x_m x_l x_h x_m x_l, 9-15 = 0
@@ -786,6 +788,10 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
         long long base = 0;
         const int len = in ? seq_row(cu, bh, H, N, seq_rows, base) : 0;
         const bool valid = in && i < len;
+        // Rows the dK/dV kernel reads or reduces into: the query blocks of the
+        // sequence, up to its length rounded up to 128 (all Np rows of a dense
+        // batch; packed sequences shorter than the longest one skip the rest).
+        const bool used = in && i < (len + kRowPad - 1) / kRowPad * kRowPad;
         float x = -1e30f;
         if (FULL && valid) x = -lse[base + i] * 1.4426950408889634f;
         float acc = 0.0f;
@@ -818,8 +824,8 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
         }
 #pragma unroll
         for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (in && sl == 0 && FULL) write_lse_ext_row(lse_ext, r, x);   // lane 0: -LSE row
-        if (in && sl == 1) {
+        if (used && sl == 0 && FULL) write_lse_ext_row(lse_ext, r, x);   // lane 0: -LSE row
+        if (used && sl == 1) {
             // lane 1 of the row: the d_ext row, -D in columns 9-11
             const float v = -acc;
             const float h = bf16_round(v), m = bf16_round(v - h), l = bf16_round(v - h - m);
@@ -828,7 +834,7 @@ fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ do
             *reinterpret_cast<uint4*>(row + 64) =                       // K half 1: + 8 rows x 8
                 make_uint4(pack_bf16x2(0.0f, h), pack_bf16x2(m, l), 0u, 0u);
         }
-        if (FULL && in) {
+        if (FULL && used) {
             float4* z = reinterpret_cast<float4*>(dq_acc + r * D) + sl * 2;
             z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
             z[1] = make_float4(0.f, 0.f, 0.f, 0.f);

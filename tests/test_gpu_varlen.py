@@ -117,6 +117,34 @@ def test_varlen_equal_lengths_match_dense():
     assert rel_fro(dense(grads[0]), f64(gd[0].cpu())) <= 1e-3
 
 
+def test_varlen_backward_reads_only_what_the_preprocess_writes():
+    """The preprocess writes a sequence's workspace rows only up to its length
+    rounded up to 128, not up to max_seqlen: a workspace filled with NaN bytes
+    and one filled with zeros give the same gradients (dK, dV bit for bit, dQ
+    up to the order of its fp32 additions), so nothing past those rows is
+    read.  Mixed lengths, with max_seqlen well above the longest one."""
+    for w in (SMALL[0], SMALL[4]):
+        q, k, v, do = make_varlen_inputs(w)
+        dev = torch.device("cuda:0")
+        qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+        cu = w.cu_seqlens().to(dev)
+        ms = w.max_seqlen + 200
+        o, lse = fa.attention_varlen(qd, kd, vd, cu, ms, w.causal, w.scale)
+        n = fa.fa_bwd_varlen_workspace_size(w.B, w.H, w.Hkv, ms, w.d)
+        out = []
+        for fill in (0xFF, 0x00):
+            ws = torch.full((n,), fill, dtype=torch.uint8, device=dev)
+            out.append(fa.attention_varlen_backward(qd, kd, vd, o, lse, dod, cu, ms, w.causal,
+                                                    w.scale, workspace=ws))
+        torch.cuda.synchronize()
+        assert fa.fa_device_status() == 0
+        (dq1, dk1, dv1), (dq2, dk2, dv2) = ([t.cpu() for t in g] for g in out)
+        for t in (dq1, dk1, dv1):
+            assert torch.isfinite(t.float()).all()
+        assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+        assert rel_fro(dq1, f64(dq2)) <= 1e-3
+
+
 def test_varlen_rejects():
     dev = torch.device("cuda:0")
     q = torch.zeros((2, 100, 64), dtype=torch.bfloat16, device=dev)
