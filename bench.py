@@ -55,20 +55,20 @@ L2_BYTES = 129 * 1024 * 1024
 # workload, together with the sha256 of the kernel source it was taken on.  A
 # source change makes the figure stale and it is then reported as null.
 NCU_TRAFFIC = {
-    # 236.5 MB read + 99.4 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 335.90e6, "src_sha": "8b297de3a9a409ec"},
+    # 238.1 MB read + 104.3 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 342.35e6, "src_sha": "634d08a0dee239a7"},
     # 133.1 MB read + 58.9 MB written (training forward), one launch
     ("fa_fwd", "mha_d64"): {"bytes": 192.05e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 1385.3 MB read + 637.6 MB written, one launch
-    ("fa_bwd_dkdv", "window"): {"bytes": 2022.89e6, "src_sha": "8b297de3a9a409ec"},
+    # 1384.9 MB read + 640.0 MB written, one launch
+    ("fa_bwd_dkdv", "window"): {"bytes": 2024.90e6, "src_sha": "634d08a0dee239a7"},
     # 204.7 MB read + 98.0 MB written, one launch
     ("fa_fwd", "window"): {"bytes": 302.66e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 426.9 MB read + 223.8 MB written, one launch
-    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 650.68e6, "src_sha": "8b297de3a9a409ec"},
+    # 427.1 MB read + 226.5 MB written, one launch
+    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 653.56e6, "src_sha": "634d08a0dee239a7"},
     # 559.2 MB read + 160.2 MB written (training forward), one launch
     ("fa_fwd", "gpt_long"): {"bytes": 719.39e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 771.2 MB read + 347.9 MB written, one launch
-    ("fa_bwd_dkdv", "gqa"): {"bytes": 1119.02e6, "src_sha": "8b297de3a9a409ec"},
+    # 762.0 MB read + 347.4 MB written, one launch
+    ("fa_bwd_dkdv", "gqa"): {"bytes": 1109.32e6, "src_sha": "634d08a0dee239a7"},
     # 409.2 MB read + 496.3 MB written (training forward, fp32 O), one launch
     ("fa_fwd", "gqa"): {"bytes": 905.51e6, "src_sha": "4ea3adf4eb4f28a7"},
     # 1.0739 GB read + 3.6 MB written, one launch
