@@ -7,7 +7,9 @@ One step = one pass of the whole hot path over one batch of synthetic input,
 as a training step makes it: fa_fwd_train (the online-softmax forward, whose
 epilogue also writes the backward's -LSE table and zeroes its dQ accumulator)
 then fa_bwd_train (D = rowsum(dO o O), the dK/dV kernel with the dQ reduction,
-the dQ conversion), four kernel launches on the current CUDA stream.  The sliding-window line runs fa_fwd_window + fa_bwd_window.  FLOPs per step use the
+the dQ conversion), four kernel launches on the current CUDA stream.  The
+sliding-window line runs the window's training pair (fa_fwd_window_train +
+fa_bwd_window_train), also four launches.  FLOPs per step use the
 headline count: forward 4*B*H*N^2*d (halved under the causal mask) and
 forward+backward 2.5x that.
 
@@ -61,8 +63,9 @@ NCU_TRAFFIC = {
     ("fa_fwd", "mha_d64"): {"bytes": 192.05e6, "src_sha": "4ea3adf4eb4f28a7"},
     # 1384.9 MB read + 640.0 MB written, one launch
     ("fa_bwd_dkdv", "window"): {"bytes": 2024.90e6, "src_sha": "634d08a0dee239a7"},
-    # 204.7 MB read + 98.0 MB written, one launch
-    ("fa_fwd", "window"): {"bytes": 302.66e6, "src_sha": "4ea3adf4eb4f28a7"},
+    # 247.3 MB read + 363.1 MB written (training forward: the -LSE table and
+    # the zeroed dQ accumulator), one launch
+    ("fa_fwd", "window"): {"bytes": 610.47e6, "src_sha": "4ea3adf4eb4f28a7"},
     # 427.1 MB read + 226.5 MB written, one launch
     ("fa_bwd_dkdv", "gpt_long"): {"bytes": 653.56e6, "src_sha": "634d08a0dee239a7"},
     # 559.2 MB read + 160.2 MB written (training forward), one launch
@@ -494,16 +497,18 @@ def run_native(args, w):
     stream = torch.cuda.current_stream(dev)
 
     # One training step through the public calls: the training forward (it
-    # also prepares the backward's workspace) and its backward; the sliding
-    # window keeps fa_fwd_window + fa_bwd_window.  step_inst() runs the same
-    # kernels through the stage entry points with an event after each, for
-    # per-kernel times (instrumented loop only).
+    # also prepares the backward's workspace) and its backward, the sliding
+    # window's pair for the window line.  step_inst() runs the same kernels
+    # through the stage entry points with an event after each, for per-kernel
+    # times (instrumented loop only).
     def run_step(q_, k_, v_, do_, o_, l_, dq_, dk_, dv_):
         if w.window:
-            fa.fa_fwd_window(q_, k_, v_, o_, l_, w.window, w.scale, stream)
-            if not fwd_only:
-                fa.fa_bwd_window(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, w.window, w.scale,
-                                 stream)
+            if fwd_only:
+                fa.fa_fwd_window(q_, k_, v_, o_, l_, w.window, w.scale, stream)
+                return
+            fa.fa_fwd_window_train(q_, k_, v_, o_, l_, work, w.window, w.scale, stream)
+            fa.fa_bwd_window_train(q_, k_, v_, o_, do_, dq_, dk_, dv_, work, w.window, w.scale,
+                                   stream)
             return
         if fwd_only:
             if precise:
@@ -523,9 +528,9 @@ def run_native(args, w):
             ev[1].record(stream)
             return
         if w.window:
-            fa.fa_fwd_window(qd, kd, vd, o, lse, w.window, w.scale, stream)
+            fa.fa_fwd_window_train(qd, kd, vd, o, lse, work, w.window, w.scale, stream)
             ev[1].record(stream)
-            fa.fa_bwd_preprocess(o, dod, lse, work, Hkv, stream)
+            fa.fa_bwd_preprocess_train(o, dod, work, Hkv, stream)
             ev[2].record(stream)
             fa.fa_bwd_dkdv_window(qd, kd, vd, dod, dk, dv, work, w.window, w.scale, stream)
             ev[3].record(stream)
@@ -618,9 +623,10 @@ def run_native(args, w):
                 "frac_of_sustained_peak": ach / peaks["bf16_tflops_sustained"],
                 "kernel_times": {"source": f"separate instrumented loop of {n_inst} steps "
                                            f"(events between kernels), after the timed region",
-                                 "kernels": ("fa_fwd = fa_fwd_train (forward + backward "
-                                             "workspace), fa_bwd_preprocess = -D only"
-                                             if not (fwd_only or w.window) else "as named"),
+                                 "kernels": ("fa_fwd = fa_fwd_train or fa_fwd_window_train "
+                                             "(forward + backward workspace), "
+                                             "fa_bwd_preprocess = -D only"
+                                             if not fwd_only else "as named"),
                                  "ms_per_step_instrumented": inst_ms,
                                  "ms": kern_ms,
                                  "share": {n: t / inst_ms for n, t in kern_ms.items()}},

@@ -34,7 +34,8 @@ __all__ = ["build", "lib", "LIB_PATH", "EXPORTS", "FAError", "fa_fwd", "fa_fwd_p
            "fa_fp8_buffer_size", "fa_fp8_quantize", "fa_fwd_fp8", "attention_fp8",
            "fa_fwd_decode_workspace_size", "fa_fwd_decode", "attention_decode",
            "fa_fwd_train", "fa_bwd_train", "fa_bwd_preprocess_train", "fa_exp2_check",
-           "fa_ex2_rate"]
+           "fa_ex2_rate",
+           "fa_fwd_window_train", "fa_bwd_window_train"]
 
 
 class FAError(RuntimeError):
@@ -304,6 +305,32 @@ def fa_bwd_window(q, k, v, o, dout, lse, dq, dk, dv, workspace, window: int, sca
                                _bf16(dout, "dout", qs), _f32(lse, "lse", ls), _bf16(dq, "dq", qs),
                                _bf16(dk, "dk", ks), _bf16(dv, "dv", ks), wp, wb, B, H, Hkv, N, d,
                                int(window), float(scale), _stream(stream)), "fa_bwd_window")
+
+
+def fa_fwd_window_train(q, k, v, o, lse, workspace, window: int, scale: float,
+                        stream=None) -> None:
+    """fa_fwd_window, plus the backward's workspace prepared for
+    fa_bwd_window_train."""
+    B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_fwd_window_train(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks),
+                                     _bf16(o, "o", qs), _f32(lse, "lse", ls), wp, wb, B, H, Hkv,
+                                     N, d, int(window), float(scale), _stream(stream)),
+           "fa_fwd_window_train")
+
+
+def fa_bwd_window_train(q, k, v, o, dout, dq, dk, dv, workspace, window: int, scale: float,
+                        stream=None) -> None:
+    """The backward of fa_fwd_window_train, on the workspace it prepared."""
+    B, H, Hkv, N, d = _dims(q, k)
+    qs, ks, ls = _shapes(B, H, Hkv, N, d)
+    wp, wb = _ws(workspace)
+    _check(lib().fa_bwd_window_train(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v", ks),
+                                     _bf16(o, "o", qs), _bf16(dout, "dout", qs),
+                                     _bf16(dq, "dq", qs), _bf16(dk, "dk", ks), _bf16(dv, "dv", ks),
+                                     wp, wb, B, H, Hkv, N, d, int(window), float(scale),
+                                     _stream(stream)), "fa_bwd_window_train")
 
 
 def _dims_of(t, name):

@@ -107,6 +107,11 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.fa_fwd_train_precise.restype = i
     L.fa_bwd_train.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
     L.fa_bwd_train.restype = i
+    L.fa_fwd_window_train.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, vp]
+    L.fa_fwd_window_train.restype = i
+    L.fa_bwd_window_train.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i,
+                                      f, vp]
+    L.fa_bwd_window_train.restype = i
     L.fa_bwd_train_precise.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i,
                                        f, vp]
     L.fa_bwd_train_precise.restype = i
@@ -177,4 +182,5 @@ EXPORTS = ["fa_fwd", "fa_fwd_precise", "fa_bwd_workspace_size", "fa_bwd", "fa_bw
            "fa_bwd_dkdv_window", "fa_fwd_varlen", "fa_bwd_varlen_workspace_size",
            "fa_bwd_varlen", "fa_fwd_train", "fa_fwd_train_precise", "fa_bwd_train",
            "fa_bwd_train_precise", "fa_bwd_preprocess_train", "fa_bwd_preprocess_train_precise", "fa_exp2_check",
-           "fa_ex2_rate"]
+           "fa_ex2_rate",
+           "fa_fwd_window_train", "fa_bwd_window_train"]

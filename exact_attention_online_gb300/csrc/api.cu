@@ -362,8 +362,8 @@ fa_status fa_bwd_window(const void* q, const void* k, const void* v, const void*
 static fa_status fwd_train_impl(const void* q, const void* k, const void* v, void* o,
                                 bool precise, float* lse, void* workspace,
                                 size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
-                                int causal, float scale, fa_stream_t stream) {
-    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+                                int causal, float scale, fa_stream_t stream, int window = 0) {
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale, window};
     fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
                                 check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(lse)});
     if (st != FA_OK) return st;
@@ -393,8 +393,9 @@ fa_status fa_fwd_train_precise(const void* q, const void* k, const void* v, floa
 static fa_status bwd_train_impl(const void* q, const void* k, const void* v, const void* o,
                                 bool o_f32, const void* dout, void* dq, void* dk, void* dv,
                                 void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
-                                int N, int d, int causal, float scale, fa_stream_t stream) {
-    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale};
+                                int N, int d, int causal, float scale, fa_stream_t stream,
+                                int window = 0) {
+    const Shape s{B, H, Hkv, N, d, causal ? 1 : 0, scale, window};
     fa_status st = first_error({check_shape(B, H, Hkv, N, d), check_scale(scale), check_ptr(q),
                                 check_ptr(k), check_ptr(v), check_ptr(o), check_ptr(dout),
                                 check_ptr(dq), check_ptr(dk), check_ptr(dv)});
@@ -427,6 +428,23 @@ fa_status fa_bwd_train_precise(const void* q, const void* k, const void* v, cons
                                int causal, float scale, fa_stream_t stream) {
     return bwd_train_impl(q, k, v, o, true, dout, dq, dk, dv, workspace, workspace_bytes, B, H,
                           Hkv, N, d, causal, scale, stream);
+}
+
+fa_status fa_fwd_window_train(const void* q, const void* k, const void* v, void* o, float* lse,
+                              void* workspace, size_t workspace_bytes, int B, int H, int Hkv,
+                              int N, int d, int window, float scale, fa_stream_t stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return fwd_train_impl(q, k, v, o, false, lse, workspace, workspace_bytes, B, H, Hkv, N, d, 1,
+                          scale, stream, window);
+}
+
+fa_status fa_bwd_window_train(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, int B, int H, int Hkv, int N, int d,
+                              int window, float scale, fa_stream_t stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return bwd_train_impl(q, k, v, o, false, dout, dq, dk, dv, workspace, workspace_bytes, B, H,
+                          Hkv, N, d, 1, scale, stream, window);
 }
 
 static fa_status pre_train_impl(const void* o, bool o_f32, const void* dout, void* workspace,

@@ -286,6 +286,23 @@ FA_API fa_status fa_bwd_train_precise(const void* q, const void* k, const void* 
                                       fa_stream_t stream);
 
 /*
+ * The training pair for the causal sliding window of fa_fwd_window() /
+ * fa_bwd_window(): fa_fwd_window_train is fa_fwd_window() (same arguments,
+ * outputs and errors) plus the workspace prepared as by fa_fwd_train();
+ * fa_bwd_window_train is fa_bwd_window() on that workspace (no lse
+ * argument), three launches.  window < 1 is FA_ERR_INVALID_ARG.
+ */
+FA_API fa_status fa_fwd_window_train(const void* q, const void* k, const void* v, void* o,
+                                     float* lse, void* workspace, size_t workspace_bytes, int B,
+                                     int H, int Hkv, int N, int d, int window, float scale,
+                                     fa_stream_t stream);
+FA_API fa_status fa_bwd_window_train(const void* q, const void* k, const void* v, const void* o,
+                                     const void* dout, void* dq, void* dk, void* dv,
+                                     void* workspace, size_t workspace_bytes, int B, int H,
+                                     int Hkv, int N, int d, int window, float scale,
+                                     fa_stream_t stream);
+
+/*
  * Stage 1 of fa_bwd_train(), for callers that time or interleave the stages:
  * -D into the workspace a training forward prepared (one launch; _precise:
  * fp32 o).  fa_bwd_train() is fa_bwd_preprocess_train() + fa_bwd_dkdv() +

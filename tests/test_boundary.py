@@ -162,6 +162,16 @@ def test_window_entry_points_validate(L):
                            None) == fa.FA_ERR_WORKSPACE
     assert L.fa_bwd_dkdv_window(A, A, A, A, A, A, A, ws, 1, 2, 1, 128, 64, 0, 0.125,
                                 None) == fa.FA_ERR_INVALID_ARG
+    # the training pair of the window: window < 1, a short workspace
+    for w in (0, -1):
+        assert L.fa_fwd_window_train(A, A, A, A, A, A, ws, 1, 2, 1, 128, 64, w, 0.125,
+                                     None) == fa.FA_ERR_INVALID_ARG
+        assert L.fa_bwd_window_train(A, A, A, A, A, A, A, A, A, ws, 1, 2, 1, 128, 64, w, 0.125,
+                                     None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_window_train(A, A, A, A, A, A, 16, 1, 2, 1, 128, 64, 8, 0.125,
+                                 None) == fa.FA_ERR_WORKSPACE
+    assert L.fa_bwd_window_train(A, A, A, A, A, A, A, A, A, 16, 1, 2, 1, 128, 64, 8, 0.125,
+                                 None) == fa.FA_ERR_WORKSPACE
     assert fa.fa_kernel_launches() == before
 
 

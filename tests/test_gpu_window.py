@@ -71,6 +71,35 @@ def test_window_small_full(w):
         assert e <= GRAD_REL_FRO, f"{name} relative Frobenius error {e:.3e}"
 
 
+@pytest.mark.parametrize("w", [SMALL[3], SMALL[5], SMALL[6], SMALL[7]], ids=lambda w: w.name)
+def test_window_train_pair_equals_window_pair(w):
+    """fa_fwd_window_train + fa_bwd_window_train on a workspace of NaN bytes
+    give the O, LSE, dK and dV of fa_fwd_window + fa_bwd_window bit for bit
+    and the same dQ up to the order of its fp32 additions: the training
+    forward leaves the backward a complete workspace."""
+    q, k, v, do = make_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    n = fa.fa_bwd_workspace_size(w.B, w.H, w.Hkv, w.N, w.d)
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=dev)
+    o, lse = torch.empty_like(qd), torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    fa.fa_fwd_window_train(qd, kd, vd, o, lse, ws, w.window, w.scale)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    fa.fa_bwd_window_train(qd, kd, vd, o, dod, dq, dk, dv, ws, w.window, w.scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    o2, l2 = fa.attention_window(qd, kd, vd, w.window, w.scale)
+    g2 = fa.attention_window_backward(qd, kd, vd, o2, l2, dod, w.window, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+    assert torch.equal(dk, g2[1]) and torch.equal(dv, g2[2])
+    assert rel_fro(dq.cpu(), f64(g2[0].cpu())) <= 1e-3
+    rq, rk, rv, _ = oracle.attn_bwd_window(f64(q), f64(k), f64(v), f64(do), w.window, w.scale)
+    for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        e = rel_fro(got.cpu(), ref)
+        assert e <= GRAD_REL_FRO, f"{name} relative Frobenius error {e:.3e}"
+
+
 def test_window_one_is_value_row():
     """W = 1: each query sees only its own key, so O_i = V_i bit for bit, LSE_i
     = scale <q_i, k_i>, dV_i = dO_i (up to bf16 rounding of the fp32 sum of
