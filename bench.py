@@ -715,7 +715,8 @@ def run_native(args, w):
                         dst.copy_(src_, non_blocking=True)
                     ev["out"][sl].record(s_out)
 
-        pipelined(2)
+        pipelined(8)    # untimed: the three streams and both buffer slots in use first
+        torch.cuda.synchronize()
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(s_in)
