@@ -462,6 +462,54 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ GPU side
+def pipelined_e2e(torch, dev, stream, dev_in, host_in, dev_out, host_out, compute, n, barrier):
+    """End-to-end steps as a training loop runs them: step k's inputs copied in
+    from pinned host memory on a stream of their own, its kernels on `stream`,
+    its outputs copied back on a third stream, and two slots of device
+    buffers, so that the copies of step k+1's inputs and of step k-1's outputs
+    overlap step k's kernels.  Every step copies all of host_in in and fills
+    all of host_out.  compute(*inputs, *outputs) launches one step on `stream`
+    (inputs and outputs of one slot).  Eight untimed steps and a device
+    synchronisation come first; returns the elapsed ms of the n timed steps,
+    from the first input copy to the last output copy."""
+    slot_in = [list(dev_in), [torch.empty_like(t) for t in dev_in]]
+    slot_out = [list(dev_out), [torch.empty_like(t) for t in dev_out]]
+    # one copy stream each way (two each way measured slower)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = {k_: [torch.cuda.Event(), torch.cuda.Event()] for k_ in ("in", "comp", "out")}
+
+    def run(steps):
+        for k_ in range(steps):
+            sl = k_ % 2
+            with torch.cuda.stream(s_in):
+                if k_ >= 2:
+                    s_in.wait_event(ev["comp"][sl])     # step k-2 done with these inputs
+                for dst, src in zip(slot_in[sl], host_in):
+                    dst.copy_(src, non_blocking=True)
+                ev["in"][sl].record(s_in)
+            stream.wait_event(ev["in"][sl])
+            if k_ >= 2:
+                stream.wait_event(ev["out"][sl])        # step k-2's outputs copied out
+            compute(*slot_in[sl], *slot_out[sl])
+            ev["comp"][sl].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["comp"][sl])
+                for dst, src in zip(host_out, slot_out[sl]):
+                    dst.copy_(src, non_blocking=True)
+                ev["out"][sl].record(s_out)
+
+    run(8)
+    torch.cuda.synchronize()
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_in)
+    run(n)
+    b.record(s_out)
+    barrier()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
 def run_native(args, w):
     import torch
     import torch.distributed as dist
@@ -677,53 +725,11 @@ def run_native(args, w):
         barrier()
         serial_ms = replicas.max_over_ranks(a.elapsed_time(b), dev)
 
-        # The same steps pipelined as a training loop would run them: three
-        # streams (host->device, compute, device->host) and two slots of
-        # device buffers, so that the copies of step k+1's inputs and of step
-        # k-1's outputs overlap the kernels of step k.  Every step still copies
-        # all of its inputs in and all of its outputs out.
-        dev_in = [[qd, kd, vd, dod], [torch.empty_like(t) for t in (qd, kd, vd, dod)]]
-        dev_out = [[o, lse, dq, dk, dv], [torch.empty_like(t) for t in (o, lse, dq, dk, dv)]]
-        host_in = [hq, hk, hv, hdo]
+        # The same steps pipelined as a training loop would run them.
         n_in = 3 if fwd_only else 4
-        n_out = len(outs_h)
-        # one copy stream each way (two each way measured slower)
-        s_in = torch.cuda.Stream(dev)
-        s_out = torch.cuda.Stream(dev)
-        ev = {k_: [torch.cuda.Event(), torch.cuda.Event()] for k_ in ("in", "comp", "out")}
-
-        def compute(slot):
-            run_step(*dev_in[slot], *dev_out[slot])
-
-        def pipelined(n):
-            for k_ in range(n):
-                sl = k_ % 2
-                with torch.cuda.stream(s_in):
-                    if k_ >= 2:
-                        s_in.wait_event(ev["comp"][sl])     # step k-2 done with these inputs
-                    for dst, src_ in zip(dev_in[sl][:n_in], host_in[:n_in]):
-                        dst.copy_(src_, non_blocking=True)
-                    ev["in"][sl].record(s_in)
-                stream.wait_event(ev["in"][sl])
-                if k_ >= 2:
-                    stream.wait_event(ev["out"][sl])        # step k-2's outputs copied out
-                compute(sl)
-                ev["comp"][sl].record(stream)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev["comp"][sl])
-                    for dst, src_ in zip(outs_h, dev_out[sl][:n_out]):
-                        dst.copy_(src_, non_blocking=True)
-                    ev["out"][sl].record(s_out)
-
-        pipelined(8)    # untimed: the three streams and both buffer slots in use first
-        torch.cuda.synchronize()
-        barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s_in)
-        pipelined(e2e_steps)
-        b.record(s_out)
-        barrier()
-        e_ms = replicas.max_over_ranks(a.elapsed_time(b), dev)
+        e_ms = pipelined_e2e(torch, dev, stream, [qd, kd, vd, dod], [hq, hk, hv, hdo][:n_in],
+                             [o, lse, dq, dk, dv], outs_h, run_step, e2e_steps, barrier)
+        e_ms = replicas.max_over_ranks(e_ms, dev)
         st = fa.fa_device_status(stream)
         if st != 0:
             raise RuntimeError(f"device status after e2e steps: {fa.fa_status_string(st)}")
@@ -930,10 +936,23 @@ def run_native_fp8(args, w):
         for _ in range(2):
             e2e_step()
         barrier()
-        n_e = max(3, min(args.steps // 2, 100))
-        e_ms = replicas.max_over_ranks(timed(e2e_step, n_e), dev)
+        n_e = max(50, min(args.steps // 2, 100))
+        serial_ms = replicas.max_over_ranks(timed(e2e_step, n_e), dev)
+
+        def compute(q_, k_, v_, o_, l_):
+            fa.fa_fp8_quantize(v_, buf, H, stream)
+            fa.fa_fwd_fp8(q_, k_, buf, o_, l_, w.causal, w.scale, stream)
+
+        e_ms = replicas.max_over_ranks(
+            pipelined_e2e(torch, dev, stream, [qd, kd, vd], [hq, hk, hv], [o, lse], [ho, hl],
+                          compute, n_e, barrier), dev)
         e2e = {"value": replicas.whole_job_rate(flops_step, n_e, ws, e_ms) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / n_e}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / n_e,
+               "steps": n_e,
+               "pipelined": "inputs of step k+1 copied in and outputs of step k-1 copied out "
+                            "while step k computes (three streams, two device buffer slots)",
+               "serial_value": replicas.whole_job_rate(flops_step, n_e, ws, serial_ms) / 1e12,
+               "serial_ms_per_step": serial_ms / n_e}
     if rank == 0:
         line = {
             "metric": "attention fwd TFLOP/s (P V in fp8 e4m3, Q K^T in bf16, causal) and % of "
@@ -1205,12 +1224,25 @@ def run_native_varlen(args):
         for _ in range(2):
             e2e_step()
         barrier()
-        n_e = max(3, min(args.steps // 2, 300))
-        e_ms = replicas.max_over_ranks(timed(e2e_step, n_e), dev)
+        n_e = max(50, min(args.steps // 2, 300))
+        serial_ms = replicas.max_over_ranks(timed(e2e_step, n_e), dev)
+
+        def compute(q_, k_, v_, do_, o_, l_, dq_, dk_, dv_):
+            fa.fa_fwd_varlen(q_, k_, v_, o_, l_, cu, ms, w.causal, w.scale, stream)
+            fa.fa_bwd_varlen(q_, k_, v_, o_, do_, l_, dq_, dk_, dv_, work, cu, ms, w.causal,
+                             w.scale, stream)
+
+        e_ms = replicas.max_over_ranks(
+            pipelined_e2e(torch, dev, stream, [qd, kd, vd, dod], hin, [o, lse, dq, dk, dv], hout,
+                          compute, n_e, barrier), dev)
         e2e = {"value": flops_step * n_e * ws / (e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
-               "ms_per_step": e_ms / n_e}
+               "ms_per_step": e_ms / n_e, "steps": n_e,
+               "pipelined": "inputs of step k+1 copied in and outputs of step k-1 copied out "
+                            "while step k computes (three streams, two device buffer slots)",
+               "serial_value": flops_step * n_e * ws / (serial_ms * 1e-3) / 1e12,
+               "serial_ms_per_step": serial_ms / n_e}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
