@@ -74,10 +74,10 @@ NCU_TRAFFIC = {
     ("fa_bwd_dkdv", "gqa"): {"bytes": 1109.32e6, "src_sha": "634d08a0dee239a7"},
     # 409.2 MB read + 496.3 MB written (training forward, fp32 O), one launch
     ("fa_fwd", "gqa"): {"bytes": 905.51e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 1.0739 GB read + 3.6 MB written, one launch
-    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0775e9, "src_sha": "38a45fea4cd86473"},
-    # 537.0 MB read + 3.4 MB written, one launch
-    ("fa_decode_split", "decode_mha_d64"): {"bytes": 540.33e6, "src_sha": "38a45fea4cd86473"},
+    # 1.0739 GB read + 3.7 MB written, one launch
+    ("fa_decode_split", "decode_gqa"): {"bytes": 1.0775e9, "src_sha": "70c5a2dfe3a994c9"},
+    # 537.0 MB read + 3.3 MB written, one launch (persistent, 304 CTAs)
+    ("fa_decode_split", "decode_mha_d64"): {"bytes": 540.28e6, "src_sha": "70c5a2dfe3a994c9"},
     # 386.7 MB read + 43.7 MB written, one launch
     ("fa_fwd_fp8", "long16k"): {"bytes": 430.44e6, "src_sha": "7bf0ac776fe40c35"},
 }
