@@ -171,7 +171,7 @@ bool make_tmap_u8_3d(CUtensorMap* map, const void* base, int inner, int rows, in
 
 size_t bwd_workspace_bytes(const Shape& s) {
     const size_t rows = (size_t)s.B * s.H * padded_rows(s.N);
-    return align256(rows * kExtCols * 2) * 2 + align256(rows * (size_t)s.d * 4);
+    return align256(rows * kExtCols * 2) * 2 + align256(rows * (size_t)s.d * 4) + align256(4);
 }
 
 BwdWorkspace bwd_workspace_carve(void* base, const Shape& s) {
@@ -181,6 +181,8 @@ BwdWorkspace bwd_workspace_carve(void* base, const Shape& s) {
     w.lse_ext = reinterpret_cast<uint16_t*>(p);
     w.d_ext = reinterpret_cast<uint16_t*>(p + align256(rows * kExtCols * 2));
     w.dq_acc = reinterpret_cast<float*>(p + 2 * align256(rows * kExtCols * 2));
+    w.work = reinterpret_cast<int*>(p + 2 * align256(rows * kExtCols * 2) +
+                                    align256(rows * (size_t)s.d * 4));
     return w;
 }
 

@@ -6,8 +6,11 @@
 //
 //   preprocess  writes -D_i = -<dO_i, O_i> and -LSE_i * log2(e) (padded rows:
 //               -inf, so P = 0 there), both negated so that the main kernel
-//               adds them in paired fp32 FMAs; zeroes the dQ accumulator.
-//   dkdv        one CTA per (batch, kv head, block j of 128 keys).  K_j and V_j
+//               adds them in paired fp32 FMAs; zeroes the dQ accumulator and
+//               the dkdv kernel's work counter.
+//   dkdv        one work item per (batch, kv head, block j of 128 keys), taken
+//               by persistent CTAs (one an SM) from a counter in the
+//               workspace.  K_j and V_j
 //               stay in shared memory; dK_j and dV_j accumulate in TMEM over
 //               every query head of the GQA group and every query block i that
 //               can see the keys (causal: i*Br + Br - 1 >= 128 j).  Per block i:
@@ -103,14 +106,18 @@ struct BwdParams {
     const uint16_t* lse_ext;          // workspace tables (fa_internal.h)
     const uint16_t* d_ext;
     float* dq_acc;
+    int* work;                        // next work item (zero on entry, left zero)
+    int n_bg, n_items;                // B * Hkv; work items (B * Hkv * key blocks)
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     DeviceStatus* status;
 };
 
-// What one dK/dV CTA works on: (batch, kv head, key block j) and the range of
-// query blocks (of br rows) that see some key of the block.  The CTAs go out
-// in blockIdx order.  Dense causal batches: key-block-major, so that the
+// What one dK/dV work item covers: (batch, kv head, key block j) and the
+// range of query blocks (of br rows) that see some key of the block.  The
+// persistent CTAs take the items in index order from the work counter, so
+// that, as with one CTA per item, the hardware-like first-come order decides
+// which SM runs which item.  Dense causal batches: key-block-major, so that the
 // longest CTAs (small j, every query block after them) start first and the
 // shortest fill the tail (a CPU model of the bench workloads puts the busiest
 // SM within 1-2 % of the mean instead of 7-14 %; measured: dK/dV +2 % to
@@ -125,19 +132,19 @@ struct BwdCta {
     bool idle;   // a key block past its packed sequence's end: nothing to do
 };
 template <bool CAUSAL, bool WINDOW, bool VARLEN>
-__device__ __forceinline__ BwdCta bwd_cta(const BwdParams& p, int br) {
+__device__ __forceinline__ BwdCta bwd_cta(const BwdParams& p, int br, int item) {
     BwdCta c;
     constexpr bool kKeyMajor = CAUSAL && !VARLEN;
     const int n_kblk = (p.N + kBN - 1) / kBN;
-    const int n_bg = gridDim.x / n_kblk;          // B * Hkv
+    const int n_bg = p.n_bg;                      // B * Hkv
     if (kKeyMajor) {
-        const int chunk = blockIdx.x / (p.chunk * n_kblk), loc = blockIdx.x % (p.chunk * n_kblk);
+        const int chunk = item / (p.chunk * n_kblk), loc = item % (p.chunk * n_kblk);
         const int width = min(p.chunk, n_bg - chunk * p.chunk);
         c.jblk = loc / width;
         c.bg = chunk * p.chunk + loc % width;
     } else {
-        c.jblk = blockIdx.x % n_kblk;
-        c.bg = blockIdx.x / n_kblk;
+        c.jblk = item % n_kblk;
+        c.bg = item / n_kblk;
     }
     c.b = c.bg / p.Hkv;
     c.g = c.bg % p.Hkv;
@@ -205,15 +212,17 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                                ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_kv, bar_full[2], bar_empty[2], bar_s, bar_dp, bar_p, bar_ds,
         bar_dq_full, bar_dq_free, bar_done, bar_ktm;
+    // Persistent CTAs: the producer takes work items from p.work and passes
+    // them on through a two-slot ring (-1: no more); an item's dK, dV leave
+    // tensor memory (bar_acc_free) before the next item's MMAs overwrite them.
+    __shared__ uint64_t bar_item_full[2], bar_item_empty[2], bar_acc_free;
+    __shared__ int item_sh[2];
+    constexpr int kItemConsumers = kComputeWarps + 4 + (kTwoIssuers ? 2 : 1);
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     const WaitCtx wc{p.status, &abort_sh};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR);
-    if (cta.idle) return;   // the whole CTA leaves before any barrier or TMEM is set up
-    const int jblk = cta.jblk, b = cta.b, g = cta.g, tok0 = cta.tok0, seq_len = cta.seq_len;
-    const int z_kv = cta.z_kv, i_start = cta.i_start, n_i = cta.n_i, n_it = cta.n_it;
 
     uint8_t* sK = smem + Cfg::kOffK;
     uint8_t* sV = smem + Cfg::kOffV;
@@ -241,6 +250,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(&bar_dq_free, kReadoutThreads);
         mbar_init(&bar_done, kTwoIssuers ? 2 : 1);   // one arrival per MMA issuer
         mbar_init(&bar_ktm, kComputeThreads);        // K_j copied into tensor memory
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bar_item_full[s], 1);
+            mbar_init(&bar_item_empty[s], kItemConsumers);
+        }
+        mbar_init(&bar_acc_free, kComputeThreads);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -252,6 +266,24 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
+    // The work item of rank n for a consumer warp (all lanes) or thread: false
+    // if the wait gave up; item < 0 when there is no more work.
+    auto next_item_warp = [&](int n, int& item) -> bool {
+        const int slot = n & 1;
+        if (!fa_wait_warp(&bar_item_full[slot], (n >> 1) & 1, 65, wc)) return false;
+        item = item_sh[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_item_empty[slot]);
+        return true;
+    };
+    auto next_item_thread = [&](int n, int& item) -> bool {
+        const int slot = n & 1;
+        if (!fa_wait(&bar_item_full[slot], (n >> 1) & 1, 65, wc)) return false;
+        item = item_sh[slot];
+        mbar_arrive(&bar_item_empty[slot]);
+        return true;
+    };
+
     // One register-budget change per warpgroup (all its warps, same
     // instruction); each role below is dominated by exactly one of them.
     if (warp < kComputeWarps) {
@@ -261,147 +293,164 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int quarter = warp & 3, hf = warp >> 2;
         const int rl = quarter * 32 + lane;          // key row within the block
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        const int key = jblk * kBN + rl;
         const int cb = hf * HALF;                    // first query column of this warp
         const float c = p.scale_log2;
-        bool ok = n_it > 0;
-        if (Cfg::kKInTmem && ok) {
-            // K_j -> tensor memory: this thread's key row, the 64 head-dim
-            // columns of its half (one 128-byte swizzled row of chunk hf),
-            // as 32 bf16 pairs; the S^T MMAs take it from there.
-            if (!fa_wait_warp(&bar_kv, 0, 64, wc)) {
-                ok = false;
-            } else {
-                const uint8_t* rowp = sK + hf * (kBN * 128) + rl * 128;
-                uint32_t kw[32];
+        bool ok = true;
+        int gi = 0, nb = 0;   // query-block steps and work items of this CTA so far
+        for (int n = 0; ok; ++n) {
+            int item;
+            if (!next_item_warp(n, item) || item < 0) break;
+            const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+            if (cta.idle || cta.n_it == 0) continue;
+            const int jblk = cta.jblk, tok0 = cta.tok0, seq_len = cta.seq_len, z_kv = cta.z_kv;
+            const int i_start = cta.i_start, n_i = cta.n_i, n_it = cta.n_it;
+            const int key = jblk * kBN + rl;
+            if (Cfg::kKInTmem) {
+                // K_j -> tensor memory: this thread's key row, the 64 head-dim
+                // columns of its half (one 128-byte swizzled row of chunk hf),
+                // as 32 bf16 pairs; the S^T MMAs take it from there.
+                if (!fa_wait_warp(&bar_kv, nb & 1, 64, wc)) {
+                    ok = false;
+                } else {
+                    const uint8_t* rowp = sK + hf * (kBN * 128) + rl * 128;
+                    uint32_t kw[32];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((u ^ (rl & 7)) * 16));
-                    kw[4 * u + 0] = x.x;
-                    kw[4 * u + 1] = x.y;
-                    kw[4 * u + 2] = x.z;
-                    kw[4 * u + 3] = x.w;
+                    for (int u = 0; u < 8; ++u) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(rowp + ((u ^ (rl & 7)) * 16));
+                        kw[4 * u + 0] = x.x;
+                        kw[4 * u + 1] = x.y;
+                        kw[4 * u + 2] = x.z;
+                        kw[4 * u + 3] = x.w;
+                    }
+                    tmem_st32(lane_addr + Cfg::kColKT + hf * 32, kw);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(&bar_ktm);
                 }
-                tmem_st32(lane_addr + Cfg::kColKT + hf * 32, kw);
+            }
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int git = gi + it;
+                const int i = i_start + it % n_i;
+                // (no wait for the Q_i / dO_i stage: these warps read neither, and
+                // S^T(i) completing implies the stage has landed)
+                if (!fa_wait_warp(&bar_s, git & 1, 61, wc)) { ok = false; break; }
+                tc_fence_after();
+                const int q0 = i * BR;
+                const bool need_mask = (CAUSAL && (q0 < jblk * kBN + kBN - 1 ||
+                                                   (WINDOW && q0 + BR - 1 > jblk * kBN + p.window - 1))) ||
+                                       (jblk * kBN + kBN > seq_len);
+                // column e visible iff key_lim <= e <= key_hi
+                const int key_lim = CAUSAL ? key - q0 : -1;
+                const int key_hi = WINDOW ? key + p.window - 1 - q0 : BR;
+                const bool key_valid = key < seq_len;
+                // P^T = 2^(S'^T c) with S'^T = S^T - LSE log2(e) / c from the
+                // tensor core, kept in fp32 for dS; bf16 copy into TMEM over this
+                // warp's own S^T columns (already read).  Two columns per
+                // paired-fp32 instruction.
+                float pf[HALF];
+                const uint64_t c2 = f2(c, c);
+#pragma unroll
+                for (int ch = 0; ch < HALF / 32; ++ch) {
+                    uint32_t sr[32];
+                    tmem_ld32(lane_addr + Cfg::kColS + cb + ch * 32, sr);
+                    tmem_ld_wait(sr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const int qe = cb + ch * 32 + 2 * e2;
+                        float x0, x1;
+                        f2_split(f2_mul(f2(__uint_as_float(sr[2 * e2]), __uint_as_float(sr[2 * e2 + 1])),
+                                        c2),
+                                 x0, x1);
+                        float p0 = ex2(x0), p1 = ex2(x1);
+                        if (need_mask) {
+                            if (qe < key_lim || qe > key_hi || !key_valid) p0 = 0.0f;
+                            if (qe + 1 < key_lim || qe + 1 > key_hi || !key_valid) p1 = 0.0f;
+                        }
+                        pf[ch * 32 + 2 * e2] = p0;
+                        pf[ch * 32 + 2 * e2 + 1] = p1;
+                        pk[e2] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(lane_addr + Cfg::kColS + cb + ch * 16, pk);
+                }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bar_ktm);
-            }
-        }
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int i = i_start + it % n_i;
-            // (no wait for the Q_i / dO_i stage: these warps read neither, and
-            // S^T(i) completing implies the stage has landed)
-            if (!fa_wait_warp(&bar_s, it & 1, 61, wc)) { ok = false; break; }
-            tc_fence_after();
-            const int q0 = i * BR;
-            const bool need_mask = (CAUSAL && (q0 < jblk * kBN + kBN - 1 ||
-                                               (WINDOW && q0 + BR - 1 > jblk * kBN + p.window - 1))) ||
-                                   (jblk * kBN + kBN > seq_len);
-            // column e visible iff key_lim <= e <= key_hi
-            const int key_lim = CAUSAL ? key - q0 : -1;
-            const int key_hi = WINDOW ? key + p.window - 1 - q0 : BR;
-            const bool key_valid = key < seq_len;
-            // P^T = 2^(S'^T c) with S'^T = S^T - LSE log2(e) / c from the
-            // tensor core, kept in fp32 for dS; bf16 copy into TMEM over this
-            // warp's own S^T columns (already read).  Two columns per
-            // paired-fp32 instruction.
-            float pf[HALF];
-            const uint64_t c2 = f2(c, c);
-#pragma unroll
-            for (int ch = 0; ch < HALF / 32; ++ch) {
-                uint32_t sr[32];
-                tmem_ld32(lane_addr + Cfg::kColS + cb + ch * 32, sr);
-                tmem_ld_wait(sr);
-                uint32_t pk[16];
-#pragma unroll
-                for (int e2 = 0; e2 < 16; ++e2) {
-                    const int qe = cb + ch * 32 + 2 * e2;
-                    float x0, x1;
-                    f2_split(f2_mul(f2(__uint_as_float(sr[2 * e2]), __uint_as_float(sr[2 * e2 + 1])),
-                                    c2),
-                             x0, x1);
-                    float p0 = ex2(x0), p1 = ex2(x1);
-                    if (need_mask) {
-                        if (qe < key_lim || qe > key_hi || !key_valid) p0 = 0.0f;
-                        if (qe + 1 < key_lim || qe + 1 > key_hi || !key_valid) p1 = 0.0f;
-                    }
-                    pf[ch * 32 + 2 * e2] = p0;
-                    pf[ch * 32 + 2 * e2 + 1] = p1;
-                    pk[e2] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(lane_addr + Cfg::kColS + cb + ch * 16, pk);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bar_p);
+                mbar_arrive(&bar_p);
 
-            // dS^T = P^T o (dP^T - D) -> bf16, swizzled [key][query] tile in
-            // smem; dP^T - D comes from the tensor core.
-            if (!fa_wait_warp(&bar_dp, it & 1, 62, wc)) { ok = false; break; }
-            tc_fence_after();
+                // dS^T = P^T o (dP^T - D) -> bf16, swizzled [key][query] tile in
+                // smem; dP^T - D comes from the tensor core.
+                if (!fa_wait_warp(&bar_dp, git & 1, 62, wc)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll
-            for (int ch = 0; ch < HALF / 32; ++ch) {
-                uint32_t dpr[32];
-                tmem_ld32(lane_addr + Cfg::kColDP + cb + ch * 32, dpr);
-                tmem_ld_wait(dpr);
-                uint32_t dsk[16];
+                for (int ch = 0; ch < HALF / 32; ++ch) {
+                    uint32_t dpr[32];
+                    tmem_ld32(lane_addr + Cfg::kColDP + cb + ch * 32, dpr);
+                    tmem_ld_wait(dpr);
+                    uint32_t dsk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float d0, d1;
-                    f2_split(f2_mul(f2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]),
-                                    f2(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1]))),
-                             d0, d1);
-                    dsk[e] = pack_bf16x2(d0, d1);
+                    for (int e = 0; e < 16; ++e) {
+                        float d0, d1;
+                        f2_split(f2_mul(f2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]),
+                                        f2(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1]))),
+                                 d0, d1);
+                        dsk[e] = pack_bf16x2(d0, d1);
+                    }
+                    const int qc = (cb + ch * 32) >> 6;       // 64-query chunk of the tile
+                    const int u0 = ((cb + ch * 32) & 63) >> 3;  // first 16-byte unit in the row
+                    uint8_t* rowp = sDS + qc * (kBN * 128) + rl * 128;
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const int unit = u0 + u4;
+                        *reinterpret_cast<uint4*>(rowp + ((unit ^ (rl & 7)) * 16)) =
+                            make_uint4(dsk[u4 * 4 + 0], dsk[u4 * 4 + 1], dsk[u4 * 4 + 2],
+                                       dsk[u4 * 4 + 3]);
+                    }
                 }
-                const int qc = (cb + ch * 32) >> 6;       // 64-query chunk of the tile
-                const int u0 = ((cb + ch * 32) & 63) >> 3;  // first 16-byte unit in the row
-                uint8_t* rowp = sDS + qc * (kBN * 128) + rl * 128;
-#pragma unroll
-                for (int u4 = 0; u4 < 4; ++u4) {
-                    const int unit = u0 + u4;
-                    *reinterpret_cast<uint4*>(rowp + ((unit ^ (rl & 7)) * 16)) =
-                        make_uint4(dsk[u4 * 4 + 0], dsk[u4 * 4 + 1], dsk[u4 * 4 + 2],
-                                   dsk[u4 * 4 + 3]);
-                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bar_ds);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&bar_ds);
-        }
-        // ---------------------------------------------------- dK, dV epilogue
-        if (ok && fa_wait_warp(&bar_done, 0, 63, wc)) {
-            tc_fence_after();
-            const bool valid = key < seq_len;
-            const size_t row = ((size_t)z_kv * p.rows + tok0 + (valid ? key : 0)) * D;
-            const int c_lo = hf * (D / 2);
+            // ---------------------------------------------------- dK, dV epilogue
+            if (ok && fa_wait_warp(&bar_done, nb & 1, 63, wc)) {
+                tc_fence_after();
+                const bool valid = key < seq_len;
+                const size_t row = ((size_t)z_kv * p.rows + tok0 + (valid ? key : 0)) * D;
+                const int c_lo = hf * (D / 2);
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which ? Cfg::kColDV : Cfg::kColDK;
-                const float mul = which ? 1.0f : p.scale;
-                __nv_bfloat16* dst = (which ? p.dv : p.dk) + row;
+                for (int which = 0; which < 2; ++which) {
+                    const uint32_t col = which ? Cfg::kColDV : Cfg::kColDK;
+                    const float mul = which ? 1.0f : p.scale;
+                    __nv_bfloat16* dst = (which ? p.dv : p.dk) + row;
 #pragma unroll
-                for (int c0 = c_lo; c0 < c_lo + D / 2; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(lane_addr + col + c0, r);
-                    tmem_ld_wait(r);
-                    if (valid) {
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+                    for (int c0 = c_lo; c0 < c_lo + D / 2; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_addr + col + c0, r);
+                        tmem_ld_wait(r);
+                        if (valid) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * mul,
-                                              __uint_as_float(r[q4 * 8 + 1]) * mul);
-                            w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * mul,
-                                              __uint_as_float(r[q4 * 8 + 3]) * mul);
-                            w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * mul,
-                                              __uint_as_float(r[q4 * 8 + 5]) * mul);
-                            w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * mul,
-                                              __uint_as_float(r[q4 * 8 + 7]) * mul);
-                            d4[q4] = w;
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                uint4 w;
+                                w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * mul,
+                                                  __uint_as_float(r[q4 * 8 + 1]) * mul);
+                                w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * mul,
+                                                  __uint_as_float(r[q4 * 8 + 3]) * mul);
+                                w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * mul,
+                                                  __uint_as_float(r[q4 * 8 + 5]) * mul);
+                                w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * mul,
+                                                  __uint_as_float(r[q4 * 8 + 7]) * mul);
+                                d4[q4] = w;
+                            }
                         }
                     }
                 }
+                // dK, dV read out: the next item's first dV / dK MMA may overwrite them
+                tc_fence_before();
+                mbar_arrive(&bar_acc_free);
+            } else {
+                ok = false;
             }
+            gi += n_it;
+            ++nb;
         }
     } else if (warp >= kReadoutWarp0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsReadout));
@@ -412,202 +461,265 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
         const int rl = quarter * 32 + lane;
         const bool leader = (warp == kReadoutWarp0 && lane == 0);
-        bool ok = n_it > 0;
-        for (int it = 0; ok && it < n_it; ++it) {
-            const int hq = g * p.G + it / n_i;
-            const int i = i_start + it % n_i;
-            const int bh = b * p.H + hq;
-            // The four read-out warps leave together (they meet at named
-            // barriers below), so a failed wait in one of them stops all.
-            const bool w_ok = fa_wait_warp(&bar_dq_full, it & 1, 70, wc);
-            if (named_bar_or(1, kReadoutThreads, !w_ok)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t r0[32], r1[32];
-            tmem_ld32(lane_addr + Cfg::kColDQ, r0);
-            tmem_ld32(lane_addr + Cfg::kColDQ + 32, r1);
-            tmem_ld_wait(r0);
-            asm volatile("" : FA_R32(r1) : : "memory");
-            tc_fence_before();
-            mbar_arrive(&bar_dq_free);
-            float* stg = sStage + (it & 1) * (BR * D);
-            if (leader) bulk_wait_group_read<1>();   // the copy that last read this buffer
-            named_bar_sync(1, kReadoutThreads);
-            if (D == 128) {
-                // dQ^T: lane = head-dim index dd, column = query -> stg[q][dd]
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    stg[e * D + rl] = __uint_as_float(r0[e]);
-                    stg[(32 + e) * D + rl] = __uint_as_float(r1[e]);
-                }
-            } else {
-                // dQ: lane = query row, column = head-dim index.  Two boxes of
-                // 32 columns, 128-byte swizzled (16-byte piece u of row r at
-                // u ^ (r & 7)), so eight neighbouring rows write eight
-                // different bank groups; a tensor reduce undoes the swizzle.
-#pragma unroll
-                for (int box = 0; box < 2; ++box) {
-                    uint8_t* rowp = reinterpret_cast<uint8_t*>(stg) + box * (128 * 128) + rl * 128;
-                    const uint32_t* src = box ? r1 : r0;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        *reinterpret_cast<uint4*>(rowp + ((u ^ (rl & 7)) * 16)) =
-                            make_uint4(src[4 * u], src[4 * u + 1], src[4 * u + 2], src[4 * u + 3]);
-                }
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(1, kReadoutThreads);
-            if (leader) {
+        bool ok = true;
+        int gi = 0;   // query-block steps of this CTA so far
+        for (int n = 0; ok; ++n) {
+            int item;
+            if (!next_item_warp(n, item) || item < 0) break;
+            const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+            if (cta.idle || cta.n_it == 0) continue;
+            const int b = cta.b, g = cta.g, i_start = cta.i_start, n_i = cta.n_i, n_it = cta.n_it;
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int git = gi + it;
+                const int hq = g * p.G + it / n_i;
+                const int i = i_start + it % n_i;
+                const int bh = b * p.H + hq;
+                // The four read-out warps leave together (they meet at named
+                // barriers below), so a failed wait in one of them stops all.
+                const bool w_ok = fa_wait_warp(&bar_dq_full, git & 1, 70, wc);
+                if (named_bar_or(1, kReadoutThreads, !w_ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                tmem_ld32(lane_addr + Cfg::kColDQ, r0);
+                tmem_ld32(lane_addr + Cfg::kColDQ + 32, r1);
+                tmem_ld_wait(r0);
+                asm volatile("" : FA_R32(r1) : : "memory");
+                tc_fence_before();
+                mbar_arrive(&bar_dq_free);
+                float* stg = sStage + (git & 1) * (BR * D);
+                if (leader) bulk_wait_group_read<1>();   // the copy that last read this buffer
+                named_bar_sync(1, kReadoutThreads);
                 if (D == 128) {
-                    bulk_reduce_add_f32(p.dq_acc + ((size_t)bh * p.Np + (size_t)i * BR) * D, stg,
-                                        BR * D * 4);
+                    // dQ^T: lane = head-dim index dd, column = query -> stg[q][dd]
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        stg[e * D + rl] = __uint_as_float(r0[e]);
+                        stg[(32 + e) * D + rl] = __uint_as_float(r1[e]);
+                    }
                 } else {
-                    const int y = bh * p.Np + i * BR;
-                    tma_reduce_add_2d(&tm_dq, stg, 0, y);
-                    tma_reduce_add_2d(&tm_dq, reinterpret_cast<uint8_t*>(stg) + 128 * 128, 32, y);
+                    // dQ: lane = query row, column = head-dim index.  Two boxes of
+                    // 32 columns, 128-byte swizzled (16-byte piece u of row r at
+                    // u ^ (r & 7)), so eight neighbouring rows write eight
+                    // different bank groups; a tensor reduce undoes the swizzle.
+#pragma unroll
+                    for (int box = 0; box < 2; ++box) {
+                        uint8_t* rowp = reinterpret_cast<uint8_t*>(stg) + box * (128 * 128) + rl * 128;
+                        const uint32_t* src = box ? r1 : r0;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            *reinterpret_cast<uint4*>(rowp + ((u ^ (rl & 7)) * 16)) =
+                                make_uint4(src[4 * u], src[4 * u + 1], src[4 * u + 2], src[4 * u + 3]);
+                    }
                 }
-                bulk_commit_group();
+                fence_proxy_async_smem();
+                named_bar_sync(1, kReadoutThreads);
+                if (leader) {
+                    if (D == 128) {
+                        bulk_reduce_add_f32(p.dq_acc + ((size_t)bh * p.Np + (size_t)i * BR) * D, stg,
+                                            BR * D * 4);
+                    } else {
+                        const int y = bh * p.Np + i * BR;
+                        tma_reduce_add_2d(&tm_dq, stg, 0, y);
+                        tma_reduce_add_2d(&tm_dq, reinterpret_cast<uint8_t*>(stg) + 128 * 128, 32, y);
+                    }
+                    bulk_commit_group();
+                }
             }
+            gi += n_it;
         }
         if (leader) bulk_wait_group<0>();
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
         if (warp == kProducerWarp) {
-            if (lane == 0 && n_it > 0) {
+            if (lane == 0) {
                 tma_prefetch_desc(&tm_q);
                 tma_prefetch_desc(&tm_do);
-                mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
-                for (int c = 0; c < D / 64; ++c) {
-                    tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64, tok0 + jblk * kBN,
-                                z_kv);
-                    tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64, tok0 + jblk * kBN,
-                                z_kv);
-                }
-                int issued = 0;
-                for (int it = 0; it < n_it; ++it) {
-                    const int st = it & 1, u = it >> 1;
-                    if (it >= 2 && !fa_wait(&bar_empty[st], (u - 1) & 1, 40, wc)) break;
-                    const int hq = g * p.G + it / n_i;
-                    const int i = i_start + it % n_i;
-                    const int bh = b * p.H + hq;
-                    const int z_q = VARLEN ? hq : bh;
-                    mbar_arrive_expect_tx(&bar_full[st], Cfg::kStageBytes);
-                    for (int c = 0; c < D / 64; ++c) {
-                        tma_load_3d(sQ + st * Cfg::kQBytes + c * (BR * 128), &tm_q, &bar_full[st],
-                                    c * 64, tok0 + i * BR, z_q);
-                        tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do,
-                                    &bar_full[st], c * 64, tok0 + i * BR, z_q);
+                int gi = 0, nb = 0;          // query-block steps and work items so far
+                int issued = 0, kv_issued = 0;
+                bool ok = true;
+                for (int n = 0; ok; ++n) {
+                        const int slot = n & 1;
+                        if (n >= 2 && !fa_wait(&bar_item_empty[slot], ((n >> 1) - 1) & 1, 66, wc))
+                            break;
+                        // Every CTA's last take finds no item; the last of those
+                        // takes leaves the counter zero for the next launch.
+                        const int old = atomicAdd(p.work, 1);
+                        const int item = old < p.n_items ? old : -1;
+                        if (old == p.n_items + (int)gridDim.x - 1) *p.work = 0;
+                        item_sh[slot] = item;
+                        mbar_arrive(&bar_item_full[slot]);
+                        if (item < 0) break;
+                        const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+                        if (cta.idle || cta.n_it == 0) continue;
+                        const int jblk = cta.jblk, b = cta.b, g = cta.g, tok0 = cta.tok0;
+                        const int z_kv = cta.z_kv, i_start = cta.i_start, n_i = cta.n_i;
+                        const int n_it = cta.n_it;
+                        // K_j, V_j over the previous item's, whose MMAs have completed
+                        if (nb > 0 && !fa_wait(&bar_done, (nb - 1) & 1, 42, wc)) break;
+                        mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
+                        for (int c = 0; c < D / 64; ++c) {
+                            tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64,
+                                        tok0 + jblk * kBN, z_kv);
+                            tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64,
+                                        tok0 + jblk * kBN, z_kv);
+                        }
+                        ++kv_issued;
+                        for (int it = 0; it < n_it; ++it) {
+                            const int git = gi + it;
+                            const int st = git & 1, u = git >> 1;
+                            if (git >= 2 && !fa_wait(&bar_empty[st], (u - 1) & 1, 40, wc)) {
+                                ok = false;
+                                break;
+                            }
+                            const int hq = g * p.G + it / n_i;
+                            const int i = i_start + it % n_i;
+                            const int bh = b * p.H + hq;
+                            const int z_q = VARLEN ? hq : bh;
+                            mbar_arrive_expect_tx(&bar_full[st], Cfg::kStageBytes);
+                            for (int c = 0; c < D / 64; ++c) {
+                                tma_load_3d(sQ + st * Cfg::kQBytes + c * (BR * 128), &tm_q,
+                                            &bar_full[st], c * 64, tok0 + i * BR, z_q);
+                                tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do,
+                                            &bar_full[st], c * 64, tok0 + i * BR, z_q);
+                            }
+                            const size_t xrow = (size_t)bh * p.Np + (size_t)i * BR;
+                            bulk_load(sExt + (2 * st) * Cfg::kExtBytes, p.lse_ext + xrow * kExtCols,
+                                      Cfg::kExtBytes, &bar_full[st]);
+                            bulk_load(sExt + (2 * st + 1) * Cfg::kExtBytes,
+                                      p.d_ext + xrow * kExtCols, Cfg::kExtBytes, &bar_full[st]);
+                            issued = git + 1;
+                        }
+                        gi += n_it;
+                        ++nb;
                     }
-                    const size_t xrow = (size_t)bh * p.Np + (size_t)i * BR;
-                    bulk_load(sExt + (2 * st) * Cfg::kExtBytes, p.lse_ext + xrow * kExtCols,
-                              Cfg::kExtBytes, &bar_full[st]);
-                    bulk_load(sExt + (2 * st + 1) * Cfg::kExtBytes, p.d_ext + xrow * kExtCols,
-                              Cfg::kExtBytes, &bar_full[st]);
-                    issued = it + 1;
-                }
-                if (abort_sh) {
-                    fa_wait(&bar_kv, 0, 41, WaitCtx{p.status, nullptr});
-                    for (int it = max(0, issued - 2); it < issued; ++it)
-                        fa_wait(&bar_full[it & 1], (it >> 1) & 1, 41, WaitCtx{p.status, nullptr});
-                }
-            }
-            __syncwarp();
-        } else if (!kTwoIssuers && warp == kMmaWarp) {
-            // One MMA-issuing thread (d = 64): dV, S^T for the next block, dK,
-            // the dQ partial, dP^T for the next block, in that order.
-            if (lane == 0 && n_it > 0) {
-                constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
-                constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
-                constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
-                const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
-                               sdo = smem_u32(sDO), sds = smem_u32(sDS);
-                // Descriptors are built once per operand tile and stepped by
-                // constants, keeping the issuing thread's work between MMAs small.
-                const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
-                const uint32_t sext = smem_u32(sExt);
-                const uint64_t onesd = sdesc_plain(smem_u32(sOnes), 128, 256);
-                auto issue_s = [&](int st) {      // S^T = K_j Q_i^T - LSE log2(e) / c
-                    const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        if constexpr (Cfg::kKInTmem)
-                            mma_ts(tmem + Cfg::kColS, tmem + Cfg::kColKT + kk * 8,
-                                   qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
-                        else
-                            mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
-                                   qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                    if (abort_sh) {   // drain the copies still in flight (bounded)
+                        const WaitCtx dc{p.status, nullptr};
+                        if (kv_issued > 0) fa_wait(&bar_kv, (kv_issued - 1) & 1, 41, dc);
+                        for (int x = max(0, issued - 2); x < issued; ++x)
+                            fa_wait(&bar_full[x & 1], (x >> 1) & 1, 41, dc);
                     }
-                    mma_ss(tmem + Cfg::kColS, onesd, sdesc_plain(sext + 2 * st * Cfg::kExtBytes,
-                                                                 128, 256), id_s, 1u);
-                    mma_commit(&bar_s);
-                };
-                auto issue_dp = [&](int st) {     // dP^T - D = V_j dO_i^T - D
-                    const uint64_t dod = sdesc_sw128(sdo + st * Cfg::kQBytes, 16, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDP, vd + kmajor_step(kk, kBN * 128),
-                               dod + kmajor_step(kk, BR * 128), id_s, kk > 0);
-                    mma_ss(tmem + Cfg::kColDP, onesd,
-                           sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s, 1u);
-                    mma_commit(&bar_dp);
-                };
-                bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc) &&
-                          (!Cfg::kKInTmem || fa_wait(&bar_ktm, 0, 57, wc));
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(0);
-                    issue_dp(0);
                 }
-                for (int it = 0; ok && it < n_it; ++it) {
-                    const int st = it & 1, st1 = (it + 1) & 1;
-                    const bool next = it + 1 < n_it;
-                    const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
-                    // dV += P^T dO_i  (P^T in TMEM; query half h of the K dimension
-                    // sits in the S^T columns of the warps of half h)
-                    if (!fa_wait(&bar_p, it & 1, 52, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t dod_mn = sdesc_sw128(do_, BR * 128, 1024);
+                __syncwarp();
+            } else if (!kTwoIssuers && warp == kMmaWarp) {
+                // One MMA-issuing thread (d = 64): dV, S^T for the next block, dK,
+                // the dQ partial, dP^T for the next block, in that order.
+                if (lane == 0) {
+                    constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
+                    constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+                    constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
+                    const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
+                                   sdo = smem_u32(sDO), sds = smem_u32(sDS);
+                    // Descriptors are built once per operand tile and stepped by
+                    // constants, keeping the issuing thread's work between MMAs small.
+                    const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
+                    const uint32_t sext = smem_u32(sExt);
+                    const uint64_t onesd = sdesc_plain(smem_u32(sOnes), 128, 256);
+                    auto issue_s = [&](int st) {      // S^T = K_j Q_i^T - LSE log2(e) / c
+                        const uint64_t qd = sdesc_sw128(sq + st * Cfg::kQBytes, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BR / 16; ++kk) {
-                        const int qs = kk * 16;
-                        const uint32_t pcol = Cfg::kColS + (qs / HALF) * HALF + (qs % HALF) / 2;
-                        mma_ts(tmem + Cfg::kColDV, tmem + pcol, dod_mn + mnmajor_step(kk), id_kv,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    if (next) {
-                        if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            if constexpr (Cfg::kKInTmem)
+                                mma_ts(tmem + Cfg::kColS, tmem + Cfg::kColKT + kk * 8,
+                                       qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                            else
+                                mma_ss(tmem + Cfg::kColS, kd + kmajor_step(kk, kBN * 128),
+                                       qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                        }
+                        mma_ss(tmem + Cfg::kColS, onesd, sdesc_plain(sext + 2 * st * Cfg::kExtBytes,
+                                                                     128, 256), id_s, 1u);
+                        mma_commit(&bar_s);
+                    };
+                    auto issue_dp = [&](int st) {     // dP^T - D = V_j dO_i^T - D
+                        const uint64_t dod = sdesc_sw128(sdo + st * Cfg::kQBytes, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(tmem + Cfg::kColDP, vd + kmajor_step(kk, kBN * 128),
+                                   dod + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                        mma_ss(tmem + Cfg::kColDP, onesd,
+                               sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s, 1u);
+                        mma_commit(&bar_dp);
+                    };
+                    bool ok = true;
+                    int gi = 0, nb = 0;   // query-block steps and work items so far
+                    for (int n = 0; ok; ++n) {
+                    int item;
+                    if (!next_item_thread(n, item)) { ok = false; break; }
+                    if (item < 0) break;
+                    const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+                    if (cta.idle || cta.n_it == 0) continue;
+                    const int n_it = cta.n_it;
+                    // K_j, V_j (and K_j in tensor memory) of this item, its first
+                    // stage, and the previous item's dK, dV read out
+                    ok = fa_wait(&bar_kv, nb & 1, 50, wc) &&
+                         fa_wait(&bar_full[gi & 1], (gi >> 1) & 1, 51, wc) &&
+                         (!Cfg::kKInTmem || fa_wait(&bar_ktm, nb & 1, 57, wc)) &&
+                         (nb == 0 || fa_wait(&bar_acc_free, (nb - 1) & 1, 58, wc));
+                    if (ok) {
                         tc_fence_after();
-                        issue_s(st1);
+                        issue_s(gi & 1);
+                        issue_dp(gi & 1);
                     }
-                    // dK += dS^T Q_i
-                    if (!fa_wait(&bar_ds, it & 1, 55, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t dsd = sdesc_sw128(sds, 16, 1024);
-                    const uint64_t qd_mn = sdesc_sw128(q_, BR * 128, 1024);
+                    for (int it = 0; ok && it < n_it; ++it) {
+                        const int git = gi + it;
+                        const int st = git & 1, st1 = (git + 1) & 1;
+                        const bool next = it + 1 < n_it;
+                        const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
+                        // dV += P^T dO_i  (P^T in TMEM; query half h of the K dimension
+                        // sits in the S^T columns of the warps of half h)
+                        if (!fa_wait(&bar_p, git & 1, 52, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t dod_mn = sdesc_sw128(do_, BR * 128, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BR / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDK, dsd + kmajor_step(kk, kBN * 128),
-                               qd_mn + mnmajor_step(kk), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bar_empty[st]);
-                    // dQ partial (K dimension = the 128 keys)
-                    if (it > 0 && !fa_wait(&bar_dq_free, (it - 1) & 1, 53, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t a_ = (D == 128) ? sk : sds;
-                    const uint32_t b_ = (D == 128) ? sds : sk;
-                    const uint64_t ad_mn = sdesc_sw128(a_, kBN * 128, 1024);
-                    const uint64_t bd_mn = sdesc_sw128(b_, kBN * 128, 1024);
+                        for (int kk = 0; kk < BR / 16; ++kk) {
+                            const int qs = kk * 16;
+                            const uint32_t pcol = Cfg::kColS + (qs / HALF) * HALF + (qs % HALF) / 2;
+                            mma_ts(tmem + Cfg::kColDV, tmem + pcol, dod_mn + mnmajor_step(kk), id_kv,
+                                   (it > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (next) {
+                            if (!fa_wait(&bar_full[st1], ((git + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_s(st1);
+                        }
+                        // dK += dS^T Q_i
+                        if (!fa_wait(&bar_ds, git & 1, 55, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t dsd = sdesc_sw128(sds, 16, 1024);
+                        const uint64_t qd_mn = sdesc_sw128(q_, BR * 128, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDQ, ad_mn + mnmajor_step(kk), bd_mn + mnmajor_step(kk),
-                               id_dq, kk > 0);
-                    mma_commit(&bar_dq_full);
-                    if (next) issue_dp(st1);
+                        for (int kk = 0; kk < BR / 16; ++kk)
+                            mma_ss(tmem + Cfg::kColDK, dsd + kmajor_step(kk, kBN * 128),
+                                   qd_mn + mnmajor_step(kk), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bar_empty[st]);
+                        // dQ partial (K dimension = the 128 keys)
+                        if (git > 0 && !fa_wait(&bar_dq_free, (git - 1) & 1, 53, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a_ = (D == 128) ? sk : sds;
+                        const uint32_t b_ = (D == 128) ? sds : sk;
+                        const uint64_t ad_mn = sdesc_sw128(a_, kBN * 128, 1024);
+                        const uint64_t bd_mn = sdesc_sw128(b_, kBN * 128, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ss(tmem + Cfg::kColDQ, ad_mn + mnmajor_step(kk), bd_mn + mnmajor_step(kk),
+                                   id_dq, kk > 0);
+                        mma_commit(&bar_dq_full);
+                        if (next) issue_dp(st1);
+                    }
+                    if (ok) mma_commit(&bar_done);   // every MMA of the item
+                    gi += n_it;
+                    ++nb;
                 }
-                mma_commit(&bar_done);
-                if (!ok) fa_wait(&bar_done, 0, 59, WaitCtx{p.status, nullptr});
+                if (!ok) {   // no MMA of this thread may still write TMEM at teardown
+                    __shared__ uint64_t bar_drain1;
+                    mbar_init(&bar_drain1, 1);
+                    fence_mbar_init();
+                    mma_commit(&bar_drain1);
+                    fa_wait(&bar_drain1, 0, 59, WaitCtx{p.status, nullptr});
+                }
             }
             __syncwarp();
         } else if (kTwoIssuers && (warp == kMmaWarp || warp == kMma2Warp)) {
-          if (lane == 0 && n_it > 0) {
+          if (lane == 0) {
             // MMA issue.  Half A: dV += P^T dO_i, then S^T for block i+1 (it
             // overwrites P^T, so after the dV MMA, in issue order).  Half B:
             // dK += dS^T Q_i, the dQ partial, then dP^T for block i+1 (its
@@ -654,70 +766,86 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                        sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s, 1u);
                 mma_commit(&bar_dp);
             };
-            bool ok = fa_wait(&bar_kv, 0, 50, wc) && fa_wait(&bar_full[0], 0, 51, wc) &&
-                      (!(Cfg::kKInTmem && half_a) || fa_wait(&bar_ktm, 0, 57, wc));
-            if (ok) {
-                tc_fence_after();
-                if (half_a) issue_s(0);
-                if (half_b) issue_dp(0);
-            }
-            for (int it = 0; ok && it < n_it; ++it) {
-                const int st = it & 1, st1 = (it + 1) & 1;
-                const bool next = it + 1 < n_it;
-                if (half_a) {
-                    // dV += P^T dO_i  (P^T in TMEM; query half h of the K
-                    // dimension sits in the S^T columns of the warps of half h)
-                    if (!fa_wait(&bar_p, it & 1, 52, wc)) { ok = false; break; }
+            bool ok = true;
+            int gi = 0, nb = 0;   // query-block steps and work items so far
+            for (int n = 0; ok; ++n) {
+                int item;
+                if (!next_item_thread(n, item)) { ok = false; break; }
+                if (item < 0) break;
+                const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+                if (cta.idle || cta.n_it == 0) continue;
+                const int n_it = cta.n_it;
+                // K_j, V_j (and for half A K_j in tensor memory) of this item, its
+                // first stage, and the previous item's dK, dV read out
+                ok = fa_wait(&bar_kv, nb & 1, 50, wc) &&
+                     fa_wait(&bar_full[gi & 1], (gi >> 1) & 1, 51, wc) &&
+                     (!(Cfg::kKInTmem && half_a) || fa_wait(&bar_ktm, nb & 1, 57, wc)) &&
+                     (nb == 0 || fa_wait(&bar_acc_free, (nb - 1) & 1, 58, wc));
+                if (ok) {
                     tc_fence_after();
-                    const uint64_t dod_mn = sdesc_sw128(sdo + st * Cfg::kQBytes, BR * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < BR / 16; ++kk) {
-                        const int qs = kk * 16;
-                        const uint32_t pcol = Cfg::kColS + (qs / HALF) * HALF + (qs % HALF) / 2;
-                        mma_ts(tmem + Cfg::kColDV, tmem + pcol, dod_mn + mnmajor_step(kk), id_kv,
-                               (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&bar_empty[st]);      // half A is done with Q_i, dO_i
-                    if (next) {
-                        if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
+                    if (half_a) issue_s(gi & 1);
+                    if (half_b) issue_dp(gi & 1);
+                }
+                for (int it = 0; ok && it < n_it; ++it) {
+                    const int git = gi + it;
+                    const int st = git & 1, st1 = (git + 1) & 1;
+                    const bool next = it + 1 < n_it;
+                    if (half_a) {
+                        // dV += P^T dO_i  (P^T in TMEM; query half h of the K
+                        // dimension sits in the S^T columns of the warps of half h)
+                        if (!fa_wait(&bar_p, git & 1, 52, wc)) { ok = false; break; }
                         tc_fence_after();
-                        issue_s(st1);
+                        const uint64_t dod_mn = sdesc_sw128(sdo + st * Cfg::kQBytes, BR * 128, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < BR / 16; ++kk) {
+                            const int qs = kk * 16;
+                            const uint32_t pcol = Cfg::kColS + (qs / HALF) * HALF + (qs % HALF) / 2;
+                            mma_ts(tmem + Cfg::kColDV, tmem + pcol, dod_mn + mnmajor_step(kk), id_kv,
+                                   (it > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&bar_empty[st]);      // half A is done with Q_i, dO_i
+                        if (next) {
+                            if (!fa_wait(&bar_full[st1], ((git + 1) >> 1) & 1, 54, wc)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_s(st1);
+                        }
+                    }
+                    if (half_b) {
+                        // dK += dS^T Q_i
+                        if (!fa_wait(&bar_ds, git & 1, 55, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t dsd = sdesc_sw128(sds, 16, 1024);
+                        const uint64_t qd_mn = sdesc_sw128(sq + st * Cfg::kQBytes, BR * 128, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < BR / 16; ++kk)
+                            mma_ss(tmem + Cfg::kColDK, dsd + kmajor_step(kk, kBN * 128),
+                                   qd_mn + mnmajor_step(kk), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bar_empty[st]);      // half B is done with Q_i, dO_i
+                        // dQ partial (K dimension = the 128 keys)
+                        if (git > 0 && !fa_wait(&bar_dq_free, (git - 1) & 1, 53, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a_ = (D == 128) ? sk : sds;
+                        const uint32_t b_ = (D == 128) ? sds : sk;
+                        const uint64_t ad_mn = sdesc_sw128(a_, kBN * 128, 1024);
+                        const uint64_t bd_mn = sdesc_sw128(b_, kBN * 128, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ss(tmem + Cfg::kColDQ, ad_mn + mnmajor_step(kk), bd_mn + mnmajor_step(kk),
+                                   id_dq, kk > 0);
+                        mma_commit(&bar_dq_full);
+                        if (next) {
+                            if (!fa_wait(&bar_full[st1], ((git + 1) >> 1) & 1, 56, wc)) { ok = false; break; }
+                            tc_fence_after();
+                            issue_dp(st1);
+                        }
                     }
                 }
-                if (half_b) {
-                    // dK += dS^T Q_i
-                    if (!fa_wait(&bar_ds, it & 1, 55, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t dsd = sdesc_sw128(sds, 16, 1024);
-                    const uint64_t qd_mn = sdesc_sw128(sq + st * Cfg::kQBytes, BR * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < BR / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDK, dsd + kmajor_step(kk, kBN * 128),
-                               qd_mn + mnmajor_step(kk), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bar_empty[st]);      // half B is done with Q_i, dO_i
-                    // dQ partial (K dimension = the 128 keys)
-                    if (it > 0 && !fa_wait(&bar_dq_free, (it - 1) & 1, 53, wc)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t a_ = (D == 128) ? sk : sds;
-                    const uint32_t b_ = (D == 128) ? sds : sk;
-                    const uint64_t ad_mn = sdesc_sw128(a_, kBN * 128, 1024);
-                    const uint64_t bd_mn = sdesc_sw128(b_, kBN * 128, 1024);
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ss(tmem + Cfg::kColDQ, ad_mn + mnmajor_step(kk), bd_mn + mnmajor_step(kk),
-                               id_dq, kk > 0);
-                    mma_commit(&bar_dq_full);
-                    if (next) {
-                        if (!fa_wait(&bar_full[st1], ((it + 1) >> 1) & 1, 56, wc)) { ok = false; break; }
-                        tc_fence_after();
-                        issue_dp(st1);
-                    }
-                }
+                if (ok) mma_commit(&bar_done);   // one arrival per issuing thread, per item
+                gi += n_it;
+                ++nb;
             }
             const bool first = half_a;
-            if (ok) {
-                mma_commit(&bar_done);               // one arrival per issuing thread
-            } else {   // no MMA of this thread may still write TMEM at teardown
+            if (!ok) {   // no MMA of this thread may still write TMEM at teardown
                 __shared__ uint64_t bar_drain[2];
                 uint64_t* dbar = &bar_drain[first ? 0 : 1];
                 mbar_init(dbar, 1);
@@ -773,8 +901,10 @@ template <int D, typename OT, bool FULL>
 __global__ void __launch_bounds__(256)
 fa_bwd_pre_kernel(const OT* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                   const float* __restrict__ lse, uint16_t* __restrict__ lse_ext,
-                  uint16_t* __restrict__ d_ext, float* __restrict__ dq_acc, int N, int Np,
-                  long long rows, const int* __restrict__ cu, int H, long long seq_rows) {
+                  uint16_t* __restrict__ d_ext, float* __restrict__ dq_acc,
+                  int* __restrict__ work, int N, int Np, long long rows,
+                  const int* __restrict__ cu, int H, long long seq_rows) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *work = 0;   // the dK/dV kernel's work counter
     constexpr int LPR = D / 8;          // lanes per row, 8 elements each
     constexpr int RPW = 32 / LPR;       // rows per warp
     const int lane = threadIdx.x & 31, sub = lane / LPR, sl = lane % LPR;
@@ -968,8 +1098,8 @@ cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, con
     count_launch();
     auto* d_ = static_cast<const __nv_bfloat16*>(dout);
     auto go = [&](auto kern, auto* o_) {
-        kern<<<grid, 256, 0, stream>>>(o_, d_, lse, ws.lse_ext, ws.d_ext, ws.dq_acc, s.N, Np, rows,
-                                       s.cu_seqlens, s.H, seq_rows);
+        kern<<<grid, 256, 0, stream>>>(o_, d_, lse, ws.lse_ext, ws.d_ext, ws.dq_acc, ws.work, s.N,
+                                       Np, rows, s.cu_seqlens, s.H, seq_rows);
         return cudaGetLastError();
     };
     auto* ob = static_cast<const __nv_bfloat16*>(o);
@@ -1035,8 +1165,14 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     p.dk = static_cast<__nv_bfloat16*>(dk);
     p.dv = static_cast<__nv_bfloat16*>(dv);
     p.status = status;
+    p.work = ws.work;
     const int n_kblk = (s.N + kBN - 1) / kBN;
-    const int grid = n_kblk * s.B * s.Hkv;
+    p.n_bg = s.B * s.Hkv;
+    p.n_items = n_kblk * s.B * s.Hkv;
+    // Persistent: one CTA per SM (fewer when there are fewer work items),
+    // taking items in the order above from the work counter.
+    const int sms = device_sm_count() > 0 ? device_sm_count() : 148;
+    const int grid = p.n_items < sms ? p.n_items : sms;
     count_launch();
     if (varlen) {   // packed variable-length sequences (no window)
         if (s.window > 0) return cudaErrorInvalidValue;

@@ -73,7 +73,8 @@ constexpr int kRowPad = 128;
 inline int padded_rows(int N) { return (N + kRowPad - 1) / kRowPad * kRowPad; }
 
 // Backward workspace: [lse_ext bf16 B*H*Np x 16][d_ext bf16 B*H*Np x 16]
-// [dQacc fp32 B*H*Np*d], each region 256-byte aligned.  The two ext tables
+// [dQacc fp32 B*H*Np*d][work int32], each region 256-byte aligned.  The two
+// ext tables
 // are the B operands of the K = 16 MMAs that add -LSE (scaled) to S^T and -D
 // to dP^T inside the tensor core: per row 16 bf16 columns, stored as
 // 8-row x 16-byte core matrices (row group g, K half kc at (2 g + kc) * 128
@@ -82,6 +83,9 @@ struct BwdWorkspace {
     uint16_t* lse_ext;  // cols 0-8: -LSE log2(e) as three bf16 terms, three times
     uint16_t* d_ext;    // cols 9-11: -D = -rowsum(dO o O) as three bf16 terms
     float* dq_acc;      // fp32 accumulator of dQ / scale
+    // The dK/dV kernel's work counter (next work item); zeroed by the
+    // preprocess, left zero by the dK/dV kernel.
+    int* work;
 };
 constexpr int kExtCols = 16;   // bf16 columns per row of an ext table
 

@@ -76,12 +76,14 @@ def test_fwd_rejects_before_launch(L, kw, code):
 
 def test_workspace_size(L):
     # -LSE and -D extension tables: bf16 [B][H][Np][16] each, accumulator fp32
-    # [B][H][Np][d]; Np = N rounded to 128.
+    # [B][H][Np][d], the dK/dV kernel's work counter (int32, 256-byte region);
+    # Np = N rounded to 128.
     B, H, Hkv, N, d = 2, 4, 2, 200, 64
     Np = 256
     rows = B * H * Np
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, Hkv, N, d) == 2 * r256(rows * 32) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_size(B, H, Hkv, N, d) == \
+        2 * r256(rows * 32) + r256(rows * d * 4) + 256
     assert fa.fa_bwd_workspace_size(B, H, 3, N, d) == 0
     assert fa.fa_bwd_workspace_size(B, H, Hkv, N, 80) == 0
 
