@@ -57,21 +57,21 @@ L2_BYTES = 129 * 1024 * 1024
 # workload, together with the sha256 of the kernel source it was taken on.  A
 # source change makes the figure stale and it is then reported as null.
 NCU_TRAFFIC = {
-    # 238.1 MB read + 104.3 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 342.35e6, "src_sha": "634d08a0dee239a7"},
+    # 234.4 MB read + 97.7 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 332.11e6, "src_sha": "3d86bd9e8fa43878"},
     # 133.1 MB read + 58.9 MB written (training forward), one launch
     ("fa_fwd", "mha_d64"): {"bytes": 192.05e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 1384.9 MB read + 640.0 MB written, one launch
-    ("fa_bwd_dkdv", "window"): {"bytes": 2024.90e6, "src_sha": "634d08a0dee239a7"},
+    # 1384.0 MB read + 640.8 MB written, one launch
+    ("fa_bwd_dkdv", "window"): {"bytes": 2024.80e6, "src_sha": "3d86bd9e8fa43878"},
     # 247.3 MB read + 363.1 MB written (training forward: the -LSE table and
     # the zeroed dQ accumulator), one launch
     ("fa_fwd", "window"): {"bytes": 610.47e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 427.1 MB read + 226.5 MB written, one launch
-    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 653.56e6, "src_sha": "634d08a0dee239a7"},
+    # 427.3 MB read + 226.0 MB written, one launch
+    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 653.28e6, "src_sha": "3d86bd9e8fa43878"},
     # 559.2 MB read + 160.2 MB written (training forward), one launch
     ("fa_fwd", "gpt_long"): {"bytes": 719.39e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 762.0 MB read + 347.4 MB written, one launch
-    ("fa_bwd_dkdv", "gqa"): {"bytes": 1109.32e6, "src_sha": "634d08a0dee239a7"},
+    # 761.1 MB read + 347.9 MB written, one launch
+    ("fa_bwd_dkdv", "gqa"): {"bytes": 1108.98e6, "src_sha": "3d86bd9e8fa43878"},
     # 409.2 MB read + 496.3 MB written (training forward, fp32 O), one launch
     ("fa_fwd", "gqa"): {"bytes": 905.51e6, "src_sha": "4ea3adf4eb4f28a7"},
     # 1.0739 GB read + 3.7 MB written, one launch
