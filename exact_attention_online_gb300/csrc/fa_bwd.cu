@@ -58,25 +58,34 @@ constexpr int kRegsReadout = 96;
 constexpr int kRegsControl = 112;
 constexpr int kRegsNeeded = 256 * kRegsCompute + 128 * kRegsReadout + 128 * kRegsControl;
 
-template <int D>
+template <int D, bool KV2 = false>
 struct BwdCfg {
     static constexpr int kBR = (D == 128) ? 64 : 128;        // queries per step
     static constexpr int kKVBytes = kBN * D * 2;              // K_j or V_j
     static constexpr int kQBytes = kBR * D * 2;               // Q_i or dO_i
     static constexpr int kDSBytes = kBN * kBR * 2;            // dS^T tile
-    static constexpr int kOffK = 0;
-    static constexpr int kOffV = kOffK + kKVBytes;
-    static constexpr int kOffQ = kOffV + kKVBytes;            // 2 stages
+    // KV2 (causal d = 64): two K/V slots, the next work item's K_j, V_j
+    // loading while the current item runs, and one dQ staging tile to make
+    // room.  Otherwise one K/V slot and two staging tiles: at d = 128 a second
+    // slot does not fit, and without the mask the items are long enough that
+    // the second staging tile is worth more (-2 % vs +2 % at d = 64).
+    static_assert(!KV2 || D == 64, "two K/V slots fit at d = 64 only");
+    static constexpr int kKVSlots = KV2 ? 2 : 1;
+    static constexpr int kStageTiles = KV2 ? 1 : 2;
+    static constexpr int kKVSlotBytes = 2 * kKVBytes;         // K_j, then V_j
+    static constexpr int kOffK = 0;                           // + slot * kKVSlotBytes
+    static constexpr int kOffV = kOffK + kKVBytes;            // + slot * kKVSlotBytes
+    static constexpr int kOffQ = kKVSlots * kKVSlotBytes;     // 2 stages
     static constexpr int kOffDO = kOffQ + 2 * kQBytes;        // 2 stages
     static constexpr int kOffDS = kOffDO + 2 * kQBytes;
-    static constexpr int kOffStage = kOffDS + kDSBytes;       // 2 x fp32 dQ staging tile
+    static constexpr int kOffStage = kOffDS + kDSBytes;       // kStageTiles fp32 dQ staging tiles
     static constexpr int kStageTileBytes = kBR * D * 4;        // 32 KB for both head dims
     // The K = 16 extension operands (unswizzled core matrices, 32 bytes a
     // row): the constant A tile for the 128 key rows, and per stage the -LSE
     // and -D tables of the BR query rows.
     static constexpr int kOnesBytes = kBN * 32;
     static constexpr int kExtBytes = kBR * 32;
-    static constexpr int kOffOnes = kOffStage + 2 * kStageTileBytes;
+    static constexpr int kOffOnes = kOffStage + kStageTiles * kStageTileBytes;
     static constexpr int kOffExt = kOffOnes + kOnesBytes;     // [2 stages][lse, d]
     static constexpr int kSmemBytes = kOffExt + 4 * kExtBytes;
     static constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -201,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
-    using Cfg = BwdCfg<D>;
+    using Cfg = BwdCfg<D, (D == 64 && CAUSAL)>;
     constexpr int BR = Cfg::kBR;
     // Two MMA-issuing threads at d = 128 and without the mask (d = 64: +8 %);
     // one for causal d = 64 (two measured 3 % slower there).
@@ -210,8 +219,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    __shared__ uint64_t bar_kv, bar_full[2], bar_empty[2], bar_s, bar_dp, bar_p, bar_ds,
-        bar_dq_full, bar_dq_free, bar_done, bar_ktm;
+    constexpr int KVS = Cfg::kKVSlots;
+    // bar_kv[s]: K_j, V_j of slot s landed; bar_kv_free[s]: every MMA that
+    // reads slot s's K_j, V_j has completed (one arrival per MMA issuer)
+    __shared__ uint64_t bar_kv[KVS], bar_kv_free[KVS];
+    __shared__ uint64_t bar_full[2], bar_empty[2], bar_s, bar_dp, bar_p, bar_ds, bar_dq_full,
+        bar_dq_free, bar_done, bar_ktm;
     // Persistent CTAs: the producer takes work items from p.work and passes
     // them on through a two-slot ring (-1: no more); an item's dK, dV leave
     // tensor memory (bar_acc_free) before the next item's MMAs overwrite them.
@@ -229,7 +242,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint8_t* sQ = smem + Cfg::kOffQ;
     uint8_t* sDO = smem + Cfg::kOffDO;
     uint8_t* sDS = smem + Cfg::kOffDS;
-    float* sStage = reinterpret_cast<float*>(smem + Cfg::kOffStage);   // [2][BR*D] fp32
+    float* sStage = reinterpret_cast<float*>(smem + Cfg::kOffStage);   // [tiles][BR*D] fp32
     uint8_t* sOnes = smem + Cfg::kOffOnes;
     uint8_t* sExt = smem + Cfg::kOffExt;      // stage st: lse at 2 st, d at 2 st + 1
 
@@ -237,7 +250,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
     if (threadIdx.x == 0) {
         abort_sh = 0;
-        mbar_init(&bar_kv, 1);
+        for (int s = 0; s < KVS; ++s) {
+            mbar_init(&bar_kv[s], 1);
+            mbar_init(&bar_kv_free[s], kTwoIssuers ? 2 : 1);
+        }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bar_full[s], 1);
             mbar_init(&bar_empty[s], kTwoIssuers ? 2 : 1);   // every MMA issuer lets go of the stage
@@ -309,10 +325,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 // K_j -> tensor memory: this thread's key row, the 64 head-dim
                 // columns of its half (one 128-byte swizzled row of chunk hf),
                 // as 32 bf16 pairs; the S^T MMAs take it from there.
-                if (!fa_wait_warp(&bar_kv, nb & 1, 64, wc)) {
+                if (!fa_wait_warp(&bar_kv[nb % KVS], (nb / KVS) & 1, 64, wc)) {
                     ok = false;
                 } else {
-                    const uint8_t* rowp = sK + hf * (kBN * 128) + rl * 128;
+                    const uint8_t* rowp =
+                        sK + (nb % KVS) * Cfg::kKVSlotBytes + hf * (kBN * 128) + rl * 128;
                     uint32_t kw[32];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
@@ -486,8 +503,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 asm volatile("" : FA_R32(r1) : : "memory");
                 tc_fence_before();
                 mbar_arrive(&bar_dq_free);
-                float* stg = sStage + (git & 1) * (BR * D);
-                if (leader) bulk_wait_group_read<1>();   // the copy that last read this buffer
+                float* stg = sStage + (git % Cfg::kStageTiles) * (BR * D);
+                // the copy that last read this tile
+                if (leader) bulk_wait_group_read<Cfg::kStageTiles - 1>();
                 named_bar_sync(1, kReadoutThreads);
                 if (D == 128) {
                     // dQ^T: lane = head-dim index dd, column = query -> stg[q][dd]
@@ -554,13 +572,20 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         const int jblk = cta.jblk, b = cta.b, g = cta.g, tok0 = cta.tok0;
                         const int z_kv = cta.z_kv, i_start = cta.i_start, n_i = cta.n_i;
                         const int n_it = cta.n_it;
-                        // K_j, V_j over the previous item's, whose MMAs have completed
-                        if (nb > 0 && !fa_wait(&bar_done, (nb - 1) & 1, 42, wc)) break;
-                        mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
+                        // K_j, V_j into slot nb % KVS, over the item there
+                        // before, whose MMAs have completed (with two slots
+                        // this load runs while the previous item's MMAs do)
+                        const int kvs = nb % KVS;
+                        if (nb >= KVS &&
+                            !fa_wait(&bar_kv_free[kvs], ((nb / KVS) - 1) & 1, 42, wc))
+                            break;
+                        uint8_t* sk_ = sK + kvs * Cfg::kKVSlotBytes;
+                        uint8_t* sv_ = sV + kvs * Cfg::kKVSlotBytes;
+                        mbar_arrive_expect_tx(&bar_kv[kvs], 2 * Cfg::kKVBytes);
                         for (int c = 0; c < D / 64; ++c) {
-                            tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64,
+                            tma_load_3d(sk_ + c * (kBN * 128), &tm_k, &bar_kv[kvs], c * 64,
                                         tok0 + jblk * kBN, z_kv);
-                            tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64,
+                            tma_load_3d(sv_ + c * (kBN * 128), &tm_v, &bar_kv[kvs], c * 64,
                                         tok0 + jblk * kBN, z_kv);
                         }
                         ++kv_issued;
@@ -594,7 +619,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     }
                     if (abort_sh) {   // drain the copies still in flight (bounded)
                         const WaitCtx dc{p.status, nullptr};
-                        if (kv_issued > 0) fa_wait(&bar_kv, (kv_issued - 1) & 1, 41, dc);
+                        for (int x = max(0, kv_issued - KVS); x < kv_issued; ++x)
+                            fa_wait(&bar_kv[x % KVS], (x / KVS) & 1, 41, dc);
                         for (int x = max(0, issued - 2); x < issued; ++x)
                             fa_wait(&bar_full[x & 1], (x >> 1) & 1, 41, dc);
                     }
@@ -607,11 +633,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
                     constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
                     constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
-                    const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
-                                   sdo = smem_u32(sDO), sds = smem_u32(sDS);
+                    const uint32_t sq = smem_u32(sQ), sdo = smem_u32(sDO), sds = smem_u32(sDS);
                     // Descriptors are built once per operand tile and stepped by
-                    // constants, keeping the issuing thread's work between MMAs small.
-                    const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
+                    // constants, keeping the issuing thread's work between MMAs small;
+                    // K_j's and V_j's are set per item (their slot alternates).
+                    uint32_t sk = smem_u32(sK);
+                    uint64_t kd = 0, vd = 0;
                     const uint32_t sext = smem_u32(sExt);
                     const uint64_t onesd = sdesc_plain(smem_u32(sOnes), 128, 256);
                     auto issue_s = [&](int st) {      // S^T = K_j Q_i^T - LSE log2(e) / c
@@ -650,7 +677,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const int n_it = cta.n_it;
                     // K_j, V_j (and K_j in tensor memory) of this item, its first
                     // stage, and the previous item's dK, dV read out
-                    ok = fa_wait(&bar_kv, nb & 1, 50, wc) &&
+                    const int kvs = nb % KVS;
+                    sk = smem_u32(sK) + kvs * Cfg::kKVSlotBytes;
+                    kd = sdesc_sw128(sk, 16, 1024);
+                    vd = sdesc_sw128(smem_u32(sV) + kvs * Cfg::kKVSlotBytes, 16, 1024);
+                    ok = fa_wait(&bar_kv[kvs], (nb / KVS) & 1, 50, wc) &&
                          fa_wait(&bar_full[gi & 1], (gi >> 1) & 1, 51, wc) &&
                          (!Cfg::kKInTmem || fa_wait(&bar_ktm, nb & 1, 57, wc)) &&
                          (nb == 0 || fa_wait(&bar_acc_free, (nb - 1) & 1, 58, wc));
@@ -705,7 +736,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         mma_commit(&bar_dq_full);
                         if (next) issue_dp(st1);
                     }
-                    if (ok) mma_commit(&bar_done);   // every MMA of the item
+                    if (ok) {   // every MMA of the item, and so every read of its slot
+                        mma_commit(&bar_done);
+                        mma_commit(&bar_kv_free[kvs]);
+                    }
                     gi += n_it;
                     ++nb;
                 }
@@ -733,9 +767,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
             constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
             constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
-            const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
-                           sdo = smem_u32(sDO), sds = smem_u32(sDS);
-            const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
+            const uint32_t sq = smem_u32(sQ), sdo = smem_u32(sDO), sds = smem_u32(sDS);
+            uint32_t sk = smem_u32(sK);   // K_j's, V_j's slot is set per item
+            uint64_t kd = 0, vd = 0;
             const uint32_t sext = smem_u32(sExt);
             const uint64_t onesd = sdesc_plain(smem_u32(sOnes), 128, 256);
             const bool half_a = (warp == kMmaWarp);
@@ -777,7 +811,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const int n_it = cta.n_it;
                 // K_j, V_j (and for half A K_j in tensor memory) of this item, its
                 // first stage, and the previous item's dK, dV read out
-                ok = fa_wait(&bar_kv, nb & 1, 50, wc) &&
+                const int kvs = nb % KVS;
+                sk = smem_u32(sK) + kvs * Cfg::kKVSlotBytes;
+                kd = sdesc_sw128(sk, 16, 1024);
+                vd = sdesc_sw128(smem_u32(sV) + kvs * Cfg::kKVSlotBytes, 16, 1024);
+                ok = fa_wait(&bar_kv[kvs], (nb / KVS) & 1, 50, wc) &&
                      fa_wait(&bar_full[gi & 1], (gi >> 1) & 1, 51, wc) &&
                      (!(Cfg::kKInTmem && half_a) || fa_wait(&bar_ktm, nb & 1, 57, wc)) &&
                      (nb == 0 || fa_wait(&bar_acc_free, (nb - 1) & 1, 58, wc));
@@ -840,7 +878,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                         }
                     }
                 }
-                if (ok) mma_commit(&bar_done);   // one arrival per issuing thread, per item
+                if (ok) {   // one arrival per issuing thread, per item
+                    mma_commit(&bar_done);
+                    mma_commit(&bar_kv_free[kvs]);
+                }
                 gi += n_it;
                 ++nb;
             }
@@ -1066,6 +1107,7 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                           int grid, cudaStream_t stream) {
     auto kern = fa_bwd_dkdv_kernel<D, CAUSAL, WINDOW, VARLEN>;
+    using Cfg = BwdCfg<D, (D == 64 && CAUSAL)>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1077,11 +1119,11 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
         if (e != cudaSuccess) return e;
         if (attr.numRegs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 BwdCfg<D>::kSmemAlloc);
+                                 Cfg::kSmemAlloc);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    kern<<<grid, kThreads, BwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, tdo, tdq, p);
+    kern<<<grid, kThreads, Cfg::kSmemAlloc, stream>>>(tq, tk, tv, tdo, tdq, p);
     return cudaGetLastError();
 }
 
