@@ -57,23 +57,25 @@ L2_BYTES = 129 * 1024 * 1024
 # workload, together with the sha256 of the kernel source it was taken on.  A
 # source change makes the figure stale and it is then reported as null.
 NCU_TRAFFIC = {
-    # 234.4 MB read + 97.7 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 332.11e6, "src_sha": "3d86bd9e8fa43878"},
-    # 133.1 MB read + 58.9 MB written (training forward), one launch
-    ("fa_fwd", "mha_d64"): {"bytes": 192.05e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 1384.0 MB read + 640.8 MB written, one launch
-    ("fa_bwd_dkdv", "window"): {"bytes": 2024.80e6, "src_sha": "3d86bd9e8fa43878"},
-    # 247.3 MB read + 363.1 MB written (training forward: the -LSE table and
+    # 234.7 MB read + 98.1 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 332.83e6, "src_sha": "c378ba06e01f5a03"},
+    # 136.7 MB read + 59.2 MB written (training forward), one launch
+    ("fa_fwd", "mha_d64"): {"bytes": 195.86e6, "src_sha": "9c1ea912cf1c1295"},
+    # 1383.3 MB read + 641.0 MB written, one launch
+    ("fa_bwd_dkdv", "window"): {"bytes": 2024.23e6, "src_sha": "c378ba06e01f5a03"},
+    # 246.8 MB read + 363.2 MB written (training forward: the -LSE table and
     # the zeroed dQ accumulator), one launch
-    ("fa_fwd", "window"): {"bytes": 610.47e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 427.3 MB read + 226.0 MB written, one launch
-    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 653.28e6, "src_sha": "3d86bd9e8fa43878"},
-    # 559.2 MB read + 160.2 MB written (training forward), one launch
-    ("fa_fwd", "gpt_long"): {"bytes": 719.39e6, "src_sha": "4ea3adf4eb4f28a7"},
-    # 761.1 MB read + 347.9 MB written, one launch
-    ("fa_bwd_dkdv", "gqa"): {"bytes": 1108.98e6, "src_sha": "3d86bd9e8fa43878"},
-    # 409.2 MB read + 496.3 MB written (training forward, fp32 O), one launch
-    ("fa_fwd", "gqa"): {"bytes": 905.51e6, "src_sha": "4ea3adf4eb4f28a7"},
+    ("fa_fwd", "window"): {"bytes": 610.01e6, "src_sha": "9c1ea912cf1c1295"},
+    # 426.6 MB read + 225.5 MB written, one launch
+    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 652.02e6, "src_sha": "c378ba06e01f5a03"},
+    # 558.1 MB read + 159.8 MB written (training forward), one launch
+    ("fa_fwd", "gpt_long"): {"bytes": 717.86e6, "src_sha": "9c1ea912cf1c1295"},
+    # 763.9 MB read + 349.4 MB written, one launch
+    ("fa_bwd_dkdv", "gqa"): {"bytes": 1113.29e6, "src_sha": "c378ba06e01f5a03"},
+    # 424.6 MB read + 496.8 MB written (training forward, fp32 O), one launch
+    ("fa_fwd", "gqa"): {"bytes": 921.44e6, "src_sha": "9c1ea912cf1c1295"},
+    # 541.5 MB read + 96.6 MB written (fp32 O), one launch
+    ("fa_fwd", "long16k"): {"bytes": 638.11e6, "src_sha": "9c1ea912cf1c1295"},
     # 1.0739 GB read + 3.7 MB written, one launch
     ("fa_decode_split", "decode_gqa"): {"bytes": 1.0775e9, "src_sha": "70c5a2dfe3a994c9"},
     # 537.0 MB read + 3.3 MB written, one launch (persistent, 304 CTAs)

@@ -9,8 +9,12 @@
 // shared-memory rings:
 //   warp 8      TMA producer of K_j; K_j is released when both S MMAs that
 //               read it have completed, so K loads run whole blocks ahead.
+//               In the PRECISE variant the whole warp also re-encodes the
+//               second half of each landed V_j as fp16, in place.
 //   warp 10     TMA producer of V_j and of the Q tiles (each item's Q ahead of
-//               its V blocks); V_j is released after both P V MMAs.
+//               its V blocks); V_j is released after both P V MMAs.  In the
+//               PRECISE variant the whole warp also re-encodes the first half
+//               of each landed V_j as fp16, in place.
 //   warp 9      S MMA issuer (one thread): S_t = Q_t K_j^T into TMEM (SS MMA).
 //   warp 11     P V MMA issuer (one thread): O_t += P_t V_j, P_t read from
 //               TMEM (TS MMA).  An MMA issue blocks while the tensor pipe is
@@ -35,11 +39,17 @@
 // use the same m, so the result is unchanged in exact arithmetic.  O is
 // divided by l once, in the epilogue, and LSE = ln2 * (m + log2 l).
 //
-// PRECISE variant: P enters the P V product as two bf16 terms, P_hi = bf16(p)
-// in the first half of S_t and P_lo = bf16(p - P_hi) in the second half, each
-// multiplied by V_j (two TS MMAs), and O is written in fp32.  This removes the
-// bf16 rounding of P and of O from the error, which matters when values reach
-// tens (outliers of magnitude 30: half a bf16 ulp of 30 is 0.06).
+// PRECISE variant: the P V product runs in fp16 instead of bf16 (same tensor
+// rate): P is rounded to fp16 (11 significant bits against bf16's 8), V_j is
+// re-encoded as fp16 in shared memory (exact for magnitudes in [2^-14,
+// 65280]; 65536 and above overflow to infinity), and O is written in fp32.
+// This takes the bf16 rounding of O out of the error (half a bf16 ulp of 30 is
+// 0.06) and cuts that of P eightfold: each p is off by at most 2^-11 of
+// itself (2^-25 absolute below 2^-14).  The row sum l is corrected by what
+// the rounding added to each key block's largest p, so a row whose weight
+// sits on one key returns that key's V row unrounded; in general a row of O
+// moves by at most 2^-11 (sum over block maxima of w |v - O| + sum over the
+// other keys of w |v|) <= 2^-10 max|V|, w = p / l.
 #include <cuda_bf16.h>
 #include <type_traits>
 #include <cuda_runtime.h>
@@ -78,12 +88,14 @@ struct Exp2FmaEvery {
     static constexpr int mod = value > 0 ? value : 1;
 };
 
-template <int D>
+template <int D, bool PRECISE = false>
 struct FwdCfg {
     // K and V have rings of their own: K is released as soon as both S MMAs of
-    // a block are issued, V after both P V MMAs.
-    static constexpr int kStagesK = (D == 128) ? 3 : 4;
-    static constexpr int kStagesV = (D == 128) ? 2 : 3;
+    // a block are issued, V after both P V MMAs.  The PRECISE variant holds
+    // each V_j longer (its fp16 re-encoding sits between landing and use) and
+    // at d = 128 trades a K stage for a third V stage.
+    static constexpr int kStagesK = (D == 128) ? (PRECISE ? 2 : 3) : 4;
+    static constexpr int kStagesV = (D == 128) ? (PRECISE ? 3 : 2) : 3;
     static constexpr int kTileBytes = kBM * D * 2;          // one Q, K or V tile
     static constexpr int kChunks = D / 64;                  // 128-byte swizzle chunks
     static constexpr int kChunkBytes = 128 * 128;           // 128 rows x 128 bytes
@@ -206,16 +218,43 @@ __device__ __forceinline__ FwdTile fwd_tile(int item, const FwdParams& p, bool c
 
 // WINDOW (with CAUSAL): the causal sliding window of p.window keys.
 // VARLEN: packed variable-length sequences (p.cu_seqlens).
+// PRECISE: one warp's half (part 0 or 1) of the fp16 re-encoding of V_x, in
+// place, once V_x has landed; the P V issuer waits for both halves (bar_v_cvt
+// counts two arrivals).  Spread over two warps on two SM sub-partitions, the
+// conversion takes issue slots from fewer softmax warps each.
+template <int SV, int TILE_BYTES>
+__device__ __forceinline__ bool convert_v_half(uint8_t* sV, uint64_t* bar_v, uint64_t* bar_v_cvt,
+                                               uint32_t x, int part, int lane, const WaitCtx& wc) {
+    const uint32_t s = x % SV;
+    if (!fa_wait_warp(&bar_v[s], (x / SV) & 1, 16 + part, wc)) return false;
+    constexpr int kHalf = TILE_BYTES / 32;   // 16-byte pieces in half a tile
+    uint4* v4 = reinterpret_cast<uint4*>(sV + s * TILE_BYTES) + part * kHalf;
+#pragma unroll 8
+    for (int i = lane; i < kHalf; i += 32) {
+        uint4 w = v4[i];
+        w.x = bf16x2_to_f16x2(w.x);
+        w.y = bf16x2_to_f16x2(w.y);
+        w.z = bf16x2_to_f16x2(w.z);
+        w.w = bf16x2_to_f16x2(w.w);
+        v4[i] = w;
+    }
+    fence_proxy_async_smem();   // visible to the tensor core's reads
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_v_cvt[s]);
+    return true;
+}
+
 template <int D, bool CAUSAL, bool PRECISE, bool WINDOW, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using Cfg = FwdCfg<D>;
+    using Cfg = FwdCfg<D, PRECISE>;
     constexpr int SK = Cfg::kStagesK, SV = Cfg::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     __shared__ uint64_t bar_k[SK], bar_k_empty[SK], bar_v[SV], bar_v_empty[SV];
+    __shared__ uint64_t bar_v_cvt[SV];        // PRECISE: V_j re-encoded as fp16
     __shared__ uint64_t bar_q[kTiles], bar_q_free[kTiles];
     __shared__ uint64_t bar_s[kTiles], bar_p[kTiles], bar_pv[kTiles], bar_o_free[kTiles];
     __shared__ uint64_t bar_s_free[kTiles];   // separate-P form only
@@ -236,6 +275,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int s = 0; s < SV; ++s) {
             mbar_init(&bar_v[s], 1);
             mbar_init(&bar_v_empty[s], 1);
+            mbar_init(&bar_v_cvt[s], 2);   // one arrival per converting warp
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(&bar_q[t], 1);
@@ -288,6 +328,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const int lo = t ? wt.lo[1] : wt.lo[0], n_kv = t ? wt.n_kv[1] : wt.n_kv[0];
             float m2 = -CUDART_INF_F;   // running max, log2-scaled
             float l = 0.0f;
+            // PRECISE: what the fp16 rounding of each block's largest p added
+            // to the P V product, scaled like l.  O is divided by l + lc, so a
+            // row whose weight sits on one key returns that key's V row
+            // without the rounding of its p (up to 2^-11 |V| otherwise); the
+            // LSE keeps l.
+            float lc = 0.0f;
             for (int j = lo; j < n_kv; ++j) {
                 if (!fa_wait_warp(&bar_s[t], cs & 1, 30 + t, wc)) { ok = false; break; }
                 ++cs;
@@ -354,10 +400,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const float m_new = need ? mx2 : m2;
                     alpha = (m_new == m2) ? 1.0f : ex2(m2 - m_new);
                     l *= alpha;
+                    if (PRECISE) lc *= alpha;
                     if (!SEP && j > lo) rescale_o(alpha);
                     m2 = m_new;
                 }
                 const float m_use = (m2 == -CUDART_INF_F) ? 0.0f : m2;
+                if (PRECISE) {   // the block max's p, as the loop below computes it
+                    const float pm = ex2(fmaf(mx, c, -m_use));
+                    float h0, h1;
+                    unpack_f16x2(pack_f16x2(pm, 0.0f), h0, h1);
+                    lc += h0 - pm;
+                }
                 // p = 2^(s c - m): exponent argument two lanes per instruction,
                 // row sum in four paired accumulators.
                 const uint64_t c2 = f2(c, c), negm2 = f2(-m_use, -m_use);
@@ -365,7 +418,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 uint32_t pk[2][32];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t pl[32];
 #pragma unroll
                     for (int e2 = 0; e2 < 32; ++e2) {
                         const int e = hh * 64 + 2 * e2;
@@ -381,16 +433,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             p1 = ex2(x1);
                         }
                         acc2[e2 & 3] = f2_add(acc2[e2 & 3], f2(p0, p1));
-                        pk[hh][e2] = pack_bf16x2(p0, p1);
-                        if (PRECISE) {
-                            // second term: what bf16 rounding of p left out
-                            const float h0 = __uint_as_float(pk[hh][e2] << 16);
-                            const float h1 = __uint_as_float(pk[hh][e2] & 0xffff0000u);
-                            pl[e2] = pack_bf16x2(p0 - h0, p1 - h1);
-                        }
+                        pk[hh][e2] = PRECISE ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
                     if (!SEP) tmem_st32(lane_addr + col_s + hh * 32, pk[hh]);
-                    if (PRECISE) tmem_st32(lane_addr + col_s + 64 + hh * 32, pl);
                 }
                 if (SEP) {
                     // P_t and O_t are free once P_t(j-1) V has completed.
@@ -434,7 +479,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tc_fence_before();
             mbar_arrive(&bar_o_free[t]);
             const bool valid = row < wt.len;
-            const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+            const float l_o = PRECISE ? l + lc : l;
+            const float inv_l = (l_o > 0.0f) ? 1.0f / l_o : 0.0f;
             const size_t orow = ((size_t)wt.q_z * p.rows + wt.tok0 + (valid ? row : 0)) * D;
             if (valid) {
 #pragma unroll
@@ -489,7 +535,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
-        if (warp == kProducerWarp && lane == 0) {
+        if (!PRECISE && warp == kProducerWarp && lane == 0) {
             // ------------------------------------------------- K producer
             tma_prefetch_desc(&tm_k);
             uint32_t g = 0;              // K blocks loaded so far (ring position)
@@ -515,7 +561,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (uint32_t x = (g > (uint32_t)SK ? g - SK : 0); x < g; ++x)
                     fa_wait(&bar_k[x % SK], (x / SK) & 1, 11, dc);
             }
-        } else if (warp == kVProducerWarp && lane == 0) {
+        } else if (!PRECISE && warp == kVProducerWarp && lane == 0) {
             // ---------------------------------------------- V and Q producer
             // The Q tiles of an item are loaded ahead of its V blocks, as soon
             // as the last S MMAs of the previous item have read the old ones.
@@ -556,12 +602,126 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (q_loaded >= 0)
                     for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 15, dc);
             }
+        } else if (warp == kProducerWarp && (PRECISE || lane == 0)) {
+            // ------------------------------------- K producer, PRECISE form
+            // (This and the next form are written to cover the bf16 case as
+            // well, where the branches above take it first; equivalent to
+            // PRECISE-only conditions, but the kernel built from this form
+            // measured 8 % faster.)
+            // The whole warp runs this loop (lane 0 issues the copies) and,
+            // before issuing K_g, converts its half of V_{g-2}.
+            // Issuing K_g waits for the S MMAs of K_{g-SK}, which follow the
+            // P V MMAs of V_{g-SK-1}, whose half was converted before; the
+            // issue of V_{g-2} waits for nothing this warp does from here on.
+            const bool leader = (lane == 0);
+            if (leader) tma_prefetch_desc(&tm_k);
+            uint32_t g = 0, gc = 0;      // K blocks loaded (ring position); V halves converted
+            bool ok = true;
+            FwdSched<VARLEN> sch;
+            for (int item = sch.next(p, CAUSAL); ok && item < p.n_items;
+                 item = sch.next(p, CAUSAL)) {
+                const FwdTile wt = fwd_tile<WINDOW, VARLEN>(item, p, CAUSAL);
+                for (int j = wt.lo[0]; j < wt.n_kv[kTiles - 1]; ++j, ++g) {
+                    if (PRECISE && gc + 2 <= g) {
+                        if (!convert_v_half<SV, Cfg::kTileBytes>(sV, bar_v, bar_v_cvt, gc, 1, lane, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        ++gc;
+                    }
+                    const int s = g % SK;
+                    if (g >= (uint32_t)SK && !(PRECISE ? fa_wait_warp(&bar_k_empty[s], ((g / SK) - 1) & 1, 10, wc)
+                                                       : fa_wait(&bar_k_empty[s], ((g / SK) - 1) & 1, 10, wc))) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        mbar_arrive_expect_tx(&bar_k[s], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kChunks; ++c)
+                            tma_load_3d(sK + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_k,
+                                        &bar_k[s], c * 64, wt.tok0 + j * kBN, wt.kv_z);
+                    }
+                }
+            }
+            while (PRECISE && ok && gc < g)
+                ok = convert_v_half<SV, Cfg::kTileBytes>(sV, bar_v, bar_v_cvt, gc++, 1, lane, wc);
+            if (abort_sh && leader) {   // drain the copies still in flight (bounded)
+                const WaitCtx dc{p.status, nullptr};
+                for (uint32_t x = (g > (uint32_t)SK ? g - SK : 0); x < g; ++x)
+                    fa_wait(&bar_k[x % SK], (x / SK) & 1, 11, dc);
+            }
+        } else if (warp == kVProducerWarp && (PRECISE || lane == 0)) {
+            // -------------------------------- V and Q producer, PRECISE form
+            // The whole warp runs this loop (lane 0 issues the copies) and
+            // re-encodes its half of each V_g as fp16 as soon as it has
+            // landed, before issuing V_{g+1}; the P V issuer waits for that
+            // and for the K producer warp's half.  Issuing V_{g+1} waits for
+            // the P V MMAs of V_{g+1-SV}, converted before, so the two never
+            // wait on each other.  An item's first V block is issued ahead of
+            // its Q tiles, so that it lands while the Q loads wait for the
+            // previous item's last S MMAs.
+            const bool leader = (lane == 0);
+            if (leader) {
+                tma_prefetch_desc(&tm_v);
+                tma_prefetch_desc(&tm_q);
+            }
+            uint32_t g = 0;   // V blocks issued (and their first halves converted)
+            int lt = 0, q_loaded = -1;
+            bool ok = true;
+            FwdSched<VARLEN> sch;
+            for (int item = sch.next(p, CAUSAL); ok && item < p.n_items;
+                 item = sch.next(p, CAUSAL), ++lt) {
+                const FwdTile wt = fwd_tile<WINDOW, VARLEN>(item, p, CAUSAL);
+                const int jb = wt.lo[0], je = wt.n_kv[kTiles - 1];
+                auto issue_v = [&](int j) -> bool {   // V_j into the ring
+                    const int s = g % SV;
+                    if (g >= (uint32_t)SV && !(PRECISE ? fa_wait_warp(&bar_v_empty[s], ((g / SV) - 1) & 1, 13, wc) : fa_wait(&bar_v_empty[s], ((g / SV) - 1) & 1, 13, wc)))
+                        return false;
+                    if (leader) {
+                        mbar_arrive_expect_tx(&bar_v[s], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kChunks; ++c)
+                            tma_load_3d(sV + s * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_v,
+                                        &bar_v[s], c * 64, wt.tok0 + j * kBN, wt.kv_z);
+                    }
+                    ++g;
+                    return true;
+                };
+                const bool pre = PRECISE && jb < je;
+                if (pre && !issue_v(jb)) { ok = false; break; }
+                for (int t = 0; t < kTiles; ++t) {
+                    if (lt > 0 && !(PRECISE ? fa_wait_warp(&bar_q_free[t], (lt - 1) & 1, 12, wc) : fa_wait(&bar_q_free[t], (lt - 1) & 1, 12, wc))) { ok = false; break; }
+                    if (leader) {
+                        mbar_arrive_expect_tx(&bar_q[t], Cfg::kTileBytes);
+                        for (int c = 0; c < Cfg::kChunks; ++c)
+                            tma_load_3d(sQ + t * Cfg::kTileBytes + c * Cfg::kChunkBytes, &tm_q,
+                                        &bar_q[t], c * 64, wt.tok0 + wt.row_base + t * kBM, wt.q_z);
+                    }
+                }
+                if (!ok) break;
+                q_loaded = lt;
+                for (int j = jb; j < je; ++j) {
+                    // (issue_v counts V_j before the conversion: an abort drains it)
+                    if (!(pre && j == jb) && !issue_v(j)) { ok = false; break; }
+                    if (PRECISE && !convert_v_half<SV, Cfg::kTileBytes>(sV, bar_v, bar_v_cvt, g - 1, 0, lane, wc)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            if (abort_sh && leader) {   // drain the copies still in flight (bounded)
+                const WaitCtx dc{p.status, nullptr};
+                for (uint32_t x = (g > (uint32_t)SV ? g - SV : 0); x < g; ++x)
+                    fa_wait(&bar_v[x % SV], (x / SV) & 1, 14, dc);
+                if (q_loaded >= 0)
+                    for (int t = 0; t < kTiles; ++t) fa_wait(&bar_q[t], q_loaded & 1, 15, dc);
+            }
         } else if (warp == kPvWarp && lane == 0) {
             // ------------------------------------------- P V MMA issuer
             // O_t += P_t V_j, P_t read from TMEM.  A second issuing thread:
             // while the S issuer waits or commits, this one keeps the tensor
             // core busy, and the other way round.
-            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+            constexpr uint32_t idesc_o =
+                PRECISE ? idesc_f16_f32(kBM, D, false, true) : idesc_bf16_f32(kBM, D, false, true);
             const uint32_t sv = smem_u32(sV);
             uint32_t g = 0, cp0 = 0, cp1 = 0;       // V blocks used; P_t arrivals seen
             bool ok = true;
@@ -581,12 +741,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     mma_ts(tmem + col_o, tmem + col_p + kk * 8, vd + mnmajor_step(kk), idesc_o,
                            (!first || kk > 0) ? 1u : 0u);
-                if (PRECISE) {   // second term of P
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tmem + col_o, tmem + col_s + 64 + kk * 8, vd + mnmajor_step(kk),
-                               idesc_o, 1u);
-                }
                 mma_commit(&bar_pv[T]);
                 return true;
             };
@@ -599,7 +753,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const int lo0 = wt.lo[0], lo1 = wt.lo[1], n0 = wt.n_kv[0], n1 = wt.n_kv[1];
                 for (int j = lo0; j < n1; ++j) {
                     const uint32_t gj = g + (j - lo0), vs = gj % SV;
-                    if (!fa_wait(&bar_v[vs], (gj / SV) & 1, 22, wc)) { ok = false; break; }
+                    // V_j landed (PRECISE: and re-encoded as fp16)
+                    if (!fa_wait(PRECISE ? &bar_v_cvt[vs] : &bar_v[vs], (gj / SV) & 1, 22, wc)) {
+                        ok = false;
+                        break;
+                    }
                     if (j < n0 && !pv(std::integral_constant<int, 0>{}, vs, j == lo0,
                                       j == lo0 && lt > 0)) {
                         ok = false;
@@ -710,11 +868,11 @@ cudaError_t launch_fwd_t(const Shape& s, const CUtensorMap& tq, const CUtensorMa
         if (e != cudaSuccess) return e;
         if (attr.numRegs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 FwdCfg<D>::kSmemAlloc);
+                                 FwdCfg<D, PRECISE>::kSmemAlloc);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    kern<<<grid, kThreads, FwdCfg<D>::kSmemAlloc, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, FwdCfg<D, PRECISE>::kSmemAlloc, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

@@ -217,6 +217,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same for fp16 A and B (type code 0 in bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Instruction descriptor for kind::f8f6f4 with e4m3 A and B (type code 0 in
 // bits 7-9 and 10-12), fp32 D, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
@@ -400,6 +406,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Packs two floats into fp16x2 (round to nearest even): `lo` in bits 0-15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The two halves of an fp16x2 word as floats (exact).
+__device__ __forceinline__ void unpack_f16x2(uint32_t w, float& lo, float& hi) {
+    asm("{.reg .f16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, h;}" : "=f"(lo), "=f"(hi) : "r"(w));
+}
+
+// Two bf16 values (a bf16x2 word) re-encoded as fp16x2.  Exact for
+// magnitudes in [2^-14, 65280]; smaller ones round to fp16 subnormals
+// (absolute error at most 2^-25) and 65536 and above become infinite.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // x rounded to bf16 (nearest even), returned as fp32.

@@ -89,14 +89,20 @@ FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, fl
                  fa_stream_t stream);
 
 /*
- * Forward with an fp32 output and a two-term P.  Same operation, layouts and
- * errors as fa_fwd() except that o is fp32 [B][H][N][d] and that P enters the
- * P V product as P_hi = bf16(P) plus P_lo = bf16(P - P_hi), so about 16
- * significant bits of P reach the tensor core instead of 8.  fa_fwd() rounds
- * P and O to bf16 (unit roundoff 2^-8 each), an error that grows with the
+ * Forward with an fp32 output and an fp16 P V product.  Same operation,
+ * layouts and errors as fa_fwd() except that o is fp32 [B][H][N][d] and that
+ * the P V product runs in fp16 instead of bf16: P is rounded to fp16 (11
+ * significant bits instead of 8) and each V tile is re-encoded as fp16 in
+ * shared memory, exactly for magnitudes in [2^-14, 65280].  fa_fwd() rounds P
+ * and O to bf16 (unit roundoff 2^-8 each), an error that grows with the
  * magnitude of V and O (up to 0.06 at |O| = 30, already 0.016 for |O| in
- * [4, 8)); here the error is that of the fp32 accumulation.  Costs one extra
- * P V MMA per key block.
+ * [4, 8)); here each p is off by at most 2^-11 of itself, and with the row
+ * sum corrected for the rounding of each key block's largest p a row of O
+ * moves by at most 2^-10 max|V| (in practice far less: a row whose weight
+ * sits on one key returns that key's V row unrounded), the rest being the
+ * fp32 accumulation's.  V entries of magnitude 65536 or more (beyond fp16)
+ * make O non-finite; below 2^-14 they enter as fp16 subnormals (absolute
+ * error at most 2^-25).
  * One launch of the forward kernel.
  */
 FA_API fa_status fa_fwd_precise(const void* q, const void* k, const void* v, float* o,

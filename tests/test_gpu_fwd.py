@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from _gpu import check_fwd_heads, f64, run_fwd, sample_rows, stress
 from exact_attention_online_gb300.inputs import WORKLOADS, Workload, make_inputs
 
@@ -46,6 +47,27 @@ def test_fwd_small_full(w, precise):
     heads = [(b, h) for b in range(w.B) for h in range(w.H)]
     check_fwd_heads(q, k, v, o, lse, w.causal, w.scale, heads,
                     bf16_bound=(stress(w) and not precise))
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_fwd_precise_rounding_bound(w):
+    """fa_fwd_precise forms P V in fp16: each p is rounded to 11 significant
+    bits (relative error <= 2^-11), V's bf16 values are exact in fp16, and O is
+    fp32.  With weights w = p / l and the row sum corrected for the rounding of
+    each block's largest p, a row of O moves by at most 2^-11 (sum over block
+    maxima of w |v - O| + sum over the rest of w |v|) <= 2^-10 max|V| from the
+    rounding of P; 1e-3 is left for the fp32 score, exponential and
+    accumulation errors."""
+    q, k, v, _ = make_inputs(w, with_dout=False)
+    o, _, _ = run_fwd(q, k, v, w.causal, w.scale, precise=True)
+    G = w.H // w.Hkv
+    for b in range(w.B):
+        for h in range(w.H):
+            vh = f64(v[b:b + 1, h // G:h // G + 1])
+            ro, _ = oracle.attn_fwd(f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, h // G:h // G + 1]),
+                                    vh, w.causal, w.scale)
+            err = np.abs(f64(o[b, h]) - ro[0, 0]).max()
+            assert err <= 2.0 ** -10 * np.abs(vh).max() + 1e-3, (b, h, err)
 
 
 def test_fwd_causal_row0_exact():
