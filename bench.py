@@ -464,7 +464,8 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ GPU side
-def pipelined_e2e(torch, dev, stream, dev_in, host_in, dev_out, host_out, compute, n, barrier):
+def pipelined_e2e(torch, dev, stream, dev_in, host_in, dev_out, host_out, compute, n, barrier,
+                  reps=3):
     """End-to-end steps as a training loop runs them: step k's inputs copied in
     from pinned host memory on a stream of their own, its kernels on `stream`,
     its outputs copied back on a third stream, and two slots of device
@@ -472,8 +473,10 @@ def pipelined_e2e(torch, dev, stream, dev_in, host_in, dev_out, host_out, comput
     overlap step k's kernels.  Every step copies all of host_in in and fills
     all of host_out.  compute(*inputs, *outputs) launches one step on `stream`
     (inputs and outputs of one slot).  Eight untimed steps and a device
-    synchronisation come first; returns the elapsed ms of the n timed steps,
-    from the first input copy to the last output copy."""
+    synchronisation come first; returns the elapsed ms of n timed steps, from
+    the first input copy to the last output copy: the median of `reps` such
+    runs (the copies share the host's memory and link with whatever else runs
+    on the machine, and one run of about 0.1 s can catch a slow moment)."""
     slot_in = [list(dev_in), [torch.empty_like(t) for t in dev_in]]
     slot_out = [list(dev_out), [torch.empty_like(t) for t in dev_out]]
     # one copy stream each way (two each way measured slower)
@@ -502,14 +505,17 @@ def pipelined_e2e(torch, dev, stream, dev_in, host_in, dev_out, host_out, comput
 
     run(8)
     torch.cuda.synchronize()
-    barrier()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s_in)
-    run(n)
-    b.record(s_out)
-    barrier()
-    torch.cuda.synchronize()
-    return a.elapsed_time(b)
+    times = []
+    for _ in range(reps):
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_in)
+        run(n)
+        b.record(s_out)
+        barrier()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return sorted(times)[len(times) // 2]
 
 
 def run_native(args, w):
@@ -740,7 +746,8 @@ def run_native(args, w):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / e2e_steps, "steps": e2e_steps,
                "pipelined": "inputs of step k+1 copied in and outputs of step k-1 copied out "
-                            "while step k computes (three streams, two device buffer slots)",
+                            "while step k computes (three streams, two device buffer slots); "
+                            "median of three timed runs of the steps",
                "serial_value": replicas.whole_job_rate(flops_step, e2e_steps, ws,
                                                        serial_ms) / 1e12,
                "serial_ms_per_step": serial_ms / e2e_steps}
@@ -952,7 +959,8 @@ def run_native_fp8(args, w):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / n_e,
                "steps": n_e,
                "pipelined": "inputs of step k+1 copied in and outputs of step k-1 copied out "
-                            "while step k computes (three streams, two device buffer slots)",
+                            "while step k computes (three streams, two device buffer slots); "
+                            "median of three timed runs of the steps",
                "serial_value": replicas.whole_job_rate(flops_step, n_e, ws, serial_ms) / 1e12,
                "serial_ms_per_step": serial_ms / n_e}
     if rank == 0:
@@ -1242,7 +1250,8 @@ def run_native_varlen(args):
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
                "ms_per_step": e_ms / n_e, "steps": n_e,
                "pipelined": "inputs of step k+1 copied in and outputs of step k-1 copied out "
-                            "while step k computes (three streams, two device buffer slots)",
+                            "while step k computes (three streams, two device buffer slots); "
+                            "median of three timed runs of the steps",
                "serial_value": flops_step * n_e * ws / (serial_ms * 1e-3) / 1e12,
                "serial_ms_per_step": serial_ms / n_e}
     if rank == 0:
