@@ -1127,6 +1127,582 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// d = 128 with two query blocks in flight.
+//
+// The kernel above keeps one query block in flight at d = 128: its period is
+// the hand-off chain S^T -> P -> dV -> next S^T and dP^T -> dS -> dK, dQ ->
+// next dP^T through the compute warps, over which the tensor pipe idles about
+// half the time.  This form runs two pipelines, the even and the odd
+// query-block steps of a CTA, each with its own tensor-memory columns, four
+// compute warps, dS^T tile and MMA-issuing thread, so that one pipeline's MMAs
+// run while the other waits for its compute warps:
+//   TMEM  dK 0-127 | dV 128-255 | S^T_0 | dP^T_0 / dQ^T_0 | S^T_1 | dP^T_1 / dQ^T_1
+// (64 columns each).  A step's dQ^T goes over its pipeline's dP^T columns
+// once the compute warps have read them (they have when dS^T is written), and
+// the pipeline's next dP^T waits until the read-out warps have taken dQ^T.
+// K_j is read from shared memory (no columns left for a tensor-memory copy).
+// Both pipelines accumulate into dK and dV, so the compute warps zero them
+// before an item's first dV / dK MMA instead of an accumulate flag doing it,
+// and each issuing thread issues step git's dV (dK) MMAs only after the other
+// has issued step git - 1's (a turn barrier per accumulator): the tensor core
+// takes MMAs in issue order, so dK and dV sum their terms in step order and
+// come out bit-reproducible.
+// Used at d = 128 under the causal mask without a window (dense or packed
+// batches), where it measured faster (A/B on one box: dK/dV -2.1 % gpt_long,
+// -2.8 % gqa; steps +0.7 to +2.6 %, +1.9 % packed); with the sliding window
+// (long items) it measured 3.5 % slower and without the mask it was not
+// measured, so those keep the one-pipeline kernel.
+// Q_i / dO_i stream through three stages so that a pipeline's next block has
+// landed while its current one is in use; a stage's landing is signalled on
+// one of six barriers (step mod 6), so that each issuing thread waits on
+// barriers only it waits on, phase after phase.  The dQ partial leaves
+// through a 16 KB staging tile in two halves.
+struct Bwd2Cfg {
+    static constexpr int D = 128;
+    static constexpr int kBR = 64;
+    static constexpr int kStages = 3;
+    static constexpr int kKVBytes = kBN * D * 2;               // 32 KB
+    static constexpr int kQBytes = kBR * D * 2;                // 16 KB
+    static constexpr int kDSBytes = kBN * kBR * 2;             // 16 KB
+    static constexpr int kStageTileBytes = (kBR / 2) * D * 4;  // 16 KB: half a dQ partial
+    static constexpr int kOnesBytes = kBN * 32;
+    static constexpr int kExtBytes = kBR * 32;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kKVBytes;
+    static constexpr int kOffQ = kOffV + kKVBytes;               // kStages
+    static constexpr int kOffDO = kOffQ + kStages * kQBytes;     // kStages
+    static constexpr int kOffDS = kOffDO + kStages * kQBytes;    // one per pipeline
+    static constexpr int kOffStage = kOffDS + 2 * kDSBytes;
+    static constexpr int kOffOnes = kOffStage + kStageTileBytes;
+    static constexpr int kOffExt = kOffOnes + kOnesBytes;        // [stage][lse, d]
+    static constexpr int kSmemBytes = kOffExt + kStages * 2 * kExtBytes;
+    static constexpr int kSmemAlloc = kSmemBytes + 1024;
+    static constexpr int kStepBytes = 2 * kQBytes + 2 * kExtBytes;
+    static constexpr uint32_t kColDK = 0, kColDV = 128;
+    __host__ __device__ static constexpr uint32_t col_s(int pp) { return 256 + 128 * pp; }
+    __host__ __device__ static constexpr uint32_t col_dpq(int pp) { return 320 + 128 * pp; }
+};
+static_assert(Bwd2Cfg::kSmemAlloc <= 227 * 1024 - 1024, "shared memory of the two-pipeline kernel");
+
+template <bool CAUSAL, bool WINDOW, bool VARLEN>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_bwd_dkdv2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p) {
+    using Cfg = Bwd2Cfg;
+    constexpr int D = Cfg::D, BR = Cfg::kBR, NS = Cfg::kStages;
+    constexpr int kPipeThreads = 128;            // compute threads of one pipeline
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    // bar_full[git % 6]: step git's Q_i, dO_i and tables landed (stage git % 3)
+    __shared__ uint64_t bar_kv, bar_kv_free, bar_full[2 * NS], bar_empty[NS];
+    __shared__ uint64_t bar_s[2], bar_dp[2], bar_p[2], bar_ds[2], bar_dq_full[2], bar_dq_free[2];
+    __shared__ uint64_t bar_done, bar_acc_free;
+    // bar_dv_turn / bar_dk_turn: phase git completes when step git's dV (dK)
+    // MMAs have been issued
+    __shared__ uint64_t bar_dv_turn, bar_dk_turn;
+    __shared__ uint64_t bar_item_full[2], bar_item_empty[2];
+    __shared__ int item_sh[2];
+    constexpr int kItemConsumers = kComputeWarps + 4 + 2;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+    const WaitCtx wc{p.status, &abort_sh};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    uint8_t* sK = smem + Cfg::kOffK;
+    uint8_t* sV = smem + Cfg::kOffV;
+    uint8_t* sQ = smem + Cfg::kOffQ;
+    uint8_t* sDO = smem + Cfg::kOffDO;
+    uint8_t* sDS = smem + Cfg::kOffDS;
+    float* sStage = reinterpret_cast<float*>(smem + Cfg::kOffStage);
+    uint8_t* sOnes = smem + Cfg::kOffOnes;
+    uint8_t* sExt = smem + Cfg::kOffExt;      // stage st: lse at 2 st, d at 2 st + 1
+
+    bwd_fill_ones(sOnes, p.scale_log2);
+
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        mbar_init(&bar_kv, 1);
+        mbar_init(&bar_kv_free, 2);                  // one commit per MMA issuer
+        for (int s = 0; s < 2 * NS; ++s) mbar_init(&bar_full[s], 1);
+        for (int s = 0; s < NS; ++s) mbar_init(&bar_empty[s], 1);   // the step's MMA issuer
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&bar_s[q], 1);
+            mbar_init(&bar_dp[q], 1);
+            mbar_init(&bar_p[q], kPipeThreads);
+            mbar_init(&bar_ds[q], kPipeThreads);
+            mbar_init(&bar_dq_full[q], 1);
+            mbar_init(&bar_dq_free[q], kReadoutThreads);
+            mbar_init(&bar_item_full[q], 1);
+            mbar_init(&bar_item_empty[q], kItemConsumers);
+        }
+        mbar_init(&bar_done, 2);                     // one commit per MMA issuer, per item
+        mbar_init(&bar_acc_free, kComputeThreads);   // dK, dV zeroed for the item
+        mbar_init(&bar_dv_turn, 1);
+        mbar_init(&bar_dk_turn, 1);
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&tmem_base_sh, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    auto next_item_warp = [&](int n, int& item) -> bool {
+        const int slot = n & 1;
+        if (!fa_wait_warp(&bar_item_full[slot], (n >> 1) & 1, 65, wc)) return false;
+        item = item_sh[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_item_empty[slot]);
+        return true;
+    };
+    auto next_item_thread = [&](int n, int& item) -> bool {
+        const int slot = n & 1;
+        if (!fa_wait(&bar_item_full[slot], (n >> 1) & 1, 65, wc)) return false;
+        item = item_sh[slot];
+        mbar_arrive(&bar_item_empty[slot]);
+        return true;
+    };
+
+    if (warp < kComputeWarps) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
+        // ------------------------------------------------------------ compute
+        // warp w: pipeline w / 4 (the steps of that parity), TMEM lane quarter
+        // w % 4 (= 32 key rows), all 64 query columns of the step.
+        const int cp = warp >> 2, quarter = warp & 3;
+        const int rl = quarter * 32 + lane;          // key row within the block
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t col_s = Cfg::col_s(cp), col_dp = Cfg::col_dpq(cp);
+        uint8_t* const sds = sDS + cp * Cfg::kDSBytes;
+        const float c = p.scale_log2;
+        bool ok = true;
+        int gi = 0, nb = 0;   // query-block steps and work items of this CTA so far
+        for (int n = 0; ok; ++n) {
+            int item;
+            if (!next_item_warp(n, item) || item < 0) break;
+            const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+            if (cta.idle || cta.n_it == 0) continue;
+            const int jblk = cta.jblk, tok0 = cta.tok0, seq_len = cta.seq_len, z_kv = cta.z_kv;
+            const int i_start = cta.i_start, n_i = cta.n_i, n_it = cta.n_it;
+            const int key = jblk * kBN + rl;
+            // dK (pipeline 0's warps) and dV (pipeline 1's) of this item start
+            // from zero; the previous item's were read out below
+            {
+                uint32_t z[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) z[e] = 0u;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32)
+                    tmem_st32(lane_addr + (cp ? Cfg::kColDV : Cfg::kColDK) + c0, z);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bar_acc_free);
+            }
+            for (int it = (gi & 1) == cp ? 0 : 1; ok && it < n_it; it += 2) {
+                const int git = gi + it;
+                const uint32_t k = (uint32_t)git >> 1;       // this pipeline's step count
+                const int i = i_start + it % n_i;
+                if (!fa_wait_warp(&bar_s[cp], k & 1, 61, wc)) { ok = false; break; }
+                tc_fence_after();
+                const int q0 = i * BR;
+                const bool need_mask = (CAUSAL && (q0 < jblk * kBN + kBN - 1 ||
+                                                   (WINDOW && q0 + BR - 1 > jblk * kBN + p.window - 1))) ||
+                                       (jblk * kBN + kBN > seq_len);
+                const int key_lim = CAUSAL ? key - q0 : -1;
+                const int key_hi = WINDOW ? key + p.window - 1 - q0 : BR;
+                const bool key_valid = key < seq_len;
+                // P^T = 2^(S'^T c), S'^T = S^T - LSE log2(e) / c from the tensor
+                // core; fp32 kept for dS, the bf16 pairs written over the first
+                // 32 columns of S^T (already read) for the dV MMA.
+                float pf[BR];
+                const uint64_t c2 = f2(c, c);
+#pragma unroll
+                for (int ch = 0; ch < BR / 32; ++ch) {
+                    uint32_t sr[32];
+                    tmem_ld32(lane_addr + col_s + ch * 32, sr);
+                    tmem_ld_wait(sr);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e2 = 0; e2 < 16; ++e2) {
+                        const int qe = ch * 32 + 2 * e2;
+                        float x0, x1;
+                        f2_split(f2_mul(f2(__uint_as_float(sr[2 * e2]), __uint_as_float(sr[2 * e2 + 1])),
+                                        c2),
+                                 x0, x1);
+                        float p0 = ex2(x0), p1 = ex2(x1);
+                        if (need_mask) {
+                            if (qe < key_lim || qe > key_hi || !key_valid) p0 = 0.0f;
+                            if (qe + 1 < key_lim || qe + 1 > key_hi || !key_valid) p1 = 0.0f;
+                        }
+                        pf[qe] = p0;
+                        pf[qe + 1] = p1;
+                        pk[e2] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(lane_addr + col_s + ch * 16, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bar_p[cp]);
+
+                // dS^T = P^T o (dP^T - D) -> bf16, swizzled [key][query] tile;
+                // dP^T - D comes from the tensor core.  The pipeline's previous
+                // dK and dQ MMAs, which read this tile, were issued before this
+                // dP^T, so its completion frees the tile.
+                if (!fa_wait_warp(&bar_dp[cp], k & 1, 62, wc)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int ch = 0; ch < BR / 32; ++ch) {
+                    uint32_t dpr[32];
+                    tmem_ld32(lane_addr + col_dp + ch * 32, dpr);
+                    tmem_ld_wait(dpr);
+                    uint32_t dsk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float d0, d1;
+                        f2_split(f2_mul(f2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]),
+                                        f2(__uint_as_float(dpr[2 * e]), __uint_as_float(dpr[2 * e + 1]))),
+                                 d0, d1);
+                        dsk[e] = pack_bf16x2(d0, d1);
+                    }
+                    uint8_t* rowp = sds + rl * 128;
+#pragma unroll
+                    for (int u4 = 0; u4 < 4; ++u4) {
+                        const int unit = ch * 4 + u4;
+                        *reinterpret_cast<uint4*>(rowp + ((unit ^ (rl & 7)) * 16)) =
+                            make_uint4(dsk[u4 * 4 + 0], dsk[u4 * 4 + 1], dsk[u4 * 4 + 2],
+                                       dsk[u4 * 4 + 3]);
+                    }
+                }
+                tc_fence_before();   // the dP^T reads precede the dQ^T MMA over them
+                fence_proxy_async_smem();
+                mbar_arrive(&bar_ds[cp]);
+            }
+            // ---------------------------------------------------- dK, dV epilogue
+            if (ok && fa_wait_warp(&bar_done, nb & 1, 63, wc)) {
+                tc_fence_after();
+                const bool valid = key < seq_len;
+                const size_t row = ((size_t)z_kv * p.rows + tok0 + (valid ? key : 0)) * D;
+                const uint32_t col = cp ? Cfg::kColDV : Cfg::kColDK;
+                const float mul = cp ? 1.0f : p.scale;
+                __nv_bfloat16* dst = (cp ? p.dv : p.dk) + row;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + col + c0, r);
+                    tmem_ld_wait(r);
+                    if (valid) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[q4 * 8 + 0]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 1]) * mul);
+                            w.y = pack_bf16x2(__uint_as_float(r[q4 * 8 + 2]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 3]) * mul);
+                            w.z = pack_bf16x2(__uint_as_float(r[q4 * 8 + 4]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 5]) * mul);
+                            w.w = pack_bf16x2(__uint_as_float(r[q4 * 8 + 6]) * mul,
+                                              __uint_as_float(r[q4 * 8 + 7]) * mul);
+                            d4[q4] = w;
+                        }
+                    }
+                }
+            } else {
+                ok = false;
+            }
+            gi += n_it;
+            ++nb;
+        }
+    } else if (warp >= kReadoutWarp0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsReadout));
+        // ----------------------------------------------------- dQ read-out
+        // TMEM (the step's pipeline) -> registers -> fp32 staging tile in two
+        // halves of 32 query rows -> a 16 KB bulk reduce-add each.
+        const int quarter = warp & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int rl = quarter * 32 + lane;          // head-dim index
+        const bool leader = (warp == kReadoutWarp0 && lane == 0);
+        bool ok = true;
+        int gi = 0;
+        for (int n = 0; ok; ++n) {
+            int item;
+            if (!next_item_warp(n, item) || item < 0) break;
+            const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+            if (cta.idle || cta.n_it == 0) continue;
+            const int b = cta.b, g = cta.g, i_start = cta.i_start, n_i = cta.n_i, n_it = cta.n_it;
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int git = gi + it;
+                const int pp = git & 1;
+                const uint32_t k = (uint32_t)git >> 1;
+                const int hq = g * p.G + it / n_i;
+                const int i = i_start + it % n_i;
+                const int bh = b * p.H + hq;
+                const bool w_ok = fa_wait_warp(&bar_dq_full[pp], k & 1, 70, wc);
+                if (named_bar_or(1, kReadoutThreads, !w_ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                tmem_ld32(lane_addr + Cfg::col_dpq(pp), r0);
+                tmem_ld32(lane_addr + Cfg::col_dpq(pp) + 32, r1);
+                tmem_ld_wait(r0);
+                asm volatile("" : FA_R32(r1) : : "memory");
+                tc_fence_before();
+                mbar_arrive(&bar_dq_free[pp]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // the copy that last read the staging tile
+                    if (leader) bulk_wait_group_read<0>();
+                    named_bar_sync(1, kReadoutThreads);
+                    // dQ^T: lane = head-dim index, column = query -> stg[q][dd]
+                    const uint32_t* src = h ? r1 : r0;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sStage[e * D + rl] = __uint_as_float(src[e]);
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, kReadoutThreads);
+                    if (leader) {
+                        bulk_reduce_add_f32(
+                            p.dq_acc + ((size_t)bh * p.Np + (size_t)i * BR + h * (BR / 2)) * D, sStage,
+                            Cfg::kStageTileBytes);
+                        bulk_commit_group();
+                    }
+                }
+            }
+            gi += n_it;
+        }
+        if (leader) bulk_wait_group<0>();
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+        if (warp == kProducerWarp) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_do);
+                int gi = 0, nb = 0;
+                int issued = 0, kv_issued = 0;
+                bool ok = true;
+                for (int n = 0; ok; ++n) {
+                    const int slot = n & 1;
+                    if (n >= 2 && !fa_wait(&bar_item_empty[slot], ((n >> 1) - 1) & 1, 66, wc)) break;
+                    // Every CTA's last take finds no item; the last of those
+                    // takes leaves the counter zero for the next launch.
+                    const int old = atomicAdd(p.work, 1);
+                    const int item = old < p.n_items ? old : -1;
+                    if (old == p.n_items + (int)gridDim.x - 1) *p.work = 0;
+                    item_sh[slot] = item;
+                    mbar_arrive(&bar_item_full[slot]);
+                    if (item < 0) break;
+                    const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+                    if (cta.idle || cta.n_it == 0) continue;
+                    const int jblk = cta.jblk, b = cta.b, g = cta.g, tok0 = cta.tok0;
+                    const int z_kv = cta.z_kv, i_start = cta.i_start, n_i = cta.n_i;
+                    const int n_it = cta.n_it;
+                    // K_j, V_j over the previous item's, whose MMAs have completed
+                    if (nb > 0 && !fa_wait(&bar_kv_free, (nb - 1) & 1, 42, wc)) break;
+                    mbar_arrive_expect_tx(&bar_kv, 2 * Cfg::kKVBytes);
+                    for (int c = 0; c < D / 64; ++c) {
+                        tma_load_3d(sK + c * (kBN * 128), &tm_k, &bar_kv, c * 64, tok0 + jblk * kBN,
+                                    z_kv);
+                        tma_load_3d(sV + c * (kBN * 128), &tm_v, &bar_kv, c * 64, tok0 + jblk * kBN,
+                                    z_kv);
+                    }
+                    ++kv_issued;
+                    for (int it = 0; it < n_it; ++it) {
+                        const int git = gi + it;
+                        const int st = git % NS, u = git / NS;
+                        if (git >= NS && !fa_wait(&bar_empty[st], (u - 1) & 1, 40, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        const int hq = g * p.G + it / n_i;
+                        const int i = i_start + it % n_i;
+                        const int bh = b * p.H + hq;
+                        const int z_q = VARLEN ? hq : bh;
+                        uint64_t* full = &bar_full[git % (2 * NS)];
+                        mbar_arrive_expect_tx(full, Cfg::kStepBytes);
+                        for (int c = 0; c < D / 64; ++c) {
+                            tma_load_3d(sQ + st * Cfg::kQBytes + c * (BR * 128), &tm_q, full, c * 64,
+                                        tok0 + i * BR, z_q);
+                            tma_load_3d(sDO + st * Cfg::kQBytes + c * (BR * 128), &tm_do, full, c * 64,
+                                        tok0 + i * BR, z_q);
+                        }
+                        const size_t xrow = (size_t)bh * p.Np + (size_t)i * BR;
+                        bulk_load(sExt + (2 * st) * Cfg::kExtBytes, p.lse_ext + xrow * kExtCols,
+                                  Cfg::kExtBytes, full);
+                        bulk_load(sExt + (2 * st + 1) * Cfg::kExtBytes, p.d_ext + xrow * kExtCols,
+                                  Cfg::kExtBytes, full);
+                        issued = git + 1;
+                    }
+                    gi += n_it;
+                    ++nb;
+                }
+                if (abort_sh) {   // drain the copies still in flight (bounded)
+                    const WaitCtx dc{p.status, nullptr};
+                    if (kv_issued > 0) fa_wait(&bar_kv, (kv_issued - 1) & 1, 41, dc);
+                    for (int x = max(0, issued - NS); x < issued; ++x)
+                        fa_wait(&bar_full[x % (2 * NS)], (x / (2 * NS)) & 1, 41, dc);
+                }
+            }
+            __syncwarp();
+        } else if (warp == kMmaWarp || warp == kMma2Warp) {
+            if (lane == 0) {
+                // MMA issue for pipeline pp: per step S^T, dP^T (once the
+                // read-out has taken the pipeline's previous dQ^T), dV (once P^T
+                // is in TMEM), dK and dQ^T (once dS^T is in SMEM).
+                const int pp = (warp == kMmaWarp) ? 0 : 1;
+                constexpr uint32_t id_s = idesc_bf16_f32(128, BR, false, false);
+                constexpr uint32_t id_kv = idesc_bf16_f32(128, D, false, true);
+                constexpr uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);
+                const uint32_t sk = smem_u32(sK), sv = smem_u32(sV), sq = smem_u32(sQ),
+                               sdo = smem_u32(sDO), sds = smem_u32(sDS) + pp * Cfg::kDSBytes;
+                const uint64_t kd = sdesc_sw128(sk, 16, 1024), vd = sdesc_sw128(sv, 16, 1024);
+                const uint64_t dsd = sdesc_sw128(sds, 16, 1024);
+                const uint64_t kd_mn = sdesc_sw128(sk, kBN * 128, 1024);
+                const uint64_t dsd_mn = sdesc_sw128(sds, kBN * 128, 1024);
+                const uint32_t sext = smem_u32(sExt);
+                const uint64_t onesd = sdesc_plain(smem_u32(sOnes), 128, 256);
+                const uint32_t col_s = Cfg::col_s(pp), col_dpq = Cfg::col_dpq(pp);
+                bool ok = true;
+                int gi = 0, nb = 0;
+                for (int n = 0; ok; ++n) {
+                    int item;
+                    if (!next_item_thread(n, item)) { ok = false; break; }
+                    if (item < 0) break;
+                    const BwdCta cta = bwd_cta<CAUSAL, WINDOW, VARLEN>(p, BR, item);
+                    if (cta.idle || cta.n_it == 0) continue;
+                    const int n_it = cta.n_it;
+                    // Every per-item phase is waited on by both issuers, whether
+                    // or not the item has steps of their parity: K_j, V_j landed
+                    // and dK, dV zeroed (a waiter never falls two phases behind).
+                    ok = fa_wait(&bar_kv, nb & 1, 50, wc) && fa_wait(&bar_acc_free, nb & 1, 58, wc);
+                    for (int it = (gi & 1) == pp ? 0 : 1; ok && it < n_it; it += 2) {
+                        const int git = gi + it;
+                        const uint32_t k = (uint32_t)git >> 1;
+                        const int st = git % NS;
+                        if (!fa_wait(&bar_full[git % (2 * NS)], (git / (2 * NS)) & 1, 51, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t q_ = sq + st * Cfg::kQBytes, do_ = sdo + st * Cfg::kQBytes;
+                        // S^T = K_j Q_i^T - LSE log2(e) / c
+                        {
+                            const uint64_t qd = sdesc_sw128(q_, 16, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_ss(tmem + col_s, kd + kmajor_step(kk, kBN * 128),
+                                       qd + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                            mma_ss(tmem + col_s, onesd,
+                                   sdesc_plain(sext + 2 * st * Cfg::kExtBytes, 128, 256), id_s, 1u);
+                            mma_commit(&bar_s[pp]);
+                        }
+                        // dP^T - D = V_j dO_i^T - D, over the previous dQ^T
+                        if (k > 0 && !fa_wait(&bar_dq_free[pp], (k - 1) & 1, 53, wc)) { ok = false; break; }
+                        tc_fence_after();
+                        {
+                            const uint64_t dod = sdesc_sw128(do_, 16, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                mma_ss(tmem + col_dpq, vd + kmajor_step(kk, kBN * 128),
+                                       dod + kmajor_step(kk, BR * 128), id_s, kk > 0);
+                            mma_ss(tmem + col_dpq, onesd,
+                                   sdesc_plain(sext + (2 * st + 1) * Cfg::kExtBytes, 128, 256), id_s,
+                                   1u);
+                            mma_commit(&bar_dp[pp]);
+                        }
+                        // dV += P^T dO_i (P^T: bf16 pairs in the first 32 S^T columns),
+                        // after step git - 1's dV MMAs
+                        if (!fa_wait(&bar_p[pp], k & 1, 52, wc) ||
+                            (git > 0 && !fa_wait(&bar_dv_turn, (git - 1) & 1, 46, wc))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        {
+                            const uint64_t dod_mn = sdesc_sw128(do_, BR * 128, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < BR / 16; ++kk)
+                                mma_ts(tmem + Cfg::kColDV, tmem + col_s + kk * 8,
+                                       dod_mn + mnmajor_step(kk), id_kv, 1u);
+                        }
+                        tc_fence_before();   // the MMAs above precede the turn's arrival
+                        mbar_arrive(&bar_dv_turn);
+                        // dK += dS^T Q_i, after step git - 1's dK MMAs
+                        if (!fa_wait(&bar_ds[pp], k & 1, 55, wc) ||
+                            (git > 0 && !fa_wait(&bar_dk_turn, (git - 1) & 1, 47, wc))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        {
+                            const uint64_t qd_mn = sdesc_sw128(q_, BR * 128, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < BR / 16; ++kk)
+                                mma_ss(tmem + Cfg::kColDK, dsd + kmajor_step(kk, kBN * 128),
+                                       qd_mn + mnmajor_step(kk), id_kv, 1u);
+                        }
+                        tc_fence_before();   // the MMAs above precede the turn's arrival
+                        mbar_arrive(&bar_dk_turn);
+                        mma_commit(&bar_empty[st]);      // Q_i, dO_i no longer read
+                        // dQ^T partial = K_j^T dS^T (K dimension = the 128 keys),
+                        // over dP^T, which the compute warps have read
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ss(tmem + col_dpq, kd_mn + mnmajor_step(kk), dsd_mn + mnmajor_step(kk),
+                                   id_dq, kk > 0);
+                        mma_commit(&bar_dq_full[pp]);
+                    }
+                    if (ok) {   // every MMA of the item from this thread (possibly none)
+                        mma_commit(&bar_done);
+                        mma_commit(&bar_kv_free);
+                    }
+                    gi += n_it;
+                    ++nb;
+                }
+                if (!ok) {   // no MMA of this thread may still write TMEM at teardown
+                    __shared__ uint64_t bar_drain2[2];
+                    mbar_init(&bar_drain2[pp], 1);
+                    fence_mbar_init();
+                    mma_commit(&bar_drain2[pp]);
+                    fa_wait(&bar_drain2[pp], 0, 59, WaitCtx{p.status, nullptr});
+                }
+            }
+            __syncwarp();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <bool CAUSAL, bool WINDOW = false, bool VARLEN = false>
+cudaError_t launch_dkdv2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const BwdParams& p, int grid,
+                           cudaStream_t stream) {
+    auto kern = fa_bwd_dkdv2_kernel<CAUSAL, WINDOW, VARLEN>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaFuncAttributes attr;
+        cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+        if (e != cudaSuccess) return e;
+        if (attr.numRegs * kThreads < kRegsNeeded) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Bwd2Cfg::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    kern<<<grid, kThreads, Bwd2Cfg::kSmemAlloc, stream>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const Shape& s, const void* o, bool o_f32, const void* dout,
@@ -1220,7 +1796,7 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
         if (s.window > 0) return cudaErrorInvalidValue;
         if (s.d == 128)
             return s.causal
-                       ? launch_dkdv_t<128, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
+                       ? launch_dkdv2_t<true, false, true>(tq, tk, tv, tdo, p, grid, stream)
                        : launch_dkdv_t<128, false, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream);
         return s.causal
                    ? launch_dkdv_t<64, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
@@ -1232,7 +1808,7 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
                           : launch_dkdv_t<64, true, true>(tq, tk, tv, tdo, tdq, p, grid, stream);
     }
     if (s.d == 128)
-        return s.causal ? launch_dkdv_t<128, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
+        return s.causal ? launch_dkdv2_t<true>(tq, tk, tv, tdo, p, grid, stream)
                         : launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdq, p, grid, stream);
     return s.causal ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
                     : launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdq, p, grid, stream);
