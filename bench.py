@@ -57,21 +57,21 @@ L2_BYTES = 129 * 1024 * 1024
 # workload, together with the sha256 of the kernel source it was taken on.  A
 # source change makes the figure stale and it is then reported as null.
 NCU_TRAFFIC = {
-    # 234.3 MB read + 97.4 MB written, one launch
-    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 331.71e6, "src_sha": "2946e01d138793f1"},
+    # 234.1 MB read + 97.6 MB written, one launch
+    ("fa_bwd_dkdv", "mha_d64"): {"bytes": 331.71e6, "src_sha": "59bcd1c401f82867"},
     # 136.7 MB read + 59.2 MB written (training forward), one launch
     ("fa_fwd", "mha_d64"): {"bytes": 195.86e6, "src_sha": "9c1ea912cf1c1295"},
-    # 1382.4 MB read + 638.9 MB written, one launch
-    ("fa_bwd_dkdv", "window"): {"bytes": 2021.29e6, "src_sha": "2946e01d138793f1"},
+    # 1383.5 MB read + 641.6 MB written, one launch
+    ("fa_bwd_dkdv", "window"): {"bytes": 2025.16e6, "src_sha": "59bcd1c401f82867"},
     # 246.8 MB read + 363.2 MB written (training forward: the -LSE table and
     # the zeroed dQ accumulator), one launch
     ("fa_fwd", "window"): {"bytes": 610.01e6, "src_sha": "9c1ea912cf1c1295"},
-    # 427.1 MB read + 225.2 MB written, one launch (two-pipeline kernel)
-    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 652.33e6, "src_sha": "2946e01d138793f1"},
+    # 427.0 MB read + 225.6 MB written, one launch (two-pipeline kernel)
+    ("fa_bwd_dkdv", "gpt_long"): {"bytes": 652.59e6, "src_sha": "59bcd1c401f82867"},
     # 558.1 MB read + 159.8 MB written (training forward), one launch
     ("fa_fwd", "gpt_long"): {"bytes": 717.86e6, "src_sha": "9c1ea912cf1c1295"},
-    # 759.3 MB read + 346.3 MB written, one launch (two-pipeline kernel)
-    ("fa_bwd_dkdv", "gqa"): {"bytes": 1105.62e6, "src_sha": "2946e01d138793f1"},
+    # 773.9 MB read + 353.8 MB written, one launch (two-pipeline kernel)
+    ("fa_bwd_dkdv", "gqa"): {"bytes": 1127.69e6, "src_sha": "59bcd1c401f82867"},
     # 424.6 MB read + 496.8 MB written (training forward, fp32 O), one launch
     ("fa_fwd", "gqa"): {"bytes": 921.44e6, "src_sha": "9c1ea912cf1c1295"},
     # 541.5 MB read + 96.6 MB written (fp32 O), one launch

@@ -1148,11 +1148,12 @@ cudaError_t launch_dkdv_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 // has issued step git - 1's (a turn barrier per accumulator): the tensor core
 // takes MMAs in issue order, so dK and dV sum their terms in step order and
 // come out bit-reproducible.
-// Used at d = 128 under the causal mask without a window (dense or packed
-// batches), where it measured faster (A/B on one box: dK/dV -2.1 % gpt_long,
-// -2.8 % gqa; steps +0.7 to +2.6 %, +1.9 % packed); with the sliding window
-// (long items) it measured 3.5 % slower and without the mask it was not
-// measured, so those keep the one-pipeline kernel.
+// Used at d = 128 except with the sliding window (dense or packed batches,
+// with or without the causal mask), where it measured faster (A/B on one
+// box: dK/dV -2.1 % gpt_long, -2.8 % gqa; steps +0.7 to +2.6 %, +1.9 %
+// packed; the whole backward without the mask -3.5 to -4 % at B4 H16 N4096
+// and B8 H16 N2048); with the window it measured 3.5 % slower, so the window
+// keeps the one-pipeline kernel.
 // Q_i / dO_i stream through three stages so that a pipeline's next block has
 // landed while its current one is in use; a stage's landing is signalled on
 // one of six barriers (step mod 6), so that each issuing thread waits on
@@ -1795,9 +1796,8 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     if (varlen) {   // packed variable-length sequences (no window)
         if (s.window > 0) return cudaErrorInvalidValue;
         if (s.d == 128)
-            return s.causal
-                       ? launch_dkdv2_t<true, false, true>(tq, tk, tv, tdo, p, grid, stream)
-                       : launch_dkdv_t<128, false, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream);
+            return s.causal ? launch_dkdv2_t<true, false, true>(tq, tk, tv, tdo, p, grid, stream)
+                            : launch_dkdv2_t<false, false, true>(tq, tk, tv, tdo, p, grid, stream);
         return s.causal
                    ? launch_dkdv_t<64, true, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
                    : launch_dkdv_t<64, false, false, true>(tq, tk, tv, tdo, tdq, p, grid, stream);
@@ -1809,7 +1809,7 @@ cudaError_t launch_bwd_dkdv(const Shape& s, const void* q, const void* k, const 
     }
     if (s.d == 128)
         return s.causal ? launch_dkdv2_t<true>(tq, tk, tv, tdo, p, grid, stream)
-                        : launch_dkdv_t<128, false>(tq, tk, tv, tdo, tdq, p, grid, stream);
+                        : launch_dkdv2_t<false>(tq, tk, tv, tdo, p, grid, stream);
     return s.causal ? launch_dkdv_t<64, true>(tq, tk, tv, tdo, tdq, p, grid, stream)
                     : launch_dkdv_t<64, false>(tq, tk, tv, tdo, tdq, p, grid, stream);
 }
