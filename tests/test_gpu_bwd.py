@@ -60,6 +60,28 @@ def test_bwd_dv_column_sum_invariant():
             assert np.abs(lhs - rhs).max() <= 2e-2 * np.abs(rhs).max() + 0.5
 
 
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_bwd_dkdv_reproducible(causal):
+    """dK and dV are the same bit for bit from call to call: at d = 128 the
+    even and odd query-block steps of a CTA run in two pipelines whose dV and
+    dK MMAs add into the same accumulators, in step order.  Many CTAs, many
+    steps each, GQA; five calls."""
+    w = small("repro", 2, 8, 2, 2048 + 77, 128, causal, 57)
+    q, k, v, do = make_inputs(w)
+    _, _, dev = run_fwd(q, k, v, w.causal, w.scale)
+    qd, kd, vd, o, lse = dev
+    dod = do.cuda()
+    first = None
+    for _ in range(5):
+        g = fa.attention_backward(qd, kd, vd, o, lse, dod, causal=causal, scale=w.scale)
+        torch.cuda.synchronize()
+        if first is None:
+            first = g
+        else:
+            assert torch.equal(g[1], first[1]) and torch.equal(g[2], first[2])
+    assert fa.fa_device_status() == 0
+
+
 def test_bwd_stages_equal_fused_call():
     """fa_bwd equals fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq_convert."""
     w = small("stages", 1, 4, 2, 300, 128, True, 53)
