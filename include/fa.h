@@ -181,7 +181,10 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int Hkv, int N, int d);
  * `workspace` (device, >= fa_bwd_workspace_size bytes, 16-byte aligned) is
  * scratch owned by the caller; its contents on entry do not matter.
  * Equivalent to fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq_convert in that
- * order on `stream` (three kernel launches).
+ * order on `stream` (three kernel launches).  dk and dv are the same bit for
+ * bit on every call with the same inputs (each key block's sums run in a
+ * fixed order); dq sums the key blocks' partials with reduce-adds in the
+ * order the CTAs finish, so its last bits can differ between calls.
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o,
                  const void* dout, const float* lse, void* dq, void* dk, void* dv,
